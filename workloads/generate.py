@@ -1,0 +1,192 @@
+"""Seeded synthetic inputs for the verify-and-sample epilogue.
+
+Input synthesis only (numpy, CPU): target logits, draft probabilities, draft ids,
+completion-count histories, per-request sampling parameters and the Philox
+uniforms.  Both the oracle and the CUDA path consume these arrays; neither side's
+arithmetic lives here.
+
+Shapes (one batch of B requests, K_max drafted tokens at most):
+  x      [B, K_max+1, V]  target logits, bf16 (stored as uint16 bit patterns) or fp32
+  q      [B, K_max, V]    draft probabilities, fp32 (softmax of synthetic draft logits)
+  d      [B, K_max]       draft token ids, int32 (positions >= K_b are padding, 0)
+  hist   CSR over requests: offsets [B+1], ids (ascending per request), counts (>0)
+  rows   structured [B]: temperature, top_k, top_p, presence, frequency, num_drafts
+  u      [B, K_max+1, 2]  fp32 uniforms (accept draw, resample/bonus draw)
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from .philox import epilogue_uniforms
+
+ROW_DTYPE = np.dtype([
+    ("temperature", np.float32),
+    ("top_k", np.int32),
+    ("top_p", np.float32),
+    ("presence_penalty", np.float32),
+    ("frequency_penalty", np.float32),
+    ("num_drafts", np.int32),
+])
+
+
+def row_params(temperature=0.0, top_k=0, top_p=1.0, presence=0.0, frequency=0.0, num_drafts=0):
+    return (np.float32(temperature), np.int32(top_k), np.float32(top_p),
+            np.float32(presence), np.float32(frequency), np.int32(num_drafts))
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 to bfloat16 (nearest, ties to even); returns uint16 bit patterns."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+@dataclass
+class Batch:
+    B: int
+    K_max: int
+    V: int
+    logits_dtype: str                 # "bf16" or "fp32"
+    x: np.ndarray                     # uint16 bits (bf16) or float32
+    q: np.ndarray                     # float32 [B, K_max, V]
+    draft_ids: np.ndarray             # int32 [B, K_max]
+    hist_offsets: np.ndarray          # int32 [B+1]
+    hist_ids: np.ndarray              # int32 [nnz]
+    hist_counts: np.ndarray           # int32 [nnz]
+    rows: np.ndarray                  # ROW_DTYPE [B]
+    uniforms: np.ndarray              # float32 [B, K_max+1, 2]
+    want_logprobs: bool = False
+    n_top_logprobs: int = 0
+    name: str = ""
+    meta: dict = field(default_factory=dict)
+
+    def x_f32(self, b=None) -> np.ndarray:
+        """Target logits as float32 (exact upcast of bf16)."""
+        xs = self.x if b is None else self.x[b]
+        return bf16_bits_to_f32(xs) if self.logits_dtype == "bf16" else np.asarray(xs, np.float32)
+
+    def history(self, b):
+        lo, hi = int(self.hist_offsets[b]), int(self.hist_offsets[b + 1])
+        return self.hist_ids[lo:hi], self.hist_counts[lo:hi]
+
+    def algorithmic_bytes(self) -> int:
+        """One read of each needed logit and draft probability."""
+        sx = 2 if self.logits_dtype == "bf16" else 4
+        total = 0
+        for b in range(self.B):
+            K = int(self.rows["num_drafts"][b])
+            total += (K + 1) * self.V * sx
+            if float(self.rows["temperature"][b]) > 0.0:
+                total += K * self.V * 4
+        return total
+
+    def verify_rows(self) -> int:
+        return int(np.sum(self.rows["num_drafts"].astype(np.int64) + 1))
+
+
+def zipf_history(rng, V, H, s, perm):
+    """H tokens with P(rank r) proportional to r^-s over ranks 1..V, mapped to ids by perm.
+
+    Returns (ids ascending, counts)."""
+    if H <= 0:
+        return np.zeros(0, np.int32), np.zeros(0, np.int32)
+    w = np.arange(1, V + 1, dtype=np.float64) ** (-s)
+    cdf = np.cumsum(w)
+    cdf /= cdf[-1]
+    ranks = np.searchsorted(cdf, rng.random(H), side="right")
+    ranks = np.minimum(ranks, V - 1)
+    toks = perm[ranks]
+    ids, counts = np.unique(toks, return_counts=True)
+    return ids.astype(np.int32), counts.astype(np.int32)
+
+
+def _softmax_f32(z64: np.ndarray) -> np.ndarray:
+    m = z64.max(axis=-1, keepdims=True)
+    e = np.exp(z64 - m)
+    return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
+               x_sigma=3.0, draft_sigma=1.0, boost_frac=0.0, boost=8.0,
+               history_len=0, zipf_s=1.1, draft_mode="q", argmax_frac=0.0,
+               x_quant=None, want_logprobs=False, n_top_logprobs=0, name="") -> Batch:
+    """Build one seeded batch.
+
+    rows: sequence of row_params tuples (length B).
+    draft_mode: "q"      -- d_i drawn from q_i (plain categorical draw, generator-side uniforms)
+                "argmax" -- d_i = argmax of the raw target logits at position i
+                "copy"   -- q_i = softmax of the target logits themselves (draft == target)
+    argmax_frac: after drawing, that fraction of draft tokens (seeded) is replaced by the
+                 raw target argmax at its position.
+    x_quant: if set, target logits are rounded to multiples of this step (tie-heavy rows).
+    """
+    rng = np.random.default_rng(seed)
+    rows_arr = np.array(list(rows), dtype=ROW_DTYPE)
+    assert rows_arr.shape == (B,)
+    n_rows = B * (K_max + 1)
+    boosted = np.zeros(n_rows, bool)
+    if boost_frac > 0:
+        nb = int(np.ceil(boost_frac * n_rows))
+        boosted[rng.choice(n_rows, size=nb, replace=False)] = True
+    boosted = boosted.reshape(B, K_max + 1)
+
+    x_store = np.empty((B, K_max + 1, V), np.uint16 if logits_dtype == "bf16" else np.float32)
+    q = np.empty((B, K_max, V), np.float32)
+    d = np.zeros((B, K_max), np.int32)
+    perm = rng.permutation(V)
+    offs = [0]
+    h_ids, h_cnt = [], []
+    for b in range(B):
+        xf = rng.standard_normal((K_max + 1, V), dtype=np.float32) * np.float32(x_sigma)
+        if x_quant is not None:
+            xf = (np.round(xf / np.float32(x_quant)) * np.float32(x_quant)).astype(np.float32)
+        for j in np.nonzero(boosted[b])[0]:
+            t = int(np.argmax(xf[j]))
+            xf[j, t] += np.float32(boost)
+        if logits_dtype == "bf16":
+            bits = f32_to_bf16_bits(xf)
+            x_store[b] = bits
+            xr = bf16_bits_to_f32(bits)
+        else:
+            x_store[b] = xf
+            xr = xf
+        if K_max > 0:
+            if draft_mode == "copy":
+                q[b] = _softmax_f32(xr[:K_max].astype(np.float64))
+            else:
+                noise = rng.standard_normal((K_max, V), dtype=np.float32) * np.float32(draft_sigma)
+                q[b] = _softmax_f32(xr[:K_max].astype(np.float64) + noise.astype(np.float64))
+            K_b = int(rows_arr["num_drafts"][b])
+            for i in range(K_max):
+                if draft_mode == "argmax":
+                    d[b, i] = int(np.argmax(xr[i]))
+                else:
+                    cdf = np.cumsum(q[b, i], dtype=np.float64)
+                    t = int(np.searchsorted(cdf, rng.random() * cdf[-1], side="right"))
+                    d[b, i] = min(t, V - 1)
+                if argmax_frac > 0 and rng.random() < argmax_frac:
+                    d[b, i] = int(np.argmax(xr[i]))
+                if i >= K_b:
+                    d[b, i] = 0
+        ids, cnt = zipf_history(rng, V, history_len, zipf_s, perm)
+        h_ids.append(ids)
+        h_cnt.append(cnt)
+        offs.append(offs[-1] + len(ids))
+    batch = Batch(
+        B=B, K_max=K_max, V=V, logits_dtype=logits_dtype, x=x_store, q=q, draft_ids=d,
+        hist_offsets=np.array(offs, np.int32),
+        hist_ids=np.concatenate(h_ids).astype(np.int32) if h_ids else np.zeros(0, np.int32),
+        hist_counts=np.concatenate(h_cnt).astype(np.int32) if h_cnt else np.zeros(0, np.int32),
+        rows=rows_arr, uniforms=epilogue_uniforms(philox_seed, B, K_max),
+        want_logprobs=want_logprobs, n_top_logprobs=n_top_logprobs, name=name,
+        meta=dict(seed=seed, philox_seed=philox_seed, x_sigma=x_sigma, draft_sigma=draft_sigma,
+                  boost_frac=boost_frac, history_len=history_len, draft_mode=draft_mode,
+                  argmax_frac=argmax_frac),
+    )
+    return batch
