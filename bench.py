@@ -1,0 +1,335 @@
+#!/usr/bin/env python3
+"""Throughput of the batched verify-and-sample epilogue on one or more GB300s.
+
+One step = one call of the whole epilogue (penalties, temperature, top-k / top-p on target
+and draft, acceptance, residual / bonus draws, logprobs) over one batch of the
+B=64, K=8, V=262,144 workload (bf16 logits, fp32 draft probabilities, inputs resident in
+HBM; 839 MB per batch, larger than the 129 MB L2, so no flush is needed between steps).
+
+Prints one JSON line: verify rows/s (whole job), the streaming kernel's roofline, clocks
+seen during the timed region, an end-to-end figure through the host-buffer entry point,
+and the float64 oracle timed on the host cores on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "b64k8v262144"
+METRIC = "verify rows/s & HBM GB/s (% roofline), B=64 K=8 V=262144 bf16, 1×GB300"
+UNIT = "verify rows/s"
+DOMINANT = "stream_stats_kernel"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stream_stats_kernel_b64k8v262144.md")
+KERNEL_SOURCES = [os.path.join(ROOT, "sample_verify_epilogue_gb300", "csrc", f)
+                  for f in ("stream_stats.cu", "dspark_internal.cuh")]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None
+    when the summary is missing or was taken on a different kernel source."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    vals = {}
+    for ln in txt.splitlines():
+        if ":" in ln and ln.strip().startswith(("traffic_bytes_per_launch", "kernel_source_hash")):
+            k, v = ln.split(":", 1)
+            vals[k.strip().strip("-* ")] = v.strip().strip("`")
+    if vals.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for ln in open(self.path):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0] or rows
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def time_oracle(batch, requests):
+    from oracle import epilogue as O
+    t = time.perf_counter()
+    O.verify_batch(batch, requests)
+    return time.perf_counter() - t
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        if rank != 0:
+            dist.destroy_process_group()
+            return
+    from workloads import configs
+    batch = configs.build(WORKLOAD, B=1)
+    rows_per_step = batch.verify_rows()
+    for _ in range(args.warmup):
+        time_oracle(batch, [0])
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle(batch, [0])
+    el = time.perf_counter() - t
+    value = rows_per_step * args.steps / el
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "one request (9 verify rows) per step", "B": 64, "K": 8,
+                   "V": 262144},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "one request of the workload per step, float64 numpy oracle"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_native(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    from sample_verify_epilogue_gb300 import binding
+    from sample_verify_epilogue_gb300.runner import EpilogueCall
+    from workloads import configs
+
+    ws, rank, local = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if rank == 0 or ws == 1:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+    binding.load_library()
+
+    # each rank owns its own 64 requests (independent problems: weak scaling, no collective)
+    batch = configs.build(WORKLOAD)
+    call = EpilogueCall(batch, device=device)
+    stream = torch.cuda.current_stream(device)
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+
+    for _ in range(args.warmup):
+        call.run()
+    torch.cuda.synchronize(device)
+    res = call.results()
+    accepted = int(np.sum(res["accept_len"].astype(np.int64) + 1))
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    w0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        call.run(stage_events=(ev_s[i].cuda_event, ev_e[i].cuda_event))
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    if dist is not None:
+        dist.barrier()
+    w1 = time.time()
+    clocks = sampler.stop(w0, w1) if sampler else None
+    elapsed_ms = t_start.elapsed_time(t_end)
+    kern_ms = statistics.mean(ev_s[i].elapsed_time(ev_e[i]) for i in range(args.steps))
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    rows_per_step = batch.verify_rows()
+    algo_bytes = batch.algorithmic_bytes()
+    value = rows_per_step * args.steps * ws / (elapsed_ms / 1e3)
+    peak, peak_kind = peaks()
+    achieved = algo_bytes / (kern_ms / 1e3) / 1e9
+    traffic = measured_traffic()
+
+    # end to end through the host-buffer entry point: pinned inputs in, results out, every step
+    e2e = None
+    if rank == 0 or ws > 1:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        hx = pin(np.ascontiguousarray(batch.x).view(np.int16))
+        hq = pin(batch.q)
+        hd = pin(batch.draft_ids)
+        hrows = pin(np.ascontiguousarray(batch.rows).view(np.uint8))
+        hcounts = (pin(batch.hist_offsets), pin(batch.hist_ids), pin(batch.hist_counts))
+        hu = pin(batch.uniforms)
+        W = batch.K_max + 1
+        hout = {"accept_len": torch.empty(batch.B, dtype=torch.int32).pin_memory(),
+                "tokens": torch.empty(batch.B, W, dtype=torch.int32).pin_memory(),
+                "logprobs": torch.empty(batch.B, W, dtype=torch.float32).pin_memory(),
+                "top_ids": torch.empty(batch.B, W, batch.n_top_logprobs, dtype=torch.int32).pin_memory(),
+                "top_logprobs": torch.empty(batch.B, W, batch.n_top_logprobs, dtype=torch.float32).pin_memory()}
+        hst = torch.empty(batch.B, dtype=torch.int32).pin_memory()
+        nbytes = binding.dspark_host_workspace_bytes(batch.B, batch.K_max, batch.V, "bf16", batch.n_top_logprobs,
+                                                     int(batch.hist_offsets[-1]))
+        del call
+        torch.cuda.empty_cache()
+        hws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        sid = stream.cuda_stream
+
+        def host_call():
+            binding.dspark_verify_sample_host(hx, hq, hd, hcounts, hrows, hu, out=hout, row_status=hst,
+                                              workspace=hws, logits_dtype="bf16", want_logprobs=True,
+                                              n_top_logprobs=batch.n_top_logprobs, stream=sid)
+
+        e2e_steps = max(1, min(args.steps, 200))
+        for _ in range(max(1, min(args.warmup, 5))):
+            host_call()
+        t = time.perf_counter()
+        for _ in range(e2e_steps):
+            host_call()
+        el = time.perf_counter() - t
+        h2d = sum(int(a.numel() * a.element_size()) for a in (hx, hq, hd, hrows, hu, *hcounts))
+        d2h = sum(int(a.numel() * a.element_size()) for a in (*hout.values(), hst))
+        e2e = {"value": rows_per_step * e2e_steps * ws / el, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        assert np.array_equal(hout["accept_len"].numpy(), res["accept_len"])
+
+    cpu = None
+    if rank == 0 and ws == 1:
+        sample = configs.build(WORKLOAD, B=2)
+        t = time_oracle(sample, [0, 1])
+        cpu = {"value": sample.verify_rows() / t, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "2 requests (18 verify rows) of the workload, float64 numpy oracle, single thread"}
+
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "B": batch.B, "K": batch.K_max, "V": batch.V,
+                       "logits": "bf16", "q": "fp32", "T": 1.0, "top_k": 64, "top_p": 0.95,
+                       "penalties": "presence 0.2 / frequency 0.2, 4096-token Zipf histories",
+                       "top_logprobs": 20, "l2": "inputs (839 MB) larger than L2, no flush",
+                       "parallelism": f"{ws} independent replica(s), no collective"},
+            "sampled_tokens_per_s": accepted * args.steps * ws / (elapsed_ms / 1e3),
+            "hbm_gbs_per_call": algo_bytes * args.steps * ws / (elapsed_ms / 1e3) / 1e9 / ws,
+            "algorithmic_bytes_per_step": algo_bytes,
+            "roofline": {"bound": "hbm", "kernel": DOMINANT, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
+                         "kernel_ms": kern_ms},
+            "gpu_launches": binding.dspark_launches_per_call() * args.steps,
+            "clocks": clocks,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(out))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=("native", "reference"), default="native")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        args.steps = 10 if args.steps is None else args.steps
+        args.warmup = 3 if args.warmup is None else args.warmup
+        run_reference(args)
+    else:
+        args.steps = 2000 if args.steps is None else args.steps
+        args.warmup = 20 if args.warmup is None else args.warmup
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,424 @@
+// accept_kernel: one CTA per request.  The acceptance decisions of all drafted positions
+// are independent given the rows' truncated distributions, so thread i takes position i:
+//   greedy (T = 0): accept iff d_i equals the penalised argmax of target row i (lowest id
+//     on ties); the accepted length is the first mismatch (mlx-dspark Changelog, [0.2.0]
+//     Changed: cumprod of positionwise matches);
+//   T > 0: accept iff u_i < P'_i(d_i) / Q'_i(d_i), always when Q'_i(d_i) = 0 < P'_i(d_i)
+//     (v0.0.2 release notes, Highlights: accept with probability min(1, p/q)).
+// At the first rejection a the residual max(0, P'_a - Q'_a) is drawn from, or P'_K when all
+// K drafts were accepted; greedy emits the argmax.  When the target row's support is a short
+// list the draw happens here: weights in double, ids sorted ascending, an exclusive scan, and
+// the smallest id whose cumulative mass exceeds u * total.  Whole-vocabulary supports are
+// left to finish_kernel.
+//
+// finish_kernel: one CTA per request.  Whole-row inverse-CDF draws (two passes over the
+// row in fixed-size chunks, fixed summation order so both passes agree bit for bit), then
+// the logprob outputs: raw log-softmax at each emitted token and the top-n list (mlx-dspark
+// Changelog, [0.2.0] Added, logprobs / top_logprobs).
+#include "block_utils.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kAcceptThreads = 512;
+
+struct AccSmem {
+    int acc[DSPARK_MAX_K + 1];
+    unsigned long long sk[kKeptCap];
+    double r[kKeptCap];
+    double rs[kKeptCap];
+    double ex[kKeptCap + 1];
+    double dwarp[33];
+    int iwarp[32];
+    int a;
+    int tok;
+};
+
+__device__ __forceinline__ int prefix_count(const Args& a, int b, int i, int t) {
+    int c = 0;
+    for (int q = 0; q < i; ++q) c += (a.d[static_cast<long long>(b) * a.Km + q] == t);
+    return c;
+}
+
+// Target probability P'_j(d_j) of the drafted token at position j (0 outside the support).
+// Its count is the history count recorded by the penalty index plus the draft prefix.
+__device__ __forceinline__ double target_prob_of_draft(const Args& a, const XRowOut& xo, int b, int j, int t,
+                                                       const dspark_row_params_t& r) {
+    const long long slot = static_cast<long long>(b) * (a.Km + 1) + j;
+    const float xv = load_x(a.x, a.sx, slot * a.V + t);
+    int c = 0;
+    if (has_penalty(r)) c = a.draft_base[static_cast<long long>(b) * a.Km + j] + prefix_count(a, b, j, t);
+    const float xp = penalise(xv, c, r.frequency_penalty, r.presence_penalty);
+    if (!(xp >= xo.tau)) return 0.0;
+    return static_cast<double>(target_weight(xp, xo.m_pen, xo.c_l2e)) / xo.Z;
+}
+
+__device__ __forceinline__ double draft_prob(const Args& a, const QRowOut& qo, int b, int i, int t, bool t_one) {
+    const long long qs = static_cast<long long>(b) * a.Km + i;
+    const float qv = __ldg(a.q + qs * a.V + t);
+    if (!(qv >= qo.tau)) return 0.0;
+    return static_cast<double>(draft_weight(qv, qo.qmax, qo.inv_t, t_one)) / qo.Z;
+}
+
+__device__ void write_error(const Args& a, int b, int st) {
+    const int tid = threadIdx.x;
+    const int W = a.Km + 1;
+    for (int j = tid; j < W; j += blockDim.x) {
+        a.out_tokens[static_cast<long long>(b) * W + j] = -1;
+        if (a.out_lp) a.out_lp[static_cast<long long>(b) * W + j] = -INFINITY;
+    }
+    for (int e = tid; e < W * a.n_top; e += blockDim.x) {
+        if (a.out_top_ids) a.out_top_ids[static_cast<long long>(b) * W * a.n_top + e] = -1;
+        if (a.out_top_lp) a.out_top_lp[static_cast<long long>(b) * W * a.n_top + e] = -INFINITY;
+    }
+    if (tid == 0) {
+        a.out_accept[b] = -1;
+        a.req[b] = ReqOut{-1, 0, st, 0};
+    }
+}
+
+__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
+    extern __shared__ __align__(16) unsigned char acc_raw[];
+    AccSmem& s = *reinterpret_cast<AccSmem*>(acc_raw);
+    const int b = blockIdx.x, tid = threadIdx.x;
+    int st = a.row_status[b];
+    if (a.plan->pad[0]) st |= DSPARK_ROW_INTERNAL;
+    if (st) { write_error(a, b, st); return; }
+    const dspark_row_params_t r = a.rows[b];
+    const int K = r.num_drafts;
+    const bool greedy = !(r.temperature > 0.f);
+    const bool t_one = r.temperature == 1.f;
+    const int W = a.Km + 1;
+    const long long xs0 = static_cast<long long>(b) * W;
+    const long long qs0 = static_cast<long long>(b) * a.Km;
+    // ---- acceptance decisions, one thread per drafted position
+    if (tid < K) {
+        const int t = a.d[qs0 + tid];
+        bool ok;
+        if (greedy) {
+            ok = (t == a.xout[xs0 + tid].argmax);
+        } else {
+            const XRowOut xo = a.xout[xs0 + tid];
+            const QRowOut qo = a.qout[qs0 + tid];
+            const double P = target_prob_of_draft(a, xo, b, tid, t, r);
+            const double Q = draft_prob(a, qo, b, tid, t, t_one);
+            const double u = static_cast<double>(a.u[(xs0 + tid) * 2 + 0]);
+            ok = (Q == 0.0) ? (P > 0.0) : (u < P / Q);
+        }
+        s.acc[tid] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    int first = K;
+    if (tid < K && !s.acc[tid]) first = tid;
+    const int acc_len = block_min_i(first, s.iwarp);
+    // ---- the emitted token at position acc_len
+    int draw = 0;
+    int tok = -1;
+    const XRowOut xa = a.xout[xs0 + acc_len];
+    if (greedy) {
+        tok = xa.argmax;
+    } else if (xa.mode == kModeList) {
+        const int n = xa.n_kept;
+        const bool residual = acc_len < K;
+        QRowOut qa{};
+        if (residual) qa = a.qout[qs0 + acc_len];
+        const KeptEntry* kl = a.kept + (xs0 + acc_len) * kKeptCap;
+        for (int e = tid; e < n; e += blockDim.x) {
+            const KeptEntry ke = kl[e];
+            const double P = static_cast<double>(ke.w) / xa.Z;
+            double rv = P;
+            if (residual) rv = fmax(0.0, P - draft_prob(a, qa, b, acc_len, ke.id, t_one));
+            s.r[e] = rv;
+            s.sk[e] = (static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<unsigned>(ke.id)) << 32) |
+                      static_cast<unsigned>(e);
+        }
+        const int P2 = next_pow2(max(n, 2));
+        for (int e = n + tid; e < P2; e += blockDim.x) s.sk[e] = 0ull;
+        block_bitonic_desc(s.sk, P2);                   // ascending token id
+        for (int e = tid; e < n; e += blockDim.x) s.rs[e] = s.r[s.sk[e] & 0xFFFFFFFFull];
+        __syncthreads();
+        block_scan_excl_d(s.rs, s.ex, n, s.dwarp);
+        if (!(s.ex[n] > 0.0)) {                          // empty residual: draw from P'
+            for (int e = tid; e < n; e += blockDim.x)
+                s.rs[e] = static_cast<double>(kl[s.sk[e] & 0xFFFFFFFFull].w) / xa.Z;
+            __syncthreads();
+            block_scan_excl_d(s.rs, s.ex, n, s.dwarp);
+        }
+        const double target = static_cast<double>(a.u[(xs0 + acc_len) * 2 + 1]) * s.ex[n];
+        if (tid == 0) s.tok = -1;
+        __syncthreads();
+        for (int e = tid; e < n; e += blockDim.x)
+            if (s.ex[e + 1] > target && s.ex[e] <= target) s.tok = e;
+        __syncthreads();
+        int pos = s.tok;
+        if (pos < 0) {                                    // rounding put u*total at the very top
+            int last = -1;
+            for (int e = tid; e < n; e += blockDim.x) if (s.rs[e] > 0.0) last = max(last, e);
+            pos = -block_min_i(-last, s.iwarp);
+        }
+        tok = pos >= 0 ? static_cast<int>(0xFFFFFFFFu - static_cast<unsigned>(s.sk[pos] >> 32)) : -1;
+    } else {
+        draw = (acc_len < K) ? 1 : 2;                     // whole-row draw in finish_kernel
+    }
+    for (int j = tid; j < W; j += blockDim.x) {
+        int v = -1;
+        if (j < acc_len) v = a.d[qs0 + j];
+        else if (j == acc_len) v = tok;
+        a.out_tokens[xs0 + j] = v;
+    }
+    if (tid == 0) {
+        a.out_accept[b] = acc_len;
+        a.req[b] = ReqOut{acc_len, draw, 0, 0};
+    }
+}
+
+// ============================================================================ finish
+constexpr int kFinishThreads = 512;
+constexpr int kPerThread = 8;
+constexpr int kChunk = kFinishThreads * kPerThread;     // 4096 elements: divides both tile sizes
+constexpr int kMaxChunks = (DSPARK_MAX_V + kChunk - 1) / kChunk;
+
+struct FinishSmem {
+    double chunk_sum[kMaxChunks];
+    double dwarp[33];
+    unsigned bm[kBitmapWordsMax];
+    PenEntry ent[kPenCap];
+    double th_ex[kFinishThreads + 1];
+    double th_sum[kFinishThreads];
+    int found_chunk;
+    int tok;
+    int pen_n, pen_nh, pen_over, pen_tile;
+};
+
+struct DrawCtx {
+    const Args* a;
+    int b, row_j;
+    long long xslot, qslot;
+    XRowOut xo;
+    QRowOut qo;
+    bool residual, t_one, pen, use_p_only;
+    float f, p;
+};
+
+__device__ void stage_penalty_tile(FinishSmem& s, const DrawCtx& c, int tile) {
+    const Args& a = *c.a;
+    __syncthreads();
+    const long long pt = static_cast<long long>(c.b) * a.tiles_x + tile;
+    const PenHdr h = a.pen_hdr[pt];
+    for (int w = threadIdx.x; w < a.bm_words; w += blockDim.x) s.bm[w] = a.pen_bm[pt * a.bm_words + w];
+    if (!h.overflow) for (int k = threadIdx.x; k < h.n; k += blockDim.x) s.ent[k] = a.pen_ent[pt * kPenCap + k];
+    if (threadIdx.x == 0) { s.pen_n = h.n; s.pen_nh = h.pad[0]; s.pen_over = h.overflow; s.pen_tile = tile; }
+    __syncthreads();
+}
+
+__device__ int staged_count(const FinishSmem& s, const DrawCtx& c, int tok) {
+    const Args& a = *c.a;
+    if (!s.pen_over) {
+        int l = 0, h = s.pen_nh;
+        while (l < h) { const int m = (l + h) >> 1; if (s.ent[m].token < tok) l = m + 1; else h = m; }
+        int e = -1;
+        if (l < s.pen_nh && s.ent[l].token == tok) e = l;
+        else for (int k = s.pen_nh; k < s.pen_n; ++k) if (s.ent[k].token == tok) { e = k; break; }
+        if (e < 0) return 0;
+        const unsigned long long mask = (static_cast<unsigned long long>(s.ent[e].mask_hi) << 32) | s.ent[e].mask_lo;
+        const unsigned long long low = (c.row_j >= 64) ? ~0ull : ((1ull << c.row_j) - 1ull);
+        return s.ent[e].base + __popcll(mask & low);
+    }
+    int base = 0;
+    const int hlo = a.h_off ? a.h_off[c.b] : 0, hhi = a.h_off ? a.h_off[c.b + 1] : 0;
+    int l = hlo, h = hhi;
+    while (l < h) { const int m = (l + h) >> 1; if (a.h_ids[m] < tok) l = m + 1; else h = m; }
+    if (l < hhi && a.h_ids[l] == tok) base = a.h_cnt[l];
+    return base + prefix_count(a, c.b, c.row_j, tok);
+}
+
+// Residual (or target) weight of token t of the draw row, in double.
+__device__ double draw_weight(const FinishSmem& s, const DrawCtx& c, int t) {
+    const Args& a = *c.a;
+    float xv = load_x(a.x, a.sx, c.xslot * a.V + t);
+    if (c.pen) {
+        const int tl = t - s.pen_tile * a.tile_x;
+        if ((s.bm[tl >> 5] >> (tl & 31)) & 1u) xv = penalise(xv, staged_count(s, c, t), c.f, c.p);
+    }
+    double P = 0.0;
+    if (xv >= c.xo.tau) P = static_cast<double>(target_weight(xv, c.xo.m_pen, c.xo.c_l2e)) / c.xo.Z;
+    if (!c.residual || c.use_p_only) return P;
+    const float qv = __ldg(a.q + c.qslot * a.V + t);
+    double Q = 0.0;
+    if (qv >= c.qo.tau) Q = static_cast<double>(draft_weight(qv, c.qo.qmax, c.qo.inv_t, c.t_one)) / c.qo.Z;
+    return fmax(0.0, P - Q);
+}
+
+// Sum of the weights of this thread's kPerThread consecutive elements of chunk ch.
+__device__ double thread_chunk_sum(FinishSmem& s, const DrawCtx& c, int ch) {
+    const int V = c.a->V;
+    const int e0 = ch * kChunk + threadIdx.x * kPerThread;
+    double acc = 0.0;
+    for (int q = 0; q < kPerThread; ++q) {
+        const int e = e0 + q;
+        if (e < V) acc += draw_weight(s, c, e);
+    }
+    return acc;
+}
+
+__device__ void maybe_stage(FinishSmem& s, const DrawCtx& c, int ch) {
+    if (!c.pen) return;
+    const int tile = (ch * kChunk) / c.a->tile_x;
+    if (tile != s.pen_tile) stage_penalty_tile(s, c, tile);
+}
+
+__device__ int whole_row_draw(FinishSmem& s, DrawCtx& c, float u) {
+    const Args& a = *c.a;
+    const int tid = threadIdx.x;
+    const int nch = (a.V + kChunk - 1) / kChunk;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        if (tid == 0) s.pen_tile = -1;
+        __syncthreads();
+        for (int ch = 0; ch < nch; ++ch) {
+            maybe_stage(s, c, ch);
+            const double v = thread_chunk_sum(s, c, ch);
+            const double tot = block_sum_d(v, s.dwarp);
+            if (tid == 0) s.chunk_sum[ch] = tot;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            double run = 0.0;
+            for (int ch = 0; ch < nch; ++ch) run += s.chunk_sum[ch];
+            s.th_ex[0] = run;
+        }
+        __syncthreads();
+        const double total = s.th_ex[0];
+        if (!(total > 0.0) && c.residual && !c.use_p_only) { c.use_p_only = true; continue; }
+        const double target = static_cast<double>(u) * total;
+        if (tid == 0) {
+            double run = 0.0;
+            int pick = -1;
+            for (int ch = 0; ch < nch; ++ch) {
+                if (run + s.chunk_sum[ch] > target && s.chunk_sum[ch] > 0.0) { pick = ch; break; }
+                run += s.chunk_sum[ch];
+            }
+            if (pick < 0) {                            // rounding: the last chunk with mass
+                for (int ch = nch - 1; ch >= 0; --ch) if (s.chunk_sum[ch] > 0.0) { pick = ch; break; }
+                run = 0.0;
+                for (int ch = 0; ch < pick; ++ch) run += s.chunk_sum[ch];
+            }
+            s.found_chunk = pick;
+            s.th_ex[kFinishThreads] = run;             // mass before the chunk
+        }
+        __syncthreads();
+        const int ch = s.found_chunk;
+        if (ch < 0) return -1;
+        const double before = s.th_ex[kFinishThreads];
+        if (c.pen) { if (tid == 0) s.pen_tile = -1; __syncthreads(); maybe_stage(s, c, ch); }
+        const double mine = thread_chunk_sum(s, c, ch);
+        s.th_sum[tid] = mine;
+        __syncthreads();
+        if (tid == 0) {
+            double run = before;
+            int pick = -1;
+            for (int t = 0; t < kFinishThreads; ++t) {
+                if (run + s.th_sum[t] > target && s.th_sum[t] > 0.0) { pick = t; break; }
+                run += s.th_sum[t];
+            }
+            if (pick < 0) {
+                for (int t = kFinishThreads - 1; t >= 0; --t) if (s.th_sum[t] > 0.0) { pick = t; break; }
+                run = before;
+                for (int t = 0; t < pick; ++t) run += s.th_sum[t];
+            }
+            int tok = -1;
+            if (pick >= 0) {
+                const int e0 = ch * kChunk + pick * kPerThread;
+                int last = -1;
+                for (int q = 0; q < kPerThread; ++q) {
+                    const int e = e0 + q;
+                    if (e >= a.V) break;
+                    const double w = draw_weight(s, c, e);
+                    if (w > 0.0) last = e;
+                    if (run + w > target && w > 0.0) { tok = e; break; }
+                    run += w;
+                }
+                if (tok < 0) tok = last;
+            }
+            s.tok = tok;
+        }
+        __syncthreads();
+        return s.tok;
+    }
+    return -1;
+}
+
+__global__ void __launch_bounds__(kFinishThreads) finish_kernel(Args a) {
+    extern __shared__ __align__(16) unsigned char fin_raw[];
+    FinishSmem& s = *reinterpret_cast<FinishSmem*>(fin_raw);
+    const int b = blockIdx.x, tid = threadIdx.x;
+    const ReqOut ro = a.req[b];
+    if (ro.a < 0) return;
+    const int W = a.Km + 1;
+    const long long xs0 = static_cast<long long>(b) * W;
+    const int acc_len = ro.a;
+    if (ro.draw) {
+        const dspark_row_params_t r = a.rows[b];
+        DrawCtx c;
+        c.a = &a;
+        c.b = b;
+        c.row_j = acc_len;
+        c.xslot = xs0 + acc_len;
+        c.qslot = static_cast<long long>(b) * a.Km + acc_len;
+        c.xo = a.xout[c.xslot];
+        c.residual = ro.draw == 1;
+        if (c.residual) c.qo = a.qout[c.qslot];
+        c.t_one = r.temperature == 1.f;
+        c.pen = has_penalty(r);
+        c.use_p_only = false;
+        c.f = r.frequency_penalty;
+        c.p = r.presence_penalty;
+        const int tok = whole_row_draw(s, c, a.u[(xs0 + acc_len) * 2 + 1]);
+        if (tid == 0) a.out_tokens[xs0 + acc_len] = tok;
+        __syncthreads();
+    }
+    // ---- logprob outputs
+    if (a.out_lp || (a.n_top > 0 && (a.out_top_ids || a.out_top_lp))) {
+        for (int j = tid; j < W; j += blockDim.x) {
+            float lp = -INFINITY;
+            if (j <= acc_len) {
+                const int t = a.out_tokens[xs0 + j];
+                const XRowOut xo = a.xout[xs0 + j];
+                if (t >= 0) lp = load_x(a.x, a.sx, (xs0 + j) * a.V + t) - xo.lse;
+            }
+            if (a.out_lp) a.out_lp[xs0 + j] = lp;
+        }
+        for (int e = tid; e < W * a.n_top; e += blockDim.x) {
+            const int j = e / a.n_top, q = e % a.n_top;
+            int id = -1;
+            float v = -INFINITY;
+            if (j <= acc_len) {
+                const TopEntry te = a.topn[(xs0 + j) * DSPARK_MAX_TOP_LOGPROBS + q];
+                id = te.id;
+                v = te.v - a.xout[xs0 + j].lse;
+            }
+            if (a.out_top_ids) a.out_top_ids[xs0 * a.n_top + e] = id;
+            if (a.out_top_lp) a.out_top_lp[xs0 * a.n_top + e] = v;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_accept(const Args& a, cudaStream_t s) {
+    const size_t smem = sizeof(AccSmem);
+    cudaError_t e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    accept_kernel<<<a.B, kAcceptThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finish(const Args& a, cudaStream_t s) {
+    const size_t smem = sizeof(FinishSmem);
+    cudaError_t e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    finish_kernel<<<a.B, kFinishThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

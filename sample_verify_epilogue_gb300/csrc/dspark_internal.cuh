@@ -1,0 +1,332 @@
+// Internal definitions shared by the sm_103a kernels of the verify-and-sample epilogue.
+//
+// Data flow of one call (all on the caller's stream, no host synchronisation):
+//   prep_kernel          plan of work units + per-(request, vocab tile) penalty index
+//   stream_stats_kernel  the one HBM pass over x and q: per-tile maxima, sums and candidates
+//   row_finalize_kernel  per verify row: merge tiles, top-k threshold, nucleus, normaliser
+//   full_threshold_kernel  rows that need a threshold over the whole vocabulary (rare)
+//   accept_kernel        per request: accept scan, residual / bonus draw over candidates
+//   finish_kernel        per request: whole-vocabulary draws (rare) and logprob outputs
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------- sizes
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumerThreads = kConsumerWarps * 32;          // 512
+constexpr int kStreamThreads = kConsumerThreads + 32;          // + one producer warp
+constexpr int kStages = 3;
+constexpr int kStageBytes = 48 * 1024;                         // one vocab tile per stage
+constexpr int kTileBf16 = kStageBytes / 2;                     // 24576 elements
+constexpr int kTileF32 = kStageBytes / 4;                      // 12288 elements
+constexpr int kBitmapWordsMax = kTileBf16 / 32;                // 768
+constexpr int kPenCap = 512;                                   // penalised tokens per tile held in smem
+constexpr int kSmemCandPen = 1024;                             // per-tile candidate buffer (smem)
+constexpr int kSmemCandRaw = 512;
+constexpr int kCandPenGlobal = 512;                            // per-tile candidates kept in the workspace
+constexpr int kCandRawGlobal = 128;
+constexpr int kMaxCandTopK = 256;                              // top_k above this uses the whole-row path
+constexpr int kKeptCap = 1024;                                 // truncated support held as a list
+constexpr int kFinalizeThreads = 512;
+constexpr int kMergeCap = 8192;                                // merged candidates per row (smem)
+constexpr int kMaxB = 8192;
+
+// ---------------------------------------------------------------- records in the workspace
+enum UnitKind : int { kUnitX = 0, kUnitQ = 1 };
+
+struct Plan {
+    int n_units;
+    int pad[3];
+};
+
+struct UnitDesc {        // one vocab tile of one row
+    int slot;            // x: b*(K_max+1)+j ; q: b*K_max+i
+    int kind;
+    int tile;
+    int b;
+};
+
+struct TileStats {       // per (row, tile)
+    float m_raw;         // x: raw max           | q: max
+    float s_raw;         // x: sum exp(x-m_raw)  | q: sum q
+    float m_pen;         // x: penalised max
+    int   arg_pen;       // x: lowest id attaining m_pen
+    float s_temp;        // x: sum exp((x'-m_pen)/T) | q: sum (q/max)^(1/T)
+    int   n_pen;         // candidates written (penalised x / q)
+    int   n_raw;         // raw-logit candidates written
+    int   flags;         // kTileOverflow, kTileBad
+};
+constexpr int kTileOverflowPen = 1;
+constexpr int kTileOverflowRaw = 2;
+constexpr int kTileBad = 4;
+
+struct Cand { float v; int id; };
+
+struct PenEntry {        // a token that may carry a penalty in this tile
+    int token;
+    int base;            // completion-history count
+    unsigned mask_lo;    // bit i: d_i == token (i < 32)
+    unsigned mask_hi;    // bit i-32
+};
+struct PenHdr { int n; int overflow; int pad[2]; };
+
+// row modes written by row_finalize / full_threshold
+enum RowMode : int {
+    kModeInactive = 0,
+    kModeGreedy = 1,
+    kModeList = 2,       // truncated support held as a list (value-descending)
+    kModeFull = 3,       // support = {t : value >= tau}, weights evaluated on the fly
+    kModeNeedFull = 4,   // full_threshold_kernel still has to set tau / Z
+};
+
+struct XRowOut {
+    int    mode;
+    int    argmax;       // penalised argmax (lowest id on ties)
+    float  m_pen;        // penalised max
+    float  lse;          // raw log-sum-exp
+    float  tau;          // support threshold on x'
+    float  c_l2e;        // log2(e)/T
+    int    n_kept;
+    int    top_k;        // top_k still to apply (whole-row path), 0 = none
+    double Z;            // sum of support weights exp2((x'-m_pen)*c_l2e)
+    float  top_p;
+    int    flags;
+};
+
+struct QRowOut {
+    int    mode;
+    float  qmax;
+    float  tau;          // support threshold on q
+    float  inv_t;
+    double Z;            // sum of support weights (q/qmax)^(1/T) (T=1: q)
+    int    top_k;
+    float  top_p;
+    int    flags;
+    int    pad;
+};
+
+struct KeptEntry { int id; float w; };
+struct TopEntry { int id; float v; };
+
+struct ReqOut {
+    int a;               // accepted drafts
+    int draw;            // 0 none pending, 1 residual over the whole row, 2 target row over the whole row
+    int status;
+    int pad;
+};
+
+// Device-side view of the workspace and the call's arguments.
+struct Args {
+    // shapes
+    int B, Km, V, sx, xdtype;
+    int tile_x, tiles_x, tile_q, tiles_q, bm_words;
+    int n_top, want_lp;
+    int xslots, qslots;
+    // inputs (device)
+    const void* x;
+    const float* q;
+    const int* d;
+    const dspark_row_params_t* rows;
+    const int* h_off;
+    const int* h_ids;
+    const int* h_cnt;
+    const float* u;
+    // outputs (device)
+    int* out_accept;
+    int* out_tokens;
+    float* out_lp;
+    int* out_top_ids;
+    float* out_top_lp;
+    int* row_status;
+    // workspace
+    Plan* plan;
+    UnitDesc* units;
+    TileStats* ts_x;       // [xslots * tiles_x]
+    TileStats* ts_q;       // [qslots * tiles_q]
+    Cand* cand_x;          // [xslots * tiles_x * kCandPenGlobal]
+    Cand* cand_raw;        // [xslots * tiles_x * kCandRawGlobal]
+    Cand* cand_q;          // [qslots * tiles_q * kCandPenGlobal]
+    PenHdr* pen_hdr;       // [B * tiles_x]
+    unsigned* pen_bm;      // [B * tiles_x * bm_words]
+    PenEntry* pen_ent;     // [B * tiles_x * kPenCap]
+    int* draft_base;       // [B * Km]
+    XRowOut* xout;         // [xslots]
+    KeptEntry* kept;       // [xslots * kKeptCap]
+    TopEntry* topn;        // [xslots * DSPARK_MAX_TOP_LOGPROBS]
+    QRowOut* qout;         // [qslots]
+    ReqOut* req;           // [B]
+};
+
+// ---------------------------------------------------------------- small helpers
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float load_x(const void* x, int sx, long long idx) {
+    if (sx == 2) {
+        unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(x) + idx);
+        return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    }
+    return __ldg(reinterpret_cast<const float*>(x) + idx);
+}
+
+// Order-preserving 32-bit key of a float (-0 folded onto +0, so equal floats share a key).
+__device__ __forceinline__ uint32_t fkey(float v) {
+    uint32_t u = __float_as_uint(v);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_f(uint32_t k) {
+    uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+    return __uint_as_float(u);
+}
+// Composite key: value descending, then id ascending, when sorted descending.
+__device__ __forceinline__ unsigned long long ckey(float v, int id) {
+    return (static_cast<unsigned long long>(fkey(v)) << 32) | static_cast<unsigned>(0xFFFFFFFFu - static_cast<unsigned>(id));
+}
+__device__ __forceinline__ int ckey_id(unsigned long long k) {
+    return static_cast<int>(0xFFFFFFFFu - static_cast<unsigned>(k & 0xFFFFFFFFull));
+}
+__device__ __forceinline__ float ckey_v(unsigned long long k) { return key_to_f(static_cast<uint32_t>(k >> 32)); }
+
+// OpenAI penalty in float32 with a fixed operation order: x - ((f*c) + p), no contraction.
+__device__ __forceinline__ float penalise(float x, int c, float f, float p) {
+    if (c <= 0) return x;
+    return __fsub_rn(x, __fadd_rn(__fmul_rn(f, static_cast<float>(c)), p));
+}
+
+// Target weight exp((x'-m)/T), computed as 2^((x'-m)*log2(e)/T).
+__device__ __forceinline__ float target_weight(float xp, float m, float c_l2e) {
+    return exp2f(__fmul_rn(__fsub_rn(xp, m), c_l2e));
+}
+// Draft weight (q/qmax)^(1/T); at T = 1 the probability itself.
+__device__ __forceinline__ float draft_weight(float q, float qmax, float inv_t, bool t_is_one) {
+    if (t_is_one) return q;
+    if (!(q > 0.f)) return 0.f;
+    return exp2f(inv_t * log2f(q / qmax));
+}
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+    return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier / bulk-copy PTX
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait: returns false when the limit runs out (the caller records an error).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, long long limit) {
+    for (long long i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+// One-dimensional bulk copy global -> shared, completing on an mbarrier (TMA engine).
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, unsigned bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_u32(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- warp reductions
+__device__ __forceinline__ float warp_max(float v) {
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_min(float v) {
+    for (int o = 16; o; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_min_i(int v) {
+    for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+// c-th largest value across the 32 lanes (with multiplicity), c in [1, 32].
+__device__ __forceinline__ float warp_kth_largest(float v, int c) {
+    float cur = v, kth = -INFINITY;
+    const int lane = threadIdx.x & 31;
+    for (int r = 0; r < c; ++r) {
+        kth = warp_max(cur);
+        unsigned hit = __ballot_sync(0xffffffffu, cur == kth);
+        int first = __ffs(hit) - 1;
+        if (lane == first) cur = -INFINITY;
+    }
+    return kth;
+}
+
+// ---------------------------------------------------------------- request validity
+// Status bits that follow from the parameters and the draft ids alone.
+__device__ __forceinline__ int request_status(const Args& a, int b) {
+    const dspark_row_params_t r = a.rows[b];
+    int st = 0;
+    const bool t_ok = isfinite(r.temperature) && r.temperature >= 0.f;
+    const bool p_ok = r.top_p > 0.f && isfinite(r.top_p);
+    if (!t_ok || !p_ok || r.top_k < 0 || r.num_drafts < 0 || r.num_drafts > a.Km ||
+        !isfinite(r.presence_penalty) || !isfinite(r.frequency_penalty))
+        return DSPARK_ROW_BAD_PARAMS;
+    if (r.temperature > 0.f && r.num_drafts > 0 && a.q == nullptr) return DSPARK_ROW_BAD_PARAMS;
+    for (int i = 0; i < r.num_drafts; ++i) {
+        const int t = a.d[static_cast<long long>(b) * a.Km + i];
+        if (t < 0 || t >= a.V) st |= DSPARK_ROW_BAD_DRAFT;
+    }
+    return st;
+}
+
+__device__ __forceinline__ bool has_penalty(const dspark_row_params_t& r) {
+    return r.presence_penalty != 0.f || r.frequency_penalty != 0.f;
+}
+
+// ---------------------------------------------------------------- launchers (one per .cu)
+cudaError_t launch_prep(const Args& a, cudaStream_t s);
+cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid);
+cudaError_t launch_row_finalize(const Args& a, cudaStream_t s);
+cudaError_t launch_full_threshold(const Args& a, cudaStream_t s);
+cudaError_t launch_accept(const Args& a, cudaStream_t s);
+cudaError_t launch_finish(const Args& a, cudaStream_t s);
+
+}  // namespace dspark

@@ -1,0 +1,634 @@
+// row_finalize_kernel: one CTA per verify row (target position (b, j) or draft position
+// (b, i)).  Merges the per-tile statistics of the streaming pass and settles the row's
+// truncated distribution:
+//   - target rows: raw log-sum-exp (logprobs), penalised max and argmax (greedy), the top-k
+//     threshold tau_k = k-th largest penalised logit among the merged tile candidates (exact:
+//     every member of the row's top-k is a candidate of its own tile), the survivors
+//     {x' >= tau_k} sorted by (value desc, id asc), their weights exp((x'-max)/T), and the
+//     nucleus: a survivor is kept iff the renormalised mass strictly above its value is
+//     < top_p (mlx-dspark Changelog, [0.1.0] Added, top-p / top-k on draft and target;
+//     [0.20.2] Changed, selection instead of a full vocabulary sort);
+//   - draft rows: the same with q as the key and (q/qmax)^(1/T) as the weight.
+// Rows whose support is not a short list (no top-k, or more survivors than fit) keep a
+// threshold and a normaliser instead; full_threshold_kernel finishes those that still need
+// a whole-row threshold.
+#include "block_utils.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr float kL2E = 1.4426950408889634f;
+
+struct FinSmem {
+    uint32_t keys[kMergeCap];
+    int ids[kMergeCap];
+    unsigned long long sk[kKeptCap];
+    double w[kKeptCap];
+    double ex[kKeptCap + 1];
+    int tile_off[2049];
+    int hist[256];
+    int bcast[4];
+    double dwarp[33];
+    float fwarp[32];
+    int iwarp[32];
+    int n;
+};
+
+// Gather the candidate lists of a row's tiles into shared memory; returns the count, or -1
+// when they do not fit.
+__device__ int gather_candidates(FinSmem& s, const TileStats* ts, const Cand* cand, int tiles, int cap_per_tile,
+                                 bool raw) {
+    const int tid = threadIdx.x;
+    if (tiles > 2048) return -1;
+    for (int t = tid; t < tiles; t += blockDim.x) s.tile_off[t + 1] = raw ? ts[t].n_raw : ts[t].n_pen;
+    __syncthreads();
+    if (tid == 0) {
+        s.tile_off[0] = 0;
+        for (int t = 1; t <= tiles; ++t) s.tile_off[t] += s.tile_off[t - 1];
+    }
+    __syncthreads();
+    const int total = s.tile_off[tiles];
+    if (total > kMergeCap) return -1;
+    const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    for (int t = warp; t < tiles; t += nw) {
+        const int off = s.tile_off[t], n = s.tile_off[t + 1] - off;
+        const Cand* src = cand + static_cast<long long>(t) * cap_per_tile;
+        for (int i = lane; i < n; i += 32) {
+            const Cand c = src[i];
+            s.keys[off + i] = fkey(c.v);
+            s.ids[off + i] = c.id;
+        }
+    }
+    __syncthreads();
+    return total;
+}
+
+// Survivors with key >= kth among the n gathered candidates, sorted by (value desc, id asc)
+// into s.sk[0..count).  Returns count, or -1 if more than kKeptCap.
+__device__ int sorted_survivors(FinSmem& s, int n, uint32_t kth) {
+    const int tid = threadIdx.x;
+    if (tid == 0) s.n = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += blockDim.x) {
+        if (s.keys[i] >= kth) {
+            const int p = atomicAdd(&s.n, 1);
+            if (p < kKeptCap) s.sk[p] = (static_cast<unsigned long long>(s.keys[i]) << 32) |
+                                        static_cast<unsigned>(0xFFFFFFFFu - static_cast<unsigned>(s.ids[i]));
+        }
+    }
+    __syncthreads();
+    const int cnt = s.n;
+    if (cnt > kKeptCap) return -1;
+    const int P = next_pow2(max(cnt, 2));
+    for (int i = cnt + tid; i < P; i += blockDim.x) s.sk[i] = 0ull;
+    block_bitonic_desc(s.sk, P);
+    return cnt;
+}
+
+// Nucleus over s.sk[0..cnt) with weights s.w[0..cnt); returns the number kept (>= 1), and
+// writes the kept mass to *zkept.  Kept = tie groups whose exclusive mass is < top_p * Z.
+__device__ int nucleus(FinSmem& s, int cnt, float top_p, double* zkept) {
+    const int tid = threadIdx.x;
+    block_scan_excl_d(s.w, s.ex, cnt, s.dwarp);
+    const double Z = s.ex[cnt];
+    int kept = cnt;
+    if (top_p < 1.f) {
+        const double lim = static_cast<double>(top_p) * Z;
+        int first_drop = cnt;
+        for (int i = tid; i < cnt; i += blockDim.x) {
+            const bool start = (i == 0) || ((s.sk[i] >> 32) != (s.sk[i - 1] >> 32));
+            if (start && i > 0 && !(s.ex[i] < lim)) first_drop = min(first_drop, i);
+        }
+        kept = block_min_i(first_drop, s.iwarp);
+    }
+    *zkept = s.ex[kept];
+    return kept;
+}
+
+__device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
+    const int tid = threadIdx.x;
+    const dspark_row_params_t r = a.rows[b];
+    const int tiles = a.tiles_x;
+    const TileStats* ts = a.ts_x + static_cast<long long>(slot) * tiles;
+    XRowOut o{};
+    o.mode = kModeInactive;
+    // merge tile maxima
+    float mr = -INFINITY, mp = -INFINITY;
+    int fl = 0;
+    for (int t = tid; t < tiles; t += blockDim.x) {
+        const TileStats x = ts[t];
+        mr = (mr != mr || x.m_raw != x.m_raw) ? __int_as_float(0x7fc00000) : fmaxf(mr, x.m_raw);
+        mp = (mp != mp || x.m_pen != x.m_pen) ? __int_as_float(0x7fc00000) : fmaxf(mp, x.m_pen);
+        fl |= x.flags;
+    }
+    mr = block_max_nan(mr, s.fwarp);
+    mp = block_max_nan(mp, s.fwarp);
+    fl = block_or_i(fl, s.iwarp);
+    if ((fl & kTileBad) || !isfinite(mr) || !isfinite(mp)) {
+        if (tid == 0) {
+            atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
+            a.xout[slot] = o;
+        }
+        return;
+    }
+    int arg = 0x7FFFFFFF;
+    double sraw = 0.0, stemp = 0.0;
+    const bool greedy = !(r.temperature > 0.f);
+    const float c_l2e = greedy ? 0.f : kL2E / r.temperature;
+    for (int t = tid; t < tiles; t += blockDim.x) {
+        const TileStats x = ts[t];
+        if (x.m_pen == mp) arg = min(arg, x.arg_pen);
+        sraw += static_cast<double>(x.s_raw) * exp2(static_cast<double>(x.m_raw - mr) * kL2E);
+        if (!greedy) stemp += static_cast<double>(x.s_temp) * exp2(static_cast<double>(x.m_pen - mp) * c_l2e);
+    }
+    arg = block_min_i(arg, s.iwarp);
+    sraw = block_sum_d(sraw, s.dwarp);
+    stemp = block_sum_d(stemp, s.dwarp);
+    o.argmax = arg;
+    o.m_pen = mp;
+    o.lse = mr + static_cast<float>(log(sraw));
+    o.c_l2e = c_l2e;
+    o.top_p = r.top_p;
+    o.tau = -INFINITY;
+    o.top_k = 0;
+    o.n_kept = 0;
+    o.flags = fl;
+    const int k = r.top_k;
+    if (greedy) {
+        o.mode = kModeGreedy;
+    } else if (k > 0 && k < a.V) {
+        int n = -1;
+        if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
+            n = gather_candidates(s, ts, a.cand_x + static_cast<long long>(slot) * tiles * kCandPenGlobal, tiles,
+                                  kCandPenGlobal, false);
+        if (n >= k) {
+            const uint32_t kth = block_kth_largest_key(s.keys, n, k, s.hist, s.bcast);
+            const int cnt = sorted_survivors(s, n, kth);
+            if (cnt > 0) {
+                for (int i = tid; i < cnt; i += blockDim.x)
+                    s.w[i] = static_cast<double>(target_weight(ckey_v(s.sk[i]), mp, c_l2e));
+                __syncthreads();
+                double zk;
+                const int kept = nucleus(s, cnt, r.top_p, &zk);
+                KeptEntry* dst = a.kept + static_cast<long long>(slot) * kKeptCap;
+                for (int i = tid; i < kept; i += blockDim.x) dst[i] = KeptEntry{ckey_id(s.sk[i]), static_cast<float>(s.w[i])};
+                o.mode = kModeList;
+                o.n_kept = kept;
+                o.Z = zk;
+                o.tau = ckey_v(s.sk[kept - 1]);
+            } else {
+                o.mode = kModeNeedFull;                       // too many survivors: threshold known
+                o.tau = key_to_f(kth);
+            }
+        } else {
+            o.mode = kModeNeedFull;                           // select over the whole row
+            o.top_k = k;
+        }
+    } else {
+        o.Z = stemp;
+        o.mode = (r.top_p < 1.f) ? kModeNeedFull : kModeFull;
+    }
+    // raw top-n for top_logprobs
+    if (a.n_top > 0) {
+        bool done = false;
+        if (!(fl & kTileOverflowRaw)) {
+            const int n = gather_candidates(s, ts, a.cand_raw + static_cast<long long>(slot) * tiles * kCandRawGlobal,
+                                            tiles, kCandRawGlobal, true);
+            const int nt = min(a.n_top, a.V);
+            if (n >= nt) {
+                const uint32_t kth = block_kth_largest_key(s.keys, n, nt, s.hist, s.bcast);
+                const int cnt = sorted_survivors(s, n, kth);
+                if (cnt >= nt) {
+                    TopEntry* dst = a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS;
+                    for (int i = tid; i < nt; i += blockDim.x) dst[i] = TopEntry{ckey_id(s.sk[i]), ckey_v(s.sk[i])};
+                    done = true;
+                }
+            }
+        }
+        if (!done) o.flags |= kTileOverflowRaw;               // full_threshold_kernel fills the list
+    }
+    __syncthreads();
+    if (tid == 0) a.xout[slot] = o;
+}
+
+__device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
+    const int tid = threadIdx.x;
+    const dspark_row_params_t r = a.rows[b];
+    const int tiles = a.tiles_q;
+    const TileStats* ts = a.ts_q + static_cast<long long>(qslot) * tiles;
+    QRowOut o{};
+    o.mode = kModeInactive;
+    float qmax = -INFINITY;
+    int fl = 0;
+    for (int t = tid; t < tiles; t += blockDim.x) {
+        const TileStats x = ts[t];
+        qmax = (qmax != qmax || x.m_raw != x.m_raw) ? __int_as_float(0x7fc00000) : fmaxf(qmax, x.m_raw);
+        fl |= x.flags;
+    }
+    qmax = block_max_nan(qmax, s.fwarp);
+    fl = block_or_i(fl, s.iwarp);
+    const bool t_one = r.temperature == 1.f;
+    const float inv_t = 1.f / r.temperature;
+    double z = 0.0;
+    for (int t = tid; t < tiles; t += blockDim.x) {
+        const TileStats x = ts[t];
+        if (t_one) z += static_cast<double>(x.s_raw);
+        else if (x.m_raw > 0.f) z += static_cast<double>(x.s_temp) * exp2(static_cast<double>(inv_t) * log2(static_cast<double>(x.m_raw) / qmax));
+    }
+    z = block_sum_d(z, s.dwarp);
+    if ((fl & kTileBad) || !(qmax > 0.f) || !isfinite(qmax)) {
+        if (tid == 0) { atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE); a.qout[qslot] = o; }
+        return;
+    }
+    o.qmax = qmax;
+    o.inv_t = inv_t;
+    o.tau = -INFINITY;
+    o.top_k = 0;
+    o.top_p = r.top_p;
+    o.flags = fl;
+    const int k = r.top_k;
+    if (k > 0 && k < a.V) {
+        int n = -1;
+        if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
+            n = gather_candidates(s, ts, a.cand_q + static_cast<long long>(qslot) * tiles * kCandPenGlobal, tiles,
+                                  kCandPenGlobal, false);
+        if (n >= k) {
+            const uint32_t kth = block_kth_largest_key(s.keys, n, k, s.hist, s.bcast);
+            const int cnt = sorted_survivors(s, n, kth);
+            if (cnt > 0) {
+                for (int e = tid; e < cnt; e += blockDim.x)
+                    s.w[e] = static_cast<double>(draft_weight(ckey_v(s.sk[e]), qmax, inv_t, t_one));
+                __syncthreads();
+                double zk;
+                const int kept = nucleus(s, cnt, r.top_p, &zk);
+                o.mode = kModeList;
+                o.Z = zk;
+                o.tau = ckey_v(s.sk[kept - 1]);
+            } else {
+                o.mode = kModeNeedFull;
+                o.tau = key_to_f(kth);
+            }
+        } else {
+            o.mode = kModeNeedFull;
+            o.top_k = k;
+        }
+    } else {
+        o.Z = z;
+        o.mode = (r.top_p < 1.f) ? kModeNeedFull : kModeFull;
+        if (o.mode == kModeFull && !(z > 0.0)) {
+            if (tid == 0) atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) a.qout[qslot] = o;
+}
+
+__global__ void __launch_bounds__(kFinalizeThreads) row_finalize_kernel(Args a) {
+    extern __shared__ __align__(16) unsigned char fin_raw[];
+    FinSmem& s = *reinterpret_cast<FinSmem*>(fin_raw);
+    const int slot = blockIdx.x;
+    if (slot < a.xslots) {
+        const int b = slot / (a.Km + 1), j = slot % (a.Km + 1);
+        if ((request_status(a, b) & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || j > a.rows[b].num_drafts) {
+            if (threadIdx.x == 0) { XRowOut o{}; o.mode = kModeInactive; a.xout[slot] = o; }
+            return;
+        }
+        finalize_x(a, s, slot, b, j);
+    } else {
+        const int qs = slot - a.xslots;
+        const int b = qs / a.Km, i = qs % a.Km;
+        const dspark_row_params_t r = a.rows[b];
+        if ((request_status(a, b) & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || i >= r.num_drafts ||
+            !(r.temperature > 0.f)) {
+            if (threadIdx.x == 0) { QRowOut o{}; o.mode = kModeInactive; a.qout[qs] = o; }
+            return;
+        }
+        finalize_q(a, s, qs, b, i);
+    }
+}
+
+// ============================================================================ whole-row path
+// full_threshold_kernel: rows whose top-k threshold or nucleus cannot come from candidates
+// (top_k = 0 with top_p < 1, top_k above the candidate limit, tie-heavy rows that overflow
+// the candidate buffers) get an exact whole-row selection here: radix passes over the
+// order-preserving key with count histograms (top-k, top-n) and with fixed-point mass
+// histograms (nucleus), re-reading the row once per pass.  Fixed-point masses make the
+// sums independent of the order of the atomic additions.
+
+constexpr int kFullThreads = 1024;
+constexpr double kFix = 274877906944.0;         // 2^38
+
+struct FullSmem {
+    unsigned long long mass[2048];
+    unsigned cnt[2048];
+    unsigned bm[kBitmapWordsMax];
+    PenEntry ent[kPenCap];
+    int bcast[32];
+    unsigned long long ubcast[4];
+    int tl_n, tl_over;
+    int top_ids[64];
+    float top_v[64];
+    int n_gt, n_eq;
+};
+
+// Value of element e of the row: penalised target logit or draft probability.
+struct RowSource {
+    const Args* a;
+    bool is_x;
+    long long base;      // row offset in elements
+    int b, j;
+    float f, p;
+    bool pen;
+};
+
+__device__ int full_pen_count(const FullSmem& s, const RowSource& src, int tok, int nh, int n, int over) {
+    const Args& a = *src.a;
+    if (!over) {
+        int l = 0, h = nh;
+        while (l < h) { const int md = (l + h) >> 1; if (s.ent[md].token < tok) l = md + 1; else h = md; }
+        int e = -1;
+        if (l < nh && s.ent[l].token == tok) e = l;
+        else for (int k = nh; k < n; ++k) if (s.ent[k].token == tok) { e = k; break; }
+        if (e < 0) return 0;
+        const unsigned long long mask = (static_cast<unsigned long long>(s.ent[e].mask_hi) << 32) | s.ent[e].mask_lo;
+        const unsigned long long low = (src.j >= 64) ? ~0ull : ((1ull << src.j) - 1ull);
+        return s.ent[e].base + __popcll(mask & low);
+    }
+    int base = 0;
+    const int hlo = a.h_off ? a.h_off[src.b] : 0, hhi = a.h_off ? a.h_off[src.b + 1] : 0;
+    int l = hlo, h = hhi;
+    while (l < h) { const int md = (l + h) >> 1; if (a.h_ids[md] < tok) l = md + 1; else h = md; }
+    if (l < hhi && a.h_ids[l] == tok) base = a.h_cnt[l];
+    for (int i = 0; i < src.j; ++i) base += (a.d[static_cast<long long>(src.b) * a.Km + i] == tok);
+    return base;
+}
+
+// One pass over the row calling fn(e, value, raw) for every element, tile by tile (the
+// penalty index of each target tile is staged in shared memory first).
+template <typename Fn>
+__device__ void for_each_elem(FullSmem& s, const RowSource& src, Fn fn) {
+    const Args& a = *src.a;
+    const int tid = threadIdx.x;
+    const int tile_n = src.is_x ? a.tile_x : a.V;
+    for (int e0 = 0; e0 < a.V; e0 += tile_n) {
+        const int e1 = min(a.V, e0 + tile_n);
+        int nh = 0, n = 0, over = 0;
+        if (src.pen) {
+            const long long pt = static_cast<long long>(src.b) * a.tiles_x + e0 / a.tile_x;
+            const PenHdr h = a.pen_hdr[pt];
+            n = h.n; nh = h.pad[0]; over = h.overflow;
+            __syncthreads();
+            for (int w = tid; w < a.bm_words; w += blockDim.x) s.bm[w] = a.pen_bm[pt * a.bm_words + w];
+            if (!over) for (int k = tid; k < n; k += blockDim.x) s.ent[k] = a.pen_ent[pt * kPenCap + k];
+            __syncthreads();
+        }
+        for (int e = e0 + tid; e < e1; e += blockDim.x) {
+            float raw, v;
+            if (src.is_x) {
+                raw = load_x(a.x, a.sx, src.base + e);
+                v = raw;
+                if (src.pen && ((s.bm[(e - e0) >> 5] >> ((e - e0) & 31)) & 1u))
+                    v = penalise(raw, full_pen_count(s, src, e, nh, n, over), src.f, src.p);
+            } else {
+                raw = __ldg(a.q + src.base + e);
+                v = raw;
+            }
+            fn(e, v, raw);
+        }
+    }
+    __syncthreads();
+}
+
+// Exact k-th largest key (1-based) over the row; use_raw selects the raw value.
+__device__ uint32_t full_kth(FullSmem& s, const RowSource& src, int k, bool use_raw) {
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0, pmask = 0;
+    int kk = k;
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    for (int pass = 0; pass < 3; ++pass) {
+        const int sh = shifts[pass];
+        const unsigned wm = (1u << widths[pass]) - 1u;
+        for (int i = tid; i < 2048; i += blockDim.x) s.cnt[i] = 0u;
+        __syncthreads();
+        for_each_elem(s, src, [&](int, float v, float raw) {
+            const uint32_t key = fkey(use_raw ? raw : v);
+            if ((key & pmask) == prefix) atomicAdd(&s.cnt[(key >> sh) & wm], 1u);
+        });
+        if (tid == 0) {
+            int run = 0;
+            for (int d = static_cast<int>(wm); d >= 0; --d) {
+                const int c = static_cast<int>(s.cnt[d]);
+                if (run + c >= kk) { s.bcast[0] = d; s.bcast[1] = kk - run; break; }
+                run += c;
+            }
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(s.bcast[0]) << sh;
+        pmask |= wm << sh;
+        kk = s.bcast[1];
+        __syncthreads();
+    }
+    return prefix;
+}
+
+// Nucleus over {value key >= floor_key}: returns the smallest kept key and the kept mass.
+template <typename WFn>
+__device__ uint32_t full_nucleus(FullSmem& s, const RowSource& src, uint32_t floor_key, float top_p, WFn wfn,
+                                 double* zkept) {
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0, pmask = 0;
+    unsigned long long above = 0;     // fixed-point mass strictly above the current prefix range
+    const int shifts[3] = {21, 10, 0};
+    const int widths[3] = {11, 11, 10};
+    for (int pass = 0; pass < 3; ++pass) {
+        const int sh = shifts[pass];
+        const unsigned wm = (1u << widths[pass]) - 1u;
+        for (int i = tid; i < 2048; i += blockDim.x) s.mass[i] = 0ull;
+        __syncthreads();
+        for_each_elem(s, src, [&](int, float v, float) {
+            const uint32_t key = fkey(v);
+            if (key >= floor_key && (key & pmask) == prefix) {
+                const float w = wfn(v);
+                const unsigned long long fx = __float2ull_rn(w * 274877906944.0f);
+                atomicAdd(&s.mass[(key >> sh) & wm], fx);
+            }
+        });
+        if (tid == 0 && pass == 0) {
+            unsigned long long z = 0;
+            for (int d = 0; d <= static_cast<int>(wm); ++d) z += s.mass[d];
+            s.ubcast[1] = z;
+        }
+        __syncthreads();
+        if (!(top_p < 1.f)) {                 // no nucleus: only the normaliser is needed
+            *zkept = static_cast<double>(s.ubcast[1]) / kFix;
+            __syncthreads();
+            return floor_key;
+        }
+        if (tid == 0) {
+            const double zt = static_cast<double>(s.ubcast[1]);
+            const double plim = static_cast<double>(top_p) * zt;
+            // last bin (descending) whose mass-above is < top_p * Z
+            unsigned long long run = above;
+            int pick = -1;
+            unsigned long long pick_above = above;
+            for (int d = static_cast<int>(wm); d >= 0; --d) {
+                const unsigned long long m = s.mass[d];
+                if (m == 0ull) continue;
+                if (static_cast<double>(run) < plim) { pick = d; pick_above = run; }
+                else break;
+                run += m;
+            }
+            if (pick < 0) pick = 0;
+            s.bcast[0] = pick;
+            s.ubcast[0] = pick_above;
+            s.ubcast[2] = s.mass[pick];
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(s.bcast[0]) << sh;
+        pmask |= wm << sh;
+        above = s.ubcast[0];
+        __syncthreads();
+    }
+    *zkept = static_cast<double>(above + s.ubcast[2]) / kFix;
+    return prefix;
+}
+
+// Raw top-n with ties broken by lower id, over the whole row.
+__device__ void full_topn(FullSmem& s, const RowSource& src, int nt, TopEntry* dst) {
+    const int tid = threadIdx.x;
+    const uint32_t kth = full_kth(s, src, nt, true);
+    if (tid == 0) { s.n_gt = 0; s.n_eq = 0; }
+    __syncthreads();
+    // elements strictly above the n-th value (fewer than nt of them)
+    for_each_elem(s, src, [&](int e, float, float raw) {
+        if (fkey(raw) > kth) {
+            const int p = atomicAdd(&s.n_gt, 1);
+            if (p < 64) { s.top_ids[p] = e; s.top_v[p] = raw; }
+        }
+    });
+    // the lowest ids equal to the n-th value fill the rest, found in id order by an ordered
+    // block compaction over consecutive chunks of the row
+    const int have = min(s.n_gt, 64);
+    const int need = nt - have;
+    const int lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    int got = 0;
+    for (int base = 0; base < src.a->V && got < need; base += blockDim.x) {
+        const int e = base + tid;
+        float raw = 0.f;
+        bool flag = false;
+        if (e < src.a->V) {
+            raw = src.is_x ? load_x(src.a->x, src.a->sx, src.base + e) : src.a->q[src.base + e];
+            flag = fkey(raw) == kth;
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, flag);
+        if (lane == 0) s.bcast[warp] = __popc(bal);
+        __syncthreads();
+        int woff = 0, tot = 0;
+        for (int w = 0; w < nw; ++w) { if (w < warp) woff += s.bcast[w]; tot += s.bcast[w]; }
+        const int pos = got + woff + __popc(bal & ((1u << lane) - 1u));
+        if (flag && pos < need) { s.top_ids[have + pos] = e; s.top_v[have + pos] = raw; }
+        got += tot;
+        __syncthreads();
+    }
+    got = min(got, need);
+    if (tid == 0) {
+        // order: value desc, id asc (at most 20 entries: insertion sort)
+        const int tot = have + got;
+        for (int i = 1; i < tot; ++i) {
+            const int id = s.top_ids[i];
+            const float v = s.top_v[i];
+            int q = i - 1;
+            while (q >= 0 && (s.top_v[q] < v || (s.top_v[q] == v && s.top_ids[q] > id))) {
+                s.top_ids[q + 1] = s.top_ids[q]; s.top_v[q + 1] = s.top_v[q]; --q;
+            }
+            s.top_ids[q + 1] = id; s.top_v[q + 1] = v;
+        }
+        for (int i = 0; i < nt && i < tot; ++i) dst[i] = TopEntry{s.top_ids[i], s.top_v[i]};
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kFullThreads) full_threshold_kernel(Args a) {
+    extern __shared__ __align__(16) unsigned char full_raw[];
+    FullSmem& s = *reinterpret_cast<FullSmem*>(full_raw);
+    const int slot = blockIdx.x;
+    const int tid = threadIdx.x;
+    if (slot < a.xslots) {
+        XRowOut o = a.xout[slot];
+        const bool need_top = (o.mode != kModeInactive) && a.n_top > 0 && (o.flags & kTileOverflowRaw);
+        if (o.mode != kModeNeedFull && !need_top) return;
+        const int b = slot / (a.Km + 1), j = slot % (a.Km + 1);
+        const dspark_row_params_t r = a.rows[b];
+        RowSource src{&a, true, static_cast<long long>(slot) * a.V, b, j, r.frequency_penalty, r.presence_penalty,
+                      has_penalty(r)};
+        if (need_top) full_topn(s, src, min(a.n_top, a.V), a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS);
+        if (o.mode == kModeNeedFull) {
+            uint32_t floor_key = fkey(o.tau);
+            if (o.top_k > 0) floor_key = full_kth(s, src, o.top_k, false);
+            const float mp = o.m_pen, c = o.c_l2e;
+            double z;
+            if (o.top_p < 1.f) {
+                const uint32_t kk = full_nucleus(s, src, floor_key, o.top_p,
+                                                 [&](float v) { return target_weight(v, mp, c); }, &z);
+                o.tau = key_to_f(kk);
+            } else {
+                const uint32_t kk = full_nucleus(s, src, floor_key, 2.f,
+                                                 [&](float v) { return target_weight(v, mp, c); }, &z);
+                (void)kk;
+                o.tau = key_to_f(floor_key);
+            }
+            o.Z = z;
+            o.top_k = 0;
+            o.mode = kModeFull;
+        }
+        if (tid == 0) a.xout[slot] = o;
+    } else {
+        const int qs = slot - a.xslots;
+        QRowOut o = a.qout[qs];
+        if (o.mode != kModeNeedFull) return;
+        const int b = qs / a.Km, i = qs % a.Km;
+        RowSource src{&a, false, static_cast<long long>(qs) * a.V, b, i, 0.f, 0.f, false};
+        uint32_t floor_key = fkey(o.tau);
+        if (o.top_k > 0) floor_key = full_kth(s, src, o.top_k, false);
+        const float qmax = o.qmax, inv_t = o.inv_t;
+        const bool t_one = inv_t == 1.f;
+        double z;
+        if (o.top_p < 1.f) {
+            const uint32_t kk = full_nucleus(s, src, floor_key, o.top_p,
+                                             [&](float v) { return draft_weight(v, qmax, inv_t, t_one) / (t_one ? qmax : 1.f); }, &z);
+            o.tau = key_to_f(kk);
+        } else {
+            full_nucleus(s, src, floor_key, 2.f,
+                         [&](float v) { return draft_weight(v, qmax, inv_t, t_one) / (t_one ? qmax : 1.f); }, &z);
+            o.tau = key_to_f(floor_key);
+        }
+        if (t_one) z *= qmax;
+        o.Z = z;
+        o.top_k = 0;
+        o.mode = kModeFull;
+        if (!(z > 0.0) && tid == 0) atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
+        if (tid == 0) a.qout[qs] = o;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_row_finalize(const Args& a, cudaStream_t s) {
+    const size_t smem = sizeof(FinSmem);
+    cudaError_t e = cudaFuncSetAttribute(row_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    row_finalize_kernel<<<a.xslots + a.qslots, kFinalizeThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_full_threshold(const Args& a, cudaStream_t s) {
+    const size_t smem = sizeof(FullSmem);
+    cudaError_t e = cudaFuncSetAttribute(full_threshold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    full_threshold_kernel<<<a.xslots + a.qslots, kFullThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

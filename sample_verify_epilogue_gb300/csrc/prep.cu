@@ -1,0 +1,211 @@
+// prep_kernel: the work plan of the streaming pass and the per-(request, vocab tile) penalty
+// index, in one launch.
+//
+// Block 0 validates every request's parameters and draft ids (row_status bits), counts the
+// vocab tiles each valid request needs (K_b+1 target rows; K_b draft rows when T > 0) and
+// writes the flat list of work units.
+//
+// Block 1 + b*tiles_x + t builds, for request b with a non-zero penalty and the vocab tile
+// t, the tokens of that tile which may carry a penalty: the request's completion-history
+// tokens in the tile (with their counts) and its draft tokens in the tile, each with a
+// bit mask of the draft positions holding it.  Verify position j then counts
+// c = base + popcount(mask & ((1 << j) - 1)), i.e. the history plus its own draft prefix
+// (mlx-dspark Changelog, [0.2.0] Added, "presence_penalty / frequency_penalty").  A bitmap
+// over the tile marks those tokens so the streaming pass tests eight logits per byte.
+#include "dspark_internal.cuh"
+
+namespace dspark {
+
+namespace {
+
+constexpr int kPrepThreads = 256;
+
+__device__ void plan_block(const Args& a) {
+    extern __shared__ int sm_base[];                 // [B+1] unit offsets
+    __shared__ int s_chunk[kPrepThreads + 1];
+    const int tid = threadIdx.x;
+    const int B = a.B;
+    for (int b = tid; b < B; b += kPrepThreads) {
+        const int st = request_status(a, b);
+        if (st) atomicOr(&a.row_status[b], st);
+        int n = 0;
+        if (!(st & DSPARK_ROW_BAD_PARAMS) && !(st & DSPARK_ROW_BAD_DRAFT)) {
+            const dspark_row_params_t r = a.rows[b];
+            const int K = r.num_drafts;
+            n = (K + 1) * a.tiles_x + (r.temperature > 0.f ? K * a.tiles_q : 0);
+        }
+        sm_base[b + 1] = n;
+    }
+    __syncthreads();
+    // exclusive scan of the per-request unit counts: chunked per thread, then across threads
+    const int chunk = (B + kPrepThreads - 1) / kPrepThreads;
+    const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
+    int s = 0;
+    for (int b = lo; b < hi; ++b) s += sm_base[b + 1];
+    s_chunk[tid + 1] = s;
+    __syncthreads();
+    if (tid == 0) {
+        s_chunk[0] = 0;
+        for (int t = 1; t <= kPrepThreads; ++t) s_chunk[t] += s_chunk[t - 1];
+    }
+    __syncthreads();
+    int run = s_chunk[tid];
+    for (int b = lo; b < hi; ++b) {
+        const int n = sm_base[b + 1];
+        sm_base[b + 1] = run + n;               // inclusive end of b
+        run += n;
+    }
+    if (tid == 0) sm_base[0] = 0;
+    __syncthreads();
+    const int n_units = sm_base[B];
+    if (tid == 0) a.plan->n_units = n_units;
+    for (int u = tid; u < n_units; u += kPrepThreads) {
+        int l = 0, h = B;                        // find b with base[b] <= u < base[b+1]
+        while (h - l > 1) {
+            const int mid = (l + h) >> 1;
+            if (sm_base[mid] <= u) l = mid; else h = mid;
+        }
+        const int b = l;
+        int local = u - sm_base[b];
+        const dspark_row_params_t r = a.rows[b];
+        const int nx = (r.num_drafts + 1) * a.tiles_x;
+        UnitDesc ud;
+        ud.b = b;
+        if (local < nx) {
+            ud.kind = kUnitX;
+            ud.slot = b * (a.Km + 1) + local / a.tiles_x;
+            ud.tile = local % a.tiles_x;
+        } else {
+            local -= nx;
+            ud.kind = kUnitQ;
+            ud.slot = b * a.Km + local / a.tiles_q;
+            ud.tile = local % a.tiles_q;
+        }
+        a.units[u] = ud;
+    }
+}
+
+// First index in ids[lo, hi) with ids[idx] >= key, by a block-wide 256-way narrowing.
+__device__ int block_lower_bound(const int* ids, int lo, int hi, int key, int* s_tmp) {
+    const int tid = threadIdx.x;
+    while (hi - lo > 1) {
+        const int len = hi - lo;
+        const int step = (len + kPrepThreads - 1) / kPrepThreads;
+        const int p = lo + tid * step;
+        const int pred = (p < hi) && (__ldg(ids + p) < key);
+        const int cnt = __syncthreads_count(pred);   // preds form a prefix (ids ascending)
+        if (cnt == 0) return lo;
+        const int nlo = lo + (cnt - 1) * step;       // ids[nlo] < key
+        const int nhi = min(hi, nlo + step);
+        if (step == 1) return nlo + 1;
+        lo = nlo + 1;                                // ids[nlo] < key is known
+        hi = nhi;
+        if (lo >= hi) return lo;
+        (void)s_tmp;
+    }
+    if (hi - lo == 1) return (__ldg(ids + lo) < key) ? hi : lo;
+    return lo;
+}
+
+__device__ void penalty_index_block(const Args& a, int b, int t) {
+    __shared__ unsigned s_bm[kBitmapWordsMax];
+    __shared__ PenEntry s_ent[kPenCap];
+    __shared__ int s_n, s_nh, s_over, s_tmp[4];
+    const int tid = threadIdx.x;
+    if (request_status(a, b) != 0) return;
+    const dspark_row_params_t r = a.rows[b];
+    const int K = r.num_drafts;
+    const int e0 = t * a.tile_x, e1 = min(a.V, e0 + a.tile_x);
+    const int hlo = a.h_off ? a.h_off[b] : 0, hhi = a.h_off ? a.h_off[b + 1] : 0;
+    // history validation (once per request): ascending ids in range, positive counts
+    if (t == 0 && hhi > hlo) {
+        int bad = 0;
+        for (int k = hlo + tid; k < hhi; k += kPrepThreads) {
+            const int id = a.h_ids[k];
+            if (id < 0 || id >= a.V || a.h_cnt[k] <= 0 || (k > hlo && a.h_ids[k - 1] >= id)) bad = 1;
+        }
+        if (__syncthreads_or(bad) && tid == 0) atomicOr(&a.row_status[b], DSPARK_ROW_BAD_HISTORY);
+    }
+    if (!has_penalty(r)) return;
+    for (int w = tid; w < a.bm_words; w += kPrepThreads) s_bm[w] = 0u;
+    int h0 = hlo, h1 = hlo;
+    if (hhi > hlo) {
+        h0 = block_lower_bound(a.h_ids, hlo, hhi, e0, s_tmp);
+        h1 = block_lower_bound(a.h_ids, h0, hhi, e1, s_tmp);
+    }
+    const int nh = h1 - h0;
+    if (tid == 0) { s_nh = min(nh, kPenCap); s_over = nh > kPenCap; }
+    __syncthreads();
+    for (int k = tid; k < nh; k += kPrepThreads) {
+        const int id = a.h_ids[h0 + k];
+        if (k < kPenCap) s_ent[k] = PenEntry{id, a.h_cnt[h0 + k], 0u, 0u};
+        if (id >= e0 && id < e1) atomicOr(&s_bm[(id - e0) >> 5], 1u << ((id - e0) & 31));
+    }
+    __syncthreads();
+    // draft tokens in this tile: serial over positions (K <= 64), in order
+    if (tid == 0) {
+        int n = s_nh;
+        for (int i = 0; i < K; ++i) {
+            const int tok = a.d[static_cast<long long>(b) * a.Km + i];
+            if (tok < e0 || tok >= e1) continue;
+            int base = 0, slot = -1;
+            // history part (sorted): binary search in shared memory, or global when it overflowed
+            if (!s_over) {
+                int l = 0, h = s_nh;
+                while (l < h) { const int m = (l + h) >> 1; if (s_ent[m].token < tok) l = m + 1; else h = m; }
+                if (l < s_nh && s_ent[l].token == tok) { slot = l; base = s_ent[l].base; }
+            } else {
+                int l = h0, h = h1;
+                while (l < h) { const int m = (l + h) >> 1; if (a.h_ids[m] < tok) l = m + 1; else h = m; }
+                if (l < h1 && a.h_ids[l] == tok) { base = a.h_cnt[l]; slot = (l - h0 < kPenCap) ? l - h0 : -2; }
+            }
+            if (slot == -1) {
+                for (int e = s_nh; e < n; ++e) if (s_ent[e].token == tok) { slot = e; break; }
+                if (slot == -1) {
+                    if (n < kPenCap) { s_ent[n] = PenEntry{tok, 0, 0u, 0u}; slot = n++; }
+                    else { s_over = 1; slot = -2; }
+                }
+            }
+            if (slot >= 0) {
+                if (i < 32) s_ent[slot].mask_lo |= 1u << i; else s_ent[slot].mask_hi |= 1u << (i - 32);
+            }
+            a.draft_base[static_cast<long long>(b) * a.Km + i] = base;
+            s_bm[(tok - e0) >> 5] |= 1u << ((tok - e0) & 31);
+        }
+        s_n = n;
+    }
+    __syncthreads();
+    const long long pt = static_cast<long long>(b) * a.tiles_x + t;
+    for (int w = tid; w < a.bm_words; w += kPrepThreads) a.pen_bm[pt * a.bm_words + w] = s_bm[w];
+    for (int k = tid; k < s_n; k += kPrepThreads) a.pen_ent[pt * kPenCap + k] = s_ent[k];
+    if (tid == 0) {
+        PenHdr h;
+        h.n = s_n; h.overflow = s_over; h.pad[0] = s_nh; h.pad[1] = 0;
+        a.pen_hdr[pt] = h;
+    }
+}
+
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(Args a) {
+    if (blockIdx.x == 0) {
+        plan_block(a);
+        return;
+    }
+    const int w = blockIdx.x - 1;
+    penalty_index_block(a, w / a.tiles_x, w % a.tiles_x);
+}
+
+}  // namespace
+
+cudaError_t launch_prep(const Args& a, cudaStream_t s) {
+    const int grid = 1 + a.B * a.tiles_x;
+    const size_t smem = static_cast<size_t>(a.B + 1) * sizeof(int);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    prep_kernel<<<grid, kPrepThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace dspark

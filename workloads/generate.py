@@ -119,8 +119,9 @@ def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
     """Build one seeded batch.
 
     rows: sequence of row_params tuples (length B).
-    draft_mode: "q"      -- d_i drawn from q_i (plain categorical draw, generator-side uniforms)
-                "argmax" -- d_i = argmax of the raw target logits at position i
+    draft_mode: "q"        -- d_i drawn from q_i (plain categorical draw, generator-side uniforms)
+                "argmax"   -- d_i = argmax of the raw target logits at position i
+                "q_argmax" -- d_i = argmax of q_i (a greedy drafter)
                 "copy"   -- q_i = softmax of the target logits themselves (draft == target)
     argmax_frac: after drawing, that fraction of draft tokens (seeded) is replaced by the
                  raw target argmax at its position.
@@ -166,6 +167,8 @@ def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
             for i in range(K_max):
                 if draft_mode == "argmax":
                     d[b, i] = int(np.argmax(xr[i]))
+                elif draft_mode == "q_argmax":
+                    d[b, i] = int(np.argmax(q[b, i]))
                 else:
                     cdf = np.cumsum(q[b, i], dtype=np.float64)
                     t = int(np.searchsorted(cdf, rng.random() * cdf[-1], side="right"))
