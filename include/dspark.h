@@ -78,6 +78,7 @@ typedef enum { DSPARK_BF16 = 0, DSPARK_FP32 = 1 } dspark_dtype_t;
 #define DSPARK_ROW_INTERNAL   16   /* an internal limit was hit (bounded wait expired) */
 
 /* Largest supported sizes. */
+#define DSPARK_MAX_B          2048
 #define DSPARK_MAX_V          (1 << 24)
 #define DSPARK_MAX_K          64
 #define DSPARK_MAX_TOP_LOGPROBS 20
@@ -102,7 +103,7 @@ typedef struct {
 } dspark_counts_t;
 
 typedef struct {
-    int32_t B;                    /* requests, >= 1                                   */
+    int32_t B;                    /* requests, 1..DSPARK_MAX_B                        */
     int32_t K_max;                /* drafted tokens at most, 0..DSPARK_MAX_K          */
     int32_t V;                    /* vocabulary, 1..DSPARK_MAX_V                      */
     dspark_dtype_t logits_dtype;  /* dtype of x; q is always fp32                     */

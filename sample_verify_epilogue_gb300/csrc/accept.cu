@@ -175,8 +175,8 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
 
 // ============================================================================ finish
 constexpr int kFinishThreads = 512;
-constexpr int kPerThread = 8;
-constexpr int kChunk = kFinishThreads * kPerThread;     // 4096 elements: divides both tile sizes
+constexpr int kPerThread = 4;
+constexpr int kChunk = kFinishThreads * kPerThread;     // 2048 elements: divides both tile sizes
 constexpr int kMaxChunks = (DSPARK_MAX_V + kChunk - 1) / kChunk;
 
 struct FinishSmem {

@@ -13,8 +13,11 @@ constexpr size_t kAlign = 256;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
+constexpr int kMaxGrid = 1024;           // streaming CTAs on any device (an SM count bound)
+
 struct Layout {
-    int tile_x, tiles_x, tile_q, tiles_q, bm_words, xslots, qslots;
+    int tile_x, tiles_x, tile_q, tiles_q, bm_words, xslots, qslots, nseg_x, nseg_q;
+    long long seg_max;
     size_t off_plan, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_raw, off_cand_q;
     size_t off_pen_hdr, off_pen_bm, off_pen_ent, off_draft_base, off_xout, off_kept, off_topn, off_qout, off_req;
     size_t total;
@@ -41,13 +44,17 @@ Layout make_layout(const dspark_params_t* p) {
     L.bm_words = ((L.tile_x + 31) / 32 + 3) / 4 * 4;
     L.xslots = static_cast<int>(B * (Km + 1));
     L.qslots = static_cast<int>(B * Km);
-    const size_t xt = static_cast<size_t>(L.xslots) * L.tiles_x;
-    const size_t qt = static_cast<size_t>(L.qslots) * L.tiles_q;
+    L.nseg_x = (L.tiles_x + kSegTiles - 1) / kSegTiles;
+    L.nseg_q = (L.tiles_q + kSegTiles - 1) / kSegTiles;
+    const size_t xt = static_cast<size_t>(L.xslots) * L.nseg_x;
+    const size_t qt = static_cast<size_t>(L.qslots) * L.nseg_q;
     const size_t pt = static_cast<size_t>(B) * L.tiles_x;
+    L.seg_max = static_cast<long long>(xt + qt);
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     L.off_plan = take(sizeof(Plan));
-    L.off_units = take((xt + qt) * sizeof(UnitDesc));
+    // segment streams: grid x groups x ceil(S / (groups*grid)) entries <= S + groups*grid
+    L.off_units = take((xt + qt + static_cast<size_t>(kGroups) * kMaxGrid) * sizeof(UnitDesc));
     L.off_ts_x = take(xt * sizeof(TileStats));
     L.off_ts_q = take(qt * sizeof(TileStats));
     L.off_cand_x = take(xt * kCandPenGlobal * sizeof(Cand));
@@ -92,6 +99,7 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     Args a{};
     a.B = p->B; a.Km = p->K_max; a.V = p->V; a.sx = sx; a.xdtype = p->logits_dtype;
     a.tile_x = L.tile_x; a.tiles_x = L.tiles_x; a.tile_q = L.tile_q; a.tiles_q = L.tiles_q; a.bm_words = L.bm_words;
+    a.nseg_x = L.nseg_x; a.nseg_q = L.nseg_q;
     a.n_top = p->n_top_logprobs; a.want_lp = p->want_logprobs ? 1 : 0;
     a.xslots = L.xslots; a.qslots = L.qslots;
     a.x = logits; a.q = q; a.d = draft_ids; a.rows = p->rows;
@@ -121,6 +129,9 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return DSPARK_ERR_CUDA;
+    sms = sms < 1 ? 1 : (sms > kMaxGrid ? kMaxGrid : sms);
+    a.grid_ss = sms;
+    a.max_seg = static_cast<int>((L.seg_max + 2LL * sms - 1) / (2LL * sms));
 
     if (cudaMemsetAsync(p->row_status, 0, sizeof(int32_t) * p->B, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaMemsetAsync(a.plan, 0, sizeof(Plan), s) != cudaSuccess) return DSPARK_ERR_CUDA;

@@ -82,19 +82,22 @@ __device__ inline int next_pow2(int n) {
     return p;
 }
 
-// Exclusive scan in double of vals[0..n) (n <= 2*blockDim.x) into excl[0..n]; excl[n] = total.
-// Fixed order: two consecutive elements per thread, warp shuffles, then warp totals in order.
+// Exclusive scan in double of vals[0..n) (n <= 4*blockDim.x) into excl[0..n]; excl[n] = total.
+// Fixed order: four consecutive elements per thread, warp shuffles, then warp totals in order.
+// excl may alias vals.
 __device__ inline void block_scan_excl_d(const double* vals, double* excl, int n, double* s_warp) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-    const int i0 = 2 * tid;
-    const double a = i0 < n ? vals[i0] : 0.0;
-    const double b = i0 + 1 < n ? vals[i0 + 1] : 0.0;
-    const double s = a + b;
+    const int i0 = 4 * tid;
+    double v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = i0 + q < n ? vals[i0 + q] : 0.0;
+    const double s = (v[0] + v[1]) + (v[2] + v[3]);
     double incl = s;
     for (int o = 1; o < 32; o <<= 1) {
         const double y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
+    __syncthreads();
     if (lane == 31) s_warp[warp] = incl;
     __syncthreads();
     if (tid == 0) {
@@ -103,9 +106,12 @@ __device__ inline void block_scan_excl_d(const double* vals, double* excl, int n
         s_warp[nw] = run;
     }
     __syncthreads();
-    const double base = s_warp[warp] + (incl - s);
-    if (i0 < n) excl[i0] = base;
-    if (i0 + 1 < n) excl[i0 + 1] = base + a;
+    double base = s_warp[warp] + (incl - s);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        if (i0 + q < n) excl[i0 + q] = base;
+        base += v[q];
+    }
     if (tid == 0) excl[n] = s_warp[nw];
     __syncthreads();
 }

@@ -18,41 +18,53 @@
 namespace dspark {
 
 // ---------------------------------------------------------------- sizes
-constexpr int kConsumerWarps = 16;
-constexpr int kConsumerThreads = kConsumerWarps * 32;          // 512
+constexpr int kGroups = 2;                                     // independent consumer groups per CTA
+constexpr int kGroupWarps = 8;
+constexpr int kGroupThreads = kGroupWarps * 32;                // 256
+constexpr int kConsumerThreads = kGroups * kGroupThreads;      // 512
 constexpr int kStreamThreads = kConsumerThreads + 32;          // + one producer warp
-constexpr int kStages = 3;
-constexpr int kStageBytes = 48 * 1024;                         // one vocab tile per stage
-constexpr int kTileBf16 = kStageBytes / 2;                     // 24576 elements
-constexpr int kTileF32 = kStageBytes / 4;                      // 12288 elements
-constexpr int kBitmapWordsMax = kTileBf16 / 32;                // 768
-constexpr int kPenCap = 512;                                   // penalised tokens per tile held in smem
-constexpr int kSmemCandPen = 1024;                             // per-tile candidate buffer (smem)
+constexpr int kStages = 4;
+constexpr int kStageBytes = 40 * 1024;                         // one vocab tile per stage
+constexpr int kTileBf16 = kStageBytes / 2;                     // 20480 elements
+constexpr int kTileF32 = kStageBytes / 4;                      // 10240 elements
+constexpr int kBitmapWordsMax = kTileBf16 / 32;                // 640
+constexpr int kPenCap = 384;                                   // penalised tokens per tile held in smem
+constexpr int kSegTiles = 4;                                   // vocab tiles per segment (target)
+constexpr int kMaxSegTiles = 16;
+constexpr int kSmemCandPen = 1024;                             // per-segment candidate buffer (smem)
 constexpr int kSmemCandRaw = 512;
-constexpr int kCandPenGlobal = 512;                            // per-tile candidates kept in the workspace
-constexpr int kCandRawGlobal = 128;
+constexpr int kCandPenGlobal = 1024;                           // per-segment candidates kept in the workspace
+constexpr int kCandRawGlobal = 512;
 constexpr int kMaxCandTopK = 256;                              // top_k above this uses the whole-row path
 constexpr int kKeptCap = 1024;                                 // truncated support held as a list
 constexpr int kFinalizeThreads = 512;
 constexpr int kMergeCap = 8192;                                // merged candidates per row (smem)
-constexpr int kMaxB = 8192;
+constexpr int kMaxB = DSPARK_MAX_B;
 
 // ---------------------------------------------------------------- records in the workspace
 enum UnitKind : int { kUnitX = 0, kUnitQ = 1 };
 
 struct Plan {
-    int n_units;
-    int pad[3];
+    int n_units;         // segments in the call
+    int pad[3];          // pad[0]: error flag set by the streaming pass
 };
 
-struct UnitDesc {        // one vocab tile of one row
+// One segment (consecutive vocab tiles [t0, t1) of one row) with its request's parameters.
+struct UnitDesc {
     int slot;            // x: b*(K_max+1)+j ; q: b*K_max+i
     int kind;
-    int tile;
     int b;
+    int seg;             // segment index within the row
+    int t0, t1;
+    float temperature;
+    int top_k;
+    float top_p;
+    float presence;
+    float frequency;
+    int pad;
 };
 
-struct TileStats {       // per (row, tile)
+struct TileStats {       // per (row, segment)
     float m_raw;         // x: raw max           | q: max
     float s_raw;         // x: sum exp(x-m_raw)  | q: sum q
     float m_pen;         // x: penalised max
@@ -126,6 +138,9 @@ struct Args {
     // shapes
     int B, Km, V, sx, xdtype;
     int tile_x, tiles_x, tile_q, tiles_q, bm_words;
+    int nseg_x, nseg_q;    // segments per target / draft row
+    int grid_ss;           // CTAs of the streaming pass
+    int max_seg;           // segments per (CTA, group) stream, upper bound
     int n_top, want_lp;
     int xslots, qslots;
     // inputs (device)
@@ -146,12 +161,12 @@ struct Args {
     int* row_status;
     // workspace
     Plan* plan;
-    UnitDesc* units;
-    TileStats* ts_x;       // [xslots * tiles_x]
-    TileStats* ts_q;       // [qslots * tiles_q]
-    Cand* cand_x;          // [xslots * tiles_x * kCandPenGlobal]
-    Cand* cand_raw;        // [xslots * tiles_x * kCandRawGlobal]
-    Cand* cand_q;          // [qslots * tiles_q * kCandPenGlobal]
+    UnitDesc* units;       // [grid_ss * kGroups * max_seg] segment streams
+    TileStats* ts_x;       // [xslots * nseg_x]
+    TileStats* ts_q;       // [qslots * nseg_q]
+    Cand* cand_x;          // [xslots * nseg_x * kCandPenGlobal]
+    Cand* cand_raw;        // [xslots * nseg_x * kCandRawGlobal]
+    Cand* cand_q;          // [qslots * nseg_q * kCandPenGlobal]
     PenHdr* pen_hdr;       // [B * tiles_x]
     unsigned* pen_bm;      // [B * tiles_x * bm_words]
     PenEntry* pen_ent;     // [B * tiles_x * kPenCap]
@@ -238,6 +253,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
         : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
+// try_wait that may suspend the thread up to ~hint_ns while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, unsigned parity, unsigned hint_ns) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+// Non-blocking test of a phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
 // Bounded wait: returns false when the limit runs out (the caller records an error).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity, long long limit) {
     for (long long i = 0; i < limit; ++i)
@@ -286,6 +321,23 @@ __device__ __forceinline__ int warp_sum_i(int v) {
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+// Sort two values across the 32 lanes of a warp, descending (bitonic network): afterwards
+// lane i holds the (i+1)-th largest of each set.
+__device__ __forceinline__ void warp_sort2_desc(float& a, float& b) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const float oa = __shfl_xor_sync(0xffffffffu, a, j);
+            const float ob = __shfl_xor_sync(0xffffffffu, b, j);
+            const bool keep_max = (((lane & j) == 0) == ((lane & k) == 0));
+            a = keep_max ? fmaxf(a, oa) : fminf(a, oa);
+            b = keep_max ? fmaxf(b, ob) : fminf(b, ob);
+        }
+    }
+}
+
 // c-th largest value across the 32 lanes (with multiplicity), c in [1, 32].
 __device__ __forceinline__ float warp_kth_largest(float v, int c) {
     float cur = v, kth = -INFINITY;

@@ -19,62 +19,135 @@ namespace dspark {
 namespace {
 
 constexpr float kL2E = 1.4426950408889634f;
+constexpr int kFinThreads = 256;
+constexpr int kKeyCap = 4096;          // candidate keys staged in shared memory
+constexpr int kMaxSegs = 1024;         // segments per row (V <= 2^24 with 10240-element tiles: 410)
 
 struct FinSmem {
-    uint32_t keys[kMergeCap];
-    int ids[kMergeCap];
-    unsigned long long sk[kKeptCap];
+    union {
+        uint32_t keys[kKeyCap];        // candidate keys (selection)
+        double ex[kKeptCap + 1];       // exclusive prefix of survivor weights (nucleus)
+    } u;
+    unsigned long long sk[kKeptCap];   // survivors: (key << 32) | (0xFFFFFFFF - id)
     double w[kKeptCap];
-    double ex[kKeptCap + 1];
-    int tile_off[2049];
+    int off[kMaxSegs + 1];             // candidate offsets per segment
     int hist[256];
     int bcast[4];
     double dwarp[33];
     float fwarp[32];
     int iwarp[32];
     int n;
+    int staged;
 };
 
-// Gather the candidate lists of a row's tiles into shared memory; returns the count, or -1
-// when they do not fit.
-__device__ int gather_candidates(FinSmem& s, const TileStats* ts, const Cand* cand, int tiles, int cap_per_tile,
-                                 bool raw) {
+// The candidate lists of one row: segment s holds n_s (value, id) pairs at base + s*cap.
+struct CandSet {
+    const Cand* base;
+    int cap;
+    int nseg;
+    int total;
+};
+
+// Offsets of the row's candidate lists (from the segment statistics) and, when they fit, the
+// keys staged in shared memory.  Returns the set, total = -1 when any list overflowed.
+__device__ CandSet stage_candidates(FinSmem& s, const TileStats* ts, const Cand* base, int cap, int nseg, bool raw) {
     const int tid = threadIdx.x;
-    if (tiles > 2048) return -1;
-    for (int t = tid; t < tiles; t += blockDim.x) s.tile_off[t + 1] = raw ? ts[t].n_raw : ts[t].n_pen;
+    CandSet cs{base, cap, nseg, 0};
+    if (nseg > kMaxSegs) { cs.total = -1; return cs; }
+    for (int t = tid; t < nseg; t += blockDim.x) s.off[t + 1] = raw ? ts[t].n_raw : ts[t].n_pen;
     __syncthreads();
     if (tid == 0) {
-        s.tile_off[0] = 0;
-        for (int t = 1; t <= tiles; ++t) s.tile_off[t] += s.tile_off[t - 1];
+        s.off[0] = 0;
+        for (int t = 1; t <= nseg; ++t) s.off[t] += s.off[t - 1];
+        s.staged = s.off[nseg] <= kKeyCap;
     }
     __syncthreads();
-    const int total = s.tile_off[tiles];
-    if (total > kMergeCap) return -1;
-    const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-    for (int t = warp; t < tiles; t += nw) {
-        const int off = s.tile_off[t], n = s.tile_off[t + 1] - off;
-        const Cand* src = cand + static_cast<long long>(t) * cap_per_tile;
-        for (int i = lane; i < n; i += 32) {
-            const Cand c = src[i];
-            s.keys[off + i] = fkey(c.v);
-            s.ids[off + i] = c.id;
+    cs.total = s.off[nseg];
+    if (s.staged) {
+        const int warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+        for (int t = warp; t < nseg; t += nw) {
+            const int o = s.off[t], n = s.off[t + 1] - o;
+            const Cand* src = base + static_cast<long long>(t) * cap;
+            for (int i = lane; i < n; i += 32) s.u.keys[o + i] = fkey(src[i].v);
         }
     }
     __syncthreads();
-    return total;
+    return cs;
 }
 
-// Survivors with key >= kth among the n gathered candidates, sorted by (value desc, id asc)
-// into s.sk[0..count).  Returns count, or -1 if more than kKeptCap.
-__device__ int sorted_survivors(FinSmem& s, int n, uint32_t kth) {
+// Call fn(key) for every candidate (each thread a share), from shared memory when staged.
+template <typename Fn>
+__device__ __forceinline__ void for_each_key(const FinSmem& s, const CandSet& cs, Fn fn) {
+    const int tid = threadIdx.x;
+    if (s.staged) {
+        for (int i = tid; i < cs.total; i += blockDim.x) fn(s.u.keys[i]);
+    } else {
+        for (int t = 0; t < cs.nseg; ++t) {
+            const int n = s.off[t + 1] - s.off[t];
+            const Cand* src = cs.base + static_cast<long long>(t) * cs.cap;
+            for (int i = tid; i < n; i += blockDim.x) fn(fkey(src[i].v));
+        }
+    }
+}
+
+// k-th largest key (1-based, with multiplicity) of the candidate set: four 8-bit radix passes.
+__device__ uint32_t kth_largest(FinSmem& s, const CandSet& cs, int k) {
+    const int tid = threadIdx.x;
+    uint32_t prefix = 0, pmask = 0;
+    int kk = k;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += blockDim.x) s.hist[i] = 0;
+        __syncthreads();
+        for_each_key(s, cs, [&](uint32_t key) {
+            if ((key & pmask) == prefix) atomicAdd(&s.hist[(key >> shift) & 255u], 1);
+        });
+        __syncthreads();
+        if (tid < 32) {
+            int c[8], sum = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) { c[q] = s.hist[255 - 8 * tid - q]; sum += c[q]; }
+            int incl = sum;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o) incl += y;
+            }
+            const int excl = incl - sum;
+            if (excl < kk && incl >= kk) {
+                int run = excl;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (run + c[q] >= kk) { s.bcast[0] = 255 - 8 * tid - q; s.bcast[1] = kk - run; break; }
+                    run += c[q];
+                }
+            }
+        }
+        __syncthreads();
+        prefix |= static_cast<uint32_t>(s.bcast[0]) << shift;
+        pmask |= 255u << shift;
+        kk = s.bcast[1];
+        __syncthreads();
+    }
+    return prefix;
+}
+
+// Candidates with key >= kth, sorted by (value desc, id asc) into s.sk[0..count); returns the
+// count, or -1 when there are more than kKeptCap.
+__device__ int sorted_survivors(FinSmem& s, const CandSet& cs, uint32_t kth) {
     const int tid = threadIdx.x;
     if (tid == 0) s.n = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += blockDim.x) {
-        if (s.keys[i] >= kth) {
-            const int p = atomicAdd(&s.n, 1);
-            if (p < kKeptCap) s.sk[p] = (static_cast<unsigned long long>(s.keys[i]) << 32) |
-                                        static_cast<unsigned>(0xFFFFFFFFu - static_cast<unsigned>(s.ids[i]));
+    for (int t = 0; t < cs.nseg; ++t) {
+        const int n = s.off[t + 1] - s.off[t];
+        const Cand* src = cs.base + static_cast<long long>(t) * cs.cap;
+        for (int i = tid; i < n; i += blockDim.x) {
+            const Cand c = src[i];
+            const uint32_t key = fkey(c.v);
+            if (key >= kth) {
+                const int p = atomicAdd(&s.n, 1);
+                if (p < kKeptCap) s.sk[p] = (static_cast<unsigned long long>(key) << 32) |
+                                            static_cast<unsigned>(0xFFFFFFFFu - static_cast<unsigned>(c.id));
+            }
         }
     }
     __syncthreads();
@@ -86,37 +159,37 @@ __device__ int sorted_survivors(FinSmem& s, int n, uint32_t kth) {
     return cnt;
 }
 
-// Nucleus over s.sk[0..cnt) with weights s.w[0..cnt); returns the number kept (>= 1), and
-// writes the kept mass to *zkept.  Kept = tie groups whose exclusive mass is < top_p * Z.
+// Nucleus over s.sk[0..cnt) with weights s.w[0..cnt); returns the number kept (>= 1) and the
+// kept mass.  Kept = tie groups whose exclusive mass is < top_p * Z.
 __device__ int nucleus(FinSmem& s, int cnt, float top_p, double* zkept) {
     const int tid = threadIdx.x;
-    block_scan_excl_d(s.w, s.ex, cnt, s.dwarp);
-    const double Z = s.ex[cnt];
+    block_scan_excl_d(s.w, s.u.ex, cnt, s.dwarp);
+    const double Z = s.u.ex[cnt];
     int kept = cnt;
     if (top_p < 1.f) {
         const double lim = static_cast<double>(top_p) * Z;
         int first_drop = cnt;
         for (int i = tid; i < cnt; i += blockDim.x) {
             const bool start = (i == 0) || ((s.sk[i] >> 32) != (s.sk[i - 1] >> 32));
-            if (start && i > 0 && !(s.ex[i] < lim)) first_drop = min(first_drop, i);
+            if (start && i > 0 && !(s.u.ex[i] < lim)) first_drop = min(first_drop, i);
         }
         kept = block_min_i(first_drop, s.iwarp);
     }
-    *zkept = s.ex[kept];
+    *zkept = s.u.ex[kept];
+    __syncthreads();
     return kept;
 }
 
 __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
     const int tid = threadIdx.x;
     const dspark_row_params_t r = a.rows[b];
-    const int tiles = a.tiles_x;
-    const TileStats* ts = a.ts_x + static_cast<long long>(slot) * tiles;
+    const int nseg = a.nseg_x;
+    const TileStats* ts = a.ts_x + static_cast<long long>(slot) * nseg;
     XRowOut o{};
     o.mode = kModeInactive;
-    // merge tile maxima
     float mr = -INFINITY, mp = -INFINITY;
     int fl = 0;
-    for (int t = tid; t < tiles; t += blockDim.x) {
+    for (int t = tid; t < nseg; t += blockDim.x) {
         const TileStats x = ts[t];
         mr = (mr != mr || x.m_raw != x.m_raw) ? __int_as_float(0x7fc00000) : fmaxf(mr, x.m_raw);
         mp = (mp != mp || x.m_pen != x.m_pen) ? __int_as_float(0x7fc00000) : fmaxf(mp, x.m_pen);
@@ -136,7 +209,7 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
     double sraw = 0.0, stemp = 0.0;
     const bool greedy = !(r.temperature > 0.f);
     const float c_l2e = greedy ? 0.f : kL2E / r.temperature;
-    for (int t = tid; t < tiles; t += blockDim.x) {
+    for (int t = tid; t < nseg; t += blockDim.x) {
         const TileStats x = ts[t];
         if (x.m_pen == mp) arg = min(arg, x.arg_pen);
         sraw += static_cast<double>(x.s_raw) * exp2(static_cast<double>(x.m_raw - mr) * kL2E);
@@ -158,13 +231,13 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
     if (greedy) {
         o.mode = kModeGreedy;
     } else if (k > 0 && k < a.V) {
-        int n = -1;
+        CandSet cs{nullptr, 0, 0, -1};
         if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
-            n = gather_candidates(s, ts, a.cand_x + static_cast<long long>(slot) * tiles * kCandPenGlobal, tiles,
-                                  kCandPenGlobal, false);
-        if (n >= k) {
-            const uint32_t kth = block_kth_largest_key(s.keys, n, k, s.hist, s.bcast);
-            const int cnt = sorted_survivors(s, n, kth);
+            cs = stage_candidates(s, ts, a.cand_x + static_cast<long long>(slot) * nseg * kCandPenGlobal,
+                                  kCandPenGlobal, nseg, false);
+        if (cs.total >= k) {
+            const uint32_t kth = kth_largest(s, cs, k);
+            const int cnt = sorted_survivors(s, cs, kth);
             if (cnt > 0) {
                 for (int i = tid; i < cnt; i += blockDim.x)
                     s.w[i] = static_cast<double>(target_weight(ckey_v(s.sk[i]), mp, c_l2e));
@@ -185,6 +258,7 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
             o.mode = kModeNeedFull;                           // select over the whole row
             o.top_k = k;
         }
+        __syncthreads();
     } else {
         o.Z = stemp;
         o.mode = (r.top_p < 1.f) ? kModeNeedFull : kModeFull;
@@ -193,12 +267,12 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
     if (a.n_top > 0) {
         bool done = false;
         if (!(fl & kTileOverflowRaw)) {
-            const int n = gather_candidates(s, ts, a.cand_raw + static_cast<long long>(slot) * tiles * kCandRawGlobal,
-                                            tiles, kCandRawGlobal, true);
+            const CandSet cs = stage_candidates(s, ts, a.cand_raw + static_cast<long long>(slot) * nseg * kCandRawGlobal,
+                                                kCandRawGlobal, nseg, true);
             const int nt = min(a.n_top, a.V);
-            if (n >= nt) {
-                const uint32_t kth = block_kth_largest_key(s.keys, n, nt, s.hist, s.bcast);
-                const int cnt = sorted_survivors(s, n, kth);
+            if (cs.total >= nt) {
+                const uint32_t kth = kth_largest(s, cs, nt);
+                const int cnt = sorted_survivors(s, cs, kth);
                 if (cnt >= nt) {
                     TopEntry* dst = a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS;
                     for (int i = tid; i < nt; i += blockDim.x) dst[i] = TopEntry{ckey_id(s.sk[i]), ckey_v(s.sk[i])};
@@ -215,13 +289,13 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
 __device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
     const int tid = threadIdx.x;
     const dspark_row_params_t r = a.rows[b];
-    const int tiles = a.tiles_q;
-    const TileStats* ts = a.ts_q + static_cast<long long>(qslot) * tiles;
+    const int nseg = a.nseg_q;
+    const TileStats* ts = a.ts_q + static_cast<long long>(qslot) * nseg;
     QRowOut o{};
     o.mode = kModeInactive;
     float qmax = -INFINITY;
     int fl = 0;
-    for (int t = tid; t < tiles; t += blockDim.x) {
+    for (int t = tid; t < nseg; t += blockDim.x) {
         const TileStats x = ts[t];
         qmax = (qmax != qmax || x.m_raw != x.m_raw) ? __int_as_float(0x7fc00000) : fmaxf(qmax, x.m_raw);
         fl |= x.flags;
@@ -231,7 +305,7 @@ __device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
     const bool t_one = r.temperature == 1.f;
     const float inv_t = 1.f / r.temperature;
     double z = 0.0;
-    for (int t = tid; t < tiles; t += blockDim.x) {
+    for (int t = tid; t < nseg; t += blockDim.x) {
         const TileStats x = ts[t];
         if (t_one) z += static_cast<double>(x.s_raw);
         else if (x.m_raw > 0.f) z += static_cast<double>(x.s_temp) * exp2(static_cast<double>(inv_t) * log2(static_cast<double>(x.m_raw) / qmax));
@@ -249,13 +323,13 @@ __device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
     o.flags = fl;
     const int k = r.top_k;
     if (k > 0 && k < a.V) {
-        int n = -1;
+        CandSet cs{nullptr, 0, 0, -1};
         if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
-            n = gather_candidates(s, ts, a.cand_q + static_cast<long long>(qslot) * tiles * kCandPenGlobal, tiles,
-                                  kCandPenGlobal, false);
-        if (n >= k) {
-            const uint32_t kth = block_kth_largest_key(s.keys, n, k, s.hist, s.bcast);
-            const int cnt = sorted_survivors(s, n, kth);
+            cs = stage_candidates(s, ts, a.cand_q + static_cast<long long>(qslot) * nseg * kCandPenGlobal,
+                                  kCandPenGlobal, nseg, false);
+        if (cs.total >= k) {
+            const uint32_t kth = kth_largest(s, cs, k);
+            const int cnt = sorted_survivors(s, cs, kth);
             if (cnt > 0) {
                 for (int e = tid; e < cnt; e += blockDim.x)
                     s.w[e] = static_cast<double>(draft_weight(ckey_v(s.sk[e]), qmax, inv_t, t_one));
@@ -284,7 +358,7 @@ __device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
     if (tid == 0) a.qout[qslot] = o;
 }
 
-__global__ void __launch_bounds__(kFinalizeThreads) row_finalize_kernel(Args a) {
+__global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(Args a) {
     extern __shared__ __align__(16) unsigned char fin_raw[];
     FinSmem& s = *reinterpret_cast<FinSmem*>(fin_raw);
     const int slot = blockIdx.x;
@@ -619,7 +693,7 @@ cudaError_t launch_row_finalize(const Args& a, cudaStream_t s) {
     const size_t smem = sizeof(FinSmem);
     cudaError_t e = cudaFuncSetAttribute(row_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    row_finalize_kernel<<<a.xslots + a.qslots, kFinalizeThreads, smem, s>>>(a);
+    row_finalize_kernel<<<a.xslots + a.qslots, kFinThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 

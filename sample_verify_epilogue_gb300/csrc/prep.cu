@@ -21,23 +21,30 @@ namespace {
 constexpr int kPrepThreads = 256;
 
 __device__ void plan_block(const Args& a) {
-    extern __shared__ int sm_base[];                 // [B+1] unit offsets
+    // dynamic shared memory: [B] request parameters, [B+1] segment offsets, [B] target-row segments
+    extern __shared__ __align__(16) unsigned char plan_smem[];
+    dspark_row_params_t* sm_rows = reinterpret_cast<dspark_row_params_t*>(plan_smem);
+    int* sm_base = reinterpret_cast<int*>(plan_smem + sizeof(dspark_row_params_t) * a.B);
     __shared__ int s_chunk[kPrepThreads + 1];
     const int tid = threadIdx.x;
     const int B = a.B;
+    int* sm_nx = sm_base + B + 1;
     for (int b = tid; b < B; b += kPrepThreads) {
+        const dspark_row_params_t r = a.rows[b];
+        sm_rows[b] = r;
         const int st = request_status(a, b);
         if (st) atomicOr(&a.row_status[b], st);
-        int n = 0;
+        int n = 0, nx = 0;
         if (!(st & DSPARK_ROW_BAD_PARAMS) && !(st & DSPARK_ROW_BAD_DRAFT)) {
-            const dspark_row_params_t r = a.rows[b];
             const int K = r.num_drafts;
-            n = (K + 1) * a.tiles_x + (r.temperature > 0.f ? K * a.tiles_q : 0);
+            nx = (K + 1) * a.nseg_x;
+            n = nx + (r.temperature > 0.f ? K * a.nseg_q : 0);
         }
         sm_base[b + 1] = n;
+        sm_nx[b] = nx;
     }
     __syncthreads();
-    // exclusive scan of the per-request unit counts: chunked per thread, then across threads
+    // exclusive scan of the per-request segment counts: chunked per thread, then across threads
     const int chunk = (B + kPrepThreads - 1) / kPrepThreads;
     const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
     int s = 0;
@@ -57,9 +64,11 @@ __device__ void plan_block(const Args& a) {
     }
     if (tid == 0) sm_base[0] = 0;
     __syncthreads();
-    const int n_units = sm_base[B];
-    if (tid == 0) a.plan->n_units = n_units;
-    for (int u = tid; u < n_units; u += kPrepThreads) {
+    const int S = sm_base[B];
+    if (tid == 0) a.plan->n_units = S;
+    // segment s goes to CTA c = s mod G, consumer group g = (s div G) mod 2, position s div 2G
+    const int G = a.grid_ss;
+    for (int u = tid; u < S; u += kPrepThreads) {
         int l = 0, h = B;                        // find b with base[b] <= u < base[b+1]
         while (h - l > 1) {
             const int mid = (l + h) >> 1;
@@ -67,21 +76,33 @@ __device__ void plan_block(const Args& a) {
         }
         const int b = l;
         int local = u - sm_base[b];
-        const dspark_row_params_t r = a.rows[b];
-        const int nx = (r.num_drafts + 1) * a.tiles_x;
+        const int nx = sm_nx[b];
+        const dspark_row_params_t r = sm_rows[b];
         UnitDesc ud;
         ud.b = b;
+        int tiles, nseg;
         if (local < nx) {
             ud.kind = kUnitX;
-            ud.slot = b * (a.Km + 1) + local / a.tiles_x;
-            ud.tile = local % a.tiles_x;
+            ud.slot = b * (a.Km + 1) + local / a.nseg_x;
+            ud.seg = local % a.nseg_x;
+            tiles = a.tiles_x; nseg = a.nseg_x;
         } else {
             local -= nx;
             ud.kind = kUnitQ;
-            ud.slot = b * a.Km + local / a.tiles_q;
-            ud.tile = local % a.tiles_q;
+            ud.slot = b * a.Km + local / a.nseg_q;
+            ud.seg = local % a.nseg_q;
+            tiles = a.tiles_q; nseg = a.nseg_q;
         }
-        a.units[u] = ud;
+        ud.t0 = static_cast<int>(static_cast<long long>(ud.seg) * tiles / nseg);
+        ud.t1 = static_cast<int>(static_cast<long long>(ud.seg + 1) * tiles / nseg);
+        ud.temperature = r.temperature;
+        ud.top_k = r.top_k;
+        ud.top_p = r.top_p;
+        ud.presence = r.presence_penalty;
+        ud.frequency = r.frequency_penalty;
+        ud.pad = 0;
+        const int c = u % G, g = (u / G) & 1, m = u / (2 * G);
+        a.units[(static_cast<long long>(c) * kGroups + g) * a.max_seg + m] = ud;
     }
 }
 
@@ -198,7 +219,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Args a) {
 
 cudaError_t launch_prep(const Args& a, cudaStream_t s) {
     const int grid = 1 + a.B * a.tiles_x;
-    const size_t smem = static_cast<size_t>(a.B + 1) * sizeof(int);
+    const size_t smem = static_cast<size_t>(a.B) * sizeof(dspark_row_params_t) + static_cast<size_t>(2 * a.B + 1) * sizeof(int);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));

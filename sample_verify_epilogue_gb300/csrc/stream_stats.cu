@@ -1,20 +1,25 @@
 // stream_stats_kernel: the single HBM pass over the target logits x and the draft
 // probabilities q.  Everything else in the epilogue works on what this pass leaves behind.
 //
-// Persistent: one CTA per SM walks the flat list of work units (one vocab tile of one row
-// each).  A producer warp moves each tile into a 3-stage shared-memory ring with the TMA
-// bulk-copy engine (cp.async.bulk, completion counted on an mbarrier), together with the
-// tile's penalty bitmap and penalised-token list; 16 consumer warps read the tile from
-// shared memory twice:
-//   pass 1: per-thread maxima of the raw logits and of the penalised logits
-//           (x' = x - ((f*c) + p), mlx-dspark Changelog [0.2.0] Added, penalties);
-//   then    a lower bound theta on the tile's k-th largest value: every warp finds the
-//           c-th largest of its lanes' maxima (c = ceil(k / 16)), theta = the least of
-//           them, so at least 16*c >= k distinct logits of the tile are >= theta;
-//   pass 2: raw sum of exp (for the log-softmax of logprobs), the tempered sum when the row
-//           has no top-k, the lowest index attaining the penalised max (greedy), and the
-//           candidates >= theta (for the top-k threshold of the row, mlx-dspark Changelog
-//           [0.20.2] Changed: the threshold comes from small selections, not a full sort).
+// Work unit = a segment: a few consecutive vocab tiles of one row.  Persistent CTAs, one per
+// SM; each CTA has two independent consumer groups of 8 warps and a producer warp.  The
+// producer moves tiles into a 4-stage shared-memory ring (two stages per group) with the TMA
+// bulk-copy engine (cp.async.bulk, completion counted on an mbarrier), together with each
+// tile's penalty bitmap and penalised-token list, serving both groups' segment streams.
+//
+// A group processes a segment in one sweep:
+//   first tile: pass 1 gives per-thread maxima of the raw and the penalised logits
+//     (x' = x - ((f*c) + p), mlx-dspark Changelog [0.2.0] Added, penalties); every warp sorts
+//     its lanes' maxima and takes the c-th largest (c = ceil(k/8)); theta = the least of the
+//     8 warps' values, so at least 8*c >= k distinct logits of the first tile are >= theta,
+//     hence every member of the segment's top-k is >= theta.  Pass 2 then accumulates and
+//     filters as below;
+//   later tiles: one pass each: running maxima with rescaled sums of exp (raw: the
+//     log-softmax of logprobs; penalised and tempered: the normaliser when there is no
+//     top-k), the lowest index attaining the penalised max (greedy), and the candidates
+//     >= theta (the top-k threshold of the row comes from these, mlx-dspark Changelog
+//     [0.20.2] Changed: small selections instead of a full vocabulary sort);
+//   end of segment: one reduction, one write of the statistics and candidates.
 // Draft tiles get the same treatment with q as the key (top-k of q^(1/T) is top-k of q).
 #include "dspark_internal.cuh"
 
@@ -22,15 +27,43 @@ namespace dspark {
 
 namespace {
 
-constexpr long long kWaitLimit = 1ll << 22;
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s: no healthy wait comes close
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for a phase with a time bound; false when the bound expires.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, unsigned parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer() - t0 > kWaitNs) return false;
+    return true;
+}
 constexpr float kL2E = 1.4426950408889634f;
+constexpr int kVecPerThread = kStageBytes / 16 / kGroupThreads;     // 10 vectors per thread and tile
 
 struct StageMeta {
     int kind, slot, b, j;
-    int tile, e0, e1, nvec;
-    int vec_e0, pen, pen_n, pen_nh;
-    int pen_over, top_k, pad0, pad1;
+    int seg, tile, e0, e1;
+    int nvec, vec_e0, pen, pen_n;
+    int pen_nh, pen_over, top_k, first;
+    int last, pad0, pad1, pad2;
     float temperature, top_p, presence, frequency;
+};
+
+struct GroupSmem {
+    Cand cpen[kSmemCandPen];
+    Cand craw[kSmemCandRaw];
+    float4 red1[kGroupWarps];    // first-tile maxima and thresholds
+    float4 red[kGroupWarps];     // end-of-segment partials
+    float4 red2[kGroupWarps];
+    int cnt_pen;
+    int cnt_raw;
+    int error;
 };
 
 struct Smem {
@@ -38,15 +71,9 @@ struct Smem {
     alignas(16) unsigned bm[kStages][kBitmapWordsMax];
     alignas(16) PenEntry ent[kStages][kPenCap];
     StageMeta meta[kStages];
-    Cand cpen[2][kSmemCandPen];
-    Cand craw[2][kSmemCandRaw];
-    float red1[2][kConsumerWarps][4];
-    float red2[2][kConsumerWarps][4];
-    int cnt_pen[2];
-    int cnt_raw[2];
+    GroupSmem grp[kGroups];
     alignas(8) uint64_t full[kStages];
     alignas(8) uint64_t empty[kStages];
-    int error;
 };
 
 __device__ __forceinline__ float max_nan(float a, float b) {
@@ -54,6 +81,8 @@ __device__ __forceinline__ float max_nan(float a, float b) {
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
     return r;
 }
+
+__device__ __forceinline__ void group_sync(int g) { named_barrier_sync(1 + g, kGroupThreads); }
 
 // Count of token `tok` at verify position j: history base + draft prefix occurrences.
 __device__ __forceinline__ int pen_count(const Smem& sm, int stage, const StageMeta& m, const Args& a, int tok) {
@@ -87,6 +116,10 @@ __device__ __forceinline__ unsigned bitmap_bits(const unsigned* bm, int off, int
     return static_cast<unsigned>(two >> s) & ((1u << n) - 1u);
 }
 
+__device__ __forceinline__ bool bitmap_bit(const unsigned* bm, int off) {
+    return (bm[off >> 5] >> (off & 31)) & 1u;
+}
+
 template <int SX>
 __device__ __forceinline__ float elem(const uint4& w, int k) {
     if (SX == 2) {
@@ -115,292 +148,625 @@ __device__ __forceinline__ float vec_max(const uint4& w) {
     }
 }
 
+// Two elements of a vector as a float2 (pair q: elements 2q and 2q+1).
+template <int SX>
+__device__ __forceinline__ float2 elem_pair(const uint4& w, int q) {
+    if (SX == 2) {
+        const uint32_t word = (q == 0) ? w.x : (q == 1) ? w.y : (q == 2) ? w.z : w.w;
+        return make_float2(bf16_lo(word), bf16_hi(word));
+    } else {
+        return q == 0 ? make_float2(__uint_as_float(w.x), __uint_as_float(w.y))
+                      : make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+    }
+}
+
+// acc += 2^(x*scale - off) over the vector's elements, pairwise in f32x2.
+template <int SX>
+__device__ __forceinline__ float2 vec_exp_sum(const uint4& w, float2 acc, float scale, float off) {
+    const float2 sc = make_float2(scale, scale);
+    const float2 no = make_float2(-off, -off);
+#pragma unroll
+    for (int q = 0; q < 8 / SX; ++q) {
+        const float2 t = __ffma2_rn(elem_pair<SX>(w, q), sc, no);
+        acc = __fadd2_rn(acc, make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+    }
+    return acc;
+}
+
 __device__ __forceinline__ void push(Cand* buf, int* cnt, int cap, float v, int id) {
     const int p = atomicAdd(cnt, 1);
     if (p < cap) buf[p] = Cand{v, id};
 }
 
-// ------------------------------------------------------------------ one target-logit tile
-template <int SX>
-__device__ void process_x(const Args& a, Smem& sm, int stage, const StageMeta& m, int cb) {
-    constexpr int EPV = 16 / SX;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned char* data = sm.data[stage];
-    const unsigned* bm = sm.bm[stage];
-    const bool greedy = !(m.temperature > 0.f);
-    const int k = m.top_k;
-    const bool need_lp = a.want_lp || a.n_top > 0;
-    const bool need_raw = a.n_top > 0;
-    const bool need_cand = !greedy && k > 0 && k < a.V && k <= kMaxCandTopK;
-    const bool need_temp = !greedy && (k == 0 || k >= a.V);
-    const float f = m.frequency, p = m.presence;
-    const long long xrow = static_cast<long long>(m.slot) * a.V;
-    const int e_tail = m.vec_e0 + m.nvec * EPV;
-
-    // ---- pass 1: maxima
-    float mu = -INFINITY;          // unpenalised elements (raw == penalised)
-    float mpen = -INFINITY;        // penalised elements, penalised value
-    float mrawp = -INFINITY;       // penalised elements, raw value
-    for (int v = tid; v < m.nvec; v += kConsumerThreads) {
-        const uint4 w = *reinterpret_cast<const uint4*>(data + v * 16);
-        const int e = m.vec_e0 + v * EPV;
-        const unsigned bits = m.pen ? bitmap_bits(bm, e - m.e0, EPV) : 0u;
-        if (bits == 0u) {
-            mu = max_nan(mu, vec_max<SX>(w));
-        } else {
+// Group-wide reduction of (max, max, min, min) from per-warp float4 slots; every thread gets it.
+__device__ __forceinline__ float4 group_reduce_mmnn(const float4* red) {
+    const int lane = threadIdx.x & 31;
+    float4 v = lane < kGroupWarps ? red[lane] : make_float4(-INFINITY, -INFINITY, INFINITY, INFINITY);
 #pragma unroll
-            for (int q = 0; q < EPV; ++q) {
-                const float xv = elem<SX>(w, q);
-                if (bits & (1u << q)) {
-                    const float xp = penalise(xv, pen_count(sm, stage, m, a, e + q), f, p);
-                    mpen = max_nan(mpen, xp);
-                    mrawp = max_nan(mrawp, xv);
-                } else {
-                    mu = max_nan(mu, xv);
+    for (int o = kGroupWarps / 2; o; o >>= 1) {
+        v.x = max_nan(v.x, __shfl_xor_sync(0xffffffffu, v.x, o));
+        v.y = max_nan(v.y, __shfl_xor_sync(0xffffffffu, v.y, o));
+        v.z = fminf(v.z, __shfl_xor_sync(0xffffffffu, v.z, o));
+        v.w = fminf(v.w, __shfl_xor_sync(0xffffffffu, v.w, o));
+    }
+    v.x = __shfl_sync(0xffffffffu, v.x, 0);
+    v.y = __shfl_sync(0xffffffffu, v.y, 0);
+    v.z = __shfl_sync(0xffffffffu, v.z, 0);
+    v.w = __shfl_sync(0xffffffffu, v.w, 0);
+    return v;
+}
+
+// Combine (max, sum relative to max) pairs over a warp; scale converts value gaps to log2.
+__device__ __forceinline__ void warp_merge_ms(float& m, float& s, float scale) {
+    const float M = [&] {
+        float t = m;
+        for (int o = 16; o; o >>= 1) t = max_nan(t, __shfl_xor_sync(0xffffffffu, t, o));
+        return t;
+    }();
+    float r = (s > 0.f && m > -INFINITY && M > -INFINITY) ? s * ex2_approx((m - M) * scale) : 0.f;
+    for (int o = 16; o; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+    m = M;
+    s = r;
+}
+
+// ------------------------------------------------------------------ warp-cooperative appends
+// Append the elements of one 16-byte vector flagged in `mask` (bit q = element q) to a
+// candidate buffer: one ballot, one prefix across lanes and one shared atomic per warp.
+// Every lane of the warp calls it (lanes without candidates pass mask = 0).
+template <int SX>
+__device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsigned mask, const uint4& w, int e) {
+    const unsigned any = __ballot_sync(0xffffffffu, mask != 0u);
+    if (!any) return;
+    const int lane = threadIdx.x & 31;
+    const int n = __popc(mask);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int base = 0;
+    if (lane == 31) base = atomicAdd(cnt, incl);
+    base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+    while (mask) {
+        const int q = __ffs(mask) - 1;
+        mask &= mask - 1u;
+        if (base < cap) buf[base] = Cand{elem<SX>(w, q), e + q};
+        ++base;
+    }
+}
+
+// Append every element flagged in this thread's (f0, f1) bit set (bit EPV*i+q: element q of
+// the thread's i-th vector of the tile in shared memory), warp-cooperatively: one prefix and
+// one shared atomic per warp and tile.  All lanes of the warp call it.
+template <int SX>
+__device__ __forceinline__ void flush_flags(Cand* buf, int* cnt, int cap, unsigned long long f0, unsigned long long f1,
+                                            const unsigned char* data, int vec_e0, int gt) {
+    constexpr int EPV = 16 / SX;
+    const int n = __popcll(f0) + __popcll(f1);
+    if (!__ballot_sync(0xffffffffu, n != 0)) return;
+    const int lane = threadIdx.x & 31;
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int base = 0;
+    if (lane == 31) base = atomicAdd(cnt, incl);
+    base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        unsigned long long f = h ? f1 : f0;
+        while (f) {
+            const int bit = __ffsll(f) - 1 + 64 * h;
+            f &= f - 1ull;
+            const int i = bit / EPV, q = bit % EPV;
+            const int v = gt + i * kGroupThreads;
+            const uint4 w = *reinterpret_cast<const uint4*>(data + v * 16);
+            if (base < cap) buf[base] = Cand{elem<SX>(w, q), vec_e0 + v * EPV + q};
+            ++base;
+        }
+    }
+}
+
+// Bit q set where element q of the vector is >= th.
+template <int SX>
+__device__ __forceinline__ unsigned ge_mask(const uint4& w, float th) {
+    unsigned m = 0u;
+#pragma unroll
+    for (int q = 0; q < 16 / SX; ++q) m |= (elem<SX>(w, q) >= th ? 1u : 0u) << q;
+    return m;
+}
+
+// ------------------------------------------------------------------ target-logit segments
+struct XState {
+    float m_r, s_r;      // raw running max, sum of 2^((x - m_r)*L2E)
+    float m_p, s_t;      // penalised running max, sum of 2^((x' - m_p)*c_l2e)
+    int arg;             // lowest index attaining m_p seen by this thread
+    float th_p, th_r;    // candidate thresholds (segment-wide)
+};
+
+template <int SX>
+struct XCtx {
+    const Args& a;
+    Smem& sm;
+    GroupSmem& gs;
+    int g, stage;
+    const StageMeta& m;
+    bool greedy, need_lp, need_raw, need_cand, need_temp;
+    float f, p, c_l2e;
+};
+
+// Raw value of element e of the current tile: shared memory for the aligned interior,
+// a plain load for the head / tail.
+template <int SX>
+__device__ __forceinline__ float x_at(const XCtx<SX>& c, int e) {
+    const StageMeta& m = c.m;
+    if (e >= m.vec_e0 && e < m.vec_e0 + m.nvec * (16 / SX)) {
+        const unsigned char* p = c.sm.data[c.stage] + static_cast<long long>(e - m.vec_e0) * SX;
+        return SX == 2 ? __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16)
+                       : *reinterpret_cast<const float*>(p);
+    }
+    return load_x(c.a.x, SX, static_cast<long long>(m.slot) * c.a.V + e);
+}
+
+// Fold a penalised value xp (element e) into the penalised statistics; `xr` is its raw
+// value whose term was already added to the tempered sum by the vector pass (undone here).
+template <int SX>
+__device__ __forceinline__ void pen_fold(const XCtx<SX>& c, XState& st, float xp, float xr, int e, bool undo_raw) {
+    if (xp > st.m_p) {
+        if (c.need_temp) st.s_t = (st.m_p > -INFINITY) ? st.s_t * ex2_approx((st.m_p - xp) * c.c_l2e) : 0.f;
+        st.m_p = xp;
+        st.arg = e;
+    } else if (xp == st.m_p && e < st.arg) {
+        st.arg = e;
+    } else if (xp != xp) {
+        st.m_p = xp;
+    }
+    if (c.need_temp) {
+        st.s_t += ex2_approx((xp - st.m_p) * c.c_l2e);
+        if (undo_raw) st.s_t -= ex2_approx((xr - st.m_p) * c.c_l2e);
+    }
+    if (xp >= st.th_p) push(c.gs.cpen, &c.gs.cnt_pen, kSmemCandPen, xp, e);
+}
+
+// One 16-byte vector: raw statistics over all its elements, penalised statistics over the
+// elements without a penalty bit (the penalised ones are folded in by x_entries).
+template <int SX>
+__device__ __forceinline__ void x_vec(const XCtx<SX>& c, XState& st, const uint4& w, int e, unsigned bits,
+                                      unsigned& mask_r, unsigned& mask_p) {
+    constexpr int EPV = 16 / SX;
+    const float vm = vec_max<SX>(w);
+    // raw log-sum-exp with a running max (rescale only when the max grows)
+    if (c.need_lp) {
+        if (!(vm <= st.m_r)) {
+            const float nm = max_nan(st.m_r, vm);
+            st.s_r = (st.m_r > -INFINITY && nm == nm) ? st.s_r * ex2_approx((st.m_r - nm) * kL2E) : 0.f;
+            st.m_r = nm;
+        }
+        const float2 t = vec_exp_sum<SX>(w, make_float2(0.f, 0.f), kL2E, st.m_r * kL2E);
+        st.s_r += t.x + t.y;
+    } else {
+        st.m_r = max_nan(st.m_r, vm);
+    }
+    // penalised max over unpenalised elements
+    float vp = vm;
+    if (bits != 0u) {
+        vp = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < EPV; ++q)
+            if (!((bits >> q) & 1u)) vp = max_nan(vp, elem<SX>(w, q));
+    }
+    if (!(vp <= st.m_p)) {
+        const float nm = max_nan(st.m_p, vp);
+        if (c.need_temp) st.s_t = (st.m_p > -INFINITY && nm == nm) ? st.s_t * ex2_approx((st.m_p - nm) * c.c_l2e) : 0.f;
+        st.m_p = nm;
+        st.arg = 0x7FFFFFFF;
+#pragma unroll
+        for (int q = 0; q < EPV; ++q)
+            if (!((bits >> q) & 1u) && elem<SX>(w, q) == nm) st.arg = min(st.arg, e + q);
+    } else if (c.greedy && vp == st.m_p && st.arg == 0x7FFFFFFF) {
+#pragma unroll
+        for (int q = 0; q < EPV; ++q)
+            if (!((bits >> q) & 1u) && elem<SX>(w, q) == vp) st.arg = min(st.arg, e + q);
+    }
+    if (c.need_temp) {
+        // all elements; the penalised ones are corrected by x_entries
+        const float2 t = vec_exp_sum<SX>(w, make_float2(0.f, 0.f), c.c_l2e, st.m_p * c.c_l2e);
+        st.s_t += t.x + t.y;
+    }
+    // candidates: raw values for top-n, unpenalised values for top-k (penalised: x_entries);
+    // the caller appends them warp-cooperatively
+    mask_r = (c.need_raw && vm >= st.th_r) ? ge_mask<SX>(w, st.th_r) : 0u;
+    mask_p = (c.need_cand && vp >= st.th_p) ? (ge_mask<SX>(w, st.th_p) & ~bits) : 0u;
+}
+
+// The tile's possibly-penalised tokens (history and draft tokens, from the penalty index):
+// each thread takes some, computes x' = x - ((f*c) + p) with c = history + own draft prefix,
+// and folds it into the penalised statistics.  pass1: only the maximum.
+template <int SX>
+__device__ __forceinline__ void x_entries(const XCtx<SX>& c, XState& st, bool pass1, float& lane_pen) {
+    const StageMeta& m = c.m;
+    const int gt = threadIdx.x - c.g * kGroupThreads;
+    const PenEntry* ent = c.sm.ent[c.stage];
+    const unsigned long long low = (m.j >= 64) ? ~0ull : ((1ull << m.j) - 1ull);
+    for (int i = gt; i < m.pen_n; i += kGroupThreads) {
+        const PenEntry pe = ent[i];
+        const int t = pe.token;
+        if (t < m.e0 || t >= m.e1) continue;
+        const unsigned long long mask = (static_cast<unsigned long long>(pe.mask_hi) << 32) | pe.mask_lo;
+        const int cnt = pe.base + __popcll(mask & low);
+        const float xr = x_at(c, t);
+        const float xp = penalise(xr, cnt, c.f, c.p);
+        if (pass1) lane_pen = max_nan(lane_pen, xp);
+        else pen_fold(c, st, xp, xr, t, true);
+    }
+}
+
+// Overflowed penalty index (more penalised tokens in the tile than fit): element-by-element
+// over the vectors carrying penalty bits, counts looked up in the caller's history.
+template <int SX>
+__device__ __forceinline__ void x_vec_overflow(const XCtx<SX>& c, XState& st, const uint4& w, int e, unsigned bits,
+                                               bool pass1, float& lane_pen) {
+    constexpr int EPV = 16 / SX;
+#pragma unroll
+    for (int q = 0; q < EPV; ++q) {
+        if (!((bits >> q) & 1u)) continue;
+        const float xr = elem<SX>(w, q);
+        const float xp = penalise(xr, pen_count(c.sm, c.stage, c.m, c.a, e + q), c.f, c.p);
+        if (pass1) lane_pen = max_nan(lane_pen, xp);
+        else pen_fold(c, st, xp, xr, e + q, true);
+    }
+}
+
+template <int SX>
+__device__ void x_tile(const XCtx<SX>& c, XState& st) {
+    constexpr int EPV = 16 / SX;
+    const StageMeta& m = c.m;
+    const int gt = threadIdx.x - c.g * kGroupThreads;
+    const int lane = threadIdx.x & 31, warp = gt >> 5;
+    const unsigned char* data = c.sm.data[c.stage];
+    const unsigned* bm = c.sm.bm[c.stage];
+    const long long xrow = static_cast<long long>(m.slot) * c.a.V;
+    const int e_tail = m.vec_e0 + m.nvec * EPV;
+    const bool use_entries = m.pen && !m.pen_over;
+    const bool overflow = m.pen && m.pen_over;
+
+    if (m.first) {
+        // ---- pass 1 over the first tile: maxima, then the segment's candidate thresholds
+        float mu0 = -INFINITY, mu1 = -INFINITY, mrw = -INFINITY, mpen = -INFINITY;
+        int v = gt;
+        for (; v + kGroupThreads < m.nvec; v += 2 * kGroupThreads) {
+            const uint4 w0 = *reinterpret_cast<const uint4*>(data + v * 16);
+            const uint4 w1 = *reinterpret_cast<const uint4*>(data + (v + kGroupThreads) * 16);
+            const int e0 = m.vec_e0 + v * EPV, e1 = e0 + kGroupThreads * EPV;
+            const unsigned b0 = m.pen ? bitmap_bits(bm, e0 - m.e0, EPV) : 0u;
+            const unsigned b1 = m.pen ? bitmap_bits(bm, e1 - m.e0, EPV) : 0u;
+            const float v0 = vec_max<SX>(w0), v1 = vec_max<SX>(w1);
+            mrw = max_nan(mrw, max_nan(v0, v1));
+            if ((b0 | b1) == 0u) {
+                mu0 = max_nan(mu0, v0);
+                mu1 = max_nan(mu1, v1);
+            } else {
+#pragma unroll
+                for (int q = 0; q < EPV; ++q) {
+                    if (!((b0 >> q) & 1u)) mu0 = max_nan(mu0, elem<SX>(w0, q));
+                    if (!((b1 >> q) & 1u)) mu1 = max_nan(mu1, elem<SX>(w1, q));
+                }
+                if (overflow) {
+                    XState dummy{};
+                    x_vec_overflow<SX>(c, dummy, w0, e0, b0, true, mpen);
+                    x_vec_overflow<SX>(c, dummy, w1, e1, b1, true, mpen);
                 }
             }
         }
-    }
-    // head / tail elements outside the 16-byte-aligned interior: plain loads
-    if (tid < 2) {
-        const int lo = tid == 0 ? m.e0 : e_tail;
-        const int hi = tid == 0 ? m.vec_e0 : m.e1;
-        for (int e = lo; e < hi; ++e) {
-            const float xv = load_x(a.x, SX, xrow + e);
-            if (m.pen && ((bm[(e - m.e0) >> 5] >> ((e - m.e0) & 31)) & 1u)) {
-                mpen = max_nan(mpen, penalise(xv, pen_count(sm, stage, m, a, e), f, p));
-                mrawp = max_nan(mrawp, xv);
+        for (; v < m.nvec; v += kGroupThreads) {
+            const uint4 w = *reinterpret_cast<const uint4*>(data + v * 16);
+            const int e = m.vec_e0 + v * EPV;
+            const unsigned bits = m.pen ? bitmap_bits(bm, e - m.e0, EPV) : 0u;
+            const float vv = vec_max<SX>(w);
+            mrw = max_nan(mrw, vv);
+            if (bits == 0u) {
+                mu0 = max_nan(mu0, vv);
             } else {
-                mu = max_nan(mu, xv);
+#pragma unroll
+                for (int q = 0; q < EPV; ++q)
+                    if (!((bits >> q) & 1u)) mu0 = max_nan(mu0, elem<SX>(w, q));
+                if (overflow) { XState dummy{}; x_vec_overflow<SX>(c, dummy, w, e, bits, true, mpen); }
             }
         }
-    }
-    const float lane_raw = max_nan(mu, mrawp);
-    const float lane_pen = max_nan(mu, mpen);
-    {
+        if (gt < 2) {
+            const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
+            for (int e = lo; e < hi; ++e) {
+                const float xv = load_x(c.a.x, SX, xrow + e);
+                mrw = max_nan(mrw, xv);
+                if (m.pen && bitmap_bit(bm, e - m.e0)) {
+                    if (overflow) mpen = max_nan(mpen, penalise(xv, pen_count(c.sm, c.stage, m, c.a, e), c.f, c.p));
+                } else {
+                    mu0 = max_nan(mu0, xv);
+                }
+            }
+        }
+        if (use_entries) { XState dummy{}; x_entries<SX>(c, dummy, true, mpen); }
+        const float lane_raw = mrw, lane_pen = max_nan(max_nan(mu0, mu1), mpen);
         float wr = lane_raw, wp = lane_pen;
         for (int o = 16; o; o >>= 1) {
             wr = max_nan(wr, __shfl_xor_sync(0xffffffffu, wr, o));
             wp = max_nan(wp, __shfl_xor_sync(0xffffffffu, wp, o));
         }
-        const float thp = need_cand ? warp_kth_largest(lane_pen, (k + kConsumerWarps - 1) / kConsumerWarps) : 0.f;
-        const float thr = need_raw ? warp_kth_largest(lane_raw, (a.n_top + kConsumerWarps - 1) / kConsumerWarps) : 0.f;
-        if (lane == 0) {
-            sm.red1[cb][warp][0] = wr; sm.red1[cb][warp][1] = wp;
-            sm.red1[cb][warp][2] = thp; sm.red1[cb][warp][3] = thr;
+        float thp = 0.f, thr = 0.f;
+        if (c.need_cand || c.need_raw) {
+            float sp = lane_pen, sr = lane_raw;
+            warp_sort2_desc(sp, sr);
+            const int cp = c.need_cand ? (m.top_k + kGroupWarps - 1) / kGroupWarps : 1;
+            const int cr = c.need_raw ? (c.a.n_top + kGroupWarps - 1) / kGroupWarps : 1;
+            thp = __shfl_sync(0xffffffffu, sp, cp - 1);
+            thr = __shfl_sync(0xffffffffu, sr, cr - 1);
         }
+        if (lane == 0) c.gs.red1[warp] = make_float4(wr, wp, thp, thr);
+        group_sync(c.g);
+        const float4 r = group_reduce_mmnn(c.gs.red1);
+        // the segment starts from the first tile's maxima: no rescaling inside this tile
+        st.m_r = r.x;
+        st.m_p = r.y;
+        st.s_r = 0.f;
+        st.s_t = 0.f;
+        st.arg = 0x7FFFFFFF;
+        st.th_p = c.need_cand ? r.z : INFINITY;
+        st.th_r = c.need_raw ? r.w : INFINITY;
     }
-    named_barrier_sync(1, kConsumerThreads);
-    if (tid == 0) { sm.cnt_pen[cb ^ 1] = 0; sm.cnt_raw[cb ^ 1] = 0; }
-    float m_raw = -INFINITY, m_pen = -INFINITY, th_p = INFINITY, th_r = INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-        m_raw = max_nan(m_raw, sm.red1[cb][w][0]);
-        m_pen = max_nan(m_pen, sm.red1[cb][w][1]);
-        th_p = fminf(th_p, sm.red1[cb][w][2]);
-        th_r = fminf(th_r, sm.red1[cb][w][3]);
-    }
-    if (!need_cand) th_p = INFINITY;
-    if (!need_raw) th_r = INFINITY;
-    const float th_lo = fminf(th_p, th_r);
-    const float mr_l2e = m_raw * kL2E;
-    const float c_l2e = need_temp ? kL2E / m.temperature : 0.f;
-    const bool raw_ok = isfinite(m_raw);
 
-    // ---- pass 2: sums, greedy argmax, candidates
-    float s_raw = 0.f, s_temp = 0.f;
-    int arg = 0x7FFFFFFF;
-    for (int v = tid; v < m.nvec; v += kConsumerThreads) {
+    // ---- the accumulation / filter pass over this tile.  Candidate flags are kept per
+    // thread (bit EPV*i+q: element q of the thread's i-th vector) and appended once at the end.
+    float unused = 0.f;
+    unsigned long long fr0 = 0ull, fr1 = 0ull, fp0 = 0ull, fp1 = 0ull;
+#pragma unroll 2
+    for (int i = 0; i < kVecPerThread; ++i) {
+        const int v = gt + i * kGroupThreads;
+        if (v >= m.nvec) break;
         const uint4 w = *reinterpret_cast<const uint4*>(data + v * 16);
         const int e = m.vec_e0 + v * EPV;
         const unsigned bits = m.pen ? bitmap_bits(bm, e - m.e0, EPV) : 0u;
-        if (need_lp && raw_ok) {
-#pragma unroll
-            for (int q = 0; q < EPV; ++q) s_raw += ex2_approx(fmaf(elem<SX>(w, q), kL2E, -mr_l2e));
-        }
-        if (bits == 0u) {
-            if (need_temp) {
-#pragma unroll
-                for (int q = 0; q < EPV; ++q) s_temp += ex2_approx(__fsub_rn(elem<SX>(w, q), m_pen) * c_l2e);
-            }
-            const float vm = (greedy || th_lo < INFINITY) ? vec_max<SX>(w) : -INFINITY;
-            if (greedy && vm >= m_pen && arg == 0x7FFFFFFF) {
-#pragma unroll
-                for (int q = 0; q < EPV; ++q)
-                    if (elem<SX>(w, q) == m_pen) { arg = min(arg, e + q); }
-            }
-            if (vm >= th_lo) {
-#pragma unroll
-                for (int q = 0; q < EPV; ++q) {
-                    const float xv = elem<SX>(w, q);
-                    if (xv >= th_p) push(sm.cpen[cb], &sm.cnt_pen[cb], kSmemCandPen, xv, e + q);
-                    if (xv >= th_r) push(sm.craw[cb], &sm.cnt_raw[cb], kSmemCandRaw, xv, e + q);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < EPV; ++q) {
-                const float xv = elem<SX>(w, q);
-                const float xp = (bits & (1u << q)) ? penalise(xv, pen_count(sm, stage, m, a, e + q), f, p) : xv;
-                if (need_temp) s_temp += ex2_approx(__fsub_rn(xp, m_pen) * c_l2e);
-                if (greedy && xp == m_pen && arg == 0x7FFFFFFF) arg = e + q;
-                if (xp >= th_p) push(sm.cpen[cb], &sm.cnt_pen[cb], kSmemCandPen, xp, e + q);
-                if (xv >= th_r) push(sm.craw[cb], &sm.cnt_raw[cb], kSmemCandRaw, xv, e + q);
-            }
-        }
+        unsigned mr = 0u, mp = 0u;
+        x_vec<SX>(c, st, w, e, bits, mr, mp);
+        if (overflow && bits) x_vec_overflow<SX>(c, st, w, e, bits, false, unused);
+        const int sh = i * EPV;
+        if (sh < 64) { fr0 |= static_cast<unsigned long long>(mr) << sh; fp0 |= static_cast<unsigned long long>(mp) << sh; }
+        else { fr1 |= static_cast<unsigned long long>(mr) << (sh - 64); fp1 |= static_cast<unsigned long long>(mp) << (sh - 64); }
     }
-    if (tid < 2) {
-        const int lo = tid == 0 ? m.e0 : e_tail;
-        const int hi = tid == 0 ? m.vec_e0 : m.e1;
+    if (c.need_raw) flush_flags<SX>(c.gs.craw, &c.gs.cnt_raw, kSmemCandRaw, fr0, fr1, data, m.vec_e0, gt);
+    if (c.need_cand) flush_flags<SX>(c.gs.cpen, &c.gs.cnt_pen, kSmemCandPen, fp0, fp1, data, m.vec_e0, gt);
+    if (gt < 2) {
+        const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
         for (int e = lo; e < hi; ++e) {
-            const float xv = load_x(a.x, SX, xrow + e);
-            int c = 0;
-            if (m.pen && ((bm[(e - m.e0) >> 5] >> ((e - m.e0) & 31)) & 1u)) c = pen_count(sm, stage, m, a, e);
-            const float xp = penalise(xv, c, f, p);
-            if (need_lp && raw_ok) s_raw += ex2_approx(fmaf(xv, kL2E, -mr_l2e));
-            if (need_temp) s_temp += ex2_approx(__fsub_rn(xp, m_pen) * c_l2e);
-            if (greedy && xp == m_pen) arg = min(arg, e);
-            if (xp >= th_p) push(sm.cpen[cb], &sm.cnt_pen[cb], kSmemCandPen, xp, e);
-            if (xv >= th_r) push(sm.craw[cb], &sm.cnt_raw[cb], kSmemCandRaw, xv, e);
+            const float xv = load_x(c.a.x, SX, xrow + e);
+            // raw statistics and raw candidates
+            if (c.need_lp) {
+                if (!(xv <= st.m_r)) {
+                    const float nm = max_nan(st.m_r, xv);
+                    st.s_r = (st.m_r > -INFINITY && nm == nm) ? st.s_r * ex2_approx((st.m_r - nm) * kL2E) : 0.f;
+                    st.m_r = nm;
+                }
+                st.s_r += ex2_approx((xv - st.m_r) * kL2E);
+            } else {
+                st.m_r = max_nan(st.m_r, xv);
+            }
+            if (xv >= st.th_r) push(c.gs.craw, &c.gs.cnt_raw, kSmemCandRaw, xv, e);
+            const bool bit = m.pen && bitmap_bit(bm, e - m.e0);
+            if (!bit) pen_fold(c, st, xv, xv, e, false);
+            else if (overflow) pen_fold(c, st, penalise(xv, pen_count(c.sm, c.stage, m, c.a, e), c.f, c.p), xv, e, false);
+            else if (c.need_temp) st.s_t += ex2_approx((xv - st.m_p) * c.c_l2e);   // undone by x_entries
         }
     }
+    if (use_entries) x_entries<SX>(c, st, false, unused);
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.empty[stage]);    // the stage's shared memory is no longer read
-    s_raw = warp_sum(s_raw);
-    s_temp = warp_sum(s_temp);
-    arg = warp_min_i(arg);
-    if (lane == 0) {
-        sm.red2[cb][warp][0] = s_raw; sm.red2[cb][warp][1] = s_temp;
-        sm.red2[cb][warp][2] = __int_as_float(arg);
-    }
-    named_barrier_sync(1, kConsumerThreads);
-    const int n_pen = sm.cnt_pen[cb], n_raw = sm.cnt_raw[cb];
-    const long long ti = static_cast<long long>(m.slot) * a.tiles_x + m.tile;
-    if (tid == 0) {
-        float sr = 0.f, st = 0.f;
-        int ag = 0x7FFFFFFF;
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            sr += sm.red2[cb][w][0];
-            st += sm.red2[cb][w][1];
-            ag = min(ag, __float_as_int(sm.red2[cb][w][2]));
-        }
-        TileStats ts;
-        ts.m_raw = m_raw; ts.s_raw = sr; ts.m_pen = m_pen; ts.arg_pen = ag; ts.s_temp = st;
-        ts.flags = 0;
-        ts.n_pen = need_cand ? n_pen : 0;
-        ts.n_raw = need_raw ? n_raw : 0;
-        if (need_cand && n_pen > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
-        if (need_raw && n_raw > kCandRawGlobal) { ts.flags |= kTileOverflowRaw; ts.n_raw = 0; }
-        if (!isfinite(m_raw) || !isfinite(m_pen)) ts.flags |= kTileBad;
-        a.ts_x[ti] = ts;
-    }
-    if (need_cand && n_pen <= kCandPenGlobal) {
-        Cand* dst = a.cand_x + ti * kCandPenGlobal;
-        for (int i = tid; i < n_pen; i += kConsumerThreads) dst[i] = sm.cpen[cb][i];
-    }
-    if (need_raw && n_raw <= kCandRawGlobal) {
-        Cand* dst = a.cand_raw + ti * kCandRawGlobal;
-        for (int i = tid; i < n_raw; i += kConsumerThreads) dst[i] = sm.craw[cb][i];
-    }
+    if (lane == 0) mbar_arrive(&c.sm.empty[c.stage]);     // this stage is no longer read
 }
 
-// ------------------------------------------------------------------ one draft-probability tile
-__device__ void process_q(const Args& a, Smem& sm, int stage, const StageMeta& m, int cb) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+template <int SX>
+__device__ void x_finish(const XCtx<SX>& c, XState& st) {
+    const StageMeta& m = c.m;
+    const int gt = threadIdx.x - c.g * kGroupThreads;
+    const int lane = threadIdx.x & 31, warp = gt >> 5;
+    float mr = st.m_r, sr = st.s_r, mp = st.m_p, stt = st.s_t;
+    // argmax: lowest index among lanes whose running max equals the warp max
+    float wp = mp;
+    for (int o = 16; o; o >>= 1) wp = max_nan(wp, __shfl_xor_sync(0xffffffffu, wp, o));
+    int arg = (mp == wp) ? st.arg : 0x7FFFFFFF;
+    arg = warp_min_i(arg);
+    warp_merge_ms(mr, sr, kL2E);
+    warp_merge_ms(mp, stt, c.c_l2e);
+    if (lane == 0) {
+        c.gs.red[warp] = make_float4(mr, sr, mp, stt);
+        c.gs.red2[warp] = make_float4(__int_as_float(arg), 0.f, 0.f, 0.f);
+    }
+    group_sync(c.g);
+    const int n_pen = c.gs.cnt_pen, n_raw = c.gs.cnt_raw;
+    const long long ti = static_cast<long long>(m.slot) * c.a.nseg_x + m.seg;
+    if (warp == 0) {
+        float4 r = lane < kGroupWarps ? c.gs.red[lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+        int ag = lane < kGroupWarps ? __float_as_int(c.gs.red2[lane].x) : 0x7FFFFFFF;
+        float Mr = r.x, Sr = r.y, Mp = r.z, St = r.w;
+        float Mp_all = Mp;
+        for (int o = 16; o; o >>= 1) Mp_all = max_nan(Mp_all, __shfl_xor_sync(0xffffffffu, Mp_all, o));
+        ag = (Mp == Mp_all) ? ag : 0x7FFFFFFF;
+        ag = warp_min_i(ag);
+        warp_merge_ms(Mr, Sr, kL2E);
+        warp_merge_ms(Mp, St, c.c_l2e);
+        if (lane == 0) {
+            TileStats ts;
+            ts.m_raw = Mr; ts.s_raw = Sr; ts.m_pen = Mp; ts.arg_pen = ag; ts.s_temp = St;
+            ts.flags = 0;
+            ts.n_pen = c.need_cand ? n_pen : 0;
+            ts.n_raw = c.need_raw ? n_raw : 0;
+            if (c.need_cand && n_pen > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
+            if (c.need_raw && n_raw > kCandRawGlobal) { ts.flags |= kTileOverflowRaw; ts.n_raw = 0; }
+            if (!isfinite(Mr) || !isfinite(Mp)) ts.flags |= kTileBad;
+            c.a.ts_x[ti] = ts;
+        }
+    }
+    if (c.need_cand && n_pen <= kCandPenGlobal) {
+        Cand* dst = c.a.cand_x + ti * kCandPenGlobal;
+        for (int i = gt; i < n_pen; i += kGroupThreads) dst[i] = c.gs.cpen[i];
+    }
+    if (c.need_raw && n_raw <= kCandRawGlobal) {
+        Cand* dst = c.a.cand_raw + ti * kCandRawGlobal;
+        for (int i = gt; i < n_raw; i += kGroupThreads) dst[i] = c.gs.craw[i];
+    }
+    group_sync(c.g);                                      // buffers reused by the next segment
+    if (gt == 0) { c.gs.cnt_pen = 0; c.gs.cnt_raw = 0; }
+}
+
+// ------------------------------------------------------------------ draft-probability segments
+struct QState {
+    float mx, mn, sum;   // running max / min; sum of q (T = 1) or of (q/mx)^(1/T)
+    float th;
+};
+
+__device__ __forceinline__ void q_elem(QState& st, float v, bool need_sum, bool t_one, float inv_t, bool filt,
+                                       GroupSmem& gs, int e) {
+    if (need_sum && !t_one && v > st.mx) {
+        st.sum = (st.mx > 0.f) ? st.sum * exp2f(inv_t * log2f(st.mx / v)) : 0.f;
+    }
+    st.mx = max_nan(st.mx, v);
+    st.mn = fminf(st.mn, v);
+    if (need_sum) st.sum += t_one ? v : draft_weight(v, st.mx, inv_t, false);
+    if (filt && v >= st.th) push(gs.cpen, &gs.cnt_pen, kSmemCandPen, v, e);
+}
+
+__device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage, const StageMeta& m, QState& st) {
+    const int gt = threadIdx.x - g * kGroupThreads;
+    const int lane = threadIdx.x & 31, warp = gt >> 5;
     const unsigned char* data = sm.data[stage];
     const int k = m.top_k;
     const bool need_cand = k > 0 && k < a.V && k <= kMaxCandTopK;
     const bool need_sum = !need_cand && (k == 0 || k >= a.V);
     const bool t_one = m.temperature == 1.f;
+    const float inv_t = 1.f / m.temperature;
     const long long qrow = static_cast<long long>(m.slot) * a.V;
     const int e_tail = m.vec_e0 + m.nvec * 4;
-    float mx = -INFINITY, mn = INFINITY, sum = 0.f;
-    for (int v = tid; v < m.nvec; v += kConsumerThreads) {
-        const float4 w = *reinterpret_cast<const float4*>(data + v * 16);
-        mx = max_nan(max_nan(mx, w.x), max_nan(w.y, max_nan(w.z, w.w)));
-        mn = fminf(fminf(mn, w.x), fminf(w.y, fminf(w.z, w.w)));
-        if (need_sum && t_one) sum += (w.x + w.y) + (w.z + w.w);
-    }
-    if (tid < 2) {
-        const int lo = tid == 0 ? m.e0 : e_tail;
-        const int hi = tid == 0 ? m.vec_e0 : m.e1;
-        for (int e = lo; e < hi; ++e) {
-            const float v = __ldg(a.q + qrow + e);
-            mx = max_nan(mx, v); mn = fminf(mn, v);
-            if (need_sum && t_one) sum += v;
+    if (m.first) {
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+        int v = gt;
+        for (; v + kGroupThreads < m.nvec; v += 2 * kGroupThreads) {
+            const float4 w0 = *reinterpret_cast<const float4*>(data + v * 16);
+            const float4 w1 = *reinterpret_cast<const float4*>(data + (v + kGroupThreads) * 16);
+            mx0 = max_nan(max_nan(mx0, w0.x), max_nan(w0.y, max_nan(w0.z, w0.w)));
+            mx1 = max_nan(max_nan(mx1, w1.x), max_nan(w1.y, max_nan(w1.z, w1.w)));
         }
-    }
-    {
-        float wm = mx, wn = mn;
-        for (int o = 16; o; o >>= 1) {
-            wm = max_nan(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-            wn = fminf(wn, __shfl_xor_sync(0xffffffffu, wn, o));
-        }
-        const float th = need_cand ? warp_kth_largest(mx, (k + kConsumerWarps - 1) / kConsumerWarps) : 0.f;
-        if (lane == 0) {
-            sm.red1[cb][warp][0] = wm; sm.red1[cb][warp][1] = wn;
-            sm.red1[cb][warp][2] = th; sm.red1[cb][warp][3] = 0.f;
-        }
-    }
-    named_barrier_sync(1, kConsumerThreads);
-    if (tid == 0) { sm.cnt_pen[cb ^ 1] = 0; sm.cnt_raw[cb ^ 1] = 0; }
-    float qmax = -INFINITY, qmin = INFINITY, th = INFINITY;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-        qmax = max_nan(qmax, sm.red1[cb][w][0]);
-        qmin = fminf(qmin, sm.red1[cb][w][1]);
-        th = fminf(th, sm.red1[cb][w][2]);
-    }
-    if (!need_cand) th = INFINITY;
-    const float inv_t = 1.f / m.temperature;
-    float s_temp = 0.f;
-    if (need_cand || (need_sum && !t_one)) {
-        for (int v = tid; v < m.nvec; v += kConsumerThreads) {
+        for (; v < m.nvec; v += kGroupThreads) {
             const float4 w = *reinterpret_cast<const float4*>(data + v * 16);
-            const int e = m.vec_e0 + v * 4;
-            if (need_sum && !t_one) {
-                s_temp += draft_weight(w.x, qmax, inv_t, false) + draft_weight(w.y, qmax, inv_t, false) +
-                          draft_weight(w.z, qmax, inv_t, false) + draft_weight(w.w, qmax, inv_t, false);
-            }
-            if (need_cand && max_nan(max_nan(w.x, w.y), max_nan(w.z, w.w)) >= th) {
-                if (w.x >= th) push(sm.cpen[cb], &sm.cnt_pen[cb], kSmemCandPen, w.x, e);
-                if (w.y >= th) push(sm.cpen[cb], &sm.cnt_pen[cb], kSmemCandPen, w.y, e + 1);
-                if (w.z >= th) push(sm.cpen[cb], &sm.cnt_pen[cb], kSmemCandPen, w.z, e + 2);
-                if (w.w >= th) push(sm.cpen[cb], &sm.cnt_pen[cb], kSmemCandPen, w.w, e + 3);
-            }
+            mx0 = max_nan(max_nan(mx0, w.x), max_nan(w.y, max_nan(w.z, w.w)));
         }
+        if (gt < 2) {
+            const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
+            for (int e = lo; e < hi; ++e) mx0 = max_nan(mx0, __ldg(a.q + qrow + e));
+        }
+        const float mx = max_nan(mx0, mx1);
+        float wm = mx;
+        for (int o = 16; o; o >>= 1) wm = max_nan(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+        float th = 0.f;
+        if (need_cand) {
+            float s0 = mx, s1 = 0.f;
+            warp_sort2_desc(s0, s1);
+            th = __shfl_sync(0xffffffffu, s0, (k + kGroupWarps - 1) / kGroupWarps - 1);
+        }
+        if (lane == 0) gs.red1[warp] = make_float4(wm, -INFINITY, th, INFINITY);
+        group_sync(g);
+        const float4 r = group_reduce_mmnn(gs.red1);
+        st.mx = need_sum && !t_one ? r.x : -INFINITY;     // the tempered sum starts from the tile max
+        st.mn = INFINITY;
+        st.sum = 0.f;
+        st.th = need_cand ? r.z : INFINITY;
     }
-    if (tid < 2 && (need_cand || (need_sum && !t_one))) {
-        const int lo = tid == 0 ? m.e0 : e_tail;
-        const int hi = tid == 0 ? m.vec_e0 : m.e1;
-        for (int e = lo; e < hi; ++e) {
-            const float v = __ldg(a.q + qrow + e);
-            if (need_sum && !t_one) s_temp += draft_weight(v, qmax, inv_t, false);
-            if (need_cand && v >= th) push(sm.cpen[cb], &sm.cnt_pen[cb], kSmemCandPen, v, e);
+    unsigned long long fq = 0ull;
+#pragma unroll 2
+    for (int i = 0; i < kVecPerThread; ++i) {
+        const int v = gt + i * kGroupThreads;
+        if (v >= m.nvec) break;
+        const int e = m.vec_e0 + v * 4;
+        const uint4 wu = *reinterpret_cast<const uint4*>(data + v * 16);
+        const float4 w = *reinterpret_cast<const float4*>(&wu);
+        const float vm = max_nan(max_nan(w.x, w.y), max_nan(w.z, w.w));
+        const float vn = fminf(fminf(w.x, w.y), fminf(w.z, w.w));
+        if (need_sum && !t_one) {
+            if (!(vm <= st.mx)) {
+                q_elem(st, w.x, true, false, inv_t, false, gs, e);
+                q_elem(st, w.y, true, false, inv_t, false, gs, e + 1);
+                q_elem(st, w.z, true, false, inv_t, false, gs, e + 2);
+                q_elem(st, w.w, true, false, inv_t, false, gs, e + 3);
+            } else {
+                st.sum += draft_weight(w.x, st.mx, inv_t, false) + draft_weight(w.y, st.mx, inv_t, false) +
+                          draft_weight(w.z, st.mx, inv_t, false) + draft_weight(w.w, st.mx, inv_t, false);
+            }
+        } else if (need_sum) {
+            st.sum += (w.x + w.y) + (w.z + w.w);
         }
+        st.mx = max_nan(st.mx, vm);
+        st.mn = fminf(st.mn, vn);
+        if (need_cand && vm >= st.th) fq |= static_cast<unsigned long long>(ge_mask<4>(wu, st.th)) << (4 * i);
+    }
+    if (need_cand) flush_flags<4>(gs.cpen, &gs.cnt_pen, kSmemCandPen, fq, 0ull, data, m.vec_e0, gt);
+    if (gt < 2) {
+        const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
+        for (int e = lo; e < hi; ++e) q_elem(st, __ldg(a.q + qrow + e), need_sum, t_one, inv_t, need_cand, gs, e);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage]);
-    sum = warp_sum(sum);
-    s_temp = warp_sum(s_temp);
-    if (lane == 0) { sm.red2[cb][warp][0] = sum; sm.red2[cb][warp][1] = s_temp; }
-    named_barrier_sync(1, kConsumerThreads);
-    const int n = sm.cnt_pen[cb];
-    const long long ti = static_cast<long long>(m.slot) * a.tiles_q + m.tile;
-    if (tid == 0) {
-        float s1 = 0.f, s2 = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) { s1 += sm.red2[cb][w][0]; s2 += sm.red2[cb][w][1]; }
-        TileStats ts;
-        ts.m_raw = qmax; ts.s_raw = s1; ts.m_pen = qmin; ts.arg_pen = 0; ts.s_temp = s2;
-        ts.n_pen = need_cand ? n : 0; ts.n_raw = 0; ts.flags = 0;
-        if (need_cand && n > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
-        if (!(qmin >= 0.f) || !(qmax <= 3.0e38f)) ts.flags |= kTileBad;
-        a.ts_q[ti] = ts;
+}
+
+__device__ void q_finish(const Args& a, GroupSmem& gs, int g, const StageMeta& m, QState& st) {
+    const int gt = threadIdx.x - g * kGroupThreads;
+    const int lane = threadIdx.x & 31, warp = gt >> 5;
+    const int k = m.top_k;
+    const bool need_cand = k > 0 && k < a.V && k <= kMaxCandTopK;
+    const bool need_sum = !need_cand && (k == 0 || k >= a.V);
+    const bool t_one = m.temperature == 1.f;
+    const float inv_t = 1.f / m.temperature;
+    float mx = st.mx, mn = st.mn, sum = st.sum;
+    float M = mx;
+    for (int o = 16; o; o >>= 1) M = max_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float mnw = mn;
+    for (int o = 16; o; o >>= 1) mnw = fminf(mnw, __shfl_xor_sync(0xffffffffu, mnw, o));
+    // sums of (q/mx)^(1/T) are rescaled to the warp max; plain sums of q are not
+    float r = sum;
+    if (need_sum && !t_one) r = (sum > 0.f && mx > 0.f) ? sum * exp2f(inv_t * log2f(mx / M)) : 0.f;
+    r = warp_sum(r);
+    if (lane == 0) gs.red[warp] = make_float4(M, r, mnw, 0.f);
+    group_sync(g);
+    const int n = gs.cnt_pen;
+    const long long ti = static_cast<long long>(m.slot) * a.nseg_q + m.seg;
+    if (warp == 0) {
+        const float4 v = lane < kGroupWarps ? gs.red[lane] : make_float4(-INFINITY, 0.f, INFINITY, 0.f);
+        float Mg = v.x;
+        for (int o = 16; o; o >>= 1) Mg = max_nan(Mg, __shfl_xor_sync(0xffffffffu, Mg, o));
+        float s = v.y;
+        if (need_sum && !t_one) s = (s > 0.f && v.x > 0.f) ? s * exp2f(inv_t * log2f(v.x / Mg)) : 0.f;
+        s = warp_sum(s);
+        float mnn = v.z;
+        for (int o = 16; o; o >>= 1) mnn = fminf(mnn, __shfl_xor_sync(0xffffffffu, mnn, o));
+        if (lane == 0) {
+            TileStats ts;
+            ts.m_raw = Mg; ts.s_raw = t_one ? s : 0.f; ts.m_pen = mnn; ts.arg_pen = 0; ts.s_temp = t_one ? 0.f : s;
+            ts.n_pen = need_cand ? n : 0; ts.n_raw = 0; ts.flags = 0;
+            if (need_cand && n > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
+            if (!(mnn >= 0.f) || !(Mg <= 3.0e38f)) ts.flags |= kTileBad;
+            a.ts_q[ti] = ts;
+        }
     }
     if (need_cand && n <= kCandPenGlobal) {
         Cand* dst = a.cand_q + ti * kCandPenGlobal;
-        for (int i = tid; i < n; i += kConsumerThreads) dst[i] = sm.cpen[cb][i];
+        for (int i = gt; i < n; i += kGroupThreads) dst[i] = gs.cpen[i];
     }
+    group_sync(g);
+    if (gt == 0) { gs.cnt_pen = 0; gs.cnt_raw = 0; }
+}
+
+// Segments in the stream of (CTA c, group g): positions m with c + G*(g + 2m) < S.
+__device__ __forceinline__ int stream_len(int S, int G, int c, int g) {
+    const int first = c + G * g;
+    return first >= S ? 0 : (S - 1 - first) / (2 * G) + 1;
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -409,118 +775,180 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const int tid = threadIdx.x;
-    const int n_units = a.plan->n_units;
+    const int S = a.plan->n_units;
     const int G = gridDim.x;
+    const int c = blockIdx.x;
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], kConsumerWarps); }
-        sm.cnt_pen[0] = sm.cnt_pen[1] = 0;
-        sm.cnt_raw[0] = sm.cnt_raw[1] = 0;
-        sm.error = 0;
+        for (int s = 0; s < kStages; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], kGroupWarps); }
+        for (int g = 0; g < kGroups; ++g) { sm.grp[g].cnt_pen = 0; sm.grp[g].cnt_raw = 0; sm.grp[g].error = 0; }
         fence_mbar_init();
     }
     __syncthreads();
 
     if (tid >= kConsumerThreads) {
-        // ---------------- producer warp
+        // ---------------- producer warp.  Lane 16g+f holds field f of group g's current,
+        // next and next-but-one segment descriptors, and the penalty header of tile t0+f of
+        // the group's current and next segment; lane 0 issues the copies.
         const int lane = tid & 31;
-        int it = 0;
+        const int mg = lane >> 4, ml = lane & 15;
+        constexpr int kFields = sizeof(UnitDesc) / sizeof(int);
+        static_assert(kFields <= 16, "descriptor fields must fit a half warp");
+        const int* streams = reinterpret_cast<const int*>(a.units + static_cast<long long>(c) * kGroups * a.max_seg);
+        const int my_len = stream_len(S, G, c, mg);
+        auto load_field = [&](int p) { return (p < my_len && ml < kFields) ? streams[(mg * a.max_seg + p) * kFields + ml] : 0; };
+        // field f of group g's descriptor held in register r
+        auto fld = [&](int r, int g, int f) { return __shfl_sync(0xffffffffu, r, g * 16 + f); };
+        constexpr int F_SLOT = 0, F_KIND = 1, F_B = 2, F_SEG = 3, F_T0 = 4, F_T1 = 5, F_T = 6, F_TOPK = 7,
+                      F_TOPP = 8, F_PRES = 9, F_FREQ = 10;
+        auto load_hdr = [&](int r) {          // headers of the segment described by register r (own group)
+            PenHdr h{0, 0, {0, 0}};
+            const int kind = __shfl_sync(0xffffffffu, r, mg * 16 + F_KIND);
+            const int b = __shfl_sync(0xffffffffu, r, mg * 16 + F_B);
+            const int t0 = __shfl_sync(0xffffffffu, r, mg * 16 + F_T0);
+            const int t1 = __shfl_sync(0xffffffffu, r, mg * 16 + F_T1);
+            const float pres = __int_as_float(__shfl_sync(0xffffffffu, r, mg * 16 + F_PRES));
+            const float freq = __int_as_float(__shfl_sync(0xffffffffu, r, mg * 16 + F_FREQ));
+            if (kind == kUnitX && (pres != 0.f || freq != 0.f) && t0 + ml < t1)
+                h = a.pen_hdr[static_cast<long long>(b) * a.tiles_x + t0 + ml];
+            return h;
+        };
+        int dcur = load_field(0), dnxt = load_field(1), dnxt2 = load_field(2);
+        PenHdr hcur = load_hdr(dcur);
+        PenHdr hnxt = load_hdr(dnxt);
+        int len0 = stream_len(S, G, c, 0), len1 = stream_len(S, G, c, 1);
+        int pos0 = 0, pos1 = 0, iss0 = 0, iss1 = 0;
+        int tc0 = fld(dcur, 0, F_T0), tc1 = fld(dcur, 1, F_T0);
         bool failed = false;
-        for (int base = blockIdx.x; base < n_units && !failed; base += 32 * G) {
-            const int ul = base + lane * G;
-            UnitDesc ud{0, 0, 0, 0};
-            dspark_row_params_t rp{};
-            PenHdr ph{0, 0, {0, 0}};
-            if (ul < n_units) {
-                ud = a.units[ul];
-                rp = a.rows[ud.b];
-                if (ud.kind == kUnitX && has_penalty(rp)) ph = a.pen_hdr[static_cast<long long>(ud.b) * a.tiles_x + ud.tile];
-            }
-            for (int l = 0; l < 32; ++l) {
-                const int u = base + l * G;
-                if (u >= n_units) break;
-                const int slot = __shfl_sync(0xffffffffu, ud.slot, l);
-                const int kind = __shfl_sync(0xffffffffu, ud.kind, l);
-                const int tile = __shfl_sync(0xffffffffu, ud.tile, l);
-                const int b = __shfl_sync(0xffffffffu, ud.b, l);
-                const float T = __shfl_sync(0xffffffffu, rp.temperature, l);
-                const int topk = __shfl_sync(0xffffffffu, rp.top_k, l);
-                const float topp = __shfl_sync(0xffffffffu, rp.top_p, l);
-                const float pres = __shfl_sync(0xffffffffu, rp.presence_penalty, l);
-                const float freq = __shfl_sync(0xffffffffu, rp.frequency_penalty, l);
-                const int pn = __shfl_sync(0xffffffffu, ph.n, l);
-                const int pover = __shfl_sync(0xffffffffu, ph.overflow, l);
-                const int pnh = __shfl_sync(0xffffffffu, ph.pad[0], l);
-                const int stage = it % kStages;
-                const unsigned parity = ((it / kStages) & 1) ^ 1;
+        unsigned long long idle = 0;
+        while (!failed && (pos0 < len0 || pos1 < len1)) {
+            bool progressed = false;
+#pragma unroll
+            for (int g = 0; g < kGroups; ++g) {
+                const int pos = g ? pos1 : pos0, len = g ? len1 : len0, iss = g ? iss1 : iss0;
+                const int tile = g ? tc1 : tc0;
+                if (pos >= len) continue;
+                const int stage = g + 2 * (iss & 1);
+                const unsigned parity = ((iss >> 1) & 1) ^ 1;
+                int ready = 0;
+                if (lane == 0) ready = mbar_test_wait(&sm.empty[stage], parity) ? 1 : 0;
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (!ready) continue;
+                const int slot = fld(dcur, g, F_SLOT), kind = fld(dcur, g, F_KIND), b = fld(dcur, g, F_B);
+                const int seg = fld(dcur, g, F_SEG), t0 = fld(dcur, g, F_T0), t1 = fld(dcur, g, F_T1);
+                const float T = __int_as_float(fld(dcur, g, F_T));
+                const int topk = fld(dcur, g, F_TOPK);
+                const float topp = __int_as_float(fld(dcur, g, F_TOPP));
+                const float pres = __int_as_float(fld(dcur, g, F_PRES));
+                const float freq = __int_as_float(fld(dcur, g, F_FREQ));
+                const int src = g * 16 + (tile - t0);
+                const int pn = __shfl_sync(0xffffffffu, hcur.n, src);
+                const int pover = __shfl_sync(0xffffffffu, hcur.overflow, src);
+                const int pnh = __shfl_sync(0xffffffffu, hcur.pad[0], src);
                 if (lane == 0) {
-                    if (!mbar_wait_bounded(&sm.empty[stage], parity, kWaitLimit)) {
-                        sm.error = 1;
-                        failed = true;
-                    } else {
-                        StageMeta& m = sm.meta[stage];
-                        const bool isx = kind == kUnitX;
-                        const int es = isx ? SX : 4;
-                        const int tile_n = isx ? a.tile_x : a.tile_q;
-                        const int e0 = tile * tile_n, e1 = min(a.V, e0 + tile_n);
-                        const unsigned char* row = isx
-                            ? static_cast<const unsigned char*>(a.x) + static_cast<long long>(slot) * a.V * es
-                            : reinterpret_cast<const unsigned char*>(a.q) + static_cast<long long>(slot) * a.V * 4;
-                        const uintptr_t A0 = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(e0) * es;
-                        const uintptr_t A1 = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(e1) * es;
-                        uintptr_t c0 = (A0 + 15) & ~static_cast<uintptr_t>(15);
-                        uintptr_t c1 = A1 & ~static_cast<uintptr_t>(15);
-                        if (c1 < c0) c1 = c0;
-                        const unsigned bytes = static_cast<unsigned>(c1 - c0);
-                        m.kind = kind; m.slot = slot; m.b = b;
-                        m.j = isx ? slot - b * (a.Km + 1) : slot - b * a.Km;
-                        m.tile = tile; m.e0 = e0; m.e1 = e1;
-                        m.nvec = static_cast<int>(bytes / 16);
-                        m.vec_e0 = e0 + static_cast<int>((c0 - A0) / es);
-                        if (bytes == 0) m.vec_e0 = e1;
-                        m.pen = isx && (pres != 0.f || freq != 0.f);
-                        m.pen_n = pn; m.pen_nh = pnh; m.pen_over = pover;
-                        m.top_k = topk; m.temperature = T; m.top_p = topp;
-                        m.presence = pres; m.frequency = freq;
-                        unsigned tx = bytes;
-                        const unsigned bm_bytes = static_cast<unsigned>(a.bm_words) * 4u;
-                        const unsigned ent_bytes = m.pen && !pover ? static_cast<unsigned>(pn) * 16u : 0u;
-                        if (m.pen) tx += bm_bytes + ent_bytes;
-                        mbar_arrive_expect_tx(&sm.full[stage], tx);
-                        if (bytes) bulk_g2s(sm.data[stage], reinterpret_cast<const void*>(c0), bytes, &sm.full[stage]);
-                        if (m.pen) {
-                            const long long pt = static_cast<long long>(b) * a.tiles_x + tile;
-                            bulk_g2s(sm.bm[stage], a.pen_bm + pt * a.bm_words, bm_bytes, &sm.full[stage]);
-                            if (ent_bytes) bulk_g2s(sm.ent[stage], a.pen_ent + pt * kPenCap, ent_bytes, &sm.full[stage]);
-                        }
+                    StageMeta& m = sm.meta[stage];
+                    const bool isx = kind == kUnitX;
+                    const int es = isx ? SX : 4;
+                    const int tile_n = isx ? a.tile_x : a.tile_q;
+                    const int e0 = tile * tile_n, e1 = min(a.V, e0 + tile_n);
+                    const unsigned char* row = isx
+                        ? static_cast<const unsigned char*>(a.x) + static_cast<long long>(slot) * a.V * es
+                        : reinterpret_cast<const unsigned char*>(a.q) + static_cast<long long>(slot) * a.V * 4;
+                    const uintptr_t A0 = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(e0) * es;
+                    const uintptr_t A1 = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(e1) * es;
+                    uintptr_t c0 = (A0 + 15) & ~static_cast<uintptr_t>(15);
+                    uintptr_t c1 = A1 & ~static_cast<uintptr_t>(15);
+                    if (c1 < c0) c1 = c0;
+                    const unsigned bytes = static_cast<unsigned>(c1 - c0);
+                    m.kind = kind; m.slot = slot; m.b = b;
+                    m.j = isx ? slot - b * (a.Km + 1) : slot - b * a.Km;
+                    m.seg = seg; m.tile = tile; m.e0 = e0; m.e1 = e1;
+                    m.nvec = static_cast<int>(bytes / 16);
+                    m.vec_e0 = (bytes == 0) ? e1 : e0 + static_cast<int>((c0 - A0) / es);
+                    m.pen = isx && (pres != 0.f || freq != 0.f);
+                    m.pen_n = pn; m.pen_nh = pnh; m.pen_over = pover;
+                    m.top_k = topk; m.first = tile == t0; m.last = tile == t1 - 1;
+                    m.temperature = T; m.top_p = topp; m.presence = pres; m.frequency = freq;
+                    unsigned tx = bytes;
+                    const unsigned bm_bytes = static_cast<unsigned>(a.bm_words) * 4u;
+                    const unsigned ent_bytes = m.pen && !pover ? static_cast<unsigned>(pn) * 16u : 0u;
+                    if (m.pen) tx += bm_bytes + ent_bytes;
+                    mbar_arrive_expect_tx(&sm.full[stage], tx);
+                    if (bytes) bulk_g2s(sm.data[stage], reinterpret_cast<const void*>(c0), bytes, &sm.full[stage]);
+                    if (m.pen) {
+                        const long long pt = static_cast<long long>(b) * a.tiles_x + tile;
+                        bulk_g2s(sm.bm[stage], a.pen_bm + pt * a.bm_words, bm_bytes, &sm.full[stage]);
+                        if (ent_bytes) bulk_g2s(sm.ent[stage], a.pen_ent + pt * kPenCap, ent_bytes, &sm.full[stage]);
                     }
                 }
-                failed = __shfl_sync(0xffffffffu, failed, 0);
-                if (failed) break;
-                ++it;
+                progressed = true;
+                if (g) { ++iss1; ++tc1; } else { ++iss0; ++tc0; }
+                if (tile + 1 >= t1) {
+                    // next segment of group g: its descriptor and headers were prefetched
+                    const int npos = pos + 1;
+                    if (g) pos1 = npos; else pos0 = npos;
+                    if (mg == g) {
+                        dcur = dnxt;
+                        dnxt = dnxt2;
+                        hcur = hnxt;
+                        dnxt2 = load_field(npos + 2);
+                    }
+                    if (g) tc1 = fld(dcur, 1, F_T0); else tc0 = fld(dcur, 0, F_T0);
+                    // headers of the new next segment (its descriptor is already in registers)
+                    const PenHdr h = load_hdr(dnxt);
+                    if (mg == g) hnxt = h;
+                }
+            }
+            if (!progressed) {
+                if (idle == 0) idle = globaltimer();
+                else if (globaltimer() - idle > kWaitNs) failed = true;
+                __nanosleep(128);
+            } else {
+                idle = 0;
             }
         }
-        // drain: wait (bounded) for the copies of the last stages to land before exiting
+        if (failed && lane == 0) atomicOr(&a.plan->pad[0], 1);
+        // drain: wait (bounded) for the last copies of each group to land before exiting
         if (lane == 0) {
-            for (int r = max(0, it - kStages); r < it; ++r)
-                mbar_wait_bounded(&sm.full[r % kStages], (r / kStages) & 1, kWaitLimit);
+            for (int r = max(0, iss0 - 2); r < iss0; ++r) wait_phase(&sm.full[0 + 2 * (r & 1)], (r >> 1) & 1);
+            for (int r = max(0, iss1 - 2); r < iss1; ++r) wait_phase(&sm.full[1 + 2 * (r & 1)], (r >> 1) & 1);
         }
         return;
     }
 
-    // ---------------- consumer warps
-    int it = 0;
-    for (int u = blockIdx.x; u < n_units; u += G, ++it) {
-        const int stage = it % kStages;
-        const unsigned parity = (it / kStages) & 1;
-        if (!mbar_wait_bounded(&sm.full[stage], parity, kWaitLimit)) { sm.error = 1; }
-        named_barrier_sync(2, kConsumerThreads);
-        if (sm.error) break;
-        const StageMeta m = sm.meta[stage];
-        const int cb = it & 1;
-        if (m.kind == kUnitX) process_x<SX>(a, sm, stage, m, cb);
-        else process_q(a, sm, stage, m, cb);
+    // ---------------- consumer group g: its segments, tile by tile
+    const int g = tid / kGroupThreads;
+    const int gt = tid - g * kGroupThreads;
+    GroupSmem& gs = sm.grp[g];
+    const int nseg = stream_len(S, G, c, g);
+    int cnt = 0;                                           // tiles consumed by this group
+    XState xs{};
+    QState qs{};
+    for (int sgi = 0; sgi < nseg && !gs.error; ++sgi) {
+        bool last = false;
+        while (!last) {
+            const int stage = g + 2 * (cnt & 1);
+            const unsigned parity = (cnt >> 1) & 1;
+            if (!wait_phase(&sm.full[stage], parity)) gs.error = 1;
+            group_sync(g);
+            if (gs.error) break;
+            const StageMeta m = sm.meta[stage];
+            last = m.last;
+            if (m.kind == kUnitX) {
+                const bool greedy = !(m.temperature > 0.f);
+                const int k = m.top_k;
+                XCtx<SX> ctx{a, sm, gs, g, stage, m, greedy, a.want_lp || a.n_top > 0, a.n_top > 0,
+                             !greedy && k > 0 && k < a.V && k <= kMaxCandTopK, !greedy && (k == 0 || k >= a.V),
+                             m.frequency, m.presence, (!greedy && (k == 0 || k >= a.V)) ? kL2E / m.temperature : 0.f};
+                x_tile<SX>(ctx, xs);
+                if (last) x_finish<SX>(ctx, xs);
+            } else {
+                q_tile(a, sm, gs, g, stage, m, qs);
+                if (last) q_finish(a, gs, g, m, qs);
+            }
+            ++cnt;
+        }
     }
-    if (threadIdx.x == 0 && sm.error) atomicOr(&a.plan->pad[0], 1);
+    if (gt == 0 && gs.error) atomicOr(&a.plan->pad[0], 1);
 }
 
 }  // namespace

@@ -39,6 +39,7 @@ def test_workspace_sizes(lib):
     assert w3 % 256 == 0
     # shapes out of range report 0
     assert bd.dspark_workspace_bytes(0, 8, 1000, "bf16") == 0
+    assert bd.dspark_workspace_bytes(2049, 8, 1000, "bf16") == 0
     assert bd.dspark_workspace_bytes(4, 65, 1000, "bf16") == 0
     assert bd.dspark_workspace_bytes(4, 8, (1 << 24) + 1, "bf16") == 0
     assert bd.dspark_workspace_bytes(4, 8, 1000, "bf16", 21) == 0
