@@ -142,7 +142,6 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     if (launch_stream_stats(a, s, sms) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_row_finalize(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
-    if (launch_full_threshold(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_accept(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_finish(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
@@ -272,6 +271,6 @@ const char* dspark_status_string(dspark_status_t status) {
     return "unknown status";
 }
 
-int32_t dspark_launches_per_call(void) { return 6; }
+int32_t dspark_launches_per_call(void) { return 5; }
 
 }  // extern "C"

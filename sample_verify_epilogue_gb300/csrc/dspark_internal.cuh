@@ -3,8 +3,8 @@
 // Data flow of one call (all on the caller's stream, no host synchronisation):
 //   prep_kernel          plan of work units + per-(request, vocab tile) penalty index
 //   stream_stats_kernel  the one HBM pass over x and q: per-tile maxima, sums and candidates
-//   row_finalize_kernel  per verify row: merge tiles, top-k threshold, nucleus, normaliser
-//   full_threshold_kernel  rows that need a threshold over the whole vocabulary (rare)
+//   row_finalize_kernel  per verify row: merge segments, top-k threshold, nucleus, normaliser
+//                        (rows needing a whole-vocabulary threshold get it in the same block)
 //   accept_kernel        per request: accept scan, residual / bonus draw over candidates
 //   finish_kernel        per request: whole-vocabulary draws (rare) and logprob outputs
 #pragma once
@@ -88,13 +88,13 @@ struct PenEntry {        // a token that may carry a penalty in this tile
 };
 struct PenHdr { int n; int overflow; int pad[2]; };
 
-// row modes written by row_finalize / full_threshold
+// row modes written by row_finalize
 enum RowMode : int {
     kModeInactive = 0,
     kModeGreedy = 1,
     kModeList = 2,       // truncated support held as a list (value-descending)
     kModeFull = 3,       // support = {t : value >= tau}, weights evaluated on the fly
-    kModeNeedFull = 4,   // full_threshold_kernel still has to set tau / Z
+    kModeNeedFull = 4,   // the whole-row path still has to set tau / Z
 };
 
 struct XRowOut {
@@ -352,6 +352,17 @@ __device__ __forceinline__ float warp_kth_largest(float v, int c) {
 }
 
 // ---------------------------------------------------------------- request validity
+// Status bits of the parameters alone (the draft ids are checked separately).
+__device__ __forceinline__ int params_status(const Args& a, const dspark_row_params_t& r) {
+    const bool t_ok = isfinite(r.temperature) && r.temperature >= 0.f;
+    const bool p_ok = r.top_p > 0.f && isfinite(r.top_p);
+    if (!t_ok || !p_ok || r.top_k < 0 || r.num_drafts < 0 || r.num_drafts > a.Km ||
+        !isfinite(r.presence_penalty) || !isfinite(r.frequency_penalty))
+        return DSPARK_ROW_BAD_PARAMS;
+    if (r.temperature > 0.f && r.num_drafts > 0 && a.q == nullptr) return DSPARK_ROW_BAD_PARAMS;
+    return 0;
+}
+
 // Status bits that follow from the parameters and the draft ids alone.
 __device__ __forceinline__ int request_status(const Args& a, int b) {
     const dspark_row_params_t r = a.rows[b];
@@ -377,7 +388,6 @@ __device__ __forceinline__ bool has_penalty(const dspark_row_params_t& r) {
 cudaError_t launch_prep(const Args& a, cudaStream_t s);
 cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid);
 cudaError_t launch_row_finalize(const Args& a, cudaStream_t s);
-cudaError_t launch_full_threshold(const Args& a, cudaStream_t s);
 cudaError_t launch_accept(const Args& a, cudaStream_t s);
 cudaError_t launch_finish(const Args& a, cudaStream_t s);
 

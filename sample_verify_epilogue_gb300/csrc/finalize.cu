@@ -1,17 +1,17 @@
 // row_finalize_kernel: one CTA per verify row (target position (b, j) or draft position
-// (b, i)).  Merges the per-tile statistics of the streaming pass and settles the row's
+// (b, i)).  Merges the per-segment statistics of the streaming pass and settles the row's
 // truncated distribution:
 //   - target rows: raw log-sum-exp (logprobs), penalised max and argmax (greedy), the top-k
-//     threshold tau_k = k-th largest penalised logit among the merged tile candidates (exact:
-//     every member of the row's top-k is a candidate of its own tile), the survivors
+//     threshold tau_k = k-th largest penalised logit among the merged segment candidates (exact:
+//     every member of the row's top-k is a candidate of its own segment), the survivors
 //     {x' >= tau_k} sorted by (value desc, id asc), their weights exp((x'-max)/T), and the
 //     nucleus: a survivor is kept iff the renormalised mass strictly above its value is
 //     < top_p (mlx-dspark Changelog, [0.1.0] Added, top-p / top-k on draft and target;
 //     [0.20.2] Changed, selection instead of a full vocabulary sort);
 //   - draft rows: the same with q as the key and (q/qmax)^(1/T) as the weight.
 // Rows whose support is not a short list (no top-k, or more survivors than fit) keep a
-// threshold and a normaliser instead; full_threshold_kernel finishes those that still need
-// a whole-row threshold.
+// threshold and a normaliser instead; those that still need a whole-row threshold get it in
+// the same block from the whole-row path below.
 #include "block_utils.cuh"
 
 namespace dspark {
@@ -31,6 +31,7 @@ struct FinSmem {
     unsigned long long sk[kKeptCap];   // survivors: (key << 32) | (0xFFFFFFFF - id)
     double w[kKeptCap];
     int off[kMaxSegs + 1];             // candidate offsets per segment
+    int whist[kFinThreads / 32][256];  // per-warp radix histograms
     int hist[256];
     int bcast[4];
     double dwarp[33];
@@ -95,13 +96,25 @@ __device__ uint32_t kth_largest(FinSmem& s, const CandSet& cs, int k) {
     const int tid = threadIdx.x;
     uint32_t prefix = 0, pmask = 0;
     int kk = k;
+    const int warp = tid >> 5, lane = tid & 31;
+    int* wh = s.whist[warp];
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += blockDim.x) s.hist[i] = 0;
+        for (int i = tid; i < (kFinThreads / 32) * 256; i += blockDim.x) (&s.whist[0][0])[i] = 0;
         __syncthreads();
+        // keys of one row share their top bits, so lanes are grouped by bin before the atomic
         for_each_key(s, cs, [&](uint32_t key) {
-            if ((key & pmask) == prefix) atomicAdd(&s.hist[(key >> shift) & 255u], 1);
+            const unsigned bin = ((key & pmask) == prefix) ? ((key >> shift) & 255u) : 0xFFFFFFFFu;
+            const unsigned grp = __match_any_sync(__activemask(), bin);
+            if (bin != 0xFFFFFFFFu && lane == __ffs(grp) - 1) atomicAdd(&wh[bin], __popc(grp));
         });
+        __syncthreads();
+        for (int i = tid; i < 256; i += blockDim.x) {
+            int t = 0;
+#pragma unroll
+            for (int w = 0; w < kFinThreads / 32; ++w) t += s.whist[w][i];
+            s.hist[i] = t;
+        }
         __syncthreads();
         if (tid < 32) {
             int c[8], sum = 0;
@@ -180,217 +193,14 @@ __device__ int nucleus(FinSmem& s, int cnt, float top_p, double* zkept) {
     return kept;
 }
 
-__device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
-    const int tid = threadIdx.x;
-    const dspark_row_params_t r = a.rows[b];
-    const int nseg = a.nseg_x;
-    const TileStats* ts = a.ts_x + static_cast<long long>(slot) * nseg;
-    XRowOut o{};
-    o.mode = kModeInactive;
-    float mr = -INFINITY, mp = -INFINITY;
-    int fl = 0;
-    for (int t = tid; t < nseg; t += blockDim.x) {
-        const TileStats x = ts[t];
-        mr = (mr != mr || x.m_raw != x.m_raw) ? __int_as_float(0x7fc00000) : fmaxf(mr, x.m_raw);
-        mp = (mp != mp || x.m_pen != x.m_pen) ? __int_as_float(0x7fc00000) : fmaxf(mp, x.m_pen);
-        fl |= x.flags;
-    }
-    mr = block_max_nan(mr, s.fwarp);
-    mp = block_max_nan(mp, s.fwarp);
-    fl = block_or_i(fl, s.iwarp);
-    if ((fl & kTileBad) || !isfinite(mr) || !isfinite(mp)) {
-        if (tid == 0) {
-            atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
-            a.xout[slot] = o;
-        }
-        return;
-    }
-    int arg = 0x7FFFFFFF;
-    double sraw = 0.0, stemp = 0.0;
-    const bool greedy = !(r.temperature > 0.f);
-    const float c_l2e = greedy ? 0.f : kL2E / r.temperature;
-    for (int t = tid; t < nseg; t += blockDim.x) {
-        const TileStats x = ts[t];
-        if (x.m_pen == mp) arg = min(arg, x.arg_pen);
-        sraw += static_cast<double>(x.s_raw) * exp2(static_cast<double>(x.m_raw - mr) * kL2E);
-        if (!greedy) stemp += static_cast<double>(x.s_temp) * exp2(static_cast<double>(x.m_pen - mp) * c_l2e);
-    }
-    arg = block_min_i(arg, s.iwarp);
-    sraw = block_sum_d(sraw, s.dwarp);
-    stemp = block_sum_d(stemp, s.dwarp);
-    o.argmax = arg;
-    o.m_pen = mp;
-    o.lse = mr + static_cast<float>(log(sraw));
-    o.c_l2e = c_l2e;
-    o.top_p = r.top_p;
-    o.tau = -INFINITY;
-    o.top_k = 0;
-    o.n_kept = 0;
-    o.flags = fl;
-    const int k = r.top_k;
-    if (greedy) {
-        o.mode = kModeGreedy;
-    } else if (k > 0 && k < a.V) {
-        CandSet cs{nullptr, 0, 0, -1};
-        if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
-            cs = stage_candidates(s, ts, a.cand_x + static_cast<long long>(slot) * nseg * kCandPenGlobal,
-                                  kCandPenGlobal, nseg, false);
-        if (cs.total >= k) {
-            const uint32_t kth = kth_largest(s, cs, k);
-            const int cnt = sorted_survivors(s, cs, kth);
-            if (cnt > 0) {
-                for (int i = tid; i < cnt; i += blockDim.x)
-                    s.w[i] = static_cast<double>(target_weight(ckey_v(s.sk[i]), mp, c_l2e));
-                __syncthreads();
-                double zk;
-                const int kept = nucleus(s, cnt, r.top_p, &zk);
-                KeptEntry* dst = a.kept + static_cast<long long>(slot) * kKeptCap;
-                for (int i = tid; i < kept; i += blockDim.x) dst[i] = KeptEntry{ckey_id(s.sk[i]), static_cast<float>(s.w[i])};
-                o.mode = kModeList;
-                o.n_kept = kept;
-                o.Z = zk;
-                o.tau = ckey_v(s.sk[kept - 1]);
-            } else {
-                o.mode = kModeNeedFull;                       // too many survivors: threshold known
-                o.tau = key_to_f(kth);
-            }
-        } else {
-            o.mode = kModeNeedFull;                           // select over the whole row
-            o.top_k = k;
-        }
-        __syncthreads();
-    } else {
-        o.Z = stemp;
-        o.mode = (r.top_p < 1.f) ? kModeNeedFull : kModeFull;
-    }
-    // raw top-n for top_logprobs
-    if (a.n_top > 0) {
-        bool done = false;
-        if (!(fl & kTileOverflowRaw)) {
-            const CandSet cs = stage_candidates(s, ts, a.cand_raw + static_cast<long long>(slot) * nseg * kCandRawGlobal,
-                                                kCandRawGlobal, nseg, true);
-            const int nt = min(a.n_top, a.V);
-            if (cs.total >= nt) {
-                const uint32_t kth = kth_largest(s, cs, nt);
-                const int cnt = sorted_survivors(s, cs, kth);
-                if (cnt >= nt) {
-                    TopEntry* dst = a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS;
-                    for (int i = tid; i < nt; i += blockDim.x) dst[i] = TopEntry{ckey_id(s.sk[i]), ckey_v(s.sk[i])};
-                    done = true;
-                }
-            }
-        }
-        if (!done) o.flags |= kTileOverflowRaw;               // full_threshold_kernel fills the list
-    }
-    __syncthreads();
-    if (tid == 0) a.xout[slot] = o;
-}
-
-__device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
-    const int tid = threadIdx.x;
-    const dspark_row_params_t r = a.rows[b];
-    const int nseg = a.nseg_q;
-    const TileStats* ts = a.ts_q + static_cast<long long>(qslot) * nseg;
-    QRowOut o{};
-    o.mode = kModeInactive;
-    float qmax = -INFINITY;
-    int fl = 0;
-    for (int t = tid; t < nseg; t += blockDim.x) {
-        const TileStats x = ts[t];
-        qmax = (qmax != qmax || x.m_raw != x.m_raw) ? __int_as_float(0x7fc00000) : fmaxf(qmax, x.m_raw);
-        fl |= x.flags;
-    }
-    qmax = block_max_nan(qmax, s.fwarp);
-    fl = block_or_i(fl, s.iwarp);
-    const bool t_one = r.temperature == 1.f;
-    const float inv_t = 1.f / r.temperature;
-    double z = 0.0;
-    for (int t = tid; t < nseg; t += blockDim.x) {
-        const TileStats x = ts[t];
-        if (t_one) z += static_cast<double>(x.s_raw);
-        else if (x.m_raw > 0.f) z += static_cast<double>(x.s_temp) * exp2(static_cast<double>(inv_t) * log2(static_cast<double>(x.m_raw) / qmax));
-    }
-    z = block_sum_d(z, s.dwarp);
-    if ((fl & kTileBad) || !(qmax > 0.f) || !isfinite(qmax)) {
-        if (tid == 0) { atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE); a.qout[qslot] = o; }
-        return;
-    }
-    o.qmax = qmax;
-    o.inv_t = inv_t;
-    o.tau = -INFINITY;
-    o.top_k = 0;
-    o.top_p = r.top_p;
-    o.flags = fl;
-    const int k = r.top_k;
-    if (k > 0 && k < a.V) {
-        CandSet cs{nullptr, 0, 0, -1};
-        if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
-            cs = stage_candidates(s, ts, a.cand_q + static_cast<long long>(qslot) * nseg * kCandPenGlobal,
-                                  kCandPenGlobal, nseg, false);
-        if (cs.total >= k) {
-            const uint32_t kth = kth_largest(s, cs, k);
-            const int cnt = sorted_survivors(s, cs, kth);
-            if (cnt > 0) {
-                for (int e = tid; e < cnt; e += blockDim.x)
-                    s.w[e] = static_cast<double>(draft_weight(ckey_v(s.sk[e]), qmax, inv_t, t_one));
-                __syncthreads();
-                double zk;
-                const int kept = nucleus(s, cnt, r.top_p, &zk);
-                o.mode = kModeList;
-                o.Z = zk;
-                o.tau = ckey_v(s.sk[kept - 1]);
-            } else {
-                o.mode = kModeNeedFull;
-                o.tau = key_to_f(kth);
-            }
-        } else {
-            o.mode = kModeNeedFull;
-            o.top_k = k;
-        }
-    } else {
-        o.Z = z;
-        o.mode = (r.top_p < 1.f) ? kModeNeedFull : kModeFull;
-        if (o.mode == kModeFull && !(z > 0.0)) {
-            if (tid == 0) atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
-        }
-    }
-    __syncthreads();
-    if (tid == 0) a.qout[qslot] = o;
-}
-
-__global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(Args a) {
-    extern __shared__ __align__(16) unsigned char fin_raw[];
-    FinSmem& s = *reinterpret_cast<FinSmem*>(fin_raw);
-    const int slot = blockIdx.x;
-    if (slot < a.xslots) {
-        const int b = slot / (a.Km + 1), j = slot % (a.Km + 1);
-        if ((request_status(a, b) & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || j > a.rows[b].num_drafts) {
-            if (threadIdx.x == 0) { XRowOut o{}; o.mode = kModeInactive; a.xout[slot] = o; }
-            return;
-        }
-        finalize_x(a, s, slot, b, j);
-    } else {
-        const int qs = slot - a.xslots;
-        const int b = qs / a.Km, i = qs % a.Km;
-        const dspark_row_params_t r = a.rows[b];
-        if ((request_status(a, b) & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || i >= r.num_drafts ||
-            !(r.temperature > 0.f)) {
-            if (threadIdx.x == 0) { QRowOut o{}; o.mode = kModeInactive; a.qout[qs] = o; }
-            return;
-        }
-        finalize_q(a, s, qs, b, i);
-    }
-}
-
 // ============================================================================ whole-row path
-// full_threshold_kernel: rows whose top-k threshold or nucleus cannot come from candidates
+// Whole-row path: rows whose top-k threshold or nucleus cannot come from candidates
 // (top_k = 0 with top_p < 1, top_k above the candidate limit, tie-heavy rows that overflow
 // the candidate buffers) get an exact whole-row selection here: radix passes over the
 // order-preserving key with count histograms (top-k, top-n) and with fixed-point mass
 // histograms (nucleus), re-reading the row once per pass.  Fixed-point masses make the
 // sums independent of the order of the atomic additions.
 
-constexpr int kFullThreads = 1024;
 constexpr double kFix = 274877906944.0;         // 2^38
 
 struct FullSmem {
@@ -624,85 +434,260 @@ __device__ void full_topn(FullSmem& s, const RowSource& src, int nt, TopEntry* d
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kFullThreads) full_threshold_kernel(Args a) {
-    extern __shared__ __align__(16) unsigned char full_raw[];
-    FullSmem& s = *reinterpret_cast<FullSmem*>(full_raw);
-    const int slot = blockIdx.x;
-    const int tid = threadIdx.x;
-    if (slot < a.xslots) {
-        XRowOut o = a.xout[slot];
-        const bool need_top = (o.mode != kModeInactive) && a.n_top > 0 && (o.flags & kTileOverflowRaw);
-        if (o.mode != kModeNeedFull && !need_top) return;
-        const int b = slot / (a.Km + 1), j = slot % (a.Km + 1);
-        const dspark_row_params_t r = a.rows[b];
-        RowSource src{&a, true, static_cast<long long>(slot) * a.V, b, j, r.frequency_penalty, r.presence_penalty,
-                      has_penalty(r)};
-        if (need_top) full_topn(s, src, min(a.n_top, a.V), a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS);
-        if (o.mode == kModeNeedFull) {
-            uint32_t floor_key = fkey(o.tau);
-            if (o.top_k > 0) floor_key = full_kth(s, src, o.top_k, false);
-            const float mp = o.m_pen, c = o.c_l2e;
-            double z;
-            if (o.top_p < 1.f) {
-                const uint32_t kk = full_nucleus(s, src, floor_key, o.top_p,
-                                                 [&](float v) { return target_weight(v, mp, c); }, &z);
-                o.tau = key_to_f(kk);
-            } else {
-                const uint32_t kk = full_nucleus(s, src, floor_key, 2.f,
-                                                 [&](float v) { return target_weight(v, mp, c); }, &z);
-                (void)kk;
-                o.tau = key_to_f(floor_key);
-            }
-            o.Z = z;
-            o.top_k = 0;
-            o.mode = kModeFull;
-        }
-        if (tid == 0) a.xout[slot] = o;
-    } else {
-        const int qs = slot - a.xslots;
-        QRowOut o = a.qout[qs];
-        if (o.mode != kModeNeedFull) return;
-        const int b = qs / a.Km, i = qs % a.Km;
-        RowSource src{&a, false, static_cast<long long>(qs) * a.V, b, i, 0.f, 0.f, false};
+// Whole-row selection for a target row whose support could not come from candidates;
+// updates o (threshold, normaliser, mode) and, when its candidate list overflowed, the
+// raw top-n list.
+__device__ void whole_row_x(const Args& a, FullSmem& s, int slot, int b, int j, XRowOut& o) {
+    const dspark_row_params_t r = a.rows[b];
+    RowSource src{&a, true, static_cast<long long>(slot) * a.V, b, j, r.frequency_penalty, r.presence_penalty,
+                  has_penalty(r)};
+    const bool need_top = a.n_top > 0 && (o.flags & kTileOverflowRaw);
+    if (need_top) full_topn(s, src, min(a.n_top, a.V), a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS);
+    if (o.mode == kModeNeedFull) {
         uint32_t floor_key = fkey(o.tau);
         if (o.top_k > 0) floor_key = full_kth(s, src, o.top_k, false);
-        const float qmax = o.qmax, inv_t = o.inv_t;
-        const bool t_one = inv_t == 1.f;
+        const float mp = o.m_pen, c = o.c_l2e;
         double z;
-        if (o.top_p < 1.f) {
-            const uint32_t kk = full_nucleus(s, src, floor_key, o.top_p,
-                                             [&](float v) { return draft_weight(v, qmax, inv_t, t_one) / (t_one ? qmax : 1.f); }, &z);
-            o.tau = key_to_f(kk);
-        } else {
-            full_nucleus(s, src, floor_key, 2.f,
-                         [&](float v) { return draft_weight(v, qmax, inv_t, t_one) / (t_one ? qmax : 1.f); }, &z);
-            o.tau = key_to_f(floor_key);
-        }
-        if (t_one) z *= qmax;
+        const uint32_t kk = full_nucleus(s, src, floor_key, o.top_p < 1.f ? o.top_p : 2.f,
+                                         [&](float v) { return target_weight(v, mp, c); }, &z);
+        o.tau = (o.top_p < 1.f) ? key_to_f(kk) : key_to_f(floor_key);
         o.Z = z;
         o.top_k = 0;
         o.mode = kModeFull;
-        if (!(z > 0.0) && tid == 0) atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
-        if (tid == 0) a.qout[qs] = o;
+    }
+}
+
+__device__ void whole_row_q(const Args& a, FullSmem& s, int qs, int b, int i, QRowOut& o) {
+    RowSource src{&a, false, static_cast<long long>(qs) * a.V, b, i, 0.f, 0.f, false};
+    uint32_t floor_key = fkey(o.tau);
+    if (o.top_k > 0) floor_key = full_kth(s, src, o.top_k, false);
+    const float qmax = o.qmax, inv_t = o.inv_t;
+    const bool t_one = inv_t == 1.f;
+    double z;
+    const uint32_t kk = full_nucleus(s, src, floor_key, o.top_p < 1.f ? o.top_p : 2.f,
+                                     [&](float v) { return draft_weight(v, qmax, inv_t, t_one) / (t_one ? qmax : 1.f); }, &z);
+    o.tau = (o.top_p < 1.f) ? key_to_f(kk) : key_to_f(floor_key);
+    if (t_one) z *= qmax;
+    o.Z = z;
+    o.top_k = 0;
+    o.mode = kModeFull;
+    if (!(z > 0.0) && threadIdx.x == 0) atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
+}
+
+__device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
+    const int tid = threadIdx.x;
+    const dspark_row_params_t r = a.rows[b];
+    const int nseg = a.nseg_x;
+    const TileStats* ts = a.ts_x + static_cast<long long>(slot) * nseg;
+    XRowOut o{};
+    o.mode = kModeInactive;
+    float mr = -INFINITY, mp = -INFINITY;
+    int fl = 0;
+    for (int t = tid; t < nseg; t += blockDim.x) {
+        const TileStats x = ts[t];
+        mr = (mr != mr || x.m_raw != x.m_raw) ? __int_as_float(0x7fc00000) : fmaxf(mr, x.m_raw);
+        mp = (mp != mp || x.m_pen != x.m_pen) ? __int_as_float(0x7fc00000) : fmaxf(mp, x.m_pen);
+        fl |= x.flags;
+    }
+    mr = block_max_nan(mr, s.fwarp);
+    mp = block_max_nan(mp, s.fwarp);
+    fl = block_or_i(fl, s.iwarp);
+    if ((fl & kTileBad) || !isfinite(mr) || !isfinite(mp)) {
+        if (tid == 0) {
+            atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
+            a.xout[slot] = o;
+        }
+        return;
+    }
+    int arg = 0x7FFFFFFF;
+    double sraw = 0.0, stemp = 0.0;
+    const bool greedy = !(r.temperature > 0.f);
+    const float c_l2e = greedy ? 0.f : kL2E / r.temperature;
+    for (int t = tid; t < nseg; t += blockDim.x) {
+        const TileStats x = ts[t];
+        if (x.m_pen == mp) arg = min(arg, x.arg_pen);
+        sraw += static_cast<double>(x.s_raw) * exp2(static_cast<double>(x.m_raw - mr) * kL2E);
+        if (!greedy) stemp += static_cast<double>(x.s_temp) * exp2(static_cast<double>(x.m_pen - mp) * c_l2e);
+    }
+    arg = block_min_i(arg, s.iwarp);
+    sraw = block_sum_d(sraw, s.dwarp);
+    stemp = block_sum_d(stemp, s.dwarp);
+    o.argmax = arg;
+    o.m_pen = mp;
+    o.lse = mr + static_cast<float>(log(sraw));
+    o.c_l2e = c_l2e;
+    o.top_p = r.top_p;
+    o.tau = -INFINITY;
+    o.top_k = 0;
+    o.n_kept = 0;
+    o.flags = fl;
+    const int k = r.top_k;
+    if (greedy) {
+        o.mode = kModeGreedy;
+    } else if (k > 0 && k < a.V) {
+        CandSet cs{nullptr, 0, 0, -1};
+        if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
+            cs = stage_candidates(s, ts, a.cand_x + static_cast<long long>(slot) * nseg * kCandPenGlobal,
+                                  kCandPenGlobal, nseg, false);
+        if (cs.total >= k) {
+            const uint32_t kth = kth_largest(s, cs, k);
+            const int cnt = sorted_survivors(s, cs, kth);
+            if (cnt > 0) {
+                for (int i = tid; i < cnt; i += blockDim.x)
+                    s.w[i] = static_cast<double>(target_weight(ckey_v(s.sk[i]), mp, c_l2e));
+                __syncthreads();
+                double zk;
+                const int kept = nucleus(s, cnt, r.top_p, &zk);
+                KeptEntry* dst = a.kept + static_cast<long long>(slot) * kKeptCap;
+                for (int i = tid; i < kept; i += blockDim.x) dst[i] = KeptEntry{ckey_id(s.sk[i]), static_cast<float>(s.w[i])};
+                o.mode = kModeList;
+                o.n_kept = kept;
+                o.Z = zk;
+                o.tau = ckey_v(s.sk[kept - 1]);
+            } else {
+                o.mode = kModeNeedFull;                       // too many survivors: threshold known
+                o.tau = key_to_f(kth);
+            }
+        } else {
+            o.mode = kModeNeedFull;                           // select over the whole row
+            o.top_k = k;
+        }
+        __syncthreads();
+    } else {
+        o.Z = stemp;
+        o.mode = (r.top_p < 1.f) ? kModeNeedFull : kModeFull;
+    }
+    // raw top-n for top_logprobs
+    if (a.n_top > 0) {
+        bool done = false;
+        if (!(fl & kTileOverflowRaw)) {
+            const CandSet cs = stage_candidates(s, ts, a.cand_raw + static_cast<long long>(slot) * nseg * kCandRawGlobal,
+                                                kCandRawGlobal, nseg, true);
+            const int nt = min(a.n_top, a.V);
+            if (cs.total >= nt) {
+                const uint32_t kth = kth_largest(s, cs, nt);
+                const int cnt = sorted_survivors(s, cs, kth);
+                if (cnt >= nt) {
+                    TopEntry* dst = a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS;
+                    for (int i = tid; i < nt; i += blockDim.x) dst[i] = TopEntry{ckey_id(s.sk[i]), ckey_v(s.sk[i])};
+                    done = true;
+                }
+            }
+        }
+        if (!done) o.flags |= kTileOverflowRaw;               // the whole-row path fills the list
+    }
+    __syncthreads();
+    if (o.mode == kModeNeedFull || (a.n_top > 0 && (o.flags & kTileOverflowRaw)))
+        whole_row_x(a, *reinterpret_cast<FullSmem*>(&s), slot, b, j, o);
+    if (tid == 0) a.xout[slot] = o;
+}
+
+__device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
+    const int tid = threadIdx.x;
+    const dspark_row_params_t r = a.rows[b];
+    const int nseg = a.nseg_q;
+    const TileStats* ts = a.ts_q + static_cast<long long>(qslot) * nseg;
+    QRowOut o{};
+    o.mode = kModeInactive;
+    float qmax = -INFINITY;
+    int fl = 0;
+    for (int t = tid; t < nseg; t += blockDim.x) {
+        const TileStats x = ts[t];
+        qmax = (qmax != qmax || x.m_raw != x.m_raw) ? __int_as_float(0x7fc00000) : fmaxf(qmax, x.m_raw);
+        fl |= x.flags;
+    }
+    qmax = block_max_nan(qmax, s.fwarp);
+    fl = block_or_i(fl, s.iwarp);
+    const bool t_one = r.temperature == 1.f;
+    const float inv_t = 1.f / r.temperature;
+    double z = 0.0;
+    for (int t = tid; t < nseg; t += blockDim.x) {
+        const TileStats x = ts[t];
+        if (t_one) z += static_cast<double>(x.s_raw);
+        else if (x.m_raw > 0.f) z += static_cast<double>(x.s_temp) * exp2(static_cast<double>(inv_t) * log2(static_cast<double>(x.m_raw) / qmax));
+    }
+    z = block_sum_d(z, s.dwarp);
+    if ((fl & kTileBad) || !(qmax > 0.f) || !isfinite(qmax)) {
+        if (tid == 0) { atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE); a.qout[qslot] = o; }
+        return;
+    }
+    o.qmax = qmax;
+    o.inv_t = inv_t;
+    o.tau = -INFINITY;
+    o.top_k = 0;
+    o.top_p = r.top_p;
+    o.flags = fl;
+    const int k = r.top_k;
+    if (k > 0 && k < a.V) {
+        CandSet cs{nullptr, 0, 0, -1};
+        if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
+            cs = stage_candidates(s, ts, a.cand_q + static_cast<long long>(qslot) * nseg * kCandPenGlobal,
+                                  kCandPenGlobal, nseg, false);
+        if (cs.total >= k) {
+            const uint32_t kth = kth_largest(s, cs, k);
+            const int cnt = sorted_survivors(s, cs, kth);
+            if (cnt > 0) {
+                for (int e = tid; e < cnt; e += blockDim.x)
+                    s.w[e] = static_cast<double>(draft_weight(ckey_v(s.sk[e]), qmax, inv_t, t_one));
+                __syncthreads();
+                double zk;
+                const int kept = nucleus(s, cnt, r.top_p, &zk);
+                o.mode = kModeList;
+                o.Z = zk;
+                o.tau = ckey_v(s.sk[kept - 1]);
+            } else {
+                o.mode = kModeNeedFull;
+                o.tau = key_to_f(kth);
+            }
+        } else {
+            o.mode = kModeNeedFull;
+            o.top_k = k;
+        }
+    } else {
+        o.Z = z;
+        o.mode = (r.top_p < 1.f) ? kModeNeedFull : kModeFull;
+        if (o.mode == kModeFull && !(z > 0.0)) {
+            if (tid == 0) atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
+        }
+    }
+    __syncthreads();
+    if (o.mode == kModeNeedFull) whole_row_q(a, *reinterpret_cast<FullSmem*>(&s), qslot, b, i, o);
+    if (tid == 0) a.qout[qslot] = o;
+}
+
+__global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(Args a) {
+    extern __shared__ __align__(16) unsigned char fin_raw[];
+    FinSmem& s = *reinterpret_cast<FinSmem*>(fin_raw);
+    const int slot = blockIdx.x;
+    if (slot < a.xslots) {
+        const int b = slot / (a.Km + 1), j = slot % (a.Km + 1);
+        if ((request_status(a, b) & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || j > a.rows[b].num_drafts) {
+            if (threadIdx.x == 0) { XRowOut o{}; o.mode = kModeInactive; a.xout[slot] = o; }
+            return;
+        }
+        finalize_x(a, s, slot, b, j);
+    } else {
+        const int qs = slot - a.xslots;
+        const int b = qs / a.Km, i = qs % a.Km;
+        const dspark_row_params_t r = a.rows[b];
+        if ((request_status(a, b) & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || i >= r.num_drafts ||
+            !(r.temperature > 0.f)) {
+            if (threadIdx.x == 0) { QRowOut o{}; o.mode = kModeInactive; a.qout[qs] = o; }
+            return;
+        }
+        finalize_q(a, s, qs, b, i);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_row_finalize(const Args& a, cudaStream_t s) {
-    const size_t smem = sizeof(FinSmem);
+    const size_t smem = sizeof(FinSmem) > sizeof(FullSmem) ? sizeof(FinSmem) : sizeof(FullSmem);
     cudaError_t e = cudaFuncSetAttribute(row_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     row_finalize_kernel<<<a.xslots + a.qslots, kFinThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_full_threshold(const Args& a, cudaStream_t s) {
-    const size_t smem = sizeof(FullSmem);
-    cudaError_t e = cudaFuncSetAttribute(full_threshold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    full_threshold_kernel<<<a.xslots + a.qslots, kFullThreads, smem, s>>>(a);
-    return cudaGetLastError();
-}
 
 }  // namespace dspark

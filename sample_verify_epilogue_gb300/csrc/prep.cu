@@ -106,54 +106,80 @@ __device__ void plan_block(const Args& a) {
     }
 }
 
-// First index in ids[lo, hi) with ids[idx] >= key, by a block-wide 256-way narrowing.
-__device__ int block_lower_bound(const int* ids, int lo, int hi, int key, int* s_tmp) {
+// First indices in ids[lo, hi) with ids[idx] >= key0 and >= key1 (key0 <= key1), by a
+// block-wide 256-way narrowing of both ranges at once.
+__device__ void block_lower_bound2(const int* ids, int lo, int hi, int key0, int key1, int& r0, int& r1) {
     const int tid = threadIdx.x;
-    while (hi - lo > 1) {
-        const int len = hi - lo;
-        const int step = (len + kPrepThreads - 1) / kPrepThreads;
-        const int p = lo + tid * step;
-        const int pred = (p < hi) && (__ldg(ids + p) < key);
-        const int cnt = __syncthreads_count(pred);   // preds form a prefix (ids ascending)
-        if (cnt == 0) return lo;
-        const int nlo = lo + (cnt - 1) * step;       // ids[nlo] < key
-        const int nhi = min(hi, nlo + step);
-        if (step == 1) return nlo + 1;
-        lo = nlo + 1;                                // ids[nlo] < key is known
-        hi = nhi;
-        if (lo >= hi) return lo;
-        (void)s_tmp;
+    int lo0 = lo, hi0 = hi, lo1 = lo, hi1 = hi;
+    // each range is narrowed until it is empty; the answer is then its lo
+    while (hi0 > lo0 || hi1 > lo1) {
+        const int len0 = hi0 - lo0, len1 = hi1 - lo1;
+        const int st0 = max(1, (len0 + kPrepThreads - 1) / kPrepThreads);
+        const int st1 = max(1, (len1 + kPrepThreads - 1) / kPrepThreads);
+        const int p0 = lo0 + tid * st0, p1 = lo1 + tid * st1;
+        const int v0 = (len0 > 0 && p0 < hi0) ? __ldg(ids + p0) : 0;
+        const int v1 = (len1 > 0 && p1 < hi1) ? __ldg(ids + p1) : 0;
+        const int c0 = __syncthreads_count(len0 > 0 && p0 < hi0 && v0 < key0);
+        const int c1 = __syncthreads_count(len1 > 0 && p1 < hi1 && v1 < key1);
+        // predicates form a prefix (ids ascending): ids[lo + (c-1)*st] < key <= ids[lo + c*st]
+        if (len0 > 0) {
+            if (c0 == 0) hi0 = lo0;
+            else { const int nl = lo0 + (c0 - 1) * st0 + 1; hi0 = min(hi0, lo0 + c0 * st0); lo0 = nl; }
+        }
+        if (len1 > 0) {
+            if (c1 == 0) hi1 = lo1;
+            else { const int nl = lo1 + (c1 - 1) * st1 + 1; hi1 = min(hi1, lo1 + c1 * st1); lo1 = nl; }
+        }
     }
-    if (hi - lo == 1) return (__ldg(ids + lo) < key) ? hi : lo;
-    return lo;
+    r0 = lo0;
+    r1 = lo1;
 }
 
 __device__ void penalty_index_block(const Args& a, int b, int t) {
     __shared__ unsigned s_bm[kBitmapWordsMax];
     __shared__ PenEntry s_ent[kPenCap];
-    __shared__ int s_n, s_nh, s_over, s_tmp[4];
+    __shared__ int s_d[DSPARK_MAX_K];
+    __shared__ dspark_row_params_t s_r;
+    __shared__ int s_hlo, s_hhi, s_n, s_nh, s_over, s_bad;
     const int tid = threadIdx.x;
-    if (request_status(a, b) != 0) return;
-    const dspark_row_params_t r = a.rows[b];
+    // one round trip for the parameters, the drafts and the history bounds
+    if (tid == 0) s_r = a.rows[b];
+    if (tid == 32) { s_hlo = a.h_off ? a.h_off[b] : 0; s_hhi = a.h_off ? a.h_off[b + 1] : 0; }
+    if (tid >= 64 && tid < 64 + a.Km) s_d[tid - 64] = a.d[static_cast<long long>(b) * a.Km + (tid - 64)];
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    const dspark_row_params_t r = s_r;
     const int K = r.num_drafts;
+    if (params_status(a, r) != 0) return;
+    for (int i = tid; i < K; i += kPrepThreads) if (s_d[i] < 0 || s_d[i] >= a.V) s_bad = 1;
+    __syncthreads();
+    if (s_bad) return;
     const int e0 = t * a.tile_x, e1 = min(a.V, e0 + a.tile_x);
-    const int hlo = a.h_off ? a.h_off[b] : 0, hhi = a.h_off ? a.h_off[b + 1] : 0;
+    const int hlo = s_hlo, hhi = s_hhi;
     // history validation (once per request): ascending ids in range, positive counts
     if (t == 0 && hhi > hlo) {
         int bad = 0;
-        for (int k = hlo + tid; k < hhi; k += kPrepThreads) {
-            const int id = a.h_ids[k];
-            if (id < 0 || id >= a.V || a.h_cnt[k] <= 0 || (k > hlo && a.h_ids[k - 1] >= id)) bad = 1;
+        for (int k0 = hlo + tid; k0 < hhi; k0 += 4 * kPrepThreads) {
+            int id[4], pv[4], cn[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {            // four independent loads in flight
+                const int k = k0 + u * kPrepThreads;
+                id[u] = k < hhi ? a.h_ids[k] : 0;
+                pv[u] = (k < hhi && k > hlo) ? a.h_ids[k - 1] : -1;
+                cn[u] = k < hhi ? a.h_cnt[k] : 1;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int k = k0 + u * kPrepThreads;
+                if (k < hhi && (id[u] < 0 || id[u] >= a.V || cn[u] <= 0 || pv[u] >= id[u])) bad = 1;
+            }
         }
         if (__syncthreads_or(bad) && tid == 0) atomicOr(&a.row_status[b], DSPARK_ROW_BAD_HISTORY);
     }
     if (!has_penalty(r)) return;
     for (int w = tid; w < a.bm_words; w += kPrepThreads) s_bm[w] = 0u;
     int h0 = hlo, h1 = hlo;
-    if (hhi > hlo) {
-        h0 = block_lower_bound(a.h_ids, hlo, hhi, e0, s_tmp);
-        h1 = block_lower_bound(a.h_ids, h0, hhi, e1, s_tmp);
-    }
+    if (hhi > hlo) block_lower_bound2(a.h_ids, hlo, hhi, e0, e1, h0, h1);
     const int nh = h1 - h0;
     if (tid == 0) { s_nh = min(nh, kPenCap); s_over = nh > kPenCap; }
     __syncthreads();
@@ -163,14 +189,13 @@ __device__ void penalty_index_block(const Args& a, int b, int t) {
         if (id >= e0 && id < e1) atomicOr(&s_bm[(id - e0) >> 5], 1u << ((id - e0) & 31));
     }
     __syncthreads();
-    // draft tokens in this tile: serial over positions (K <= 64), in order
+    // draft tokens in this tile: serial over positions (K <= 64), in order, all in shared memory
     if (tid == 0) {
         int n = s_nh;
         for (int i = 0; i < K; ++i) {
-            const int tok = a.d[static_cast<long long>(b) * a.Km + i];
+            const int tok = s_d[i];
             if (tok < e0 || tok >= e1) continue;
             int base = 0, slot = -1;
-            // history part (sorted): binary search in shared memory, or global when it overflowed
             if (!s_over) {
                 int l = 0, h = s_nh;
                 while (l < h) { const int m = (l + h) >> 1; if (s_ent[m].token < tok) l = m + 1; else h = m; }

@@ -45,6 +45,7 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, unsigned parity) {
 }
 constexpr float kL2E = 1.4426950408889634f;
 constexpr int kVecPerThread = kStageBytes / 16 / kGroupThreads;     // 10 vectors per thread and tile
+static_assert(kVecPerThread % 2 == 0, "vectors are scanned in pairs");
 
 struct StageMeta {
     int kind, slot, b, j;
@@ -420,6 +421,129 @@ __device__ __forceinline__ void x_vec_overflow(const XCtx<SX>& c, XState& st, co
     }
 }
 
+// Specialised scan of one tile for the common row types: compile-time flags, no per-vector
+// tests of the row's options.  LP: raw log-sum-exp; RAW: raw top-n candidates; CAND: top-k
+// candidates of the penalised logits (sampled rows); GREEDY: penalised argmax; PEN: the row
+// has penalty bits.  Raw sums go to two f32x2 accumulators (even / odd vectors).
+template <int SX>
+__device__ __forceinline__ uint4 neg_inf_vec() {
+    const uint32_t ni = SX == 2 ? 0xFF80FF80u : 0xFF800000u;
+    return make_uint4(ni, ni, ni, ni);
+}
+
+// Fold one vector's penalised part into the running penalised max (and argmax for greedy
+// rows) and return its candidate masks.
+template <int SX, bool RAW, bool CAND, bool GREEDY, bool PEN>
+__device__ __forceinline__ void x_pen_part(XState& st, const uint4& w, float vm, unsigned bits, int e,
+                                           unsigned& mr, unsigned& mp) {
+    constexpr int EPV = 16 / SX;
+    float vp = vm;
+    if (PEN && bits) {
+        vp = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < EPV; ++q)
+            if (!((bits >> q) & 1u)) vp = max_nan(vp, elem<SX>(w, q));
+    }
+    if (GREEDY) {
+        if (!(vp <= st.m_p)) {
+            const float nm = max_nan(st.m_p, vp);
+            st.m_p = nm;
+            st.arg = 0x7FFFFFFF;
+#pragma unroll
+            for (int q = 0; q < EPV; ++q)
+                if (!((bits >> q) & 1u) && elem<SX>(w, q) == nm) st.arg = min(st.arg, e + q);
+        } else if (vp == st.m_p && st.arg == 0x7FFFFFFF) {
+#pragma unroll
+            for (int q = 0; q < EPV; ++q)
+                if (!((bits >> q) & 1u) && elem<SX>(w, q) == vp) st.arg = min(st.arg, e + q);
+        }
+    } else {
+        st.m_p = max_nan(st.m_p, vp);
+    }
+    mr = (RAW && vm >= st.th_r) ? ge_mask<SX>(w, st.th_r) : 0u;
+    mp = (CAND && vp >= st.th_p) ? (ge_mask<SX>(w, st.th_p) & ~bits) : 0u;
+}
+
+template <int SX, bool LP, bool RAW, bool CAND, bool GREEDY, bool PEN>
+__device__ __forceinline__ void x_scan(XState& st, const unsigned char* data, const unsigned* bm, int gt, int nvec,
+                                       int vec_e0, int bit0, unsigned long long& fr0, unsigned long long& fr1,
+                                       unsigned long long& fp0, unsigned long long& fp1) {
+    constexpr int EPV = 16 / SX;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    float mrl = st.m_r * kL2E;
+    // vectors in pairs: two loads, one rescale test, two independent exp chains
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; i += 2) {
+        const int v0 = gt + i * kGroupThreads, v1 = v0 + kGroupThreads;
+        if (v0 >= nvec) break;
+        const bool ok1 = v1 < nvec;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(data + v0 * 16);
+        const uint4 w1 = ok1 ? *reinterpret_cast<const uint4*>(data + v1 * 16) : neg_inf_vec<SX>();
+        const unsigned b0 = PEN ? bitmap_bits(bm, bit0 + v0 * EPV, EPV) : 0u;
+        const unsigned b1 = (PEN && ok1) ? bitmap_bits(bm, bit0 + v1 * EPV, EPV) : 0u;
+        const float vm0 = vec_max<SX>(w0), vm1 = vec_max<SX>(w1);
+        if (LP) {
+            const float vmb = max_nan(vm0, vm1);
+            if (!(vmb <= st.m_r)) {
+                const float nm = max_nan(st.m_r, vmb);
+                const float f = (st.m_r > -INFINITY && nm == nm) ? ex2_approx((st.m_r - nm) * kL2E) : 0.f;
+                st.s_r *= f;
+                acc0 = make_float2(acc0.x * f, acc0.y * f);
+                acc1 = make_float2(acc1.x * f, acc1.y * f);
+                st.m_r = nm;
+                mrl = nm * kL2E;
+            }
+            acc0 = vec_exp_sum<SX>(w0, acc0, kL2E, mrl);
+            acc1 = vec_exp_sum<SX>(w1, acc1, kL2E, mrl);
+        } else {
+            st.m_r = max_nan(st.m_r, max_nan(vm0, vm1));
+        }
+        unsigned mr0, mp0, mr1 = 0u, mp1 = 0u;
+        x_pen_part<SX, RAW, CAND, GREEDY, PEN>(st, w0, vm0, b0, vec_e0 + v0 * EPV, mr0, mp0);
+        // the filler past the end of the tile never reaches the maxima or the candidates
+        if (ok1) x_pen_part<SX, RAW, CAND, GREEDY, PEN>(st, w1, vm1, b1, vec_e0 + v1 * EPV, mr1, mp1);
+        if ((RAW || CAND) && (mr0 | mp0 | mr1 | mp1)) {
+            const int s0 = i * EPV, s1 = (i + 1) * EPV;
+            if (s0 < 64) { fr0 |= static_cast<unsigned long long>(mr0) << s0; fp0 |= static_cast<unsigned long long>(mp0) << s0; }
+            else { fr1 |= static_cast<unsigned long long>(mr0) << (s0 - 64); fp1 |= static_cast<unsigned long long>(mp0) << (s0 - 64); }
+            if (s1 < 64) { fr0 |= static_cast<unsigned long long>(mr1) << s1; fp0 |= static_cast<unsigned long long>(mp1) << s1; }
+            else { fr1 |= static_cast<unsigned long long>(mr1) << (s1 - 64); fp1 |= static_cast<unsigned long long>(mp1) << (s1 - 64); }
+        }
+    }
+    if (LP) st.s_r += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+}
+
+template <int SX, bool LP, bool RAW, bool CAND, bool GREEDY>
+__device__ __forceinline__ void x_scan_pen(bool pen, XState& st, const unsigned char* data, const unsigned* bm, int gt,
+                                           int nvec, int vec_e0, int bit0, unsigned long long& fr0,
+                                           unsigned long long& fr1, unsigned long long& fp0, unsigned long long& fp1) {
+    if (pen) x_scan<SX, LP, RAW, CAND, GREEDY, true>(st, data, bm, gt, nvec, vec_e0, bit0, fr0, fr1, fp0, fp1);
+    else x_scan<SX, LP, RAW, CAND, GREEDY, false>(st, data, bm, gt, nvec, vec_e0, bit0, fr0, fr1, fp0, fp1);
+}
+
+// Dispatch to a specialised scan; false when the row needs the general path.
+template <int SX>
+__device__ __forceinline__ bool x_scan_dispatch(const XCtx<SX>& c, XState& st, const unsigned char* data,
+                                                const unsigned* bm, int gt, unsigned long long& fr0,
+                                                unsigned long long& fr1, unsigned long long& fp0,
+                                                unsigned long long& fp1) {
+    const StageMeta& m = c.m;
+    if (c.need_temp || (m.pen && m.pen_over)) return false;
+    if (!c.greedy && !c.need_cand) return false;
+    const int bit0 = m.vec_e0 - m.e0;
+    const bool pen = m.pen;
+    if (c.greedy) {
+        if (c.need_raw) x_scan_pen<SX, true, true, false, true>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
+        else if (c.need_lp) x_scan_pen<SX, true, false, false, true>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
+        else x_scan_pen<SX, false, false, false, true>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
+    } else {
+        if (c.need_raw) x_scan_pen<SX, true, true, true, false>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
+        else if (c.need_lp) x_scan_pen<SX, true, false, true, false>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
+        else x_scan_pen<SX, false, false, true, false>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
+    }
+    return true;
+}
+
 template <int SX>
 __device__ void x_tile(const XCtx<SX>& c, XState& st) {
     constexpr int EPV = 16 / SX;
@@ -521,8 +645,9 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
     // thread (bit EPV*i+q: element q of the thread's i-th vector) and appended once at the end.
     float unused = 0.f;
     unsigned long long fr0 = 0ull, fr1 = 0ull, fp0 = 0ull, fp1 = 0ull;
+    const bool fast = x_scan_dispatch<SX>(c, st, data, bm, gt, fr0, fr1, fp0, fp1);
 #pragma unroll 2
-    for (int i = 0; i < kVecPerThread; ++i) {
+    for (int i = 0; i < (fast ? 0 : kVecPerThread); ++i) {
         const int v = gt + i * kGroupThreads;
         if (v >= m.nvec) break;
         const uint4 w = *reinterpret_cast<const uint4*>(data + v * 16);
@@ -681,8 +806,34 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
         st.th = need_cand ? r.z : INFINITY;
     }
     unsigned long long fq = 0ull;
+    if (need_cand && !need_sum) {
+        // common case: maxima / minima and top-k candidates, vectors in pairs
+        float mx0 = st.mx, mx1 = -INFINITY, mn0 = st.mn, mn1 = INFINITY;
+        const float th = st.th;
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; i += 2) {
+            const int v0 = gt + i * kGroupThreads, v1 = v0 + kGroupThreads;
+            if (v0 >= m.nvec) break;
+            const bool ok1 = v1 < m.nvec;
+            const uint4 u0 = *reinterpret_cast<const uint4*>(data + v0 * 16);
+            const uint4 u1 = ok1 ? *reinterpret_cast<const uint4*>(data + v1 * 16) : u0;
+            const float4 w0 = *reinterpret_cast<const float4*>(&u0);
+            const float4 w1 = *reinterpret_cast<const float4*>(&u1);
+            const float vm0 = max_nan(max_nan(w0.x, w0.y), max_nan(w0.z, w0.w));
+            const float vm1 = max_nan(max_nan(w1.x, w1.y), max_nan(w1.z, w1.w));
+            mx0 = max_nan(mx0, vm0);
+            mx1 = max_nan(mx1, vm1);
+            mn0 = fminf(mn0, fminf(fminf(w0.x, w0.y), fminf(w0.z, w0.w)));
+            mn1 = fminf(mn1, fminf(fminf(w1.x, w1.y), fminf(w1.z, w1.w)));
+            const unsigned k0 = vm0 >= th ? ge_mask<4>(u0, th) : 0u;
+            const unsigned k1 = (ok1 && vm1 >= th) ? ge_mask<4>(u1, th) : 0u;
+            if (k0 | k1) fq |= (static_cast<unsigned long long>(k0) << (4 * i)) | (static_cast<unsigned long long>(k1) << (4 * i + 4));
+        }
+        st.mx = max_nan(mx0, mx1);
+        st.mn = fminf(mn0, mn1);
+    }
 #pragma unroll 2
-    for (int i = 0; i < kVecPerThread; ++i) {
+    for (int i = 0; i < ((need_cand && !need_sum) ? 0 : kVecPerThread); ++i) {
         const int v = gt + i * kGroupThreads;
         if (v >= m.nvec) break;
         const int e = m.vec_e0 + v * 4;
