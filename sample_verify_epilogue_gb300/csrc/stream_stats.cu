@@ -280,6 +280,70 @@ __device__ __forceinline__ unsigned ge_mask(const uint4& w, float th) {
     return m;
 }
 
+// Position of the r-th (0-based) set bit of b; requires r < popc(b).
+__device__ __forceinline__ int nth_set_bit(unsigned b, int r) {
+    int pos = 0;
+#pragma unroll
+    for (int s = 16; s; s >>= 1) {
+        const int c = __popc(b & ((1u << s) - 1u));
+        if (r >= c) { r -= c; b >>= s; pos += s; }
+    }
+    return pos;
+}
+
+// Candidate extraction from the vectors the threads flagged during a scan (bit i of
+// `vflags`: the thread's i-th vector of the tile has an element at or above the lower
+// threshold).  The warp's flagged vectors are dealt out to its lanes 32 at a time, in slot
+// order, so a lane with many flags does not hold up the others.  For each vector: RAW
+// appends the elements >= th_r to the raw buffer; the elements >= th_p without a penalty
+// bit are appended to the penalised buffer (CAND) and folded into the running penalised
+// maximum and the lowest index attaining it (TRACK).  Every lane of the warp calls it.
+template <int SX, bool PEN, bool RAW, bool CAND, bool TRACK>
+__device__ __forceinline__ void flush_vectors(GroupSmem& gs, unsigned vflags, const unsigned char* data,
+                                              const unsigned* bm, int vec_e0, int bit0, int gt, float th_r,
+                                              float th_p, float& m_p, int& arg) {
+    constexpr int EPV = 16 / SX;
+    const int lane = threadIdx.x & 31;
+    const int wv = gt - lane;                             // vector index of lane 0, slot 0
+    for (int base = 0;; base += 32) {
+        const int t = base + lane;                        // this lane's item of the round
+        int run = 0, sel_i = -1, sel_r = 0;
+        unsigned sel_b = 0u;
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+            const unsigned b = __ballot_sync(0xffffffffu, (vflags >> i) & 1u);
+            const int n = __popc(b);
+            const int r = t - run;
+            if (r >= 0 && r < n) { sel_i = i; sel_r = r; sel_b = b; }
+            run += n;
+        }
+        if (run == 0) return;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        unsigned mr = 0u, mp = 0u;
+        int e = 0;
+        if (sel_i >= 0) {
+            const int v = wv + nth_set_bit(sel_b, sel_r) + sel_i * kGroupThreads;
+            w = *reinterpret_cast<const uint4*>(data + v * 16);
+            e = vec_e0 + v * EPV;
+            const unsigned bits = PEN ? bitmap_bits(bm, bit0 + v * EPV, EPV) : 0u;
+            if (RAW) mr = ge_mask<SX>(w, th_r);
+            mp = ge_mask<SX>(w, th_p) & ~bits;
+        }
+        if (RAW) warp_append<SX>(gs.craw, &gs.cnt_raw, kSmemCandRaw, mr, w, e);
+        if (CAND) warp_append<SX>(gs.cpen, &gs.cnt_pen, kSmemCandPen, mp, w, e);
+        if (TRACK) {
+            while (mp) {
+                const int q = __ffs(mp) - 1;
+                mp &= mp - 1u;
+                const float v = elem<SX>(w, q);
+                if (v > m_p) { m_p = v; arg = e + q; }
+                else if (v == m_p && e + q < arg) arg = e + q;
+            }
+        }
+        if (base + 32 >= run) return;
+    }
+}
+
 // ------------------------------------------------------------------ target-logit segments
 struct XState {
     float m_r, s_r;      // raw running max, sum of 2^((x - m_r)*L2E)
@@ -383,11 +447,22 @@ __device__ __forceinline__ void x_vec(const XCtx<SX>& c, XState& st, const uint4
     mask_p = (c.need_cand && vp >= st.th_p) ? (ge_mask<SX>(w, st.th_p) & ~bits) : 0u;
 }
 
+// A penalised value on the fast path: values >= th_p update the running maximum / lowest
+// index attaining it, and are top-k candidates when the row needs them.
+template <int SX>
+__device__ __forceinline__ void fold_fast(const XCtx<SX>& c, XState& st, float xp, int e) {
+    if (xp >= st.th_p) {
+        if (xp > st.m_p) { st.m_p = xp; st.arg = e; }
+        else if (xp == st.m_p && e < st.arg) st.arg = e;
+        if (c.need_cand) push(c.gs.cpen, &c.gs.cnt_pen, kSmemCandPen, xp, e);
+    }
+}
+
 // The tile's possibly-penalised tokens (history and draft tokens, from the penalty index):
 // each thread takes some, computes x' = x - ((f*c) + p) with c = history + own draft prefix,
 // and folds it into the penalised statistics.  pass1: only the maximum.
 template <int SX>
-__device__ __forceinline__ void x_entries(const XCtx<SX>& c, XState& st, bool pass1, float& lane_pen) {
+__device__ __forceinline__ void x_entries(const XCtx<SX>& c, XState& st, bool pass1, bool fast, float& lane_pen) {
     const StageMeta& m = c.m;
     const int gt = threadIdx.x - c.g * kGroupThreads;
     const PenEntry* ent = c.sm.ent[c.stage];
@@ -401,6 +476,7 @@ __device__ __forceinline__ void x_entries(const XCtx<SX>& c, XState& st, bool pa
         const float xr = x_at(c, t);
         const float xp = penalise(xr, cnt, c.f, c.p);
         if (pass1) lane_pen = max_nan(lane_pen, xp);
+        else if (fast) fold_fast(c, st, xp, t);
         else pen_fold(c, st, xp, xr, t, true);
     }
 }
@@ -421,57 +497,43 @@ __device__ __forceinline__ void x_vec_overflow(const XCtx<SX>& c, XState& st, co
     }
 }
 
-// Specialised scan of one tile for the common row types: compile-time flags, no per-vector
-// tests of the row's options.  LP: raw log-sum-exp; RAW: raw top-n candidates; CAND: top-k
-// candidates of the penalised logits (sampled rows); GREEDY: penalised argmax; PEN: the row
-// has penalty bits.  Raw sums go to two f32x2 accumulators (even / odd vectors).
+// Fast path over a tile whose penalty index overflowed: each thread folds the penalised
+// tokens of its own vectors, their counts looked up in the caller's history.
+template <int SX>
+__device__ void x_overflow_fast(const XCtx<SX>& c, XState& st, const unsigned char* data, const unsigned* bm,
+                                int gt) {
+    constexpr int EPV = 16 / SX;
+    const StageMeta& m = c.m;
+    for (int i = 0; i < kVecPerThread; ++i) {
+        const int v = gt + i * kGroupThreads;
+        if (v >= m.nvec) break;
+        const int e = m.vec_e0 + v * EPV;
+        unsigned bits = bitmap_bits(bm, e - m.e0, EPV);
+        if (!bits) continue;
+        const uint4 w = *reinterpret_cast<const uint4*>(data + v * 16);
+        while (bits) {
+            const int q = __ffs(bits) - 1;
+            bits &= bits - 1u;
+            fold_fast(c, st, penalise(elem<SX>(w, q), pen_count(c.sm, c.stage, m, c.a, e + q), c.f, c.p), e + q);
+        }
+    }
+}
+
 template <int SX>
 __device__ __forceinline__ uint4 neg_inf_vec() {
     const uint32_t ni = SX == 2 ? 0xFF80FF80u : 0xFF800000u;
     return make_uint4(ni, ni, ni, ni);
 }
 
-// Fold one vector's penalised part into the running penalised max (and argmax for greedy
-// rows) and return its candidate masks.
-template <int SX, bool RAW, bool CAND, bool GREEDY, bool PEN>
-__device__ __forceinline__ void x_pen_part(XState& st, const uint4& w, float vm, unsigned bits, int e,
-                                           unsigned& mr, unsigned& mp) {
-    constexpr int EPV = 16 / SX;
-    float vp = vm;
-    if (PEN && bits) {
-        vp = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < EPV; ++q)
-            if (!((bits >> q) & 1u)) vp = max_nan(vp, elem<SX>(w, q));
-    }
-    if (GREEDY) {
-        if (!(vp <= st.m_p)) {
-            const float nm = max_nan(st.m_p, vp);
-            st.m_p = nm;
-            st.arg = 0x7FFFFFFF;
-#pragma unroll
-            for (int q = 0; q < EPV; ++q)
-                if (!((bits >> q) & 1u) && elem<SX>(w, q) == nm) st.arg = min(st.arg, e + q);
-        } else if (vp == st.m_p && st.arg == 0x7FFFFFFF) {
-#pragma unroll
-            for (int q = 0; q < EPV; ++q)
-                if (!((bits >> q) & 1u) && elem<SX>(w, q) == vp) st.arg = min(st.arg, e + q);
-        }
-    } else {
-        st.m_p = max_nan(st.m_p, vp);
-    }
-    mr = (RAW && vm >= st.th_r) ? ge_mask<SX>(w, st.th_r) : 0u;
-    mp = (CAND && vp >= st.th_p) ? (ge_mask<SX>(w, st.th_p) & ~bits) : 0u;
-}
-
-template <int SX, bool LP, bool RAW, bool CAND, bool GREEDY, bool PEN>
-__device__ __forceinline__ void x_scan(XState& st, const unsigned char* data, const unsigned* bm, int gt, int nvec,
-                                       int vec_e0, int bit0, unsigned long long& fr0, unsigned long long& fr1,
-                                       unsigned long long& fp0, unsigned long long& fp1) {
-    constexpr int EPV = 16 / SX;
+// The scan of one tile for every row that needs neither the tempered sum nor the overflow
+// path: raw maximum (and with LP the raw sum of 2^((x - m_r)*log2e), in two f32x2
+// accumulators), and one flag bit per vector whose maximum is >= th.  All per-element work
+// on candidates is left to flush_vectors.
+template <int SX, bool LP>
+__device__ __forceinline__ unsigned x_scan_flags(XState& st, const unsigned char* data, int gt, int nvec, float th) {
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
     float mrl = st.m_r * kL2E;
-    // vectors in pairs: two loads, one rescale test, two independent exp chains
+    unsigned fl = 0u;
 #pragma unroll
     for (int i = 0; i < kVecPerThread; i += 2) {
         const int v0 = gt + i * kGroupThreads, v1 = v0 + kGroupThreads;
@@ -479,8 +541,6 @@ __device__ __forceinline__ void x_scan(XState& st, const unsigned char* data, co
         const bool ok1 = v1 < nvec;
         const uint4 w0 = *reinterpret_cast<const uint4*>(data + v0 * 16);
         const uint4 w1 = ok1 ? *reinterpret_cast<const uint4*>(data + v1 * 16) : neg_inf_vec<SX>();
-        const unsigned b0 = PEN ? bitmap_bits(bm, bit0 + v0 * EPV, EPV) : 0u;
-        const unsigned b1 = (PEN && ok1) ? bitmap_bits(bm, bit0 + v1 * EPV, EPV) : 0u;
         const float vm0 = vec_max<SX>(w0), vm1 = vec_max<SX>(w1);
         if (LP) {
             const float vmb = max_nan(vm0, vm1);
@@ -498,50 +558,37 @@ __device__ __forceinline__ void x_scan(XState& st, const unsigned char* data, co
         } else {
             st.m_r = max_nan(st.m_r, max_nan(vm0, vm1));
         }
-        unsigned mr0, mp0, mr1 = 0u, mp1 = 0u;
-        x_pen_part<SX, RAW, CAND, GREEDY, PEN>(st, w0, vm0, b0, vec_e0 + v0 * EPV, mr0, mp0);
-        // the filler past the end of the tile never reaches the maxima or the candidates
-        if (ok1) x_pen_part<SX, RAW, CAND, GREEDY, PEN>(st, w1, vm1, b1, vec_e0 + v1 * EPV, mr1, mp1);
-        if ((RAW || CAND) && (mr0 | mp0 | mr1 | mp1)) {
-            const int s0 = i * EPV, s1 = (i + 1) * EPV;
-            if (s0 < 64) { fr0 |= static_cast<unsigned long long>(mr0) << s0; fp0 |= static_cast<unsigned long long>(mp0) << s0; }
-            else { fr1 |= static_cast<unsigned long long>(mr0) << (s0 - 64); fp1 |= static_cast<unsigned long long>(mp0) << (s0 - 64); }
-            if (s1 < 64) { fr0 |= static_cast<unsigned long long>(mr1) << s1; fp0 |= static_cast<unsigned long long>(mp1) << s1; }
-            else { fr1 |= static_cast<unsigned long long>(mr1) << (s1 - 64); fp1 |= static_cast<unsigned long long>(mp1) << (s1 - 64); }
-        }
+        // the filler past the end of the tile is never flagged
+        fl |= (vm0 >= th ? 1u : 0u) << i;
+        fl |= ((ok1 && vm1 >= th) ? 1u : 0u) << (i + 1);
     }
     if (LP) st.s_r += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    return fl;
 }
 
-template <int SX, bool LP, bool RAW, bool CAND, bool GREEDY>
-__device__ __forceinline__ void x_scan_pen(bool pen, XState& st, const unsigned char* data, const unsigned* bm, int gt,
-                                           int nvec, int vec_e0, int bit0, unsigned long long& fr0,
-                                           unsigned long long& fr1, unsigned long long& fp0, unsigned long long& fp1) {
-    if (pen) x_scan<SX, LP, RAW, CAND, GREEDY, true>(st, data, bm, gt, nvec, vec_e0, bit0, fr0, fr1, fp0, fp1);
-    else x_scan<SX, LP, RAW, CAND, GREEDY, false>(st, data, bm, gt, nvec, vec_e0, bit0, fr0, fr1, fp0, fp1);
+template <int SX, bool PEN, bool RAW>
+__device__ __forceinline__ void x_flush_cand(bool cand, GroupSmem& gs, unsigned fl, const unsigned char* data,
+                                             const unsigned* bm, int vec_e0, int bit0, int gt, XState& st) {
+    if (cand) flush_vectors<SX, PEN, RAW, true, true>(gs, fl, data, bm, vec_e0, bit0, gt, st.th_r, st.th_p, st.m_p, st.arg);
+    else flush_vectors<SX, PEN, RAW, false, true>(gs, fl, data, bm, vec_e0, bit0, gt, st.th_r, st.th_p, st.m_p, st.arg);
 }
 
-// Dispatch to a specialised scan; false when the row needs the general path.
+// Scan and candidate flush of one tile on the fast path.
 template <int SX>
-__device__ __forceinline__ bool x_scan_dispatch(const XCtx<SX>& c, XState& st, const unsigned char* data,
-                                                const unsigned* bm, int gt, unsigned long long& fr0,
-                                                unsigned long long& fr1, unsigned long long& fp0,
-                                                unsigned long long& fp1) {
+__device__ __forceinline__ void x_fast_pass(const XCtx<SX>& c, XState& st, const unsigned char* data,
+                                            const unsigned* bm, int gt) {
     const StageMeta& m = c.m;
-    if (c.need_temp || (m.pen && m.pen_over)) return false;
-    if (!c.greedy && !c.need_cand) return false;
+    const float th = fminf(st.th_p, st.th_r);
+    const unsigned fl = c.need_lp ? x_scan_flags<SX, true>(st, data, gt, m.nvec, th)
+                                  : x_scan_flags<SX, false>(st, data, gt, m.nvec, th);
     const int bit0 = m.vec_e0 - m.e0;
-    const bool pen = m.pen;
-    if (c.greedy) {
-        if (c.need_raw) x_scan_pen<SX, true, true, false, true>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
-        else if (c.need_lp) x_scan_pen<SX, true, false, false, true>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
-        else x_scan_pen<SX, false, false, false, true>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
+    if (m.pen) {
+        if (c.need_raw) x_flush_cand<SX, true, true>(c.need_cand, c.gs, fl, data, bm, m.vec_e0, bit0, gt, st);
+        else x_flush_cand<SX, true, false>(c.need_cand, c.gs, fl, data, bm, m.vec_e0, bit0, gt, st);
     } else {
-        if (c.need_raw) x_scan_pen<SX, true, true, true, false>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
-        else if (c.need_lp) x_scan_pen<SX, true, false, true, false>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
-        else x_scan_pen<SX, false, false, true, false>(pen, st, data, bm, gt, m.nvec, m.vec_e0, bit0, fr0, fr1, fp0, fp1);
+        if (c.need_raw) x_flush_cand<SX, false, true>(c.need_cand, c.gs, fl, data, bm, m.vec_e0, bit0, gt, st);
+        else x_flush_cand<SX, false, false>(c.need_cand, c.gs, fl, data, bm, m.vec_e0, bit0, gt, st);
     }
-    return true;
 }
 
 template <int SX>
@@ -556,6 +603,9 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
     const int e_tail = m.vec_e0 + m.nvec * EPV;
     const bool use_entries = m.pen && !m.pen_over;
     const bool overflow = m.pen && m.pen_over;
+    // fast path: every row but those needing the tempered sum (a property of the row, so
+    // the same for all tiles of a segment)
+    const bool fast = !c.need_temp;
 
     if (m.first) {
         // ---- pass 1 over the first tile: maxima, then the segment's candidate thresholds
@@ -569,20 +619,13 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
             const unsigned b1 = m.pen ? bitmap_bits(bm, e1 - m.e0, EPV) : 0u;
             const float v0 = vec_max<SX>(w0), v1 = vec_max<SX>(w1);
             mrw = max_nan(mrw, max_nan(v0, v1));
-            if ((b0 | b1) == 0u) {
-                mu0 = max_nan(mu0, v0);
-                mu1 = max_nan(mu1, v1);
-            } else {
-#pragma unroll
-                for (int q = 0; q < EPV; ++q) {
-                    if (!((b0 >> q) & 1u)) mu0 = max_nan(mu0, elem<SX>(w0, q));
-                    if (!((b1 >> q) & 1u)) mu1 = max_nan(mu1, elem<SX>(w1, q));
-                }
-                if (overflow) {
-                    XState dummy{};
-                    x_vec_overflow<SX>(c, dummy, w0, e0, b0, true, mpen);
-                    x_vec_overflow<SX>(c, dummy, w1, e1, b1, true, mpen);
-                }
+            // vectors holding a penalised token are left out of the penalised lane maxima
+            mu0 = max_nan(mu0, b0 ? -INFINITY : v0);
+            mu1 = max_nan(mu1, b1 ? -INFINITY : v1);
+            if (overflow && (b0 | b1)) {
+                XState dummy{};
+                x_vec_overflow<SX>(c, dummy, w0, e0, b0, true, mpen);
+                x_vec_overflow<SX>(c, dummy, w1, e1, b1, true, mpen);
             }
         }
         for (; v < m.nvec; v += kGroupThreads) {
@@ -591,14 +634,8 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
             const unsigned bits = m.pen ? bitmap_bits(bm, e - m.e0, EPV) : 0u;
             const float vv = vec_max<SX>(w);
             mrw = max_nan(mrw, vv);
-            if (bits == 0u) {
-                mu0 = max_nan(mu0, vv);
-            } else {
-#pragma unroll
-                for (int q = 0; q < EPV; ++q)
-                    if (!((bits >> q) & 1u)) mu0 = max_nan(mu0, elem<SX>(w, q));
-                if (overflow) { XState dummy{}; x_vec_overflow<SX>(c, dummy, w, e, bits, true, mpen); }
-            }
+            mu0 = max_nan(mu0, bits ? -INFINITY : vv);
+            if (overflow && bits) { XState dummy{}; x_vec_overflow<SX>(c, dummy, w, e, bits, true, mpen); }
         }
         if (gt < 2) {
             const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
@@ -612,7 +649,7 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
                 }
             }
         }
-        if (use_entries) { XState dummy{}; x_entries<SX>(c, dummy, true, mpen); }
+        if (use_entries) { XState dummy{}; x_entries<SX>(c, dummy, true, false, mpen); }
         const float lane_raw = mrw, lane_pen = max_nan(max_nan(mu0, mu1), mpen);
         float wr = lane_raw, wp = lane_pen;
         for (int o = 16; o; o >>= 1) {
@@ -631,21 +668,30 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
         if (lane == 0) c.gs.red1[warp] = make_float4(wr, wp, thp, thr);
         group_sync(c.g);
         const float4 r = group_reduce_mmnn(c.gs.red1);
-        // the segment starts from the first tile's maxima: no rescaling inside this tile
+        // The segment starts from the first tile's maxima.  Each lane value above is the
+        // penalised value of a distinct element, so every warp has at least cp elements >= its
+        // cp-th largest lane value and the tile at least top_k elements >= the minimum over
+        // warps: nothing of the row's top-k lies below th_p.  On the fast path th_p of a row
+        // without a top-k list is the tile's penalised maximum (over the same elements), so the
+        // segment's penalised maximum and argmax are found among the values >= th_p.
         st.m_r = r.x;
-        st.m_p = r.y;
+        st.m_p = fast ? -INFINITY : r.y;
         st.s_r = 0.f;
         st.s_t = 0.f;
         st.arg = 0x7FFFFFFF;
-        st.th_p = c.need_cand ? r.z : INFINITY;
+        st.th_p = c.need_cand ? r.z : (fast ? r.y : INFINITY);
         st.th_r = c.need_raw ? r.w : INFINITY;
     }
 
-    // ---- the accumulation / filter pass over this tile.  Candidate flags are kept per
-    // thread (bit EPV*i+q: element q of the thread's i-th vector) and appended once at the end.
+    // ---- the accumulation / filter pass over this tile.  General path: candidate flags
+    // are kept per thread (bit EPV*i+q: element q of the thread's i-th vector) and appended
+    // once at the end.
     float unused = 0.f;
     unsigned long long fr0 = 0ull, fr1 = 0ull, fp0 = 0ull, fp1 = 0ull;
-    const bool fast = x_scan_dispatch<SX>(c, st, data, bm, gt, fr0, fr1, fp0, fp1);
+    if (fast) {
+        x_fast_pass<SX>(c, st, data, bm, gt);
+        if (overflow) x_overflow_fast<SX>(c, st, data, bm, gt);
+    }
 #pragma unroll 2
     for (int i = 0; i < (fast ? 0 : kVecPerThread); ++i) {
         const int v = gt + i * kGroupThreads;
@@ -660,8 +706,8 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
         if (sh < 64) { fr0 |= static_cast<unsigned long long>(mr) << sh; fp0 |= static_cast<unsigned long long>(mp) << sh; }
         else { fr1 |= static_cast<unsigned long long>(mr) << (sh - 64); fp1 |= static_cast<unsigned long long>(mp) << (sh - 64); }
     }
-    if (c.need_raw) flush_flags<SX>(c.gs.craw, &c.gs.cnt_raw, kSmemCandRaw, fr0, fr1, data, m.vec_e0, gt);
-    if (c.need_cand) flush_flags<SX>(c.gs.cpen, &c.gs.cnt_pen, kSmemCandPen, fp0, fp1, data, m.vec_e0, gt);
+    if (!fast && c.need_raw) flush_flags<SX>(c.gs.craw, &c.gs.cnt_raw, kSmemCandRaw, fr0, fr1, data, m.vec_e0, gt);
+    if (!fast && c.need_cand) flush_flags<SX>(c.gs.cpen, &c.gs.cnt_pen, kSmemCandPen, fp0, fp1, data, m.vec_e0, gt);
     if (gt < 2) {
         const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
         for (int e = lo; e < hi; ++e) {
@@ -679,12 +725,16 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
             }
             if (xv >= st.th_r) push(c.gs.craw, &c.gs.cnt_raw, kSmemCandRaw, xv, e);
             const bool bit = m.pen && bitmap_bit(bm, e - m.e0);
-            if (!bit) pen_fold(c, st, xv, xv, e, false);
+            if (fast) {
+                if (!bit) fold_fast(c, st, xv, e);
+                else if (overflow) fold_fast(c, st, penalise(xv, pen_count(c.sm, c.stage, m, c.a, e), c.f, c.p), e);
+            }
+            else if (!bit) pen_fold(c, st, xv, xv, e, false);
             else if (overflow) pen_fold(c, st, penalise(xv, pen_count(c.sm, c.stage, m, c.a, e), c.f, c.p), xv, e, false);
             else if (c.need_temp) st.s_t += ex2_approx((xv - st.m_p) * c.c_l2e);   // undone by x_entries
         }
     }
-    if (use_entries) x_entries<SX>(c, st, false, unused);
+    if (use_entries) x_entries<SX>(c, st, false, fast, unused);
     __syncwarp();
     if (lane == 0) mbar_arrive(&c.sm.empty[c.stage]);     // this stage is no longer read
 }
@@ -805,9 +855,10 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
         st.sum = 0.f;
         st.th = need_cand ? r.z : INFINITY;
     }
-    unsigned long long fq = 0ull;
-    if (need_cand && !need_sum) {
-        // common case: maxima / minima and top-k candidates, vectors in pairs
+    if (need_cand) {
+        // common case: maxima / minima, vectors in pairs, one flag per vector whose maximum
+        // reaches the threshold; the flagged vectors' candidates are extracted afterwards
+        unsigned vfl = 0u;
         float mx0 = st.mx, mx1 = -INFINITY, mn0 = st.mn, mn1 = INFINITY;
         const float th = st.th;
 #pragma unroll
@@ -825,15 +876,18 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
             mx1 = max_nan(mx1, vm1);
             mn0 = fminf(mn0, fminf(fminf(w0.x, w0.y), fminf(w0.z, w0.w)));
             mn1 = fminf(mn1, fminf(fminf(w1.x, w1.y), fminf(w1.z, w1.w)));
-            const unsigned k0 = vm0 >= th ? ge_mask<4>(u0, th) : 0u;
-            const unsigned k1 = (ok1 && vm1 >= th) ? ge_mask<4>(u1, th) : 0u;
-            if (k0 | k1) fq |= (static_cast<unsigned long long>(k0) << (4 * i)) | (static_cast<unsigned long long>(k1) << (4 * i + 4));
+            vfl |= (vm0 >= th ? 1u : 0u) << i;
+            vfl |= ((ok1 && vm1 >= th) ? 1u : 0u) << (i + 1);
         }
         st.mx = max_nan(mx0, mx1);
         st.mn = fminf(mn0, mn1);
+        float m_unused = 0.f;
+        int a_unused = 0;
+        flush_vectors<4, false, false, true, false>(gs, vfl, data, nullptr, m.vec_e0, 0, gt, INFINITY, th, m_unused,
+                                                    a_unused);
     }
 #pragma unroll 2
-    for (int i = 0; i < ((need_cand && !need_sum) ? 0 : kVecPerThread); ++i) {
+    for (int i = 0; i < (need_cand ? 0 : kVecPerThread); ++i) {
         const int v = gt + i * kGroupThreads;
         if (v >= m.nvec) break;
         const int e = m.vec_e0 + v * 4;
@@ -856,9 +910,7 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
         }
         st.mx = max_nan(st.mx, vm);
         st.mn = fminf(st.mn, vn);
-        if (need_cand && vm >= st.th) fq |= static_cast<unsigned long long>(ge_mask<4>(wu, st.th)) << (4 * i);
     }
-    if (need_cand) flush_flags<4>(gs.cpen, &gs.cnt_pen, kSmemCandPen, fq, 0ull, data, m.vec_e0, gt);
     if (gt < 2) {
         const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
         for (int e = lo; e < hi; ++e) q_elem(st, __ldg(a.q + qrow + e), need_sum, t_one, inv_t, need_cand, gs, e);
