@@ -18,7 +18,7 @@ constexpr int kMaxGrid = 1024;           // streaming CTAs on any device (an SM 
 struct Layout {
     int tile_x, tiles_x, tile_q, tiles_q, bm_words, xslots, qslots, nseg_x, nseg_q;
     long long seg_max;
-    size_t off_plan, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_raw, off_cand_q;
+    size_t off_plan, off_req_n, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_raw, off_cand_q;
     size_t off_pen_hdr, off_pen_bm, off_pen_ent, off_draft_base, off_xout, off_kept, off_topn, off_qout, off_req;
     size_t total;
 };
@@ -53,6 +53,7 @@ Layout make_layout(const dspark_params_t* p) {
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     L.off_plan = take(sizeof(Plan));
+    L.off_req_n = take(static_cast<size_t>(2 * B) * sizeof(int));
     // segment streams: grid x groups x ceil(S / (groups*grid)) entries <= S + groups*grid
     L.off_units = take((xt + qt + static_cast<size_t>(kGroups) * kMaxGrid) * sizeof(UnitDesc));
     L.off_ts_x = take(xt * sizeof(TileStats));
@@ -110,6 +111,7 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     a.out_accept = out_accept_len; a.out_tokens = out_tokens; a.out_lp = out_logprobs;
     a.out_top_ids = out_top_ids; a.out_top_lp = out_top_logprobs; a.row_status = p->row_status;
     a.plan = at<Plan>(ws, L.off_plan);
+    a.req_n = at<int>(ws, L.off_req_n);
     a.units = at<UnitDesc>(ws, L.off_units);
     a.ts_x = at<TileStats>(ws, L.off_ts_x);
     a.ts_q = at<TileStats>(ws, L.off_ts_q);

@@ -1,7 +1,7 @@
 // Internal definitions shared by the sm_103a kernels of the verify-and-sample epilogue.
 //
 // Data flow of one call (all on the caller's stream, no host synchronisation):
-//   prep_kernel          plan of work units + per-(request, vocab tile) penalty index
+//   prep_kernel          request checks, segment counts, per-(request, vocab tile) penalty index
 //   stream_stats_kernel  the one HBM pass over x and q: per-tile maxima, sums and candidates
 //   row_finalize_kernel  per verify row: merge segments, top-k threshold, nucleus, normaliser
 //                        (rows needing a whole-vocabulary threshold get it in the same block)
@@ -45,7 +45,7 @@ constexpr int kMaxB = DSPARK_MAX_B;
 enum UnitKind : int { kUnitX = 0, kUnitQ = 1 };
 
 struct Plan {
-    int n_units;         // segments in the call
+    int n_units;         // unused
     int pad[3];          // pad[0]: error flag set by the streaming pass
 };
 
@@ -171,6 +171,7 @@ struct Args {
     unsigned* pen_bm;      // [B * tiles_x * bm_words]
     PenEntry* pen_ent;     // [B * tiles_x * kPenCap]
     int* draft_base;       // [B * Km]
+    int* req_n;            // [2B]: segments of request b (0 if invalid), then its target-row segments
     XRowOut* xout;         // [xslots]
     KeptEntry* kept;       // [xslots * kKeptCap]
     TopEntry* topn;        // [xslots * DSPARK_MAX_TOP_LOGPROBS]

@@ -1,11 +1,11 @@
-// prep_kernel: the work plan of the streaming pass and the per-(request, vocab tile) penalty
-// index, in one launch.
+// prep_kernel: request checks, the segment counts of the streaming pass and the
+// per-(request, vocab tile) penalty index, in one launch.
 //
-// Block 0 validates every request's parameters and draft ids (row_status bits), counts the
-// vocab tiles each valid request needs (K_b+1 target rows; K_b draft rows when T > 0) and
-// writes the flat list of work units.
-//
-// Block 1 + b*tiles_x + t builds, for request b with a non-zero penalty and the vocab tile
+// Block b*tiles_x + t checks request b's parameters and draft ids; block t = 0 also writes
+// the row_status bits and the number of segments the request needs (K_b+1 target rows and,
+// when T > 0, K_b draft rows; none for an invalid request), from which every streaming CTA
+// derives the plan.  For a request with a non-zero penalty, the block then builds, for the
+// vocab tile
 // t, the tokens of that tile which may carry a penalty: the request's completion-history
 // tokens in the tile (with their counts) and its draft tokens in the tile, each with a
 // bit mask of the draft positions holding it.  Verify position j then counts
@@ -19,92 +19,6 @@ namespace dspark {
 namespace {
 
 constexpr int kPrepThreads = 256;
-
-__device__ void plan_block(const Args& a) {
-    // dynamic shared memory: [B] request parameters, [B+1] segment offsets, [B] target-row segments
-    extern __shared__ __align__(16) unsigned char plan_smem[];
-    dspark_row_params_t* sm_rows = reinterpret_cast<dspark_row_params_t*>(plan_smem);
-    int* sm_base = reinterpret_cast<int*>(plan_smem + sizeof(dspark_row_params_t) * a.B);
-    __shared__ int s_chunk[kPrepThreads + 1];
-    const int tid = threadIdx.x;
-    const int B = a.B;
-    int* sm_nx = sm_base + B + 1;
-    for (int b = tid; b < B; b += kPrepThreads) {
-        const dspark_row_params_t r = a.rows[b];
-        sm_rows[b] = r;
-        const int st = request_status(a, b);
-        if (st) atomicOr(&a.row_status[b], st);
-        int n = 0, nx = 0;
-        if (!(st & DSPARK_ROW_BAD_PARAMS) && !(st & DSPARK_ROW_BAD_DRAFT)) {
-            const int K = r.num_drafts;
-            nx = (K + 1) * a.nseg_x;
-            n = nx + (r.temperature > 0.f ? K * a.nseg_q : 0);
-        }
-        sm_base[b + 1] = n;
-        sm_nx[b] = nx;
-    }
-    __syncthreads();
-    // exclusive scan of the per-request segment counts: chunked per thread, then across threads
-    const int chunk = (B + kPrepThreads - 1) / kPrepThreads;
-    const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
-    int s = 0;
-    for (int b = lo; b < hi; ++b) s += sm_base[b + 1];
-    s_chunk[tid + 1] = s;
-    __syncthreads();
-    if (tid == 0) {
-        s_chunk[0] = 0;
-        for (int t = 1; t <= kPrepThreads; ++t) s_chunk[t] += s_chunk[t - 1];
-    }
-    __syncthreads();
-    int run = s_chunk[tid];
-    for (int b = lo; b < hi; ++b) {
-        const int n = sm_base[b + 1];
-        sm_base[b + 1] = run + n;               // inclusive end of b
-        run += n;
-    }
-    if (tid == 0) sm_base[0] = 0;
-    __syncthreads();
-    const int S = sm_base[B];
-    if (tid == 0) a.plan->n_units = S;
-    // segment s goes to CTA c = s mod G, consumer group g = (s div G) mod 2, position s div 2G
-    const int G = a.grid_ss;
-    for (int u = tid; u < S; u += kPrepThreads) {
-        int l = 0, h = B;                        // find b with base[b] <= u < base[b+1]
-        while (h - l > 1) {
-            const int mid = (l + h) >> 1;
-            if (sm_base[mid] <= u) l = mid; else h = mid;
-        }
-        const int b = l;
-        int local = u - sm_base[b];
-        const int nx = sm_nx[b];
-        const dspark_row_params_t r = sm_rows[b];
-        UnitDesc ud;
-        ud.b = b;
-        int tiles, nseg;
-        if (local < nx) {
-            ud.kind = kUnitX;
-            ud.slot = b * (a.Km + 1) + local / a.nseg_x;
-            ud.seg = local % a.nseg_x;
-            tiles = a.tiles_x; nseg = a.nseg_x;
-        } else {
-            local -= nx;
-            ud.kind = kUnitQ;
-            ud.slot = b * a.Km + local / a.nseg_q;
-            ud.seg = local % a.nseg_q;
-            tiles = a.tiles_q; nseg = a.nseg_q;
-        }
-        ud.t0 = static_cast<int>(static_cast<long long>(ud.seg) * tiles / nseg);
-        ud.t1 = static_cast<int>(static_cast<long long>(ud.seg + 1) * tiles / nseg);
-        ud.temperature = r.temperature;
-        ud.top_k = r.top_k;
-        ud.top_p = r.top_p;
-        ud.presence = r.presence_penalty;
-        ud.frequency = r.frequency_penalty;
-        ud.pad = 0;
-        const int c = u % G, g = (u / G) & 1, m = u / (2 * G);
-        a.units[(static_cast<long long>(c) * kGroups + g) * a.max_seg + m] = ud;
-    }
-}
 
 // First indices in ids[lo, hi) with ids[idx] >= key0 and >= key1 (key0 <= key1), by a
 // block-wide 256-way narrowing of both ranges at once.
@@ -150,10 +64,18 @@ __device__ void penalty_index_block(const Args& a, int b, int t) {
     __syncthreads();
     const dspark_row_params_t r = s_r;
     const int K = r.num_drafts;
-    if (params_status(a, r) != 0) return;
-    for (int i = tid; i < K; i += kPrepThreads) if (s_d[i] < 0 || s_d[i] >= a.V) s_bad = 1;
+    const int pst = params_status(a, r);
+    if (pst == 0)
+        for (int i = tid; i < K; i += kPrepThreads) if (s_d[i] < 0 || s_d[i] >= a.V) s_bad = 1;
     __syncthreads();
-    if (s_bad) return;
+    if (t == 0 && tid == 0) {
+        const int st = pst ? pst : (s_bad ? DSPARK_ROW_BAD_DRAFT : 0);
+        if (st) atomicOr(&a.row_status[b], st);
+        const int nx = st ? 0 : (K + 1) * a.nseg_x;
+        a.req_n[b] = st ? 0 : nx + (r.temperature > 0.f ? K * a.nseg_q : 0);
+        a.req_n[a.B + b] = nx;
+    }
+    if (pst || s_bad) return;
     const int e0 = t * a.tile_x, e1 = min(a.V, e0 + a.tile_x);
     const int hlo = s_hlo, hhi = s_hhi;
     // history validation (once per request): ascending ids in range, positive counts
@@ -232,25 +154,14 @@ __device__ void penalty_index_block(const Args& a, int b, int t) {
 }
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Args a) {
-    if (blockIdx.x == 0) {
-        plan_block(a);
-        return;
-    }
-    const int w = blockIdx.x - 1;
-    penalty_index_block(a, w / a.tiles_x, w % a.tiles_x);
+    penalty_index_block(a, blockIdx.x / a.tiles_x, blockIdx.x % a.tiles_x);
 }
 
 }  // namespace
 
 cudaError_t launch_prep(const Args& a, cudaStream_t s) {
-    const int grid = 1 + a.B * a.tiles_x;
-    const size_t smem = static_cast<size_t>(a.B) * sizeof(dspark_row_params_t) + static_cast<size_t>(2 * a.B + 1) * sizeof(int);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
-    prep_kernel<<<grid, kPrepThreads, smem, s>>>(a);
+    const int grid = a.B * a.tiles_x;
+    prep_kernel<<<grid, kPrepThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

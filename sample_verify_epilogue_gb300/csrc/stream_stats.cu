@@ -972,13 +972,87 @@ __device__ __forceinline__ int stream_len(int S, int G, int c, int g) {
     return first >= S ? 0 : (S - 1 - first) / (2 * G) + 1;
 }
 
+// The plan, derived by every CTA from the per-request segment counts: request b owns the
+// segments [base_b, base_b + n_b) of the call (its target rows' segments first, row by row,
+// then its draft rows'), and segment s goes to CTA s mod G, consumer group (s div G) mod 2,
+// position s div 2G of that group's stream.  The CTA writes the descriptors of its own two
+// streams to its slice of the unit array and returns the number of segments S.  The
+// exclusive prefix of the counts is built in the first data stage, which no copy has
+// touched yet.  Every thread of the CTA calls it.
+__device__ int build_streams(const Args& a, Smem& sm, int c, int G) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int B = a.B;
+    int* base = reinterpret_cast<int*>(sm.data[0]);          // [B + 1]
+    int* nxs = base + B + 1;                                  // [B]
+    static_assert(sizeof(int) * (2 * kMaxB + 1) <= kStageBytes, "plan scratch must fit one stage");
+    if (tid < 32) {
+        // lane l scans its own chunk of requests, then the chunk totals are scanned across lanes
+        const int chunk = (B + 31) / 32;
+        const int lo = min(B, lane * chunk), hi = min(B, lo + chunk);
+        int sum = 0;
+        for (int b = lo; b < hi; ++b) sum += a.req_n[b];
+        int incl = sum;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int run = incl - sum;
+        for (int b = lo; b < hi; ++b) {
+            base[b] = run;
+            run += a.req_n[b];
+            nxs[b] = a.req_n[B + b];
+        }
+        if (lane == 31) base[B] = incl;
+    }
+    __syncthreads();
+    const int S = base[B];
+    for (int idx = tid; idx < kGroups * a.max_seg; idx += blockDim.x) {
+        const int g = idx / a.max_seg, m = idx - g * a.max_seg;
+        const long long s = c + static_cast<long long>(G) * (g + 2 * m);
+        if (s >= S) continue;
+        int l = 0, h = B;                                     // last b with base[b] <= s
+        while (h - l > 1) {
+            const int mid = (l + h) >> 1;
+            if (base[mid] <= s) l = mid; else h = mid;
+        }
+        const int b = l;
+        int local = static_cast<int>(s - base[b]);
+        const dspark_row_params_t r = a.rows[b];
+        UnitDesc ud;
+        ud.b = b;
+        int tiles, nseg;
+        if (local < nxs[b]) {
+            ud.kind = kUnitX;
+            ud.slot = b * (a.Km + 1) + local / a.nseg_x;
+            ud.seg = local % a.nseg_x;
+            tiles = a.tiles_x; nseg = a.nseg_x;
+        } else {
+            local -= nxs[b];
+            ud.kind = kUnitQ;
+            ud.slot = b * a.Km + local / a.nseg_q;
+            ud.seg = local % a.nseg_q;
+            tiles = a.tiles_q; nseg = a.nseg_q;
+        }
+        ud.t0 = static_cast<int>(static_cast<long long>(ud.seg) * tiles / nseg);
+        ud.t1 = static_cast<int>(static_cast<long long>(ud.seg + 1) * tiles / nseg);
+        ud.temperature = r.temperature;
+        ud.top_k = r.top_k;
+        ud.top_p = r.top_p;
+        ud.presence = r.presence_penalty;
+        ud.frequency = r.frequency_penalty;
+        ud.pad = 0;
+        a.units[(static_cast<long long>(c) * kGroups + g) * a.max_seg + m] = ud;
+    }
+    __syncthreads();                                          // descriptors written, scratch free
+    return S;
+}
+
 // ------------------------------------------------------------------ the kernel
 template <int SX>
 __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const int tid = threadIdx.x;
-    const int S = a.plan->n_units;
     const int G = gridDim.x;
     const int c = blockIdx.x;
     if (tid == 0) {
@@ -986,7 +1060,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
         for (int g = 0; g < kGroups; ++g) { sm.grp[g].cnt_pen = 0; sm.grp[g].cnt_raw = 0; sm.grp[g].error = 0; }
         fence_mbar_init();
     }
-    __syncthreads();
+    const int S = build_streams(a, sm, c, G);
 
     if (tid >= kConsumerThreads) {
         // ---------------- producer warp.  Lane 16g+f holds field f of group g's current,
