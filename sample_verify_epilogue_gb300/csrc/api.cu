@@ -18,7 +18,7 @@ constexpr int kMaxGrid = 1024;           // streaming CTAs on any device (an SM 
 struct Layout {
     int tile_x, tiles_x, tile_q, tiles_q, bm_words, xslots, qslots, nseg_x, nseg_q;
     long long seg_max;
-    size_t off_plan, off_req_n, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_raw, off_cand_q;
+    size_t off_plan, off_req_n, off_fin_list, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_raw, off_cand_q;
     size_t off_pen_hdr, off_pen_bm, off_pen_ent, off_draft_base, off_xout, off_kept, off_topn, off_qout, off_req;
     size_t total;
 };
@@ -54,6 +54,7 @@ Layout make_layout(const dspark_params_t* p) {
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
     L.off_plan = take(sizeof(Plan));
     L.off_req_n = take(static_cast<size_t>(2 * B) * sizeof(int));
+    L.off_fin_list = take(static_cast<size_t>(1 + L.xslots + L.qslots) * sizeof(int));
     // segment streams: grid x groups x ceil(S / (groups*grid)) entries <= S + groups*grid
     L.off_units = take((xt + qt + static_cast<size_t>(kGroups) * kMaxGrid) * sizeof(UnitDesc));
     L.off_ts_x = take(xt * sizeof(TileStats));
@@ -112,6 +113,7 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     a.out_top_ids = out_top_ids; a.out_top_lp = out_top_logprobs; a.row_status = p->row_status;
     a.plan = at<Plan>(ws, L.off_plan);
     a.req_n = at<int>(ws, L.off_req_n);
+    a.fin_list = at<int>(ws, L.off_fin_list);
     a.units = at<UnitDesc>(ws, L.off_units);
     a.ts_x = at<TileStats>(ws, L.off_ts_x);
     a.ts_q = at<TileStats>(ws, L.off_ts_q);
@@ -143,6 +145,7 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_stream_stats(a, s, sms) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (launch_row_finalize_warp(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_row_finalize(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_accept(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_finish(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
@@ -273,6 +276,6 @@ const char* dspark_status_string(dspark_status_t status) {
     return "unknown status";
 }
 
-int32_t dspark_launches_per_call(void) { return 5; }
+int32_t dspark_launches_per_call(void) { return 7; }
 
 }  // extern "C"

@@ -172,6 +172,7 @@ struct Args {
     PenEntry* pen_ent;     // [B * tiles_x * kPenCap]
     int* draft_base;       // [B * Km]
     int* req_n;            // [2B]: segments of request b (0 if invalid), then its target-row segments
+    int* fin_list;         // [1 + xslots + qslots]: count, then the rows left to the block finalize
     XRowOut* xout;         // [xslots]
     KeptEntry* kept;       // [xslots * kKeptCap]
     TopEntry* topn;        // [xslots * DSPARK_MAX_TOP_LOGPROBS]
@@ -387,6 +388,7 @@ __device__ __forceinline__ bool has_penalty(const dspark_row_params_t& r) {
 
 // ---------------------------------------------------------------- launchers (one per .cu)
 cudaError_t launch_prep(const Args& a, cudaStream_t s);
+cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s);
 cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid);
 cudaError_t launch_row_finalize(const Args& a, cudaStream_t s);
 cudaError_t launch_accept(const Args& a, cudaStream_t s);

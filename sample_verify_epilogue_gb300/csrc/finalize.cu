@@ -1,5 +1,5 @@
-// row_finalize_kernel: one CTA per verify row (target position (b, j) or draft position
-// (b, i)).  Merges the per-segment statistics of the streaming pass and settles the row's
+// row_finalize_kernel: one CTA per verify row left by the warp finalize (target position (b, j)
+// or draft position (b, i)).  Merges the per-segment statistics of the streaming pass and settles the row's
 // truncated distribution:
 //   - target rows: raw log-sum-exp (logprobs), penalised max and argmax (greedy), the top-k
 //     threshold tau_k = k-th largest penalised logit among the merged segment candidates (exact:
@@ -655,10 +655,7 @@ __device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
     if (tid == 0) a.qout[qslot] = o;
 }
 
-__global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(Args a) {
-    extern __shared__ __align__(16) unsigned char fin_raw[];
-    FinSmem& s = *reinterpret_cast<FinSmem*>(fin_raw);
-    const int slot = blockIdx.x;
+__device__ void finalize_row(const Args& a, FinSmem& s, int slot) {
     if (slot < a.xslots) {
         const int b = slot / (a.Km + 1), j = slot % (a.Km + 1);
         if ((request_status(a, b) & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || j > a.rows[b].num_drafts) {
@@ -679,13 +676,26 @@ __global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(Args a) {
     }
 }
 
+// The rows the warp finalize left (fin_list), each by a whole block.
+__global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(Args a) {
+    extern __shared__ __align__(16) unsigned char fin_raw[];
+    FinSmem& s = *reinterpret_cast<FinSmem*>(fin_raw);
+    const int n = a.fin_list[0];
+    for (int i = blockIdx.x; i < n; i += gridDim.x) {
+        finalize_row(a, s, a.fin_list[1 + i]);
+        __syncthreads();                                  // shared memory reused by the next row
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_row_finalize(const Args& a, cudaStream_t s) {
     const size_t smem = sizeof(FinSmem) > sizeof(FullSmem) ? sizeof(FinSmem) : sizeof(FullSmem);
     cudaError_t e = cudaFuncSetAttribute(row_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    row_finalize_kernel<<<a.xslots + a.qslots, kFinThreads, smem, s>>>(a);
+    const int rows = a.xslots + a.qslots;
+    const int grid = rows < 4 * a.grid_ss ? rows : 4 * a.grid_ss;
+    row_finalize_kernel<<<grid, kFinThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 

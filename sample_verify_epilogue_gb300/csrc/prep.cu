@@ -61,6 +61,7 @@ __device__ void penalty_index_block(const Args& a, int b, int t) {
     if (tid == 32) { s_hlo = a.h_off ? a.h_off[b] : 0; s_hhi = a.h_off ? a.h_off[b + 1] : 0; }
     if (tid >= 64 && tid < 64 + a.Km) s_d[tid - 64] = a.d[static_cast<long long>(b) * a.Km + (tid - 64)];
     if (tid == 0) s_bad = 0;
+    if (b == 0 && t == 0 && tid == 0) a.fin_list[0] = 0;    // rows left to the block finalize
     __syncthreads();
     const dspark_row_params_t r = s_r;
     const int K = r.num_drafts;
