@@ -158,6 +158,32 @@ dspark_status_t dspark_verify_sample_host(const void* logits, const float* q, co
                                           const float* uniforms, int32_t* out_accept_len, int32_t* out_tokens,
                                           float* out_logprobs, int32_t* out_top_ids, float* out_top_logprobs);
 
+/* Size of the fixed device scratch of dspark_verify_sample_static (per device). */
+#define DSPARK_STATIC_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * dspark_verify_sample with no workspace argument and no allocation: the scratch is a
+ * file-scope device array of DSPARK_STATIC_WORKSPACE_BYTES (16 MiB) per device, so the call
+ * makes no cudaMalloc / cudaFree or other allocating call and can be captured in a CUDA
+ * graph.  This entry point has no counterpart in the mlx-dspark pages: it exists for callers
+ * that must not allocate (graph capture, allocator-free serving loops).
+ *   - Arguments, layouts and results are those of dspark_verify_sample;
+ *     params->workspace and params->workspace_bytes are ignored.
+ *   - Shapes whose dspark_workspace_bytes exceeds DSPARK_STATIC_WORKSPACE_BYTES are rejected
+ *     with DSPARK_ERR_UNSUPPORTED before any CUDA call.
+ *   - The first call on a device looks the array's address up (cudaGetSymbolAddress, with
+ *     that device current) and caches it; make that first call before any stream capture.
+ *     A failed lookup returns DSPARK_ERR_CUDA.
+ *   - Nothing in the scratch has to start at zero: every call clears the one record it reads
+ *     before writing (with cudaMemsetAsync on params->stream).
+ *   - All calls on one device share the array: calls that overlap on the GPU (other streams,
+ *     other host threads) race and give undefined results.  Serialise them.
+ */
+dspark_status_t dspark_verify_sample_static(const void* logits, const float* q, const int32_t* draft_ids,
+                                            const dspark_counts_t* counts, const dspark_params_t* params,
+                                            const float* uniforms, int32_t* out_accept_len, int32_t* out_tokens,
+                                            float* out_logprobs, int32_t* out_top_ids, float* out_top_logprobs);
+
 /* Human-readable name of a status code. */
 const char* dspark_status_string(dspark_status_t status);
 

@@ -47,7 +47,10 @@ class dspark_params_t(ctypes.Structure):
 _lib = None
 
 EXPORTS = ("dspark_workspace_bytes", "dspark_verify_sample", "dspark_host_workspace_bytes",
-           "dspark_verify_sample_host", "dspark_status_string", "dspark_launches_per_call")
+           "dspark_verify_sample_host", "dspark_verify_sample_static", "dspark_status_string",
+           "dspark_launches_per_call")
+
+DSPARK_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
 def load_library(path: str = LIB):
@@ -71,6 +74,8 @@ def load_library(path: str = LIB):
     lib.dspark_verify_sample.restype = ctypes.c_int
     lib.dspark_verify_sample_host.argtypes = sig
     lib.dspark_verify_sample_host.restype = ctypes.c_int
+    lib.dspark_verify_sample_static.argtypes = sig
+    lib.dspark_verify_sample_static.restype = ctypes.c_int
     lib.dspark_status_string.argtypes = [ctypes.c_int]
     lib.dspark_status_string.restype = ctypes.c_char_p
     lib.dspark_launches_per_call.argtypes = []
@@ -125,6 +130,29 @@ def _check(code):
         raise RuntimeError(f"dspark: {dspark_status_string(code)} ({code})")
 
 
+def _device_call(fn, logits, q, draft_ids, counts, rows, uniforms, out, row_status, workspace, want_logprobs,
+                 n_top_logprobs, stream, stage_events):
+    import torch
+    B, W, V = logits.shape
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device).cuda_stream
+    dt = DSPARK_BF16 if logits.dtype == torch.bfloat16 else DSPARK_FP32
+    p = make_params(B, W - 1, V, dt, rows=rows.data_ptr(), want_logprobs=want_logprobs,
+                    n_top_logprobs=n_top_logprobs,
+                    workspace=None if workspace is None else workspace.data_ptr(),
+                    workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+                    stream=stream, row_status=row_status.data_ptr(),
+                    stage_events=tuple(None if e is None else e for e in stage_events))
+    c = None
+    if counts is not None:
+        c = dspark_counts_t(counts[0].data_ptr(), counts[1].data_ptr(), counts[2].data_ptr())
+    code = fn(
+        _ptr(logits), _ptr(q), _ptr(draft_ids), ctypes.byref(c) if c is not None else None, ctypes.byref(p),
+        _ptr(uniforms), _ptr(out["accept_len"]), _ptr(out["tokens"]), _ptr(out.get("logprobs")),
+        _ptr(out.get("top_ids")), _ptr(out.get("top_logprobs")))
+    _check(code)
+
+
 def dspark_verify_sample(logits, q, draft_ids, counts, rows, uniforms, *, out, row_status, workspace,
                          want_logprobs=False, n_top_logprobs=0, stream=None, stage_events=(None, None)):
     """Enqueue the epilogue on ``stream`` (default: torch's current stream).
@@ -135,25 +163,17 @@ def dspark_verify_sample(logits, q, draft_ids, counts, rows, uniforms, *, out, r
     out: dict with "accept_len" [B], "tokens" [B, K_max+1] int32, and optionally
     "logprobs" [B, K_max+1], "top_ids" / "top_logprobs" [B, K_max+1, n] tensors.
     """
-    import torch
-    lib = load_library()
-    B, W, V = logits.shape
-    if stream is None:
-        stream = torch.cuda.current_stream(logits.device).cuda_stream
-    dt = DSPARK_BF16 if logits.dtype == torch.bfloat16 else DSPARK_FP32
-    p = make_params(B, W - 1, V, dt, rows=rows.data_ptr(), want_logprobs=want_logprobs,
-                    n_top_logprobs=n_top_logprobs, workspace=workspace.data_ptr(),
-                    workspace_bytes=workspace.numel() * workspace.element_size(), stream=stream,
-                    row_status=row_status.data_ptr(),
-                    stage_events=tuple(None if e is None else e for e in stage_events))
-    c = None
-    if counts is not None:
-        c = dspark_counts_t(counts[0].data_ptr(), counts[1].data_ptr(), counts[2].data_ptr())
-    code = lib.dspark_verify_sample(
-        _ptr(logits), _ptr(q), _ptr(draft_ids), ctypes.byref(c) if c is not None else None, ctypes.byref(p),
-        _ptr(uniforms), _ptr(out["accept_len"]), _ptr(out["tokens"]), _ptr(out.get("logprobs")),
-        _ptr(out.get("top_ids")), _ptr(out.get("top_logprobs")))
-    _check(code)
+    _device_call(load_library().dspark_verify_sample, logits, q, draft_ids, counts, rows, uniforms, out,
+                 row_status, workspace, want_logprobs, n_top_logprobs, stream, stage_events)
+
+
+def dspark_verify_sample_static(logits, q, draft_ids, counts, rows, uniforms, *, out, row_status,
+                                want_logprobs=False, n_top_logprobs=0, stream=None, stage_events=(None, None)):
+    """The same call with the library's fixed device scratch (no workspace, no allocation);
+    shapes needing more than DSPARK_STATIC_WORKSPACE_BYTES are refused.  Calls that overlap
+    on the GPU race on that scratch."""
+    _device_call(load_library().dspark_verify_sample_static, logits, q, draft_ids, counts, rows, uniforms, out,
+                 row_status, None, want_logprobs, n_top_logprobs, stream, stage_events)
 
 
 def dspark_verify_sample_host(logits, q, draft_ids, counts, rows, uniforms, *, out, row_status, workspace,

@@ -1,5 +1,6 @@
 // Host side of the C ABI: argument checks, workspace layout, the launch sequence.
 #include <cstring>
+#include <mutex>
 
 #include "dspark_internal.cuh"
 
@@ -157,6 +158,15 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
 
 using namespace dspark;
 
+// Scratch of dspark_verify_sample_static: a fixed device array (one instance per device).
+static __device__ __align__(256) unsigned char g_static_workspace[DSPARK_STATIC_WORKSPACE_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};   // cached device address of g_static_workspace, per device
+}  // namespace
+
 extern "C" {
 
 size_t dspark_workspace_bytes(const dspark_params_t* params) {
@@ -263,6 +273,31 @@ dspark_status_t dspark_verify_sample_host(const void* logits, const float* q, co
     if (!ok) return DSPARK_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
+}
+
+dspark_status_t dspark_verify_sample_static(const void* logits, const float* q, const int32_t* draft_ids,
+                                            const dspark_counts_t* counts, const dspark_params_t* params,
+                                            const float* uniforms, int32_t* out_accept_len, int32_t* out_tokens,
+                                            float* out_logprobs, int32_t* out_top_ids, float* out_top_logprobs) {
+    if (!shapes_ok(params)) return DSPARK_ERR_INVALID_ARG;
+    if (make_layout(params).total > DSPARK_STATIC_WORKSPACE_BYTES) return DSPARK_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        const bool cached = dev >= 0 && dev < kMaxDevices;
+        if (cached) ws = g_static_ptr[dev];
+        if (!ws) {
+            if (cudaGetSymbolAddress(&ws, g_static_workspace) != cudaSuccess || !ws) return DSPARK_ERR_CUDA;
+            if (cached) g_static_ptr[dev] = ws;
+        }
+    }
+    dspark_params_t p = *params;
+    p.workspace = ws;
+    p.workspace_bytes = DSPARK_STATIC_WORKSPACE_BYTES;
+    return run(logits, q, draft_ids, counts, &p, uniforms, out_accept_len, out_tokens, out_logprobs, out_top_ids,
+               out_top_logprobs);
 }
 
 const char* dspark_status_string(dspark_status_t status) {
