@@ -31,6 +31,7 @@ WORKLOAD = "b64k8v262144"
 METRIC = "verify rows/s & HBM GB/s (% roofline), B=64 K=8 V=262144 bf16, 1×GB300"
 UNIT = "verify rows/s"
 DOMINANT = "stream_stats_kernel"
+CPU_SAMPLE_S = 10.0                   # seconds of oracle work in the native arm's cpu_baseline
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stream_stats_kernel_b64k8v262144.md")
 KERNEL_SOURCES = [os.path.join(ROOT, "sample_verify_epilogue_gb300", "csrc", f)
                   for f in ("stream_stats.cu", "dspark_internal.cuh")]
@@ -53,9 +54,10 @@ def measured_traffic():
         return None
     vals = {}
     for ln in txt.splitlines():
-        if ":" in ln and ln.strip().startswith(("traffic_bytes_per_launch", "kernel_source_hash")):
+        ln = ln.strip().lstrip("-* ")
+        if ":" in ln and ln.startswith(("traffic_bytes_per_launch", "kernel_source_hash")):
             k, v = ln.split(":", 1)
-            vals[k.strip().strip("-* ")] = v.strip().strip("`")
+            vals[k.strip()] = v.strip().strip("`")
     if vals.get("kernel_source_hash") != kernel_source_hash():
         return None
     try:
@@ -314,10 +316,15 @@ def run_native(args):
 
     cpu = None
     if rank == 0 and ws == 1:
-        sample = configs.build(WORKLOAD, B=2)
-        t = time_oracle(sample, [0, 1])
-        cpu = {"value": sample.verify_rows() / t, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "2 requests (18 verify rows) of the workload, float64 numpy oracle, single thread"}
+        # the oracle on requests of this very batch, one after another, for about 10 s
+        n_req, t = 0, 0.0
+        while n_req < batch.B and (n_req == 0 or t < CPU_SAMPLE_S):
+            t += time_oracle(batch, [n_req])
+            n_req += 1
+        rows_done = int(sum(int(batch.rows[b]["num_drafts"]) + 1 for b in range(n_req)))
+        cpu = {"value": rows_done / t, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_req} requests ({rows_done} verify rows) of the timed batch, float64 numpy oracle, "
+                         f"single thread, {t:.1f} s"}
 
     if rank == 0:
         out = {
