@@ -28,13 +28,12 @@ constexpr int kStageBytes = 40 * 1024;                         // one vocab tile
 constexpr int kTileBf16 = kStageBytes / 2;                     // 20480 elements
 constexpr int kTileF32 = kStageBytes / 4;                      // 10240 elements
 constexpr int kBitmapWordsMax = kTileBf16 / 32;                // 640
-constexpr int kPenCap = 384;                                   // penalised tokens per tile held in smem
-constexpr int kSegTiles = 4;                                   // vocab tiles per segment (target)
+constexpr int kPenCap = 256;                                   // penalised tokens per tile held in smem
+constexpr int kSegTiles = 6;                                   // vocab tiles per segment (target)
 constexpr int kMaxSegTiles = 16;
-constexpr int kSmemCandPen = 1024;                             // per-segment candidate buffer (smem)
-constexpr int kSmemCandRaw = 512;
-constexpr int kCandPenGlobal = 1024;                           // per-segment candidates kept in the workspace
-constexpr int kCandRawGlobal = 512;
+constexpr int kSmemCandPool = 2048;                            // per-segment candidates (smem), both kinds
+constexpr int kCandPenGlobal = 1536;                           // per-segment candidates kept in the workspace
+constexpr int kCandRawGlobal = 1024;
 constexpr int kMaxCandTopK = 256;                              // top_k above this uses the whole-row path
 constexpr int kKeptCap = 1024;                                 // truncated support held as a list
 constexpr int kFinalizeThreads = 512;

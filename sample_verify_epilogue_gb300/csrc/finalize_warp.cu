@@ -371,7 +371,7 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
 // own top-k (with ties): s holds fewer than k values above the row's k-th largest.  So each
 // segment's candidate list can be cut to its own top-k before the row-level selection, one
 // warp per list, all lists at once.
-constexpr int kTrimCap = 1024;         // keys one warp stages (the candidate list cap)
+constexpr int kTrimCap = 1536;         // keys one warp stages (the candidate list cap)
 
 struct TrimSmem {
     uint32_t keys[kTrimCap];

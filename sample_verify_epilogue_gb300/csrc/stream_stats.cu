@@ -43,7 +43,17 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, unsigned parity) {
         if (globaltimer() - t0 > kWaitNs) return false;
     return true;
 }
+
+// The same, giving up at once when *err is set (another thread of the group already gave up).
+__device__ __forceinline__ bool wait_phase_or_err(uint64_t* bar, unsigned parity, const volatile int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity))
+        if (*err || globaltimer() - t0 > kWaitNs) return false;
+    return true;
+}
 constexpr float kL2E = 1.4426950408889634f;
+constexpr int kRawTag = static_cast<int>(0x80000000u);  // marks raw-logit candidates in the pool (ids < 2^24)
 constexpr int kVecPerThread = kStageBytes / 16 / kGroupThreads;     // 10 vectors per thread and tile
 static_assert(kVecPerThread % 2 == 0, "vectors are scanned in pairs");
 
@@ -57,13 +67,12 @@ struct StageMeta {
 };
 
 struct GroupSmem {
-    Cand cpen[kSmemCandPen];
-    Cand craw[kSmemCandRaw];
+    Cand pool[kSmemCandPool];    // the segment's candidates; raw-logit ones carry kRawTag in the id
     float4 red1[kGroupWarps];    // first-tile maxima and thresholds
     float4 red[kGroupWarps];     // end-of-segment partials
     float4 red2[kGroupWarps];
-    int cnt_pen;
-    int cnt_raw;
+    int cnt;                     // entries appended to the pool
+    int out_pen, out_raw;        // entries written to the global lists (segment finish)
     int error;
 };
 
@@ -215,7 +224,8 @@ __device__ __forceinline__ void warp_merge_ms(float& m, float& s, float scale) {
 // candidate buffer: one ballot, one prefix across lanes and one shared atomic per warp.
 // Every lane of the warp calls it (lanes without candidates pass mask = 0).
 template <int SX>
-__device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsigned mask, const uint4& w, int e) {
+__device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsigned mask, const uint4& w, int e,
+                                            int tag) {
     const unsigned any = __ballot_sync(0xffffffffu, mask != 0u);
     if (!any) return;
     const int lane = threadIdx.x & 31;
@@ -232,7 +242,7 @@ __device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsign
     while (mask) {
         const int q = __ffs(mask) - 1;
         mask &= mask - 1u;
-        if (base < cap) buf[base] = Cand{elem<SX>(w, q), e + q};
+        if (base < cap) buf[base] = Cand{elem<SX>(w, q), (e + q) | tag};
         ++base;
     }
 }
@@ -242,7 +252,7 @@ __device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsign
 // one shared atomic per warp and tile.  All lanes of the warp call it.
 template <int SX>
 __device__ __forceinline__ void flush_flags(Cand* buf, int* cnt, int cap, unsigned long long f0, unsigned long long f1,
-                                            const unsigned char* data, int vec_e0, int gt) {
+                                            const unsigned char* data, int vec_e0, int gt, int tag) {
     constexpr int EPV = 16 / SX;
     const int n = __popcll(f0) + __popcll(f1);
     if (!__ballot_sync(0xffffffffu, n != 0)) return;
@@ -265,7 +275,7 @@ __device__ __forceinline__ void flush_flags(Cand* buf, int* cnt, int cap, unsign
             const int i = bit / EPV, q = bit % EPV;
             const int v = gt + i * kGroupThreads;
             const uint4 w = *reinterpret_cast<const uint4*>(data + v * 16);
-            if (base < cap) buf[base] = Cand{elem<SX>(w, q), vec_e0 + v * EPV + q};
+            if (base < cap) buf[base] = Cand{elem<SX>(w, q), (vec_e0 + v * EPV + q) | tag};
             ++base;
         }
     }
@@ -329,8 +339,8 @@ __device__ __forceinline__ void flush_vectors(GroupSmem& gs, unsigned vflags, co
             if (RAW) mr = ge_mask<SX>(w, th_r);
             mp = ge_mask<SX>(w, th_p) & ~bits;
         }
-        if (RAW) warp_append<SX>(gs.craw, &gs.cnt_raw, kSmemCandRaw, mr, w, e);
-        if (CAND) warp_append<SX>(gs.cpen, &gs.cnt_pen, kSmemCandPen, mp, w, e);
+        if (RAW) warp_append<SX>(gs.pool, &gs.cnt, kSmemCandPool, mr, w, e, kRawTag);
+        if (CAND) warp_append<SX>(gs.pool, &gs.cnt, kSmemCandPool, mp, w, e, 0);
         if (TRACK) {
             while (mp) {
                 const int q = __ffs(mp) - 1;
@@ -393,7 +403,7 @@ __device__ __forceinline__ void pen_fold(const XCtx<SX>& c, XState& st, float xp
         st.s_t += ex2_approx((xp - st.m_p) * c.c_l2e);
         if (undo_raw) st.s_t -= ex2_approx((xr - st.m_p) * c.c_l2e);
     }
-    if (xp >= st.th_p) push(c.gs.cpen, &c.gs.cnt_pen, kSmemCandPen, xp, e);
+    if (xp >= st.th_p) push(c.gs.pool, &c.gs.cnt, kSmemCandPool, xp, e);
 }
 
 // One 16-byte vector: raw statistics over all its elements, penalised statistics over the
@@ -454,7 +464,7 @@ __device__ __forceinline__ void fold_fast(const XCtx<SX>& c, XState& st, float x
     if (xp >= st.th_p) {
         if (xp > st.m_p) { st.m_p = xp; st.arg = e; }
         else if (xp == st.m_p && e < st.arg) st.arg = e;
-        if (c.need_cand) push(c.gs.cpen, &c.gs.cnt_pen, kSmemCandPen, xp, e);
+        if (c.need_cand) push(c.gs.pool, &c.gs.cnt, kSmemCandPool, xp, e);
     }
 }
 
@@ -706,8 +716,8 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
         if (sh < 64) { fr0 |= static_cast<unsigned long long>(mr) << sh; fp0 |= static_cast<unsigned long long>(mp) << sh; }
         else { fr1 |= static_cast<unsigned long long>(mr) << (sh - 64); fp1 |= static_cast<unsigned long long>(mp) << (sh - 64); }
     }
-    if (!fast && c.need_raw) flush_flags<SX>(c.gs.craw, &c.gs.cnt_raw, kSmemCandRaw, fr0, fr1, data, m.vec_e0, gt);
-    if (!fast && c.need_cand) flush_flags<SX>(c.gs.cpen, &c.gs.cnt_pen, kSmemCandPen, fp0, fp1, data, m.vec_e0, gt);
+    if (!fast && c.need_raw) flush_flags<SX>(c.gs.pool, &c.gs.cnt, kSmemCandPool, fr0, fr1, data, m.vec_e0, gt, kRawTag);
+    if (!fast && c.need_cand) flush_flags<SX>(c.gs.pool, &c.gs.cnt, kSmemCandPool, fp0, fp1, data, m.vec_e0, gt, 0);
     if (gt < 2) {
         const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
         for (int e = lo; e < hi; ++e) {
@@ -723,7 +733,7 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
             } else {
                 st.m_r = max_nan(st.m_r, xv);
             }
-            if (xv >= st.th_r) push(c.gs.craw, &c.gs.cnt_raw, kSmemCandRaw, xv, e);
+            if (xv >= st.th_r) push(c.gs.pool, &c.gs.cnt, kSmemCandPool, xv, e | kRawTag);
             const bool bit = m.pen && bitmap_bit(bm, e - m.e0);
             if (fast) {
                 if (!bit) fold_fast(c, st, xv, e);
@@ -757,8 +767,23 @@ __device__ void x_finish(const XCtx<SX>& c, XState& st) {
         c.gs.red2[warp] = make_float4(__int_as_float(arg), 0.f, 0.f, 0.f);
     }
     group_sync(c.g);
-    const int n_pen = c.gs.cnt_pen, n_raw = c.gs.cnt_raw;
+    // the pool into the segment's two global lists (order within a list is immaterial)
     const long long ti = static_cast<long long>(m.slot) * c.a.nseg_x + m.seg;
+    Cand* gpen = c.a.cand_x + ti * kCandPenGlobal;
+    Cand* graw = c.a.cand_raw + ti * kCandRawGlobal;
+    const int total = c.gs.cnt;
+    const int n = min(total, kSmemCandPool);
+    for (int i = gt; i < n; i += kGroupThreads) {
+        const Cand e = c.gs.pool[i];
+        if (e.id & kRawTag) {
+            const int p = atomicAdd(&c.gs.out_raw, 1);
+            if (p < kCandRawGlobal) graw[p] = Cand{e.v, e.id & ~kRawTag};
+        } else {
+            const int p = atomicAdd(&c.gs.out_pen, 1);
+            if (p < kCandPenGlobal) gpen[p] = e;
+        }
+    }
+    group_sync(c.g);
     if (warp == 0) {
         float4 r = lane < kGroupWarps ? c.gs.red[lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
         int ag = lane < kGroupWarps ? __float_as_int(c.gs.red2[lane].x) : 0x7FFFFFFF;
@@ -770,27 +795,21 @@ __device__ void x_finish(const XCtx<SX>& c, XState& st) {
         warp_merge_ms(Mr, Sr, kL2E);
         warp_merge_ms(Mp, St, c.c_l2e);
         if (lane == 0) {
+            const int n_pen = c.gs.out_pen, n_raw = c.gs.out_raw;
+            const bool lost = total > kSmemCandPool;      // some appends were dropped (of either kind)
             TileStats ts;
             ts.m_raw = Mr; ts.s_raw = Sr; ts.m_pen = Mp; ts.arg_pen = ag; ts.s_temp = St;
             ts.flags = 0;
             ts.n_pen = c.need_cand ? n_pen : 0;
             ts.n_raw = c.need_raw ? n_raw : 0;
-            if (c.need_cand && n_pen > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
-            if (c.need_raw && n_raw > kCandRawGlobal) { ts.flags |= kTileOverflowRaw; ts.n_raw = 0; }
+            if (c.need_cand && (lost || n_pen > kCandPenGlobal)) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
+            if (c.need_raw && (lost || n_raw > kCandRawGlobal)) { ts.flags |= kTileOverflowRaw; ts.n_raw = 0; }
             if (!isfinite(Mr) || !isfinite(Mp)) ts.flags |= kTileBad;
             c.a.ts_x[ti] = ts;
+            // counters for the next segment (its first append follows its first-tile barrier)
+            c.gs.cnt = 0; c.gs.out_pen = 0; c.gs.out_raw = 0;
         }
     }
-    if (c.need_cand && n_pen <= kCandPenGlobal) {
-        Cand* dst = c.a.cand_x + ti * kCandPenGlobal;
-        for (int i = gt; i < n_pen; i += kGroupThreads) dst[i] = c.gs.cpen[i];
-    }
-    if (c.need_raw && n_raw <= kCandRawGlobal) {
-        Cand* dst = c.a.cand_raw + ti * kCandRawGlobal;
-        for (int i = gt; i < n_raw; i += kGroupThreads) dst[i] = c.gs.craw[i];
-    }
-    group_sync(c.g);                                      // buffers reused by the next segment
-    if (gt == 0) { c.gs.cnt_pen = 0; c.gs.cnt_raw = 0; }
 }
 
 // ------------------------------------------------------------------ draft-probability segments
@@ -807,7 +826,7 @@ __device__ __forceinline__ void q_elem(QState& st, float v, bool need_sum, bool 
     st.mx = max_nan(st.mx, v);
     st.mn = fminf(st.mn, v);
     if (need_sum) st.sum += t_one ? v : draft_weight(v, st.mx, inv_t, false);
-    if (filt && v >= st.th) push(gs.cpen, &gs.cnt_pen, kSmemCandPen, v, e);
+    if (filt && v >= st.th) push(gs.pool, &gs.cnt, kSmemCandPool, v, e);
 }
 
 __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage, const StageMeta& m, QState& st) {
@@ -938,7 +957,9 @@ __device__ void q_finish(const Args& a, GroupSmem& gs, int g, const StageMeta& m
     r = warp_sum(r);
     if (lane == 0) gs.red[warp] = make_float4(M, r, mnw, 0.f);
     group_sync(g);
-    const int n = gs.cnt_pen;
+    const int total = gs.cnt;                             // draft segments append no raw entries
+    const int n = min(total, kSmemCandPool);
+    const bool lost = total > kSmemCandPool;
     const long long ti = static_cast<long long>(m.slot) * a.nseg_q + m.seg;
     if (warp == 0) {
         const float4 v = lane < kGroupWarps ? gs.red[lane] : make_float4(-INFINITY, 0.f, INFINITY, 0.f);
@@ -953,17 +974,17 @@ __device__ void q_finish(const Args& a, GroupSmem& gs, int g, const StageMeta& m
             TileStats ts;
             ts.m_raw = Mg; ts.s_raw = t_one ? s : 0.f; ts.m_pen = mnn; ts.arg_pen = 0; ts.s_temp = t_one ? 0.f : s;
             ts.n_pen = need_cand ? n : 0; ts.n_raw = 0; ts.flags = 0;
-            if (need_cand && n > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
+            if (need_cand && (lost || n > kCandPenGlobal)) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
             if (!(mnn >= 0.f) || !(Mg <= 3.0e38f)) ts.flags |= kTileBad;
             a.ts_q[ti] = ts;
         }
     }
-    if (need_cand && n <= kCandPenGlobal) {
+    if (need_cand && !lost && n <= kCandPenGlobal) {
         Cand* dst = a.cand_q + ti * kCandPenGlobal;
-        for (int i = gt; i < n; i += kGroupThreads) dst[i] = gs.cpen[i];
+        for (int i = gt; i < n; i += kGroupThreads) dst[i] = gs.pool[i];
     }
     group_sync(g);
-    if (gt == 0) { gs.cnt_pen = 0; gs.cnt_raw = 0; }
+    if (gt == 0) { gs.cnt = 0; gs.out_pen = 0; gs.out_raw = 0; }
 }
 
 // Segments in the stream of (CTA c, group g): positions m with c + G*(g + 2m) < S.
@@ -1057,7 +1078,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
     const int c = blockIdx.x;
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], kGroupWarps); }
-        for (int g = 0; g < kGroups; ++g) { sm.grp[g].cnt_pen = 0; sm.grp[g].cnt_raw = 0; sm.grp[g].error = 0; }
+        for (int g = 0; g < kGroups; ++g) {
+            sm.grp[g].cnt = 0; sm.grp[g].out_pen = 0; sm.grp[g].out_raw = 0; sm.grp[g].error = 0;
+        }
         fence_mbar_init();
     }
     const int S = build_streams(a, sm, c, G);
@@ -1197,19 +1220,31 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
     const int gt = tid - g * kGroupThreads;
     GroupSmem& gs = sm.grp[g];
     const int nseg = stream_len(S, G, c, g);
+    // The tile counts come from this group's segment descriptors, so every warp of the group
+    // walks the same tiles and meets the same group barriers (one in the first tile's pass,
+    // two in a segment's finish) whatever happens to the data; warps are not synchronised
+    // tile by tile.  A tile whose wait gave up is skipped with only its barriers.
+    const UnitDesc* my = a.units + (static_cast<long long>(c) * kGroups + g) * a.max_seg;
+    int nt_next = nseg > 0 ? my[0].t1 - my[0].t0 : 0;
     int cnt = 0;                                           // tiles consumed by this group
     XState xs{};
     QState qs{};
-    for (int sgi = 0; sgi < nseg && !gs.error; ++sgi) {
-        bool last = false;
-        while (!last) {
+    for (int sgi = 0; sgi < nseg; ++sgi) {
+        const int ntile = min(nt_next, kMaxSegTiles);
+        if (sgi + 1 < nseg) nt_next = my[sgi + 1].t1 - my[sgi + 1].t0;
+        for (int ti = 0; ti < ntile; ++ti, ++cnt) {
             const int stage = g + 2 * (cnt & 1);
             const unsigned parity = (cnt >> 1) & 1;
-            if (!wait_phase(&sm.full[stage], parity)) gs.error = 1;
-            group_sync(g);
-            if (gs.error) break;
-            const StageMeta m = sm.meta[stage];
-            last = m.last;
+            if (!wait_phase_or_err(&sm.full[stage], parity, &gs.error)) {
+                gs.error = 1;
+                if (ti == 0) group_sync(g);
+                if (ti == ntile - 1) { group_sync(g); group_sync(g); }
+                continue;
+            }
+            StageMeta m = sm.meta[stage];
+            const bool last = ti == ntile - 1;
+            m.first = ti == 0;                             // barrier decisions follow the descriptor
+            m.last = last;
             if (m.kind == kUnitX) {
                 const bool greedy = !(m.temperature > 0.f);
                 const int k = m.top_k;
@@ -1222,7 +1257,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
                 q_tile(a, sm, gs, g, stage, m, qs);
                 if (last) q_finish(a, gs, g, m, qs);
             }
-            ++cnt;
         }
     }
     if (gt == 0 && gs.error) atomicOr(&a.plan->pad[0], 1);
