@@ -371,42 +371,91 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
 // own top-k (with ties): s holds fewer than k values above the row's k-th largest.  So each
 // segment's candidate list can be cut to its own top-k before the row-level selection, one
 // warp per list, all lists at once.
-constexpr int kTrimCap = 1536;         // keys one warp stages (the candidate list cap)
+constexpr int kTrimCap = 1536;         // longest list (the global caps)
+constexpr int kTrimStage = 512;        // survivors of the first stage kept for the exact second
+constexpr int kTrimMaxC = 8;           // ceil(k / 32) for k <= kMaxCandTopK
 
 struct TrimSmem {
-    uint32_t keys[kTrimCap];
+    uint32_t keys[kTrimStage];
+    int ids[kTrimStage];
 };
 static_assert(kTrimCap >= kCandPenGlobal && kTrimCap >= kCandRawGlobal, "a whole list must fit");
+static_assert(32 * kTrimMaxC >= kMaxCandTopK, "per-lane depth must cover k");
 
-// Cut the list `c[0..*n)` to its elements with key >= its k-th largest (in place; *n updated).
-// Left untouched when it is no longer than k.
+// Cut the list c[0..*n) down towards its own top-k (ties kept), in place, *n updated.
+//   1. Each lane keeps the c = ceil(k/32) largest keys of its share; the least of the
+//      lanes' c-th largest is a lower bound of the list's k-th largest (32c >= k keys reach it).
+//   2. The entries at or above that bound are compacted over the list's front; when at most
+//      kTrimStage remain they are also staged, the exact k-th largest is found among them
+//      and only the entries reaching it are kept.
 __device__ void trim_list(TrimSmem& w, Cand* c, int* n_io, int k) {
-    constexpr int kPer = kTrimCap / 32;
     const int lane = threadIdx.x & 31;
     const unsigned lt = (1u << lane) - 1u;
     const int n = *n_io;
     if (n <= k || n > kTrimCap) return;
-    int id[kPer];                                            // lane's ids, all loads in flight
+    const int cdepth = (k + 31) / 32;
+    uint32_t top[kTrimMaxC];                              // descending; 0 = nothing yet
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        const int i = lane + 32 * u;
-        if (i < n) { const Cand e = c[i]; w.keys[i] = fkey(e.v); id[u] = e.id; }
+    for (int q = 0; q < kTrimMaxC; ++q) top[q] = 0u;
+    for (int i0 = lane; i0 < n; i0 += 512) {              // sixteen loads in flight per lane
+        float v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) if (i0 + 32 * u < n) v[u] = c[i0 + 32 * u].v;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            uint32_t x = i0 + 32 * u < n ? fkey(v[u]) : 0u;
+#pragma unroll
+            for (int q = 0; q < kTrimMaxC; ++q) {         // insertion into the lane's top list
+                const bool sw = q < cdepth && x > top[q];
+                const uint32_t t = top[q];
+                top[q] = sw ? x : t;
+                x = sw ? t : x;
+            }
+        }
     }
-    __syncwarp();
-    const uint32_t kth = kth_key_bits(w.keys, n, k);
-    // keep the elements with key >= kth, compacted over the list's front (nothing of the list
-    // is read any more)
+    uint32_t lb = 0u;
+#pragma unroll
+    for (int q = 0; q < kTrimMaxC; ++q) if (q == cdepth - 1) lb = top[q];
+    lb = __reduce_min_sync(0xffffffffu, lb);
+    // stage 1: keep key >= lb (each batch is read before any of it is written; writes land at
+    // or below the batch being read)
     int m = 0;
+    for (int i0 = 0; i0 < n; i0 += 512) {
+        Cand e[16];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-        if (32 * u >= n) break;
-        const int i = lane + 32 * u;
-        const bool f = i < n && w.keys[i] >= kth;
-        const unsigned b = __ballot_sync(0xffffffffu, f);
-        if (f) c[m + __popc(b & lt)] = Cand{key_to_f(w.keys[i]), id[u]};
-        m += __popc(b);
+        for (int u = 0; u < 16; ++u) { const int i = i0 + lane + 32 * u; if (i < n) e[u] = c[i]; }
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int i = i0 + lane + 32 * u;
+            const uint32_t key = i < n ? fkey(e[u].v) : 0u;
+            const bool f = i < n && key >= lb;
+            const unsigned b = __ballot_sync(0xffffffffu, f);
+            const int pos = m + __popc(b & lt);
+            if (f) {
+                c[pos] = e[u];
+                if (pos < kTrimStage) { w.keys[pos] = key; w.ids[pos] = e[u].id; }
+            }
+            m += __popc(b);
+        }
+        __syncwarp();
     }
-    if (lane == 0) *n_io = m;
+    if (m > kTrimStage) {                                 // keep the stage-1 result
+        if (lane == 0) *n_io = m;
+        __syncwarp();
+        return;
+    }
+    // stage 2: exact k-th largest among the m staged entries
+    const uint32_t kth = kth_key_bits(w.keys, m, k);
+    int r = 0;
+    for (int base = 0; base < m; base += 32) {
+        const int i = base + lane;
+        const bool f = i < m && w.keys[i] >= kth;
+        const unsigned b = __ballot_sync(0xffffffffu, f);
+        if (f) c[r + __popc(b & lt)] = Cand{key_to_f(w.keys[i]), w.ids[i]};
+        r += __popc(b);
+    }
+    if (lane == 0) *n_io = r;
     __syncwarp();
 }
 
