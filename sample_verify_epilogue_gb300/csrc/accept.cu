@@ -79,6 +79,7 @@ __device__ void write_error(const Args& a, int b, int st) {
 }
 
 __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char acc_raw[];
     AccSmem& s = *reinterpret_cast<AccSmem*>(acc_raw);
     const int b = blockIdx.x, tid = threadIdx.x;
@@ -349,6 +350,7 @@ __device__ int whole_row_draw(FinishSmem& s, DrawCtx& c, float u) {
 }
 
 __global__ void __launch_bounds__(kFinishThreads) finish_kernel(Args a) {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char fin_raw[];
     FinishSmem& s = *reinterpret_cast<FinishSmem*>(fin_raw);
     const int b = blockIdx.x, tid = threadIdx.x;
@@ -409,16 +411,14 @@ cudaError_t launch_accept(const Args& a, cudaStream_t s) {
     const size_t smem = sizeof(AccSmem);
     cudaError_t e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    accept_kernel<<<a.B, kAcceptThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(accept_kernel, dim3(a.B), dim3(kAcceptThreads), smem, s, true, a);
 }
 
 cudaError_t launch_finish(const Args& a, cudaStream_t s) {
     const size_t smem = sizeof(FinishSmem);
     cudaError_t e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    finish_kernel<<<a.B, kFinishThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(finish_kernel, dim3(a.B), dim3(kFinishThreads), smem, s, true, a);
 }
 
 }  // namespace dspark

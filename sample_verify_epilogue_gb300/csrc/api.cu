@@ -144,9 +144,11 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     cudaEvent_t ev0 = static_cast<cudaEvent_t>(p->stage_events[0]);
     cudaEvent_t ev1 = static_cast<cudaEvent_t>(p->stage_events[1]);
     if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return DSPARK_ERR_CUDA;
-    if (launch_stream_stats(a, s, sms) != cudaSuccess) return DSPARK_ERR_CUDA;
+    // kernels after prep are launched as programmatic dependents of their predecessor, except
+    // across the optional stage events (an event between two kernels must see them apart)
+    if (launch_stream_stats(a, s, sms, ev0 == nullptr) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return DSPARK_ERR_CUDA;
-    if (launch_row_finalize_warp(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (launch_row_finalize_warp(a, s, ev1 == nullptr) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_row_finalize(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_accept(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_finish(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;

@@ -9,6 +9,7 @@
 //   finish_kernel        per request: whole-vocabulary draws (rare) and logprob outputs
 #pragma once
 
+#include <utility>
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -227,6 +228,17 @@ __device__ __forceinline__ float draft_weight(float q, float qmax, float inv_t, 
     return exp2f(inv_t * log2f(q / qmax));
 }
 
+// Programmatic dependent launch: every kernel after the first waits for its predecessor
+// grid to complete (memory included) before touching memory, and lets its own successor
+// be launched as soon as all its CTAs are running.  Without the launch attribute both are
+// no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_trigger();
+}
+
 __device__ __forceinline__ unsigned smem_u32(const void* p) {
     return static_cast<unsigned>(__cvta_generic_to_shared(p));
 }
@@ -386,9 +398,26 @@ __device__ __forceinline__ bool has_penalty(const dspark_row_params_t& r) {
 }
 
 // ---------------------------------------------------------------- launchers (one per .cu)
+// Launch `kern` on s; pdl: as a programmatic dependent of the previous kernel in s.
+template <typename... KArgs, typename... Args2>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                            Args2&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args2>(args)...);
+}
+
 cudaError_t launch_prep(const Args& a, cudaStream_t s);
-cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s);
-cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid);
+cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s, bool pdl_first);
+cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid, bool pdl);
 cudaError_t launch_row_finalize(const Args& a, cudaStream_t s);
 cudaError_t launch_accept(const Args& a, cudaStream_t s);
 cudaError_t launch_finish(const Args& a, cudaStream_t s);

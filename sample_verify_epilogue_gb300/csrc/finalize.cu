@@ -678,6 +678,7 @@ __device__ void finalize_row(const Args& a, FinSmem& s, int slot) {
 
 // The rows the warp finalize left (fin_list), each by a whole block.
 __global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(Args a) {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char fin_raw[];
     FinSmem& s = *reinterpret_cast<FinSmem*>(fin_raw);
     const int n = a.fin_list[0];
@@ -695,8 +696,7 @@ cudaError_t launch_row_finalize(const Args& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int rows = a.xslots + a.qslots;
     const int grid = rows < 4 * a.grid_ss ? rows : 4 * a.grid_ss;
-    row_finalize_kernel<<<grid, kFinThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(row_finalize_kernel, dim3(grid), dim3(kFinThreads), smem, s, true, a);
 }
 
 

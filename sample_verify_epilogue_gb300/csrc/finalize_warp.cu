@@ -460,6 +460,7 @@ __device__ void trim_list(TrimSmem& w, Cand* c, int* n_io, int k) {
 }
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock) cand_trim_kernel(Args a) {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char trim_raw[];
     const int warp = threadIdx.x >> 5;
     TrimSmem& w = reinterpret_cast<TrimSmem*>(trim_raw)[warp];
@@ -494,6 +495,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) cand_trim_kernel(Args a) {
 }
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock) row_finalize_warp_kernel(Args a) {
+    pdl_enter();
     extern __shared__ __align__(16) unsigned char wfin_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WarpSmem& w = reinterpret_cast<WarpSmem*>(wfin_raw)[warp];
@@ -526,7 +528,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) row_finalize_warp_kernel(A
 
 }  // namespace
 
-cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s) {
+cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s, bool pdl_first) {
     {
         const long long lists = static_cast<long long>(a.xslots) * a.nseg_x + static_cast<long long>(a.qslots) * a.nseg_q;
         const int grid = static_cast<int>((lists + kRowsPerBlock - 1) / kRowsPerBlock);
@@ -534,8 +536,7 @@ cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s) {
         cudaError_t e = cudaFuncSetAttribute(cand_trim_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        cand_trim_kernel<<<grid, 32 * kRowsPerBlock, smem, s>>>(a);
-        e = cudaGetLastError();
+        e = launch_k(cand_trim_kernel, dim3(grid), dim3(32 * kRowsPerBlock), smem, s, pdl_first, a);
         if (e != cudaSuccess) return e;
     }
     const int rows = a.xslots + a.qslots;
@@ -544,8 +545,7 @@ cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(row_finalize_warp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    row_finalize_warp_kernel<<<grid, 32 * kRowsPerBlock, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(row_finalize_warp_kernel, dim3(grid), dim3(32 * kRowsPerBlock), smem, s, true, a);
 }
 
 }  // namespace dspark

@@ -155,6 +155,7 @@ __device__ void penalty_index_block(const Args& a, int b, int t) {
 }
 
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Args a) {
+    pdl_trigger();
     penalty_index_block(a, blockIdx.x / a.tiles_x, blockIdx.x % a.tiles_x);
 }
 
@@ -162,8 +163,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Args a) {
 
 cudaError_t launch_prep(const Args& a, cudaStream_t s) {
     const int grid = a.B * a.tiles_x;
-    prep_kernel<<<grid, kPrepThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(prep_kernel, dim3(grid), dim3(kPrepThreads), 0, s, false, a);
 }
 
 }  // namespace dspark

@@ -1071,6 +1071,7 @@ __device__ int build_streams(const Args& a, Smem& sm, int c, int G) {
 // ------------------------------------------------------------------ the kernel
 template <int SX>
 __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a) {
+    pdl_enter();
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
     const int tid = threadIdx.x;
@@ -1266,19 +1267,19 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
 
 size_t stream_stats_smem_bytes() { return sizeof(Smem); }
 
-cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid) {
+cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid, bool pdl) {
     const size_t smem = sizeof(Smem);
     cudaError_t e;
     if (a.sx == 2) {
         e = cudaFuncSetAttribute(stream_stats_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        stream_stats_kernel<2><<<grid, kStreamThreads, smem, s>>>(a);
+        e = launch_k(stream_stats_kernel<2>, dim3(grid), dim3(kStreamThreads), smem, s, pdl, a);
     } else {
         e = cudaFuncSetAttribute(stream_stats_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        stream_stats_kernel<4><<<grid, kStreamThreads, smem, s>>>(a);
+        e = launch_k(stream_stats_kernel<4>, dim3(grid), dim3(kStreamThreads), smem, s, pdl, a);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace dspark
