@@ -176,20 +176,13 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
 
 // ============================================================================ finish
 constexpr int kFinishThreads = 512;
-constexpr int kPerThread = 4;
-constexpr int kChunk = kFinishThreads * kPerThread;     // 2048 elements: divides both tile sizes
-constexpr int kMaxChunks = (DSPARK_MAX_V + kChunk - 1) / kChunk;
 
 struct FinishSmem {
-    double chunk_sum[kMaxChunks];
     double dwarp[33];
-    unsigned bm[kBitmapWordsMax];
-    PenEntry ent[kPenCap];
     double th_ex[kFinishThreads + 1];
     double th_sum[kFinishThreads];
     int found_chunk;
     int tok;
-    int pen_n, pen_nh, pen_over, pen_tile;
 };
 
 struct DrawCtx {
@@ -200,151 +193,144 @@ struct DrawCtx {
     QRowOut qo;
     bool residual, t_one, pen, use_p_only;
     float f, p;
+    float inv_zp, inv_zq;      // 1/Z of the target and draft supports (Z lies in [1, V])
 };
 
-__device__ void stage_penalty_tile(FinishSmem& s, const DrawCtx& c, int tile) {
+// Count of token `tok` at the draw position (history + own draft prefix), from the request's
+// penalty index in global memory: the tile's sorted history entries by binary search, then
+// its draft-only entries; an overflowed tile looks the history up directly.
+__device__ int draw_count(const DrawCtx& c, int tok) {
     const Args& a = *c.a;
-    __syncthreads();
-    const long long pt = static_cast<long long>(c.b) * a.tiles_x + tile;
+    const long long pt = static_cast<long long>(c.b) * a.tiles_x + tok / a.tile_x;
     const PenHdr h = a.pen_hdr[pt];
-    for (int w = threadIdx.x; w < a.bm_words; w += blockDim.x) s.bm[w] = a.pen_bm[pt * a.bm_words + w];
-    if (!h.overflow) for (int k = threadIdx.x; k < h.n; k += blockDim.x) s.ent[k] = a.pen_ent[pt * kPenCap + k];
-    if (threadIdx.x == 0) { s.pen_n = h.n; s.pen_nh = h.pad[0]; s.pen_over = h.overflow; s.pen_tile = tile; }
-    __syncthreads();
-}
-
-__device__ int staged_count(const FinishSmem& s, const DrawCtx& c, int tok) {
-    const Args& a = *c.a;
-    if (!s.pen_over) {
-        int l = 0, h = s.pen_nh;
-        while (l < h) { const int m = (l + h) >> 1; if (s.ent[m].token < tok) l = m + 1; else h = m; }
+    if (!h.overflow) {
+        const PenEntry* ent = a.pen_ent + pt * kPenCap;
+        const int nh = h.pad[0];
+        int l = 0, hi = nh;
+        while (l < hi) { const int m = (l + hi) >> 1; if (ent[m].token < tok) l = m + 1; else hi = m; }
         int e = -1;
-        if (l < s.pen_nh && s.ent[l].token == tok) e = l;
-        else for (int k = s.pen_nh; k < s.pen_n; ++k) if (s.ent[k].token == tok) { e = k; break; }
+        if (l < nh && ent[l].token == tok) e = l;
+        else for (int k = nh; k < h.n; ++k) if (ent[k].token == tok) { e = k; break; }
         if (e < 0) return 0;
-        const unsigned long long mask = (static_cast<unsigned long long>(s.ent[e].mask_hi) << 32) | s.ent[e].mask_lo;
+        const PenEntry pe = ent[e];
+        const unsigned long long mask = (static_cast<unsigned long long>(pe.mask_hi) << 32) | pe.mask_lo;
         const unsigned long long low = (c.row_j >= 64) ? ~0ull : ((1ull << c.row_j) - 1ull);
-        return s.ent[e].base + __popcll(mask & low);
+        return pe.base + __popcll(mask & low);
     }
     int base = 0;
     const int hlo = a.h_off ? a.h_off[c.b] : 0, hhi = a.h_off ? a.h_off[c.b + 1] : 0;
-    int l = hlo, h = hhi;
-    while (l < h) { const int m = (l + h) >> 1; if (a.h_ids[m] < tok) l = m + 1; else h = m; }
+    int l = hlo, hi = hhi;
+    while (l < hi) { const int m = (l + hi) >> 1; if (a.h_ids[m] < tok) l = m + 1; else hi = m; }
     if (l < hhi && a.h_ids[l] == tok) base = a.h_cnt[l];
     return base + prefix_count(a, c.b, c.row_j, tok);
 }
 
-// Residual (or target) weight of token t of the draw row, in double.
-__device__ double draw_weight(const FinishSmem& s, const DrawCtx& c, int t) {
+// Residual (or target) weight of token t of the draw row.  Per element in float (FP64 is
+// slow on this part); sums over elements are compensated or taken in double.
+__device__ __forceinline__ float draw_weight_of(const DrawCtx& c, int t, float xv, float qv) {
     const Args& a = *c.a;
-    float xv = load_x(a.x, a.sx, c.xslot * a.V + t);
     if (c.pen) {
-        const int tl = t - s.pen_tile * a.tile_x;
-        if ((s.bm[tl >> 5] >> (tl & 31)) & 1u) xv = penalise(xv, staged_count(s, c, t), c.f, c.p);
+        const int tl = t % a.tile_x;
+        const long long pt = static_cast<long long>(c.b) * a.tiles_x + t / a.tile_x;
+        if ((a.pen_bm[pt * a.bm_words + (tl >> 5)] >> (tl & 31)) & 1u) xv = penalise(xv, draw_count(c, t), c.f, c.p);
     }
-    double P = 0.0;
-    if (xv >= c.xo.tau) P = static_cast<double>(target_weight(xv, c.xo.m_pen, c.xo.c_l2e)) / c.xo.Z;
+    float P = 0.f;
+    if (xv >= c.xo.tau) P = target_weight(xv, c.xo.m_pen, c.xo.c_l2e) * c.inv_zp;
     if (!c.residual || c.use_p_only) return P;
-    const float qv = __ldg(a.q + c.qslot * a.V + t);
-    double Q = 0.0;
-    if (qv >= c.qo.tau) Q = static_cast<double>(draft_weight(qv, c.qo.qmax, c.qo.inv_t, c.t_one)) / c.qo.Z;
-    return fmax(0.0, P - Q);
+    float Q = 0.f;
+    if (qv >= c.qo.tau) Q = draft_weight(qv, c.qo.qmax, c.qo.inv_t, c.t_one) * c.inv_zq;
+    return fmaxf(0.f, P - Q);
 }
 
-// Sum of the weights of this thread's kPerThread consecutive elements of chunk ch.
-__device__ double thread_chunk_sum(FinishSmem& s, const DrawCtx& c, int ch) {
-    const int V = c.a->V;
-    const int e0 = ch * kChunk + threadIdx.x * kPerThread;
-    double acc = 0.0;
-    for (int q = 0; q < kPerThread; ++q) {
-        const int e = e0 + q;
-        if (e < V) acc += draw_weight(s, c, e);
+// Sum of the weights of [r0, r1) (Kahan-compensated float), loads eight at a time.
+__device__ double range_sum(const DrawCtx& c, int r0, int r1) {
+    const Args& a = *c.a;
+    const bool need_q = c.residual && !c.use_p_only;
+    float sum = 0.f, comp = 0.f;
+    for (int e0 = r0; e0 < r1; e0 += 16) {
+        float xv[16], qv[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int e = e0 + q;
+            xv[q] = e < r1 ? load_x(a.x, a.sx, c.xslot * a.V + e) : -INFINITY;
+            qv[q] = (need_q && e < r1) ? __ldg(a.q + c.qslot * a.V + e) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const float w = e0 + q < r1 ? draw_weight_of(c, e0 + q, xv[q], qv[q]) : 0.f;
+            const float y = w - comp;
+            const float t = sum + y;
+            comp = (t - sum) - y;
+            sum = t;
+        }
     }
-    return acc;
+    return static_cast<double>(sum) - static_cast<double>(comp);
 }
 
-__device__ void maybe_stage(FinishSmem& s, const DrawCtx& c, int ch) {
-    if (!c.pen) return;
-    const int tile = (ch * kChunk) / c.a->tile_x;
-    if (tile != s.pen_tile) stage_penalty_tile(s, c, tile);
-}
-
+// Inverse-CDF draw over the whole row: the smallest token whose cumulative weight exceeds
+// u * total (ascending ids).  Each thread sums a contiguous range; a block scan of the range
+// sums finds the range holding the draw, whose thread walks it in double.  An all-zero
+// residual draws from the target row instead.
 __device__ int whole_row_draw(FinishSmem& s, DrawCtx& c, float u) {
     const Args& a = *c.a;
-    const int tid = threadIdx.x;
-    const int nch = (a.V + kChunk - 1) / kChunk;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int span = (a.V + nt - 1) / nt;
+    const int r0 = min(a.V, tid * span), r1 = min(a.V, r0 + span);
     for (int attempt = 0; attempt < 2; ++attempt) {
-        if (tid == 0) s.pen_tile = -1;
-        __syncthreads();
-        for (int ch = 0; ch < nch; ++ch) {
-            maybe_stage(s, c, ch);
-            const double v = thread_chunk_sum(s, c, ch);
-            const double tot = block_sum_d(v, s.dwarp);
-            if (tid == 0) s.chunk_sum[ch] = tot;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            double run = 0.0;
-            for (int ch = 0; ch < nch; ++ch) run += s.chunk_sum[ch];
-            s.th_ex[0] = run;
-        }
-        __syncthreads();
-        const double total = s.th_ex[0];
-        if (!(total > 0.0) && c.residual && !c.use_p_only) { c.use_p_only = true; continue; }
-        const double target = static_cast<double>(u) * total;
-        if (tid == 0) {
-            double run = 0.0;
-            int pick = -1;
-            for (int ch = 0; ch < nch; ++ch) {
-                if (run + s.chunk_sum[ch] > target && s.chunk_sum[ch] > 0.0) { pick = ch; break; }
-                run += s.chunk_sum[ch];
-            }
-            if (pick < 0) {                            // rounding: the last chunk with mass
-                for (int ch = nch - 1; ch >= 0; --ch) if (s.chunk_sum[ch] > 0.0) { pick = ch; break; }
-                run = 0.0;
-                for (int ch = 0; ch < pick; ++ch) run += s.chunk_sum[ch];
-            }
-            s.found_chunk = pick;
-            s.th_ex[kFinishThreads] = run;             // mass before the chunk
-        }
-        __syncthreads();
-        const int ch = s.found_chunk;
-        if (ch < 0) return -1;
-        const double before = s.th_ex[kFinishThreads];
-        if (c.pen) { if (tid == 0) s.pen_tile = -1; __syncthreads(); maybe_stage(s, c, ch); }
-        const double mine = thread_chunk_sum(s, c, ch);
+        const double mine = range_sum(c, r0, r1);
         s.th_sum[tid] = mine;
         __syncthreads();
-        if (tid == 0) {
-            double run = before;
-            int pick = -1;
-            for (int t = 0; t < kFinishThreads; ++t) {
-                if (run + s.th_sum[t] > target && s.th_sum[t] > 0.0) { pick = t; break; }
-                run += s.th_sum[t];
-            }
-            if (pick < 0) {
-                for (int t = kFinishThreads - 1; t >= 0; --t) if (s.th_sum[t] > 0.0) { pick = t; break; }
-                run = before;
-                for (int t = 0; t < pick; ++t) run += s.th_sum[t];
-            }
-            int tok = -1;
-            if (pick >= 0) {
-                const int e0 = ch * kChunk + pick * kPerThread;
-                int last = -1;
-                for (int q = 0; q < kPerThread; ++q) {
-                    const int e = e0 + q;
-                    if (e >= a.V) break;
-                    const double w = draw_weight(s, c, e);
-                    if (w > 0.0) last = e;
-                    if (run + w > target && w > 0.0) { tok = e; break; }
-                    run += w;
-                }
-                if (tok < 0) tok = last;
-            }
-            s.tok = tok;
+        block_scan_excl_d(s.th_sum, s.th_ex, nt, s.dwarp);
+        const double total = s.th_ex[nt];
+        if (!(total > 0.0) && c.residual && !c.use_p_only) {
+            c.use_p_only = true;
+            __syncthreads();
+            continue;
         }
+        const double target = static_cast<double>(u) * total;
+        if (tid == 0) { s.found_chunk = nt; s.tok = -1; }
         __syncthreads();
-        return s.tok;
+        const double ex = s.th_ex[tid];
+        if (mine > 0.0 && ex + mine > target) atomicMin(&s.found_chunk, tid);
+        __syncthreads();
+        int owner = s.found_chunk;
+        if (owner == nt) {                              // rounding: the last range with mass
+            if (tid == 0) {
+                int last = -1;
+                for (int t = nt - 1; t >= 0; --t) if (s.th_sum[t] > 0.0) { last = t; break; }
+                s.found_chunk = last;
+            }
+            __syncthreads();
+            owner = s.found_chunk;
+        }
+        if (owner < 0) return -1;
+        // the owner's range, one element per thread (span <= blockDim whenever V <= blockDim^2;
+        // otherwise in rounds), scanned in double in id order
+        const double before = s.th_ex[owner];
+        const int o0 = min(a.V, owner * span), o1 = min(a.V, o0 + span);
+        if (tid == 0) { s.found_chunk = a.V; s.tok = -1; }
+        double run = before;
+        for (int base = o0; base < o1; base += nt) {
+            const int e = base + tid;
+            float w = 0.f;
+            if (e < o1) {
+                const float qv = (c.residual && !c.use_p_only) ? __ldg(a.q + c.qslot * a.V + e) : 0.f;
+                w = draw_weight_of(c, e, load_x(a.x, a.sx, c.xslot * a.V + e), qv);
+            }
+            __syncthreads();
+            s.th_sum[tid] = static_cast<double>(w);
+            __syncthreads();
+            block_scan_excl_d(s.th_sum, s.th_ex, nt, s.dwarp);
+            const double ex = run + s.th_ex[tid];
+            if (w > 0.f && ex + static_cast<double>(w) > target) atomicMin(&s.found_chunk, e);
+            if (w > 0.f) atomicMax(&s.tok, e);                 // last element with mass so far
+            run += s.th_ex[nt];
+            __syncthreads();
+            if (s.found_chunk < a.V) break;
+        }
+        const int tok = s.found_chunk < a.V ? s.found_chunk : s.tok;
+        __syncthreads();
+        return tok;
     }
     return -1;
 }
@@ -375,6 +361,8 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(Args a) {
         c.use_p_only = false;
         c.f = r.frequency_penalty;
         c.p = r.presence_penalty;
+        c.inv_zp = c.xo.Z > 0.0 ? static_cast<float>(1.0 / c.xo.Z) : 0.f;
+        c.inv_zq = (c.residual && c.qo.Z > 0.0) ? static_cast<float>(1.0 / c.qo.Z) : 0.f;
         const int tok = whole_row_draw(s, c, a.u[(xs0 + acc_len) * 2 + 1]);
         if (tid == 0) a.out_tokens[xs0 + acc_len] = tok;
         __syncthreads();
