@@ -170,3 +170,25 @@ def test_b64k8_full_size_sampled(runner):
         assert np.array_equal(got["tokens"][b][:a], batch.draft_ids[b][:a])
         assert 0 <= got["tokens"][b][a] < batch.V
         assert np.all(got["top_ids"][b][: a + 1] >= 0)
+
+
+def test_b256k16_full_size_sampled(runner):
+    """The largest workload (B=256, K=16, V=262144, mixed parameters) at full size: the oracle
+    checks requests covering all 18 (T, top_k, top_p) combinations and both penalty halves;
+    properties are checked on every request."""
+    batch = configs.build("b256k16v262144_mixed")
+    call = runner(batch)
+    call.run()
+    got = call.results()
+    sample = list(range(18)) + [137, 255]
+    want = O.verify_batch(batch, requests=sample)
+    ex, fr = compare(batch, got, want)
+    assert ex >= len(sample) - max(1, len(sample) // 4), f"only {ex} of {len(sample)} exact ({fr} fragile)"
+    assert np.all(got["row_status"] == 0)
+    for b in range(batch.B):
+        a = int(got["accept_len"][b])
+        K = int(batch.rows[b]["num_drafts"])
+        assert 0 <= a <= K
+        assert np.array_equal(got["tokens"][b][:a], batch.draft_ids[b][:a])
+        assert 0 <= got["tokens"][b][a] < batch.V
+        assert np.all(got["tokens"][b][a + 1:] == -1)
