@@ -225,15 +225,36 @@ __device__ int draw_count(const DrawCtx& c, int tok) {
     return base + prefix_count(a, c.b, c.row_j, tok);
 }
 
+// Penalty bit of token t of the draw row.
+__device__ __forceinline__ bool pen_bit(const DrawCtx& c, int t) {
+    const Args& a = *c.a;
+    const int tile = t / a.tile_x, tl = t - tile * a.tile_x;
+    const long long pt = static_cast<long long>(c.b) * a.tiles_x + tile;
+    return (a.pen_bm[pt * a.bm_words + (tl >> 5)] >> (tl & 31)) & 1u;
+}
+
+// Penalty bits of tokens [e0, e0 + n), n <= 16 (bit q: token e0 + q), one or two bitmap words
+// per tile the range touches.
+__device__ __forceinline__ unsigned pen_bits16(const DrawCtx& c, int e0, int n) {
+    const Args& a = *c.a;
+    unsigned bits = 0u;
+    for (int e = e0; e < e0 + n;) {
+        const int tile = e / a.tile_x, tl = e - tile * a.tile_x;
+        const int cnt = min(e0 + n - e, a.tile_x - tl);
+        const unsigned* bm = a.pen_bm + (static_cast<long long>(c.b) * a.tiles_x + tile) * a.bm_words;
+        const int w0 = tl >> 5, sh = tl & 31;
+        unsigned long long win = bm[w0];
+        if (sh + cnt > 32) win |= static_cast<unsigned long long>(bm[w0 + 1]) << 32;
+        bits |= (static_cast<unsigned>(win >> sh) & ((1u << cnt) - 1u)) << (e - e0);
+        e += cnt;
+    }
+    return bits;
+}
+
 // Residual (or target) weight of token t of the draw row.  Per element in float (FP64 is
 // slow on this part); sums over elements are compensated or taken in double.
-__device__ __forceinline__ float draw_weight_of(const DrawCtx& c, int t, float xv, float qv) {
-    const Args& a = *c.a;
-    if (c.pen) {
-        const int tl = t % a.tile_x;
-        const long long pt = static_cast<long long>(c.b) * a.tiles_x + t / a.tile_x;
-        if ((a.pen_bm[pt * a.bm_words + (tl >> 5)] >> (tl & 31)) & 1u) xv = penalise(xv, draw_count(c, t), c.f, c.p);
-    }
+__device__ __forceinline__ float draw_weight_of(const DrawCtx& c, int t, float xv, float qv, bool penalised) {
+    if (penalised) xv = penalise(xv, draw_count(c, t), c.f, c.p);
     float P = 0.f;
     if (xv >= c.xo.tau) P = target_weight(xv, c.xo.m_pen, c.xo.c_l2e) * c.inv_zp;
     if (!c.residual || c.use_p_only) return P;
@@ -242,7 +263,7 @@ __device__ __forceinline__ float draw_weight_of(const DrawCtx& c, int t, float x
     return fmaxf(0.f, P - Q);
 }
 
-// Sum of the weights of [r0, r1) (Kahan-compensated float), loads eight at a time.
+// Sum of the weights of [r0, r1) (Kahan-compensated float), sixteen loads at a time.
 __device__ double range_sum(const DrawCtx& c, int r0, int r1) {
     const Args& a = *c.a;
     const bool need_q = c.residual && !c.use_p_only;
@@ -255,9 +276,10 @@ __device__ double range_sum(const DrawCtx& c, int r0, int r1) {
             xv[q] = e < r1 ? load_x(a.x, a.sx, c.xslot * a.V + e) : -INFINITY;
             qv[q] = (need_q && e < r1) ? __ldg(a.q + c.qslot * a.V + e) : 0.f;
         }
+        const unsigned pb = c.pen ? pen_bits16(c, e0, min(16, r1 - e0)) : 0u;
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-            const float w = e0 + q < r1 ? draw_weight_of(c, e0 + q, xv[q], qv[q]) : 0.f;
+            const float w = e0 + q < r1 ? draw_weight_of(c, e0 + q, xv[q], qv[q], (pb >> q) & 1u) : 0.f;
             const float y = w - comp;
             const float t = sum + y;
             comp = (t - sum) - y;
@@ -315,7 +337,7 @@ __device__ int whole_row_draw(FinishSmem& s, DrawCtx& c, float u) {
             float w = 0.f;
             if (e < o1) {
                 const float qv = (c.residual && !c.use_p_only) ? __ldg(a.q + c.qslot * a.V + e) : 0.f;
-                w = draw_weight_of(c, e, load_x(a.x, a.sx, c.xslot * a.V + e), qv);
+                w = draw_weight_of(c, e, load_x(a.x, a.sx, c.xslot * a.V + e), qv, c.pen && pen_bit(c, e));
             }
             __syncthreads();
             s.th_sum[tid] = static_cast<double>(w);

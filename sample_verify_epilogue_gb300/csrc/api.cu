@@ -313,6 +313,6 @@ const char* dspark_status_string(dspark_status_t status) {
     return "unknown status";
 }
 
-int32_t dspark_launches_per_call(void) { return 7; }
+int32_t dspark_launches_per_call(void) { return 6; }
 
 }  // extern "C"

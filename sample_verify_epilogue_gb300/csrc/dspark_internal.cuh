@@ -416,7 +416,7 @@ inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
 }
 
 cudaError_t launch_prep(const Args& a, cudaStream_t s);
-cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s, bool pdl_first);
+cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s, bool pdl);
 cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid, bool pdl);
 cudaError_t launch_row_finalize(const Args& a, cudaStream_t s);
 cudaError_t launch_accept(const Args& a, cudaStream_t s);

@@ -214,6 +214,8 @@ struct FullSmem {
     int top_ids[64];
     float top_v[64];
     int n_gt, n_eq;
+    double dwarp_plim;
+    uint4 tb[2][kStageBytes / 16];     // double-buffered vocab tile (cp.async)
 };
 
 // Value of element e of the row: penalised target logit or draft probability.
@@ -248,40 +250,96 @@ __device__ int full_pen_count(const FullSmem& s, const RowSource& src, int tok, 
     return base;
 }
 
-// One pass over the row calling fn(e, value, raw) for every element, tile by tile (the
-// penalty index of each target tile is staged in shared memory first).
-template <typename Fn>
-__device__ void for_each_elem(FullSmem& s, const RowSource& src, Fn fn) {
+// Element k of a 16-byte vector of SX-byte values (k may be a run-time index).
+template <int SX>
+__device__ __forceinline__ float vec_elem(const uint4& w, int k) {
+    if (SX == 2) {
+        const uint32_t word = (k < 2) ? w.x : (k < 4) ? w.y : (k < 6) ? w.z : w.w;
+        return __uint_as_float((k & 1) ? (word & 0xFFFF0000u) : (word << 16));
+    }
+    return __uint_as_float((k == 0) ? w.x : (k == 1) ? w.y : (k == 2) ? w.z : w.w);
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// One pass over the row calling fn(e, value, raw) for every element, tile by tile (40 KB:
+// the penalty tiles of a target row, 10,240 probabilities of a draft row).  The 16-byte-aligned
+// interior of each tile is copied into shared memory with cp.async, the next tile's copy in
+// flight while this one is visited; the unaligned edges are read element by element.  The
+// penalty index of each target tile is staged in shared memory first.
+template <int SX, typename Fn>
+__device__ void for_each_elem_t(FullSmem& s, const RowSource& src, Fn fn) {
     const Args& a = *src.a;
-    const int tid = threadIdx.x;
-    const int tile_n = src.is_x ? a.tile_x : a.V;
-    for (int e0 = 0; e0 < a.V; e0 += tile_n) {
-        const int e1 = min(a.V, e0 + tile_n);
+    constexpr int EPV = 16 / SX;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const unsigned char* rowp = src.is_x ? static_cast<const unsigned char*>(a.x) + src.base * SX
+                                         : reinterpret_cast<const unsigned char*>(a.q + src.base);
+    const int head = static_cast<int>(((16u - static_cast<unsigned>(reinterpret_cast<uintptr_t>(rowp) & 15u)) & 15u) / SX);
+    const int tile_n = src.is_x ? a.tile_x : kStageBytes / 4;
+    const int ntiles = (a.V + tile_n - 1) / tile_n;
+    // aligned interior [va, vb) of tile t: element e starts a vector iff (e - head) % EPV == 0
+    auto interior = [&](int t, int& va, int& vb) {
+        const int e0 = t * tile_n, e1 = min(a.V, e0 + tile_n);
+        const int lo = max(e0, head);
+        va = min(e1, head + ((lo - head + EPV - 1) / EPV) * EPV);
+        vb = (e1 >= va + EPV) ? head + ((e1 - head) / EPV) * EPV : va;
+    };
+    auto issue = [&](int t) {
+        if (t < ntiles) {
+            int va, vb;
+            interior(t, va, vb);
+            const uint4* g = reinterpret_cast<const uint4*>(rowp + static_cast<long long>(va) * SX);
+            uint4* d = s.tb[t & 1];
+            for (int i = tid; i < (vb - va) / EPV; i += nt) cp_async16(d + i, g + i);
+        }
+        cp_async_commit();
+    };
+    __syncthreads();                                      // the buffers are free
+    issue(0);
+    for (int t = 0; t < ntiles; ++t) {
+        const int e0 = t * tile_n, e1 = min(a.V, e0 + tile_n);
+        __syncthreads();                                  // tile t-1 visited: its buffer is free
+        issue(t + 1);
         int nh = 0, n = 0, over = 0;
         if (src.pen) {
-            const long long pt = static_cast<long long>(src.b) * a.tiles_x + e0 / a.tile_x;
+            const long long pt = static_cast<long long>(src.b) * a.tiles_x + t;
             const PenHdr h = a.pen_hdr[pt];
             n = h.n; nh = h.pad[0]; over = h.overflow;
-            __syncthreads();
-            for (int w = tid; w < a.bm_words; w += blockDim.x) s.bm[w] = a.pen_bm[pt * a.bm_words + w];
-            if (!over) for (int k = tid; k < n; k += blockDim.x) s.ent[k] = a.pen_ent[pt * kPenCap + k];
-            __syncthreads();
+            for (int w = tid; w < a.bm_words; w += nt) s.bm[w] = a.pen_bm[pt * a.bm_words + w];
+            if (!over) for (int k = tid; k < n; k += nt) s.ent[k] = a.pen_ent[pt * kPenCap + k];
         }
-        for (int e = e0 + tid; e < e1; e += blockDim.x) {
-            float raw, v;
-            if (src.is_x) {
-                raw = load_x(a.x, a.sx, src.base + e);
-                v = raw;
-                if (src.pen && ((s.bm[(e - e0) >> 5] >> ((e - e0) & 31)) & 1u))
-                    v = penalise(raw, full_pen_count(s, src, e, nh, n, over), src.f, src.p);
-            } else {
-                raw = __ldg(a.q + src.base + e);
-                v = raw;
-            }
+        cp_async_wait_one();                              // this thread's copies of tile t landed
+        __syncthreads();                                  // everyone's, and the penalty index
+        auto visit = [&](int e, float raw) {
+            float v = raw;
+            if (src.is_x && src.pen && ((s.bm[(e - e0) >> 5] >> ((e - e0) & 31)) & 1u))
+                v = penalise(raw, full_pen_count(s, src, e, nh, n, over), src.f, src.p);
             fn(e, v, raw);
+        };
+        int va, vb;
+        interior(t, va, vb);
+        for (int e = e0 + tid; e < va; e += nt)
+            visit(e, SX == 2 ? load_x(a.x, 2, src.base + e) : __uint_as_float(reinterpret_cast<const uint32_t*>(rowp)[e]));
+        for (int e = vb + tid; e < e1; e += nt)
+            visit(e, SX == 2 ? load_x(a.x, 2, src.base + e) : __uint_as_float(reinterpret_cast<const uint32_t*>(rowp)[e]));
+        const uint4* buf = s.tb[t & 1];
+        for (int vi = tid; vi < (vb - va) / EPV; vi += nt) {
+            const uint4 w = buf[vi];
+#pragma unroll
+            for (int q = 0; q < EPV; ++q) visit(va + vi * EPV + q, vec_elem<SX>(w, q));
         }
     }
     __syncthreads();
+}
+
+template <typename Fn>
+__device__ __forceinline__ void for_each_elem(FullSmem& s, const RowSource& src, Fn fn) {
+    if (src.is_x && src.a->sx == 2) for_each_elem_t<2>(s, src, fn);
+    else for_each_elem_t<4>(s, src, fn);
 }
 
 // Exact k-th largest key (1-based) over the row; use_raw selects the raw value.
@@ -317,10 +375,11 @@ __device__ uint32_t full_kth(FullSmem& s, const RowSource& src, int k, bool use_
     return prefix;
 }
 
-// Nucleus over {value key >= floor_key}: returns the smallest kept key and the kept mass.
+// Nucleus over {value key >= floor_key} by three radix passes over the key: returns the
+// smallest kept key and the kept mass.  The fallback of full_nucleus below.
 template <typename WFn>
-__device__ uint32_t full_nucleus(FullSmem& s, const RowSource& src, uint32_t floor_key, float top_p, WFn wfn,
-                                 double* zkept) {
+__device__ uint32_t full_nucleus_radix(FullSmem& s, const RowSource& src, uint32_t floor_key, float top_p, WFn wfn,
+                                       double* zkept) {
     const int tid = threadIdx.x;
     uint32_t prefix = 0, pmask = 0;
     unsigned long long above = 0;     // fixed-point mass strictly above the current prefix range
@@ -377,6 +436,143 @@ __device__ uint32_t full_nucleus(FullSmem& s, const RowSource& src, uint32_t flo
     }
     *zkept = static_cast<double>(above + s.ubcast[2]) / kFix;
     return prefix;
+}
+
+// Nucleus over {value key >= floor_key} by a mass histogram over weight buckets:
+//   pass 1: every element's fixed-point weight goes to bucket(v), a monotone (non-increasing)
+//           function of the value that spreads the row over kNucBuckets buckets of 1/32 of a
+//           binary order of magnitude of the weight each; elements whose weight is certainly
+//           below the nucleus boundary (w < w_lo, from the bound w_cross > (1-top_p) Z / (V+1)
+//           on the crossing element's weight) are only summed, per thread, into the total;
+//   descent: the boundary bucket beta is the last bucket whose mass above is < top_p * Z;
+//           every element of an earlier bucket is kept and none of a later one;
+//   pass 2: the elements of beta are gathered into shared memory and the kept tie groups are
+//           settled exactly among them (exclusive mass of a group = mass above beta + mass of
+//           the larger keys of beta).
+// The masses are the same 2^-38 fixed-point weights as the radix path, so the threshold and the
+// kept mass are identical to it; a boundary bucket that is the last one, meets the summed-only
+// elements, or holds more than the gather capacity falls back to the radix path.
+// wfn(v) is the weight (<= 1), bfn(v) the bucket, z_est an estimate of the total weight in
+// wfn's units (0 when unknown: no element is summed-only).
+constexpr int kNucBuckets = 2048;
+constexpr int kNucGather = 2048;
+
+template <typename WFn, typename BFn>
+__device__ uint32_t full_nucleus(FullSmem& s, const RowSource& src, uint32_t floor_key, float top_p, WFn wfn,
+                                 BFn bfn, double z_est, double* zkept) {
+    const int tid = threadIdx.x;
+    const bool nuc = top_p < 1.f;
+    const float w_lo = (nuc && z_est > 0.0)
+        ? static_cast<float>(0.5 * (1.0 - static_cast<double>(top_p)) * z_est / (static_cast<double>(src.a->V) + 1.0))
+        : 0.f;
+    if (tid == 0) { s.n_gt = kNucBuckets; s.ubcast[3] = 0ull; }
+    for (int i = tid; i < kNucBuckets; i += blockDim.x) s.mass[i] = 0ull;
+    __syncthreads();
+    unsigned long long tail = 0ull;
+    int tmin = kNucBuckets;
+    for_each_elem(s, src, [&](int, float v, float) {
+        if (fkey(v) < floor_key) return;
+        const float w = wfn(v);
+        const unsigned long long fx = __float2ull_rn(w * 274877906944.0f);
+        if (!nuc) { tail += fx; return; }
+        const int bk = bfn(v);
+        if (w < w_lo) { tail += fx; tmin = min(tmin, bk); }
+        else if (fx != 0ull) atomicAdd(&s.mass[bk], fx);
+    });
+    // total of the summed-only weights (integer sums: independent of the order)
+    for (int o = 16; o > 0; o >>= 1) {
+        tail += __shfl_xor_sync(0xffffffffu, tail, o);
+        tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, o));
+    }
+    if ((tid & 31) == 0) {
+        if (tail) atomicAdd(&s.ubcast[3], tail);
+        if (tmin < kNucBuckets) atomicMin(&s.n_gt, tmin);
+    }
+    __syncthreads();
+    if (!nuc) {
+        *zkept = static_cast<double>(s.ubcast[3]) / kFix;
+        __syncthreads();
+        return floor_key;
+    }
+    // descent: total, then the boundary bucket (one warp: per-lane contiguous chunks of buckets)
+    if (tid < 32) {
+        constexpr int kPer = kNucBuckets / 32;
+        unsigned long long part = 0ull;
+        for (int d = 0; d < kPer; ++d) part += s.mass[tid * kPer + d];
+        unsigned long long incl = part;
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (tid >= o) incl += y;
+        }
+        const unsigned long long total_b = __shfl_sync(0xffffffffu, incl, 31);
+        const double zt = static_cast<double>(total_b + s.ubcast[3]);
+        const double plim = static_cast<double>(top_p) * zt;
+        // the lane whose chunk holds the last bucket with mass-above < plim: the last lane whose
+        // exclusive prefix is < plim and whose chunk is not empty
+        const unsigned long long excl = incl - part;
+        const unsigned cand = __ballot_sync(0xffffffffu, part != 0ull && static_cast<double>(excl) < plim);
+        if (tid == 0) { s.bcast[0] = -1; }
+        __syncwarp();
+        if (cand) {
+            const int L = 31 - __clz(cand);
+            if (tid == L) {
+                unsigned long long run = excl;
+                int pick = -1;
+                unsigned long long pick_above = 0ull, pick_mass = 0ull;
+                for (int d = 0; d < kPer; ++d) {
+                    const unsigned long long m = s.mass[tid * kPer + d];
+                    if (m == 0ull) continue;
+                    if (static_cast<double>(run) < plim) { pick = tid * kPer + d; pick_above = run; pick_mass = m; }
+                    else break;
+                    run += m;
+                }
+                s.bcast[0] = pick;
+                s.ubcast[0] = pick_above;
+                s.ubcast[2] = pick_mass;
+                s.dwarp_plim = plim;
+            }
+        }
+    }
+    __syncthreads();
+    const int beta = s.bcast[0];
+    const unsigned long long above = s.ubcast[0];
+    const double plim = s.dwarp_plim;
+    const bool ok = beta >= 0 && beta < kNucBuckets - 1 && beta < s.n_gt &&
+                    static_cast<double>(above + s.ubcast[2]) >= plim;
+    __syncthreads();
+    if (!ok) return full_nucleus_radix(s, src, floor_key, top_p, wfn, zkept);
+    // pass 2: gather the boundary bucket (keys in cnt[], weights in mass[])
+    if (tid == 0) s.tl_n = 0;
+    __syncthreads();
+    for_each_elem(s, src, [&](int, float v, float) {
+        const uint32_t key = fkey(v);
+        if (key < floor_key || bfn(v) != beta) return;
+        const int p = atomicAdd(&s.tl_n, 1);
+        if (p < kNucGather) { s.cnt[p] = key; s.mass[p] = __float2ull_rn(wfn(v) * 274877906944.0f); }
+    });
+    const int n = s.tl_n;
+    if (n > kNucGather) { __syncthreads(); return full_nucleus_radix(s, src, floor_key, top_p, wfn, zkept); }
+    // exact settlement: a key is kept iff above + (mass of larger keys of beta) < plim
+    if (tid == 0) { s.bcast[1] = static_cast<int>(0xFFFFFFFFu); }
+    __syncthreads();
+    for (int i = tid; i < n; i += blockDim.x) {
+        const uint32_t ki = s.cnt[i];
+        unsigned long long ex = above;
+        for (int jj = 0; jj < n; ++jj) ex += (s.cnt[jj] > ki) ? s.mass[jj] : 0ull;
+        if (static_cast<double>(ex) < plim) atomicMin(reinterpret_cast<unsigned*>(&s.bcast[1]), ki);
+    }
+    __syncthreads();
+    const uint32_t tau = static_cast<uint32_t>(s.bcast[1]);
+    unsigned long long kept = 0ull;
+    for (int i = tid; i < n; i += blockDim.x) kept += (s.cnt[i] >= tau) ? s.mass[i] : 0ull;
+    for (int o = 16; o > 0; o >>= 1) kept += __shfl_xor_sync(0xffffffffu, kept, o);
+    if (tid == 0) s.ubcast[1] = 0ull;
+    __syncthreads();
+    if ((tid & 31) == 0 && kept) atomicAdd(&s.ubcast[1], kept);
+    __syncthreads();
+    *zkept = static_cast<double>(above + s.ubcast[1]) / kFix;
+    __syncthreads();
+    return tau;
 }
 
 // Raw top-n with ties broken by lower id, over the whole row.
@@ -447,9 +643,15 @@ __device__ void whole_row_x(const Args& a, FullSmem& s, int slot, int b, int j, 
         uint32_t floor_key = fkey(o.tau);
         if (o.top_k > 0) floor_key = full_kth(s, src, o.top_k, false);
         const float mp = o.m_pen, c = o.c_l2e;
+        const float cs = c * 32.f;                       // 32 buckets per binary order of the weight
+        const double z_est = (floor_key == fkey(-INFINITY)) ? o.Z : 0.0;
         double z;
         const uint32_t kk = full_nucleus(s, src, floor_key, o.top_p < 1.f ? o.top_p : 2.f,
-                                         [&](float v) { return target_weight(v, mp, c); }, &z);
+                                         [&](float v) { return target_weight(v, mp, c); },
+                                         [&](float v) {
+                                             const float d = __fmul_rn(__fsub_rn(mp, v), cs);
+                                             return d < static_cast<float>(kNucBuckets - 1) ? max(0, static_cast<int>(d)) : kNucBuckets - 1;
+                                         }, z_est, &z);
         o.tau = (o.top_p < 1.f) ? key_to_f(kk) : key_to_f(floor_key);
         o.Z = z;
         o.top_k = 0;
@@ -463,9 +665,18 @@ __device__ void whole_row_q(const Args& a, FullSmem& s, int qs, int b, int i, QR
     if (o.top_k > 0) floor_key = full_kth(s, src, o.top_k, false);
     const float qmax = o.qmax, inv_t = o.inv_t;
     const bool t_one = inv_t == 1.f;
+    // bucket from the order of magnitude of q/qmax read off the float bits (monotone in q)
+    const int qmax_bits = __float_as_int(qmax);
+    const float sq = inv_t * (32.f / 8388608.f);
+    const double z_est = (floor_key == fkey(-INFINITY)) ? (t_one ? o.Z / qmax : o.Z) : 0.0;
     double z;
     const uint32_t kk = full_nucleus(s, src, floor_key, o.top_p < 1.f ? o.top_p : 2.f,
-                                     [&](float v) { return draft_weight(v, qmax, inv_t, t_one) / (t_one ? qmax : 1.f); }, &z);
+                                     [&](float v) { return draft_weight(v, qmax, inv_t, t_one) / (t_one ? qmax : 1.f); },
+                                     [&](float v) {
+                                         const int vb = __float_as_int(v);    // q <= qmax: no overflow for q >= 0
+                                         const float d = vb < 0 ? 3.0e38f : static_cast<float>(qmax_bits - vb) * sq;
+                                         return d < static_cast<float>(kNucBuckets - 1) ? max(0, static_cast<int>(d)) : kNucBuckets - 1;
+                                     }, z_est, &z);
     o.tau = (o.top_p < 1.f) ? key_to_f(kk) : key_to_f(floor_key);
     if (t_one) z *= qmax;
     o.Z = z;
@@ -506,15 +717,15 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
     for (int t = tid; t < nseg; t += blockDim.x) {
         const TileStats x = ts[t];
         if (x.m_pen == mp) arg = min(arg, x.arg_pen);
-        sraw += static_cast<double>(x.s_raw) * exp2(static_cast<double>(x.m_raw - mr) * kL2E);
-        if (!greedy) stemp += static_cast<double>(x.s_temp) * exp2(static_cast<double>(x.m_pen - mp) * c_l2e);
+        sraw += static_cast<double>(x.s_raw) * static_cast<double>(exp2f((x.m_raw - mr) * kL2E));
+        if (!greedy) stemp += static_cast<double>(x.s_temp) * static_cast<double>(exp2f((x.m_pen - mp) * c_l2e));
     }
     arg = block_min_i(arg, s.iwarp);
     sraw = block_sum_d(sraw, s.dwarp);
     stemp = block_sum_d(stemp, s.dwarp);
     o.argmax = arg;
     o.m_pen = mp;
-    o.lse = mr + static_cast<float>(log(sraw));
+    o.lse = mr + logf(static_cast<float>(sraw));
     o.c_l2e = c_l2e;
     o.top_p = r.top_p;
     o.tau = -INFINITY;
@@ -604,7 +815,7 @@ __device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
     for (int t = tid; t < nseg; t += blockDim.x) {
         const TileStats x = ts[t];
         if (t_one) z += static_cast<double>(x.s_raw);
-        else if (x.m_raw > 0.f) z += static_cast<double>(x.s_temp) * exp2(static_cast<double>(inv_t) * log2(static_cast<double>(x.m_raw) / qmax));
+        else if (x.m_raw > 0.f) z += static_cast<double>(x.s_temp) * static_cast<double>(exp2f(inv_t * log2f(x.m_raw / qmax)));
     }
     z = block_sum_d(z, s.dwarp);
     if ((fl & kTileBad) || !(qmax > 0.f) || !isfinite(qmax)) {
@@ -677,7 +888,7 @@ __device__ void finalize_row(const Args& a, FinSmem& s, int slot) {
 }
 
 // The rows the warp finalize left (fin_list), each by a whole block.
-__global__ void __launch_bounds__(kFinThreads) row_finalize_kernel(Args a) {
+__global__ void __launch_bounds__(kFinThreads, 2) row_finalize_kernel(Args a) {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char fin_raw[];
     FinSmem& s = *reinterpret_cast<FinSmem*>(fin_raw);

@@ -4,7 +4,9 @@
 // weights, nucleus, raw top-n; mlx-dspark Changelog, [0.1.0] Added, top-p / top-k sampling;
 // [0.20.2] Changed, selection instead of a full vocabulary sort) with warp shuffles and
 // per-warp shared memory instead of block barriers: the candidates' order-preserving keys
-// are staged, the threshold is selected on them, and only the survivors' ids are fetched.
+// are staged (long lists after a first read that bounds the k-th largest key from below, so
+// only keys that can be in the top-k are kept), the threshold is selected on them, and the
+// survivors are sorted.
 // Rows it cannot settle here (more candidates, segments or survivors than a warp holds,
 // overflowed candidate lists, rows that need a whole-row pass) are appended to a list that
 // row_finalize_kernel then works through.
@@ -24,7 +26,8 @@ struct WarpSmem {
     uint32_t keys[kWKeyCap];
     int ids[kWKeyCap];
     unsigned long long sk[kWSurvCap];  // survivors: (key << 32) | (0xFFFFFFFF - id)
-    int off[kWSegCap + 1];             // staged position of each segment's first candidate
+    int off[kWSegCap + 1];             // flat position of each segment's first candidate pair
+    int cnt[kWSegCap];                 // candidates of each segment
 };
 
 // The row's candidate lists: segment t holds its candidates at base + t*cap.
@@ -38,49 +41,121 @@ __device__ __forceinline__ float nan_max(float a, float b) {
     return (a != a || b != b) ? __int_as_float(0x7fc00000) : fmaxf(a, b);
 }
 
-// Stage the keys of the row's candidates (segment t: n_t entries) in shared memory, with the
-// segment offsets; all segments' loads are issued together (flat index -> segment from the
-// offsets).  Returns the total, or -1 when it exceeds kWKeyCap or there are more than
-// kWSegCap segments.
-__device__ int warp_stage(WarpSmem& w, const TileStats* ts, const WCands& cs, bool raw) {
+// Walks the row's flat index of candidate pairs (segment l holds pair positions
+// [off[l], off[l+1]); pair j of a segment is its candidates 2j and 2j+1, one 16-byte load) in
+// increasing order, one position at a time per lane.
+struct PairCursor {
+    int l, lo, hi;
+    __device__ __forceinline__ explicit PairCursor(const WarpSmem& w) : l(0), lo(0), hi(w.off[1]) {}
+    // The pair's address; *second = whether its second candidate exists.
+    __device__ __forceinline__ const uint4* at(const WarpSmem& w, const WCands& cs, int p, bool* second) {
+        while (p >= hi) { ++l; lo = hi; hi = w.off[l + 1]; }
+        const int j = p - lo;
+        *second = 2 * j + 1 < w.cnt[l];
+        return reinterpret_cast<const uint4*>(cs.base + static_cast<long long>(l) * cs.cap) + j;
+    }
+};
+
+// Stage the keys of the row's candidates (segment t: n_t entries) in shared memory in one read
+// of the lists (eight 16-byte loads, sixteen candidates, in flight per lane).  With k > 0
+// only keys reaching a lower bound of the k-th largest key are staged: every lane keeps the
+// C >= c = ceil(k/32) largest keys it has read, and at least 32c >= k keys reach the least of
+// the lanes' c-th largest, so that bound, raised after every batch, never passes a member of
+// the top-k (ties included).  Returns the number staged, or -1 when it exceeds kWKeyCap or
+// there are more than kWSegCap segments.
+constexpr int kWMaxC = 8;                                 // ceil(k / 32) for k <= kMaxCandTopK
+static_assert(32 * kWMaxC >= kMaxCandTopK, "per-lane depth must cover k");
+
+template <int C>
+__device__ int warp_stage_t(WarpSmem& w, const WCands& cs, int npairs, int c) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    uint32_t top[C];                                      // descending; 0 = nothing yet
+#pragma unroll
+    for (int q = 0; q < C; ++q) top[q] = 0u;
+    uint32_t lb = 0u;
+    int m = 0;
+    PairCursor cur(w);
+    for (int p0 = 0; p0 < npairs; p0 += 32 * 8) {
+        uint4 v[8];
+        unsigned two = 0u;                                // bit u: pair u has its second candidate
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int p = p0 + lane + 32 * u;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (p < npairs) {
+                bool sec;
+                v[u] = *cur.at(w, cs, p, &sec);
+                two |= (sec ? 1u : 0u) << u;
+            }
+        }
+        uint32_t key[16];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool one = p0 + lane + 32 * u < npairs;
+            key[2 * u] = one ? fkey(__uint_as_float(v[u].x)) : 0u;
+            key[2 * u + 1] = (one && ((two >> u) & 1u)) ? fkey(__uint_as_float(v[u].z)) : 0u;
+        }
+        if (c > 0) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                uint32_t x = key[e];
+#pragma unroll
+                for (int q = 0; q < C; ++q) {             // insertion into the lane's top list
+                    const uint32_t t = top[q];
+                    const bool sw = x > t;
+                    top[q] = sw ? x : t;
+                    x = sw ? t : x;
+                }
+            }
+            uint32_t mine = 0u;
+#pragma unroll
+            for (int q = 0; q < C; ++q) if (q == c - 1) mine = top[q];
+            lb = max(lb, __reduce_min_sync(0xffffffffu, mine));
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const bool f = key[e] != 0u && key[e] >= lb;
+            const unsigned b = __ballot_sync(0xffffffffu, f);
+            const int pos = m + __popc(b & lt);
+            if (f && pos < kWKeyCap) {
+                w.keys[pos] = key[e];
+                w.ids[pos] = static_cast<int>((e & 1) ? v[e >> 1].w : v[e >> 1].y);
+            }
+            m += __popc(b);
+        }
+    }
+    __syncwarp();
+    return m > kWKeyCap ? -1 : m;
+}
+
+__device__ int warp_stage(WarpSmem& w, const TileStats* ts, const WCands& cs, bool raw, int k) {
     const int lane = threadIdx.x & 31;
     if (cs.nseg > kWSegCap) return -1;
-    int total = 0;
+    int total = 0, npairs = 0;
     for (int t0 = 0; t0 < cs.nseg; t0 += 32) {
         const int t = t0 + lane;
         const int n = t < cs.nseg ? (raw ? ts[t].n_raw : ts[t].n_pen) : 0;
-        int incl = n;
+        const int np = (n + 1) >> 1;
+        int incl = np;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        if (t < cs.nseg) w.off[t] = total + incl - n;
-        total += __shfl_sync(0xffffffffu, incl, 31);
+        if (t < cs.nseg) { w.off[t] = npairs + incl - np; w.cnt[t] = n; }
+        npairs += __shfl_sync(0xffffffffu, incl, 31);
+        total += __reduce_add_sync(0xffffffffu, static_cast<unsigned>(n));
     }
-    if (total > kWKeyCap) return -1;
-    if (lane == 0) w.off[cs.nseg] = total;
+    if (lane == 0) w.off[cs.nseg] = npairs;
     __syncwarp();
-    for (int i0 = lane; i0 < total; i0 += 512) {             // sixteen loads in flight per lane
-        Cand v[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int i = i0 + 32 * u;
-            if (i < total) {
-                int l = 0, h = cs.nseg;                       // segment with off[l] <= i < off[l+1]
-                while (h - l > 1) {
-                    const int mid = (l + h) >> 1;
-                    if (w.off[mid] <= i) l = mid; else h = mid;
-                }
-                v[u] = cs.base[static_cast<long long>(l) * cs.cap + (i - w.off[l])];
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-            if (i0 + 32 * u < total) { w.keys[i0 + 32 * u] = fkey(v[u].v); w.ids[i0 + 32 * u] = v[u].id; }
-    }
-    __syncwarp();
-    return total;
+    if (total == 0) return 0;
+    const int c = (k > 0 && k <= 32 * kWMaxC && total > 64) ? (k + 31) / 32 : 0;
+    if (c == 0 && total > kWKeyCap) return -1;
+    return c <= 1 ? warp_stage_t<1>(w, cs, npairs, c)
+         : c == 2 ? warp_stage_t<2>(w, cs, npairs, c)
+         : c <= 4 ? warp_stage_t<4>(w, cs, npairs, c)
+                  : warp_stage_t<kWMaxC>(w, cs, npairs, c);
 }
 
 // k-th largest (1-based, with multiplicity) of the keys keys[0..n), 1 <= k <= n, by a bitwise
@@ -202,7 +277,7 @@ __device__ bool warp_topn(WarpSmem& w, const Args& a, const TileStats* ts, int s
     const int lane = threadIdx.x & 31;
     const int nseg = a.nseg_x;
     const WCands cs{a.cand_raw + static_cast<long long>(slot) * nseg * kCandRawGlobal, kCandRawGlobal, nseg};
-    const int n = warp_stage(w, ts, cs, true);
+    const int n = warp_stage(w, ts, cs, true, min(a.n_top, a.V));
     const int nt = min(a.n_top, a.V);
     if (n < nt) return false;                  // also n = -1
     const uint32_t kth = warp_kth(w, n, nt);
@@ -255,8 +330,8 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
     for (int t = lane; t < nseg; t += 32) {
         const TileStats x = ts[t];
         if (x.m_pen == mp) arg = min(arg, x.arg_pen);
-        sraw += static_cast<double>(x.s_raw) * exp2(static_cast<double>(x.m_raw - mr) * kL2E);
-        if (!greedy) stemp += static_cast<double>(x.s_temp) * exp2(static_cast<double>(x.m_pen - mp) * c_l2e);
+        sraw += static_cast<double>(x.s_raw) * static_cast<double>(exp2f((x.m_raw - mr) * kL2E));
+        if (!greedy) stemp += static_cast<double>(x.s_temp) * static_cast<double>(exp2f((x.m_pen - mp) * c_l2e));
     }
     for (int off = 16; off; off >>= 1) {
         arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, off));
@@ -265,7 +340,7 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
     }
     o.argmax = arg;
     o.m_pen = mp;
-    o.lse = mr + static_cast<float>(log(sraw));
+    o.lse = mr + logf(static_cast<float>(sraw));
     o.c_l2e = c_l2e;
     o.top_p = r.top_p;
     o.tau = -INFINITY;
@@ -276,7 +351,7 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
         o.mode = kModeGreedy;
     } else if (list) {
         const WCands cs{a.cand_x + static_cast<long long>(slot) * nseg * kCandPenGlobal, kCandPenGlobal, nseg};
-        const int n = warp_stage(w, ts, cs, false);
+        const int n = warp_stage(w, ts, cs, false, k);
         if (n < k) return false;               // too many candidates to stage, or fewer than k
         const uint32_t kth = warp_kth(w, n, k);
         const int cnt = warp_survivors(w, n, kth);
@@ -322,7 +397,7 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
         const TileStats x = ts[t];
         if (t_one) z += static_cast<double>(x.s_raw);
         else if (x.m_raw > 0.f)
-            z += static_cast<double>(x.s_temp) * exp2(static_cast<double>(inv_t) * log2(static_cast<double>(x.m_raw) / qmax));
+            z += static_cast<double>(x.s_temp) * static_cast<double>(exp2f(inv_t * log2f(x.m_raw / qmax)));
     }
     for (int off = 16; off; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
     QRowOut o{};
@@ -343,7 +418,7 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
     o.flags = fl;
     if (list) {
         const WCands cs{a.cand_q + static_cast<long long>(qslot) * nseg * kCandPenGlobal, kCandPenGlobal, nseg};
-        const int n = warp_stage(w, ts, cs, false);
+        const int n = warp_stage(w, ts, cs, false, k);
         if (n < k) return false;
         const uint32_t kth = warp_kth(w, n, k);
         const int cnt = warp_survivors(w, n, kth);
@@ -364,134 +439,6 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
     }
     if (lane == 0) a.qout[qslot] = o;
     return true;
-}
-
-// ------------------------------------------------------------------ segment trimming
-// Every member of a row's top-k (ties included) that lies in segment s is also among s's
-// own top-k (with ties): s holds fewer than k values above the row's k-th largest.  So each
-// segment's candidate list can be cut to its own top-k before the row-level selection, one
-// warp per list, all lists at once.
-constexpr int kTrimCap = 1536;         // longest list (the global caps)
-constexpr int kTrimStage = 512;        // survivors of the first stage kept for the exact second
-constexpr int kTrimMaxC = 8;           // ceil(k / 32) for k <= kMaxCandTopK
-
-struct TrimSmem {
-    uint32_t keys[kTrimStage];
-    int ids[kTrimStage];
-};
-static_assert(kTrimCap >= kCandPenGlobal && kTrimCap >= kCandRawGlobal, "a whole list must fit");
-static_assert(32 * kTrimMaxC >= kMaxCandTopK, "per-lane depth must cover k");
-
-// Cut the list c[0..*n) down towards its own top-k (ties kept), in place, *n updated.
-//   1. Each lane keeps the c = ceil(k/32) largest keys of its share; the least of the
-//      lanes' c-th largest is a lower bound of the list's k-th largest (32c >= k keys reach it).
-//   2. The entries at or above that bound are compacted over the list's front; when at most
-//      kTrimStage remain they are also staged, the exact k-th largest is found among them
-//      and only the entries reaching it are kept.
-__device__ void trim_list(TrimSmem& w, Cand* c, int* n_io, int k) {
-    const int lane = threadIdx.x & 31;
-    const unsigned lt = (1u << lane) - 1u;
-    const int n = *n_io;
-    if (n <= k || n > kTrimCap) return;
-    const int cdepth = (k + 31) / 32;
-    uint32_t top[kTrimMaxC];                              // descending; 0 = nothing yet
-#pragma unroll
-    for (int q = 0; q < kTrimMaxC; ++q) top[q] = 0u;
-    for (int i0 = lane; i0 < n; i0 += 512) {              // sixteen loads in flight per lane
-        float v[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) if (i0 + 32 * u < n) v[u] = c[i0 + 32 * u].v;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            uint32_t x = i0 + 32 * u < n ? fkey(v[u]) : 0u;
-#pragma unroll
-            for (int q = 0; q < kTrimMaxC; ++q) {         // insertion into the lane's top list
-                const bool sw = q < cdepth && x > top[q];
-                const uint32_t t = top[q];
-                top[q] = sw ? x : t;
-                x = sw ? t : x;
-            }
-        }
-    }
-    uint32_t lb = 0u;
-#pragma unroll
-    for (int q = 0; q < kTrimMaxC; ++q) if (q == cdepth - 1) lb = top[q];
-    lb = __reduce_min_sync(0xffffffffu, lb);
-    // stage 1: keep key >= lb (each batch is read before any of it is written; writes land at
-    // or below the batch being read)
-    int m = 0;
-    for (int i0 = 0; i0 < n; i0 += 512) {
-        Cand e[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) { const int i = i0 + lane + 32 * u; if (i < n) e[u] = c[i]; }
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int i = i0 + lane + 32 * u;
-            const uint32_t key = i < n ? fkey(e[u].v) : 0u;
-            const bool f = i < n && key >= lb;
-            const unsigned b = __ballot_sync(0xffffffffu, f);
-            const int pos = m + __popc(b & lt);
-            if (f) {
-                c[pos] = e[u];
-                if (pos < kTrimStage) { w.keys[pos] = key; w.ids[pos] = e[u].id; }
-            }
-            m += __popc(b);
-        }
-        __syncwarp();
-    }
-    if (m > kTrimStage) {                                 // keep the stage-1 result
-        if (lane == 0) *n_io = m;
-        __syncwarp();
-        return;
-    }
-    // stage 2: exact k-th largest among the m staged entries
-    const uint32_t kth = kth_key_bits(w.keys, m, k);
-    int r = 0;
-    for (int base = 0; base < m; base += 32) {
-        const int i = base + lane;
-        const bool f = i < m && w.keys[i] >= kth;
-        const unsigned b = __ballot_sync(0xffffffffu, f);
-        if (f) c[r + __popc(b & lt)] = Cand{key_to_f(w.keys[i]), w.ids[i]};
-        r += __popc(b);
-    }
-    if (lane == 0) *n_io = r;
-    __syncwarp();
-}
-
-__global__ void __launch_bounds__(32 * kRowsPerBlock) cand_trim_kernel(Args a) {
-    pdl_enter();
-    extern __shared__ __align__(16) unsigned char trim_raw[];
-    const int warp = threadIdx.x >> 5;
-    TrimSmem& w = reinterpret_cast<TrimSmem*>(trim_raw)[warp];
-    const long long gw = static_cast<long long>(blockIdx.x) * kRowsPerBlock + warp;
-    const long long nx = static_cast<long long>(a.xslots) * a.nseg_x;
-    if (gw < nx) {
-        const int slot = static_cast<int>(gw / a.nseg_x), t = static_cast<int>(gw % a.nseg_x);
-        const int b = slot / (a.Km + 1), j = slot % (a.Km + 1);
-        const dspark_row_params_t r = a.rows[b];
-        if ((a.row_status[b] & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || j > r.num_drafts) return;
-        TileStats* ts = a.ts_x + static_cast<long long>(slot) * a.nseg_x + t;
-        const long long ti = static_cast<long long>(slot) * a.nseg_x + t;
-        const int fl = ts->flags;
-        const int k = r.top_k;
-        if (r.temperature > 0.f && k > 0 && k < a.V && k <= kMaxCandTopK && !(fl & kTileOverflowPen))
-            trim_list(w, a.cand_x + ti * kCandPenGlobal, &ts->n_pen, k);
-        if (a.n_top > 0 && !(fl & kTileOverflowRaw))
-            trim_list(w, a.cand_raw + ti * kCandRawGlobal, &ts->n_raw, min(a.n_top, a.V));
-    } else {
-        const long long gq = gw - nx;
-        if (gq >= static_cast<long long>(a.qslots) * a.nseg_q) return;
-        const int qs = static_cast<int>(gq / a.nseg_q), t = static_cast<int>(gq % a.nseg_q);
-        const int b = qs / a.Km, i = qs % a.Km;
-        const dspark_row_params_t r = a.rows[b];
-        if ((a.row_status[b] & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || i >= r.num_drafts ||
-            !(r.temperature > 0.f)) return;
-        TileStats* ts = a.ts_q + static_cast<long long>(qs) * a.nseg_q + t;
-        const int k = r.top_k;
-        if (k > 0 && k < a.V && k <= kMaxCandTopK && !(ts->flags & kTileOverflowPen))
-            trim_list(w, a.cand_q + gq * kCandPenGlobal, &ts->n_pen, k);
-    }
 }
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock) row_finalize_warp_kernel(Args a) {
@@ -528,24 +475,14 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) row_finalize_warp_kernel(A
 
 }  // namespace
 
-cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s, bool pdl_first) {
-    {
-        const long long lists = static_cast<long long>(a.xslots) * a.nseg_x + static_cast<long long>(a.qslots) * a.nseg_q;
-        const int grid = static_cast<int>((lists + kRowsPerBlock - 1) / kRowsPerBlock);
-        const size_t smem = sizeof(TrimSmem) * kRowsPerBlock;
-        cudaError_t e = cudaFuncSetAttribute(cand_trim_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        e = launch_k(cand_trim_kernel, dim3(grid), dim3(32 * kRowsPerBlock), smem, s, pdl_first, a);
-        if (e != cudaSuccess) return e;
-    }
+cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s, bool pdl) {
     const int rows = a.xslots + a.qslots;
     const int grid = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
     const size_t smem = sizeof(WarpSmem) * kRowsPerBlock;
     cudaError_t e = cudaFuncSetAttribute(row_finalize_warp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_k(row_finalize_warp_kernel, dim3(grid), dim3(32 * kRowsPerBlock), smem, s, true, a);
+    return launch_k(row_finalize_warp_kernel, dim3(grid), dim3(32 * kRowsPerBlock), smem, s, pdl, a);
 }
 
 }  // namespace dspark
