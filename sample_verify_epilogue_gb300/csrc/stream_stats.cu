@@ -74,6 +74,7 @@ struct GroupSmem {
     int cnt;                     // entries appended to the pool
     int out_pen, out_raw;        // entries written to the global lists (segment finish)
     int error;
+    unsigned short flist[kGroupWarps][64];   // per warp: the tile's flagged vectors, (slot << 5) | lane
 };
 
 struct Smem {
@@ -247,6 +248,38 @@ __device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsign
     }
 }
 
+// Append the raw candidates (`mr`, tagged) and the penalised candidates (`mp`) of one
+// 16-byte vector with a single prefix and a single shared atomic for both.
+template <int SX>
+__device__ __forceinline__ void warp_append2(Cand* buf, int* cnt, int cap, unsigned mr, unsigned mp, const uint4& w,
+                                             int e, int tag) {
+    const unsigned any = __ballot_sync(0xffffffffu, (mr | mp) != 0u);
+    if (!any) return;
+    const int lane = threadIdx.x & 31;
+    const int n = __popc(mr) + __popc(mp);
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int base = 0;
+    if (lane == 31) base = atomicAdd(cnt, incl);
+    base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+    while (mr) {
+        const int q = __ffs(mr) - 1;
+        mr &= mr - 1u;
+        if (base < cap) buf[base] = Cand{elem<SX>(w, q), (e + q) | tag};
+        ++base;
+    }
+    while (mp) {
+        const int q = __ffs(mp) - 1;
+        mp &= mp - 1u;
+        if (base < cap) buf[base] = Cand{elem<SX>(w, q), e + q};
+        ++base;
+    }
+}
+
 // Append every element flagged in this thread's (f0, f1) bit set (bit EPV*i+q: element q of
 // the thread's i-th vector of the tile in shared memory), warp-cooperatively: one prefix and
 // one shared atomic per warp and tile.  All lanes of the warp call it.
@@ -303,11 +336,13 @@ __device__ __forceinline__ int nth_set_bit(unsigned b, int r) {
 
 // Candidate extraction from the vectors the threads flagged during a scan (bit i of
 // `vflags`: the thread's i-th vector of the tile has an element at or above the lower
-// threshold).  The warp's flagged vectors are dealt out to its lanes 32 at a time, in slot
-// order, so a lane with many flags does not hold up the others.  For each vector: RAW
-// appends the elements >= th_r to the raw buffer; the elements >= th_p without a penalty
-// bit are appended to the penalised buffer (CAND) and folded into the running penalised
-// maximum and the lowest index attaining it (TRACK).  Every lane of the warp calls it.
+// threshold).  The warp's flagged vectors are dealt out to its lanes 32 at a time, so a lane
+// with many flags does not hold up the others: a prefix over the lanes' flag counts places
+// them in a per-warp list (more than 64 fall back to slot-wise ballots).  For each vector:
+// RAW appends the elements >= th_r to the raw buffer; the elements >= th_p without a
+// penalty bit are appended to the penalised buffer (CAND; both with one prefix and one
+// atomic) and folded into the running penalised maximum and the lowest index attaining it
+// (TRACK).  Every lane of the warp calls it.
 template <int SX, bool PEN, bool RAW, bool CAND, bool TRACK>
 __device__ __forceinline__ void flush_vectors(GroupSmem& gs, unsigned vflags, const unsigned char* data,
                                               const unsigned* bm, int vec_e0, int bit0, int gt, float th_r,
@@ -315,43 +350,65 @@ __device__ __forceinline__ void flush_vectors(GroupSmem& gs, unsigned vflags, co
     constexpr int EPV = 16 / SX;
     const int lane = threadIdx.x & 31;
     const int wv = gt - lane;                             // vector index of lane 0, slot 0
-    for (int base = 0;; base += 32) {
-        const int t = base + lane;                        // this lane's item of the round
-        int run = 0, sel_i = -1, sel_r = 0;
-        unsigned sel_b = 0u;
+    // the warp's flagged vectors in (lane, slot) order: a prefix over the lanes' counts, each
+    // lane writing its own into the warp's list
+    const int nf = __popc(vflags);
+    int incl = nf;
 #pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) {
-            const unsigned b = __ballot_sync(0xffffffffu, (vflags >> i) & 1u);
-            const int n = __popc(b);
-            const int r = t - run;
-            if (r >= 0 && r < n) { sel_i = i; sel_r = r; sel_b = b; }
-            run += n;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (total == 0) return;
+    unsigned short* list = gs.flist[gt >> 5];
+    const bool listed = total <= 64;
+    if (listed) {
+        int pos = incl - nf;
+        for (unsigned f = vflags; f; f &= f - 1u) list[pos++] = static_cast<unsigned short>(((__ffs(f) - 1) << 5) | lane);
+        __syncwarp();
+    }
+    for (int base = 0; base < total; base += 32) {
+        const int t = base + lane;                        // this lane's item of the round
+        int v = -1;
+        if (listed) {
+            if (t < total) { const unsigned it = list[t]; v = wv + static_cast<int>(it & 31u) + static_cast<int>(it >> 5) * kGroupThreads; }
+        } else {
+            // more flags than the list holds: deal them out by slot-wise ballots
+            int run = 0;
+#pragma unroll
+            for (int i = 0; i < kVecPerThread; ++i) {
+                const unsigned b = __ballot_sync(0xffffffffu, (vflags >> i) & 1u);
+                const int n = __popc(b);
+                const int r = t - run;
+                if (r >= 0 && r < n) v = wv + nth_set_bit(b, r) + i * kGroupThreads;
+                run += n;
+            }
         }
-        if (run == 0) return;
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
         unsigned mr = 0u, mp = 0u;
         int e = 0;
-        if (sel_i >= 0) {
-            const int v = wv + nth_set_bit(sel_b, sel_r) + sel_i * kGroupThreads;
+        if (v >= 0) {
             w = *reinterpret_cast<const uint4*>(data + v * 16);
             e = vec_e0 + v * EPV;
             const unsigned bits = PEN ? bitmap_bits(bm, bit0 + v * EPV, EPV) : 0u;
             if (RAW) mr = ge_mask<SX>(w, th_r);
             mp = ge_mask<SX>(w, th_p) & ~bits;
         }
-        if (RAW) warp_append<SX>(gs.pool, &gs.cnt, kSmemCandPool, mr, w, e, kRawTag);
-        if (CAND) warp_append<SX>(gs.pool, &gs.cnt, kSmemCandPool, mp, w, e, 0);
+        if (RAW && CAND) warp_append2<SX>(gs.pool, &gs.cnt, kSmemCandPool, mr, mp, w, e, kRawTag);
+        else if (RAW) warp_append<SX>(gs.pool, &gs.cnt, kSmemCandPool, mr, w, e, kRawTag);
+        else if (CAND) warp_append<SX>(gs.pool, &gs.cnt, kSmemCandPool, mp, w, e, 0);
         if (TRACK) {
             while (mp) {
                 const int q = __ffs(mp) - 1;
                 mp &= mp - 1u;
-                const float v = elem<SX>(w, q);
-                if (v > m_p) { m_p = v; arg = e + q; }
-                else if (v == m_p && e + q < arg) arg = e + q;
+                const float x = elem<SX>(w, q);
+                if (x > m_p) { m_p = x; arg = e + q; }
+                else if (x == m_p && e + q < arg) arg = e + q;
             }
         }
-        if (base + 32 >= run) return;
     }
+    if (listed) __syncwarp();                             // the list is rewritten by the next flush
 }
 
 // ------------------------------------------------------------------ target-logit segments
