@@ -1050,62 +1050,67 @@ __device__ __forceinline__ int stream_len(int S, int G, int c, int g) {
     return first >= S ? 0 : (S - 1 - first) / (2 * G) + 1;
 }
 
-// The plan, derived by every CTA from the per-request segment counts: request b owns the
-// segments [base_b, base_b + n_b) of the call (its target rows' segments first, row by row,
-// then its draft rows'), and segment s goes to CTA s mod G, consumer group (s div G) mod 2,
-// position s div 2G of that group's stream.  The CTA writes the descriptors of its own two
-// streams to its slice of the unit array and returns the number of segments S.  The
-// exclusive prefix of the counts is built in the first data stage, which no copy has
-// touched yet.  Every thread of the CTA calls it.
+// The plan, derived by every CTA from the per-request segment counts: the call's target
+// segments come first (request b's at [bx_b, bx_b + nx_b), its rows' in order), then its draft
+// segments (request b's at Sx + [bq_b, bq_b + nq_b)), so that the two consumer groups of a
+// CTA mostly run the same kind of tile, and one code path, at a time.  Segment s goes to CTA
+// s mod G, consumer group (s div G) mod 2, position s div 2G of that group's stream.  The CTA
+// writes the descriptors of its own two streams to its slice of the unit array and returns
+// the number of segments S.  The exclusive prefixes of the counts are built in the first
+// data stage, which no copy has touched yet.  Every thread of the CTA calls it.
 __device__ int build_streams(const Args& a, Smem& sm, int c, int G) {
     const int tid = threadIdx.x, lane = tid & 31;
     const int B = a.B;
-    int* base = reinterpret_cast<int*>(sm.data[0]);          // [B + 1]
-    int* nxs = base + B + 1;                                  // [B]
-    static_assert(sizeof(int) * (2 * kMaxB + 1) <= kStageBytes, "plan scratch must fit one stage");
+    int* bx = reinterpret_cast<int*>(sm.data[0]);            // [B + 1]
+    int* bq = bx + B + 1;                                     // [B + 1]
+    static_assert(sizeof(int) * 2 * (kMaxB + 1) <= kStageBytes, "plan scratch must fit one stage");
     if (tid < 32) {
         // lane l scans its own chunk of requests, then the chunk totals are scanned across lanes
         const int chunk = (B + 31) / 32;
         const int lo = min(B, lane * chunk), hi = min(B, lo + chunk);
-        int sum = 0;
-        for (int b = lo; b < hi; ++b) sum += a.req_n[b];
-        int incl = sum;
+        int sx = 0, sq = 0;
+        for (int b = lo; b < hi; ++b) { const int nx = a.req_n[B + b]; sx += nx; sq += a.req_n[b] - nx; }
+        int ix = sx, iq = sq;
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+            const int yx = __shfl_up_sync(0xffffffffu, ix, o);
+            const int yq = __shfl_up_sync(0xffffffffu, iq, o);
+            if (lane >= o) { ix += yx; iq += yq; }
         }
-        int run = incl - sum;
+        int rx = ix - sx, rq = iq - sq;
         for (int b = lo; b < hi; ++b) {
-            base[b] = run;
-            run += a.req_n[b];
-            nxs[b] = a.req_n[B + b];
+            const int nx = a.req_n[B + b];
+            bx[b] = rx; rx += nx;
+            bq[b] = rq; rq += a.req_n[b] - nx;
         }
-        if (lane == 31) base[B] = incl;
+        if (lane == 31) { bx[B] = ix; bq[B] = iq; }
     }
     __syncthreads();
-    const int S = base[B];
+    const int Sx = bx[B];
+    const int S = Sx + bq[B];
     for (int idx = tid; idx < kGroups * a.max_seg; idx += blockDim.x) {
         const int g = idx / a.max_seg, m = idx - g * a.max_seg;
         const long long s = c + static_cast<long long>(G) * (g + 2 * m);
         if (s >= S) continue;
-        int l = 0, h = B;                                     // last b with base[b] <= s
+        const bool is_x = s < Sx;
+        const int* base = is_x ? bx : bq;
+        const int key = static_cast<int>(is_x ? s : s - Sx);
+        int l = 0, h = B;                                     // last b with base[b] <= key (and segments)
         while (h - l > 1) {
             const int mid = (l + h) >> 1;
-            if (base[mid] <= s) l = mid; else h = mid;
+            if (base[mid] <= key) l = mid; else h = mid;
         }
         const int b = l;
-        int local = static_cast<int>(s - base[b]);
+        const int local = key - base[b];
         const dspark_row_params_t r = a.rows[b];
         UnitDesc ud;
         ud.b = b;
         int tiles, nseg;
-        if (local < nxs[b]) {
+        if (is_x) {
             ud.kind = kUnitX;
             ud.slot = b * (a.Km + 1) + local / a.nseg_x;
             ud.seg = local % a.nseg_x;
             tiles = a.tiles_x; nseg = a.nseg_x;
         } else {
-            local -= nxs[b];
             ud.kind = kUnitQ;
             ud.slot = b * a.Km + local / a.nseg_q;
             ud.seg = local % a.nseg_q;
