@@ -830,13 +830,28 @@ __device__ void x_finish(const XCtx<SX>& c, XState& st) {
     Cand* graw = c.a.cand_raw + ti * kCandRawGlobal;
     const int total = c.gs.cnt;
     const int n = min(total, kSmemCandPool);
-    for (int i = gt; i < n; i += kGroupThreads) {
-        const Cand e = c.gs.pool[i];
-        if (e.id & kRawTag) {
-            const int p = atomicAdd(&c.gs.out_raw, 1);
+    // each warp takes 32 consecutive entries at a time: one ballot per kind and one shared
+    // atomic per kind and round
+    const unsigned lt = (1u << lane) - 1u;
+    for (int i0 = warp * 32; i0 < n; i0 += kGroupThreads) {
+        const int i = i0 + lane;
+        Cand e{0.f, 0};
+        if (i < n) e = c.gs.pool[i];
+        const bool raw = i < n && (e.id & kRawTag);
+        const unsigned br = __ballot_sync(0xffffffffu, raw);
+        const unsigned bp = __ballot_sync(0xffffffffu, i < n && !raw);
+        int base_r = 0, base_p = 0;
+        if (lane == 0) {
+            if (br) base_r = atomicAdd(&c.gs.out_raw, __popc(br));
+            if (bp) base_p = atomicAdd(&c.gs.out_pen, __popc(bp));
+        }
+        base_r = __shfl_sync(0xffffffffu, base_r, 0);
+        base_p = __shfl_sync(0xffffffffu, base_p, 0);
+        if (raw) {
+            const int p = base_r + __popc(br & lt);
             if (p < kCandRawGlobal) graw[p] = Cand{e.v, e.id & ~kRawTag};
-        } else {
-            const int p = atomicAdd(&c.gs.out_pen, 1);
+        } else if (i < n) {
+            const int p = base_p + __popc(bp & lt);
             if (p < kCandPenGlobal) gpen[p] = e;
         }
     }
