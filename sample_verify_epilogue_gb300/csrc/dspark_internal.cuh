@@ -32,7 +32,6 @@ constexpr int kBitmapWordsMax = kTileBf16 / 32;                // 640
 constexpr int kPenCap = 256;                                   // penalised tokens per tile held in smem
 constexpr int kSegTiles = 6;                                   // vocab tiles per segment (target)
 constexpr int kMaxSegTiles = 16;
-constexpr int kSmemCandPool = 2048;                            // per-segment candidates (smem), both kinds
 constexpr int kCandPenGlobal = 1536;                           // per-segment candidates kept in the workspace
 constexpr int kCandRawGlobal = 1024;
 constexpr int kMaxCandTopK = 256;                              // top_k above this uses the whole-row path

@@ -19,7 +19,9 @@
 //     top-k), the lowest index attaining the penalised max (greedy), and the candidates
 //     >= theta (the top-k threshold of the row comes from these, mlx-dspark Changelog
 //     [0.20.2] Changed: small selections instead of a full vocabulary sort);
-//   end of segment: one reduction, one write of the statistics and candidates.
+//   end of segment: one reduction and one write of the statistics (the candidates went
+//     straight to the segment's lists in global memory as they were found, positions taken
+//     from counters in shared memory).
 // Draft tiles get the same treatment with q as the key (top-k of q^(1/T) is top-k of q).
 #include "dspark_internal.cuh"
 
@@ -53,7 +55,6 @@ __device__ __forceinline__ bool wait_phase_or_err(uint64_t* bar, unsigned parity
     return true;
 }
 constexpr float kL2E = 1.4426950408889634f;
-constexpr int kRawTag = static_cast<int>(0x80000000u);  // marks raw-logit candidates in the pool (ids < 2^24)
 constexpr int kVecPerThread = kStageBytes / 16 / kGroupThreads;     // 10 vectors per thread and tile
 static_assert(kVecPerThread % 2 == 0, "vectors are scanned in pairs");
 
@@ -67,12 +68,10 @@ struct StageMeta {
 };
 
 struct GroupSmem {
-    Cand pool[kSmemCandPool];    // the segment's candidates; raw-logit ones carry kRawTag in the id
     float4 red1[kGroupWarps];    // first-tile maxima and thresholds
     float4 red[kGroupWarps];     // end-of-segment partials
     float4 red2[kGroupWarps];
-    int cnt;                     // entries appended to the pool
-    int out_pen, out_raw;        // entries written to the global lists (segment finish)
+    int n_pen, n_raw;            // entries appended to the segment's global candidate lists
     int error;
     unsigned short flist[kGroupWarps][64];   // per warp: the tile's flagged vectors, (slot << 5) | lane
 };
@@ -221,8 +220,9 @@ __device__ __forceinline__ void warp_merge_ms(float& m, float& s, float scale) {
 }
 
 // ------------------------------------------------------------------ warp-cooperative appends
-// Append the elements of one 16-byte vector flagged in `mask` (bit q = element q) to a
-// candidate buffer: one ballot, one prefix across lanes and one shared atomic per warp.
+// Append the elements of one 16-byte vector flagged in `mask` (bit q = element q) to one of
+// the segment's candidate lists in global memory: one ballot, one prefix across lanes and one
+// shared atomic (the list's counter) per warp.
 // Every lane of the warp calls it (lanes without candidates pass mask = 0).
 template <int SX>
 __device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsigned mask, const uint4& w, int e,
@@ -248,35 +248,40 @@ __device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsign
     }
 }
 
-// Append the raw candidates (`mr`, tagged) and the penalised candidates (`mp`) of one
-// 16-byte vector with a single prefix and a single shared atomic for both.
+// Append the raw candidates (`mr`, to list r) and the penalised candidates (`mp`, to list p)
+// of one 16-byte vector with a single prefix (both counts packed in one word) across lanes.
 template <int SX>
-__device__ __forceinline__ void warp_append2(Cand* buf, int* cnt, int cap, unsigned mr, unsigned mp, const uint4& w,
-                                             int e, int tag) {
+__device__ __forceinline__ void warp_append2(Cand* bufr, int* cntr, int capr, Cand* bufp, int* cntp, int capp,
+                                             unsigned mr, unsigned mp, const uint4& w, int e) {
     const unsigned any = __ballot_sync(0xffffffffu, (mr | mp) != 0u);
     if (!any) return;
     const int lane = threadIdx.x & 31;
-    const int n = __popc(mr) + __popc(mp);
+    const int n = __popc(mr) | (__popc(mp) << 16);
     int incl = n;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
-    int base = 0;
-    if (lane == 31) base = atomicAdd(cnt, incl);
-    base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+    int base_r = 0, base_p = 0;
+    if (lane == 31) {
+        if (incl & 0xFFFF) base_r = atomicAdd(cntr, incl & 0xFFFF);
+        if (incl >> 16) base_p = atomicAdd(cntp, incl >> 16);
+    }
+    const int ex = incl - n;
+    base_r = __shfl_sync(0xffffffffu, base_r, 31) + (ex & 0xFFFF);
+    base_p = __shfl_sync(0xffffffffu, base_p, 31) + (ex >> 16);
     while (mr) {
         const int q = __ffs(mr) - 1;
         mr &= mr - 1u;
-        if (base < cap) buf[base] = Cand{elem<SX>(w, q), (e + q) | tag};
-        ++base;
+        if (base_r < capr) bufr[base_r] = Cand{elem<SX>(w, q), e + q};
+        ++base_r;
     }
     while (mp) {
         const int q = __ffs(mp) - 1;
         mp &= mp - 1u;
-        if (base < cap) buf[base] = Cand{elem<SX>(w, q), e + q};
-        ++base;
+        if (base_p < capp) bufp[base_p] = Cand{elem<SX>(w, q), e + q};
+        ++base_p;
     }
 }
 
@@ -339,12 +344,12 @@ __device__ __forceinline__ int nth_set_bit(unsigned b, int r) {
 // threshold).  The warp's flagged vectors are dealt out to its lanes 32 at a time, so a lane
 // with many flags does not hold up the others: a prefix over the lanes' flag counts places
 // them in a per-warp list (more than 64 fall back to slot-wise ballots).  For each vector:
-// RAW appends the elements >= th_r to the raw buffer; the elements >= th_p without a
-// penalty bit are appended to the penalised buffer (CAND; both with one prefix and one
-// atomic) and folded into the running penalised maximum and the lowest index attaining it
-// (TRACK).  Every lane of the warp calls it.
+// RAW appends the elements >= th_r to the raw list `lr`; the elements >= th_p without a
+// penalty bit are appended to the penalised list `lp` (CAND; both with one prefix) and
+// folded into the running penalised maximum and the lowest index attaining it (TRACK).
+// Every lane of the warp calls it.
 template <int SX, bool PEN, bool RAW, bool CAND, bool TRACK>
-__device__ __forceinline__ void flush_vectors(GroupSmem& gs, unsigned vflags, const unsigned char* data,
+__device__ __forceinline__ void flush_vectors(GroupSmem& gs, Cand* lr, Cand* lp, unsigned vflags, const unsigned char* data,
                                               const unsigned* bm, int vec_e0, int bit0, int gt, float th_r,
                                               float th_p, float& m_p, int& arg) {
     constexpr int EPV = 16 / SX;
@@ -395,9 +400,9 @@ __device__ __forceinline__ void flush_vectors(GroupSmem& gs, unsigned vflags, co
             if (RAW) mr = ge_mask<SX>(w, th_r);
             mp = ge_mask<SX>(w, th_p) & ~bits;
         }
-        if (RAW && CAND) warp_append2<SX>(gs.pool, &gs.cnt, kSmemCandPool, mr, mp, w, e, kRawTag);
-        else if (RAW) warp_append<SX>(gs.pool, &gs.cnt, kSmemCandPool, mr, w, e, kRawTag);
-        else if (CAND) warp_append<SX>(gs.pool, &gs.cnt, kSmemCandPool, mp, w, e, 0);
+        if (RAW && CAND) warp_append2<SX>(lr, &gs.n_raw, kCandRawGlobal, lp, &gs.n_pen, kCandPenGlobal, mr, mp, w, e);
+        else if (RAW) warp_append<SX>(lr, &gs.n_raw, kCandRawGlobal, mr, w, e, 0);
+        else if (CAND) warp_append<SX>(lp, &gs.n_pen, kCandPenGlobal, mp, w, e, 0);
         if (TRACK) {
             while (mp) {
                 const int q = __ffs(mp) - 1;
@@ -428,6 +433,8 @@ struct XCtx {
     const StageMeta& m;
     bool greedy, need_lp, need_raw, need_cand, need_temp;
     float f, p, c_l2e;
+    Cand* lp;            // the segment's penalised-candidate list (global)
+    Cand* lr;            // the segment's raw-candidate list (global)
 };
 
 // Raw value of element e of the current tile: shared memory for the aligned interior,
@@ -460,7 +467,7 @@ __device__ __forceinline__ void pen_fold(const XCtx<SX>& c, XState& st, float xp
         st.s_t += ex2_approx((xp - st.m_p) * c.c_l2e);
         if (undo_raw) st.s_t -= ex2_approx((xr - st.m_p) * c.c_l2e);
     }
-    if (xp >= st.th_p) push(c.gs.pool, &c.gs.cnt, kSmemCandPool, xp, e);
+    if (xp >= st.th_p) push(c.lp, &c.gs.n_pen, kCandPenGlobal, xp, e);
 }
 
 // One 16-byte vector: raw statistics over all its elements, penalised statistics over the
@@ -521,7 +528,7 @@ __device__ __forceinline__ void fold_fast(const XCtx<SX>& c, XState& st, float x
     if (xp >= st.th_p) {
         if (xp > st.m_p) { st.m_p = xp; st.arg = e; }
         else if (xp == st.m_p && e < st.arg) st.arg = e;
-        if (c.need_cand) push(c.gs.pool, &c.gs.cnt, kSmemCandPool, xp, e);
+        if (c.need_cand) push(c.lp, &c.gs.n_pen, kCandPenGlobal, xp, e);
     }
 }
 
@@ -634,10 +641,10 @@ __device__ __forceinline__ unsigned x_scan_flags(XState& st, const unsigned char
 }
 
 template <int SX, bool PEN, bool RAW>
-__device__ __forceinline__ void x_flush_cand(bool cand, GroupSmem& gs, unsigned fl, const unsigned char* data,
+__device__ __forceinline__ void x_flush_cand(bool cand, GroupSmem& gs, Cand* lr, Cand* lp, unsigned fl, const unsigned char* data,
                                              const unsigned* bm, int vec_e0, int bit0, int gt, XState& st) {
-    if (cand) flush_vectors<SX, PEN, RAW, true, true>(gs, fl, data, bm, vec_e0, bit0, gt, st.th_r, st.th_p, st.m_p, st.arg);
-    else flush_vectors<SX, PEN, RAW, false, true>(gs, fl, data, bm, vec_e0, bit0, gt, st.th_r, st.th_p, st.m_p, st.arg);
+    if (cand) flush_vectors<SX, PEN, RAW, true, true>(gs, lr, lp, fl, data, bm, vec_e0, bit0, gt, st.th_r, st.th_p, st.m_p, st.arg);
+    else flush_vectors<SX, PEN, RAW, false, true>(gs, lr, lp, fl, data, bm, vec_e0, bit0, gt, st.th_r, st.th_p, st.m_p, st.arg);
 }
 
 // Scan and candidate flush of one tile on the fast path.
@@ -650,11 +657,11 @@ __device__ __forceinline__ void x_fast_pass(const XCtx<SX>& c, XState& st, const
                                   : x_scan_flags<SX, false>(st, data, gt, m.nvec, th);
     const int bit0 = m.vec_e0 - m.e0;
     if (m.pen) {
-        if (c.need_raw) x_flush_cand<SX, true, true>(c.need_cand, c.gs, fl, data, bm, m.vec_e0, bit0, gt, st);
-        else x_flush_cand<SX, true, false>(c.need_cand, c.gs, fl, data, bm, m.vec_e0, bit0, gt, st);
+        if (c.need_raw) x_flush_cand<SX, true, true>(c.need_cand, c.gs, c.lr, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
+        else x_flush_cand<SX, true, false>(c.need_cand, c.gs, c.lr, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
     } else {
-        if (c.need_raw) x_flush_cand<SX, false, true>(c.need_cand, c.gs, fl, data, bm, m.vec_e0, bit0, gt, st);
-        else x_flush_cand<SX, false, false>(c.need_cand, c.gs, fl, data, bm, m.vec_e0, bit0, gt, st);
+        if (c.need_raw) x_flush_cand<SX, false, true>(c.need_cand, c.gs, c.lr, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
+        else x_flush_cand<SX, false, false>(c.need_cand, c.gs, c.lr, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
     }
 }
 
@@ -773,8 +780,8 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
         if (sh < 64) { fr0 |= static_cast<unsigned long long>(mr) << sh; fp0 |= static_cast<unsigned long long>(mp) << sh; }
         else { fr1 |= static_cast<unsigned long long>(mr) << (sh - 64); fp1 |= static_cast<unsigned long long>(mp) << (sh - 64); }
     }
-    if (!fast && c.need_raw) flush_flags<SX>(c.gs.pool, &c.gs.cnt, kSmemCandPool, fr0, fr1, data, m.vec_e0, gt, kRawTag);
-    if (!fast && c.need_cand) flush_flags<SX>(c.gs.pool, &c.gs.cnt, kSmemCandPool, fp0, fp1, data, m.vec_e0, gt, 0);
+    if (!fast && c.need_raw) flush_flags<SX>(c.lr, &c.gs.n_raw, kCandRawGlobal, fr0, fr1, data, m.vec_e0, gt, 0);
+    if (!fast && c.need_cand) flush_flags<SX>(c.lp, &c.gs.n_pen, kCandPenGlobal, fp0, fp1, data, m.vec_e0, gt, 0);
     if (gt < 2) {
         const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
         for (int e = lo; e < hi; ++e) {
@@ -790,7 +797,7 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
             } else {
                 st.m_r = max_nan(st.m_r, xv);
             }
-            if (xv >= st.th_r) push(c.gs.pool, &c.gs.cnt, kSmemCandPool, xv, e | kRawTag);
+            if (xv >= st.th_r) push(c.lr, &c.gs.n_raw, kCandRawGlobal, xv, e);
             const bool bit = m.pen && bitmap_bit(bm, e - m.e0);
             if (fast) {
                 if (!bit) fold_fast(c, st, xv, e);
@@ -823,39 +830,8 @@ __device__ void x_finish(const XCtx<SX>& c, XState& st) {
         c.gs.red[warp] = make_float4(mr, sr, mp, stt);
         c.gs.red2[warp] = make_float4(__int_as_float(arg), 0.f, 0.f, 0.f);
     }
-    group_sync(c.g);
-    // the pool into the segment's two global lists (order within a list is immaterial)
+    group_sync(c.g);                                      // partials written, every append done
     const long long ti = static_cast<long long>(m.slot) * c.a.nseg_x + m.seg;
-    Cand* gpen = c.a.cand_x + ti * kCandPenGlobal;
-    Cand* graw = c.a.cand_raw + ti * kCandRawGlobal;
-    const int total = c.gs.cnt;
-    const int n = min(total, kSmemCandPool);
-    // each warp takes 32 consecutive entries at a time: one ballot per kind and one shared
-    // atomic per kind and round
-    const unsigned lt = (1u << lane) - 1u;
-    for (int i0 = warp * 32; i0 < n; i0 += kGroupThreads) {
-        const int i = i0 + lane;
-        Cand e{0.f, 0};
-        if (i < n) e = c.gs.pool[i];
-        const bool raw = i < n && (e.id & kRawTag);
-        const unsigned br = __ballot_sync(0xffffffffu, raw);
-        const unsigned bp = __ballot_sync(0xffffffffu, i < n && !raw);
-        int base_r = 0, base_p = 0;
-        if (lane == 0) {
-            if (br) base_r = atomicAdd(&c.gs.out_raw, __popc(br));
-            if (bp) base_p = atomicAdd(&c.gs.out_pen, __popc(bp));
-        }
-        base_r = __shfl_sync(0xffffffffu, base_r, 0);
-        base_p = __shfl_sync(0xffffffffu, base_p, 0);
-        if (raw) {
-            const int p = base_r + __popc(br & lt);
-            if (p < kCandRawGlobal) graw[p] = Cand{e.v, e.id & ~kRawTag};
-        } else if (i < n) {
-            const int p = base_p + __popc(bp & lt);
-            if (p < kCandPenGlobal) gpen[p] = e;
-        }
-    }
-    group_sync(c.g);
     if (warp == 0) {
         float4 r = lane < kGroupWarps ? c.gs.red[lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
         int ag = lane < kGroupWarps ? __float_as_int(c.gs.red2[lane].x) : 0x7FFFFFFF;
@@ -867,19 +843,19 @@ __device__ void x_finish(const XCtx<SX>& c, XState& st) {
         warp_merge_ms(Mr, Sr, kL2E);
         warp_merge_ms(Mp, St, c.c_l2e);
         if (lane == 0) {
-            const int n_pen = c.gs.out_pen, n_raw = c.gs.out_raw;
-            const bool lost = total > kSmemCandPool;      // some appends were dropped (of either kind)
+            const int n_pen = c.gs.n_pen, n_raw = c.gs.n_raw;
             TileStats ts;
             ts.m_raw = Mr; ts.s_raw = Sr; ts.m_pen = Mp; ts.arg_pen = ag; ts.s_temp = St;
             ts.flags = 0;
             ts.n_pen = c.need_cand ? n_pen : 0;
             ts.n_raw = c.need_raw ? n_raw : 0;
-            if (c.need_cand && (lost || n_pen > kCandPenGlobal)) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
-            if (c.need_raw && (lost || n_raw > kCandRawGlobal)) { ts.flags |= kTileOverflowRaw; ts.n_raw = 0; }
+            if (c.need_cand && n_pen > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
+            if (c.need_raw && n_raw > kCandRawGlobal) { ts.flags |= kTileOverflowRaw; ts.n_raw = 0; }
             if (!isfinite(Mr) || !isfinite(Mp)) ts.flags |= kTileBad;
             c.a.ts_x[ti] = ts;
-            // counters for the next segment (its first append follows its first-tile barrier)
-            c.gs.cnt = 0; c.gs.out_pen = 0; c.gs.out_raw = 0;
+            // counters for the next segment: its first append follows its first-tile barrier,
+            // which this warp reaches only after this write
+            c.gs.n_pen = 0; c.gs.n_raw = 0;
         }
     }
 }
@@ -891,14 +867,14 @@ struct QState {
 };
 
 __device__ __forceinline__ void q_elem(QState& st, float v, bool need_sum, bool t_one, float inv_t, bool filt,
-                                       GroupSmem& gs, int e) {
+                                       GroupSmem& gs, Cand* lp, int e) {
     if (need_sum && !t_one && v > st.mx) {
         st.sum = (st.mx > 0.f) ? st.sum * exp2f(inv_t * log2f(st.mx / v)) : 0.f;
     }
     st.mx = max_nan(st.mx, v);
     st.mn = fminf(st.mn, v);
     if (need_sum) st.sum += t_one ? v : draft_weight(v, st.mx, inv_t, false);
-    if (filt && v >= st.th) push(gs.pool, &gs.cnt, kSmemCandPool, v, e);
+    if (filt && v >= st.th) push(lp, &gs.n_pen, kCandPenGlobal, v, e);
 }
 
 __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage, const StageMeta& m, QState& st) {
@@ -912,6 +888,7 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
     const float inv_t = 1.f / m.temperature;
     const long long qrow = static_cast<long long>(m.slot) * a.V;
     const int e_tail = m.vec_e0 + m.nvec * 4;
+    Cand* const lp = a.cand_q + (static_cast<long long>(m.slot) * a.nseg_q + m.seg) * kCandPenGlobal;
     if (m.first) {
         float mx0 = -INFINITY, mx1 = -INFINITY;
         int v = gt;
@@ -974,7 +951,7 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
         st.mn = fminf(mn0, mn1);
         float m_unused = 0.f;
         int a_unused = 0;
-        flush_vectors<4, false, false, true, false>(gs, vfl, data, nullptr, m.vec_e0, 0, gt, INFINITY, th, m_unused,
+        flush_vectors<4, false, false, true, false>(gs, nullptr, lp, vfl, data, nullptr, m.vec_e0, 0, gt, INFINITY, th, m_unused,
                                                     a_unused);
     }
 #pragma unroll 2
@@ -988,10 +965,10 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
         const float vn = fminf(fminf(w.x, w.y), fminf(w.z, w.w));
         if (need_sum && !t_one) {
             if (!(vm <= st.mx)) {
-                q_elem(st, w.x, true, false, inv_t, false, gs, e);
-                q_elem(st, w.y, true, false, inv_t, false, gs, e + 1);
-                q_elem(st, w.z, true, false, inv_t, false, gs, e + 2);
-                q_elem(st, w.w, true, false, inv_t, false, gs, e + 3);
+                q_elem(st, w.x, true, false, inv_t, false, gs, lp, e);
+                q_elem(st, w.y, true, false, inv_t, false, gs, lp, e + 1);
+                q_elem(st, w.z, true, false, inv_t, false, gs, lp, e + 2);
+                q_elem(st, w.w, true, false, inv_t, false, gs, lp, e + 3);
             } else {
                 st.sum += draft_weight(w.x, st.mx, inv_t, false) + draft_weight(w.y, st.mx, inv_t, false) +
                           draft_weight(w.z, st.mx, inv_t, false) + draft_weight(w.w, st.mx, inv_t, false);
@@ -1004,7 +981,7 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
     }
     if (gt < 2) {
         const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
-        for (int e = lo; e < hi; ++e) q_elem(st, __ldg(a.q + qrow + e), need_sum, t_one, inv_t, need_cand, gs, e);
+        for (int e = lo; e < hi; ++e) q_elem(st, __ldg(a.q + qrow + e), need_sum, t_one, inv_t, need_cand, gs, lp, e);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[stage]);
@@ -1028,10 +1005,7 @@ __device__ void q_finish(const Args& a, GroupSmem& gs, int g, const StageMeta& m
     if (need_sum && !t_one) r = (sum > 0.f && mx > 0.f) ? sum * exp2f(inv_t * log2f(mx / M)) : 0.f;
     r = warp_sum(r);
     if (lane == 0) gs.red[warp] = make_float4(M, r, mnw, 0.f);
-    group_sync(g);
-    const int total = gs.cnt;                             // draft segments append no raw entries
-    const int n = min(total, kSmemCandPool);
-    const bool lost = total > kSmemCandPool;
+    group_sync(g);                                        // partials written, every append done
     const long long ti = static_cast<long long>(m.slot) * a.nseg_q + m.seg;
     if (warp == 0) {
         const float4 v = lane < kGroupWarps ? gs.red[lane] : make_float4(-INFINITY, 0.f, INFINITY, 0.f);
@@ -1043,20 +1017,18 @@ __device__ void q_finish(const Args& a, GroupSmem& gs, int g, const StageMeta& m
         float mnn = v.z;
         for (int o = 16; o; o >>= 1) mnn = fminf(mnn, __shfl_xor_sync(0xffffffffu, mnn, o));
         if (lane == 0) {
+            const int n = gs.n_pen;                       // draft segments append no raw entries
             TileStats ts;
             ts.m_raw = Mg; ts.s_raw = t_one ? s : 0.f; ts.m_pen = mnn; ts.arg_pen = 0; ts.s_temp = t_one ? 0.f : s;
             ts.n_pen = need_cand ? n : 0; ts.n_raw = 0; ts.flags = 0;
-            if (need_cand && (lost || n > kCandPenGlobal)) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
+            if (need_cand && n > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
             if (!(mnn >= 0.f) || !(Mg <= 3.0e38f)) ts.flags |= kTileBad;
             a.ts_q[ti] = ts;
+            // counters for the next segment: its first append follows its first-tile barrier,
+            // which this warp reaches only after this write
+            gs.n_pen = 0; gs.n_raw = 0;
         }
     }
-    if (need_cand && !lost && n <= kCandPenGlobal) {
-        Cand* dst = a.cand_q + ti * kCandPenGlobal;
-        for (int i = gt; i < n; i += kGroupThreads) dst[i] = gs.pool[i];
-    }
-    group_sync(g);
-    if (gt == 0) { gs.cnt = 0; gs.out_pen = 0; gs.out_raw = 0; }
 }
 
 // Segments in the stream of (CTA c, group g): positions m with c + G*(g + 2m) < S.
@@ -1157,7 +1129,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], kGroupWarps); }
         for (int g = 0; g < kGroups; ++g) {
-            sm.grp[g].cnt = 0; sm.grp[g].out_pen = 0; sm.grp[g].out_raw = 0; sm.grp[g].error = 0;
+            sm.grp[g].n_pen = 0; sm.grp[g].n_raw = 0; sm.grp[g].error = 0;
         }
         fence_mbar_init();
     }
@@ -1326,9 +1298,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
             if (m.kind == kUnitX) {
                 const bool greedy = !(m.temperature > 0.f);
                 const int k = m.top_k;
+                const long long ti = static_cast<long long>(m.slot) * a.nseg_x + m.seg;
                 XCtx<SX> ctx{a, sm, gs, g, stage, m, greedy, a.want_lp || a.n_top > 0, a.n_top > 0,
                              !greedy && k > 0 && k < a.V && k <= kMaxCandTopK, !greedy && (k == 0 || k >= a.V),
-                             m.frequency, m.presence, (!greedy && (k == 0 || k >= a.V)) ? kL2E / m.temperature : 0.f};
+                             m.frequency, m.presence, (!greedy && (k == 0 || k >= a.V)) ? kL2E / m.temperature : 0.f,
+                             a.cand_x + ti * kCandPenGlobal, a.cand_raw + ti * kCandRawGlobal};
                 x_tile<SX>(ctx, xs);
                 if (last) x_finish<SX>(ctx, xs);
             } else {
