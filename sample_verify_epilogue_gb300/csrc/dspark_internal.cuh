@@ -25,10 +25,10 @@ constexpr int kGroupThreads = kGroupWarps * 32;                // 256
 constexpr int kConsumerThreads = kGroups * kGroupThreads;      // 512
 constexpr int kStreamThreads = kConsumerThreads + 32;          // + one producer warp
 constexpr int kStages = 4;
-constexpr int kStageBytes = 40 * 1024;                         // one vocab tile per stage
-constexpr int kTileBf16 = kStageBytes / 2;                     // 20480 elements
-constexpr int kTileF32 = kStageBytes / 4;                      // 10240 elements
-constexpr int kBitmapWordsMax = kTileBf16 / 32;                // 640
+constexpr int kStageBytes = 48 * 1024;                         // one vocab tile per stage
+constexpr int kTileBf16 = kStageBytes / 2;                     // 24576 elements
+constexpr int kTileF32 = kStageBytes / 4;                      // 12288 elements
+constexpr int kBitmapWordsMax = kTileBf16 / 32;                // 768
 constexpr int kPenCap = 256;                                   // penalised tokens per tile held in smem
 constexpr int kSegTiles = 6;                                   // vocab tiles per segment (target)
 constexpr int kMaxSegTiles = 16;

@@ -21,7 +21,7 @@ namespace {
 constexpr float kL2E = 1.4426950408889634f;
 constexpr int kFinThreads = 256;
 constexpr int kKeyCap = 4096;          // candidate keys staged in shared memory
-constexpr int kMaxSegs = 1024;         // segments per row (V <= 2^24 with 10240-element tiles: 410)
+constexpr int kMaxSegs = 1024;         // segments per row (V <= 2^24 with 12,288-element tiles: 228)
 
 struct FinSmem {
     union {
@@ -215,7 +215,7 @@ struct FullSmem {
     float top_v[64];
     int n_gt, n_eq;
     double dwarp_plim;
-    uint4 tb[2][kStageBytes / 16];     // double-buffered vocab tile (cp.async)
+    uint4 tb[2][kStageBytes / 32];     // double-buffered half vocab tile (cp.async)
 };
 
 // Value of element e of the row: penalised target logit or draft probability.
@@ -266,11 +266,11 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
-// One pass over the row calling fn(e, value, raw) for every element, tile by tile (40 KB:
-// the penalty tiles of a target row, 10,240 probabilities of a draft row).  The 16-byte-aligned
-// interior of each tile is copied into shared memory with cp.async, the next tile's copy in
-// flight while this one is visited; the unaligned edges are read element by element.  The
-// penalty index of each target tile is staged in shared memory first.
+// One pass over the row calling fn(e, value, raw) for every element, in chunks of half a
+// vocab tile (two chunks per penalty tile of a target row).  The 16-byte-aligned interior of
+// each chunk is copied into shared memory with cp.async, the next chunk's copy in flight while
+// this one is visited; the unaligned edges are read element by element.  The penalty index of
+// each target tile is staged in shared memory before its first chunk.
 template <int SX, typename Fn>
 __device__ void for_each_elem_t(FullSmem& s, const RowSource& src, Fn fn) {
     const Args& a = *src.a;
@@ -279,7 +279,7 @@ __device__ void for_each_elem_t(FullSmem& s, const RowSource& src, Fn fn) {
     const unsigned char* rowp = src.is_x ? static_cast<const unsigned char*>(a.x) + src.base * SX
                                          : reinterpret_cast<const unsigned char*>(a.q + src.base);
     const int head = static_cast<int>(((16u - static_cast<unsigned>(reinterpret_cast<uintptr_t>(rowp) & 15u)) & 15u) / SX);
-    const int tile_n = src.is_x ? a.tile_x : kStageBytes / 4;
+    const int tile_n = (src.is_x ? a.tile_x : kStageBytes / 4) / 2;   // chunk: half a tile
     const int ntiles = (a.V + tile_n - 1) / tile_n;
     // aligned interior [va, vb) of tile t: element e starts a vector iff (e - head) % EPV == 0
     auto interior = [&](int t, int& va, int& vb) {
@@ -305,18 +305,21 @@ __device__ void for_each_elem_t(FullSmem& s, const RowSource& src, Fn fn) {
         __syncthreads();                                  // tile t-1 visited: its buffer is free
         issue(t + 1);
         int nh = 0, n = 0, over = 0;
+        const int p0 = (t >> 1) * a.tile_x;               // start of the penalty tile
         if (src.pen) {
-            const long long pt = static_cast<long long>(src.b) * a.tiles_x + t;
+            const long long pt = static_cast<long long>(src.b) * a.tiles_x + (t >> 1);
             const PenHdr h = a.pen_hdr[pt];
             n = h.n; nh = h.pad[0]; over = h.overflow;
-            for (int w = tid; w < a.bm_words; w += nt) s.bm[w] = a.pen_bm[pt * a.bm_words + w];
-            if (!over) for (int k = tid; k < n; k += nt) s.ent[k] = a.pen_ent[pt * kPenCap + k];
+            if (!(t & 1)) {                               // first chunk of the tile: stage its index
+                for (int w = tid; w < a.bm_words; w += nt) s.bm[w] = a.pen_bm[pt * a.bm_words + w];
+                if (!over) for (int k = tid; k < n; k += nt) s.ent[k] = a.pen_ent[pt * kPenCap + k];
+            }
         }
         cp_async_wait_one();                              // this thread's copies of tile t landed
         __syncthreads();                                  // everyone's, and the penalty index
         auto visit = [&](int e, float raw) {
             float v = raw;
-            if (src.is_x && src.pen && ((s.bm[(e - e0) >> 5] >> ((e - e0) & 31)) & 1u))
+            if (src.is_x && src.pen && ((s.bm[(e - p0) >> 5] >> ((e - p0) & 31)) & 1u))
                 v = penalise(raw, full_pen_count(s, src, e, nh, n, over), src.f, src.p);
             fn(e, v, raw);
         };
@@ -455,6 +458,7 @@ __device__ uint32_t full_nucleus_radix(FullSmem& s, const RowSource& src, uint32
 // wfn(v) is the weight (<= 1), bfn(v) the bucket, z_est an estimate of the total weight in
 // wfn's units (0 when unknown: no element is summed-only).
 constexpr int kNucBuckets = 2048;
+static_assert(kTileBf16 % 2 == 0 && kTileF32 % 2 == 0, "whole-row chunks are half tiles");
 constexpr int kNucGather = 2048;
 
 template <typename WFn, typename BFn>

@@ -55,7 +55,7 @@ __device__ __forceinline__ bool wait_phase_or_err(uint64_t* bar, unsigned parity
     return true;
 }
 constexpr float kL2E = 1.4426950408889634f;
-constexpr int kVecPerThread = kStageBytes / 16 / kGroupThreads;     // 10 vectors per thread and tile
+constexpr int kVecPerThread = kStageBytes / 16 / kGroupThreads;     // 12 vectors per thread and tile
 static_assert(kVecPerThread % 2 == 0, "vectors are scanned in pairs");
 
 struct StageMeta {
