@@ -339,6 +339,21 @@ __device__ __forceinline__ int nth_set_bit(unsigned b, int r) {
     return pos;
 }
 
+// Item t of the warp's flagged vectors in slot order, dealt by slot-wise ballots (-1 past
+// the end).  Out of line: it only runs when a warp flags more vectors than its list holds,
+// and keeping it out of the flush keeps the hot loop small in the instruction cache.
+__device__ __noinline__ int deal_by_ballots(unsigned vflags, int t, int wv) {
+    int run = 0, v = -1;
+    for (int i = 0; i < kVecPerThread; ++i) {
+        const unsigned b = __ballot_sync(0xffffffffu, (vflags >> i) & 1u);
+        const int n = __popc(b);
+        const int r = t - run;
+        if (r >= 0 && r < n) v = wv + nth_set_bit(b, r) + i * kGroupThreads;
+        run += n;
+    }
+    return v;
+}
+
 // Candidate extraction from the vectors the threads flagged during a scan (bit i of
 // `vflags`: the thread's i-th vector of the tile has an element at or above the lower
 // threshold).  The warp's flagged vectors are dealt out to its lanes 32 at a time, so a lane
@@ -379,16 +394,7 @@ __device__ __forceinline__ void flush_vectors(GroupSmem& gs, Cand* lr, Cand* lp,
         if (listed) {
             if (t < total) { const unsigned it = list[t]; v = wv + static_cast<int>(it & 31u) + static_cast<int>(it >> 5) * kGroupThreads; }
         } else {
-            // more flags than the list holds: deal them out by slot-wise ballots
-            int run = 0;
-#pragma unroll
-            for (int i = 0; i < kVecPerThread; ++i) {
-                const unsigned b = __ballot_sync(0xffffffffu, (vflags >> i) & 1u);
-                const int n = __popc(b);
-                const int r = t - run;
-                if (r >= 0 && r < n) v = wv + nth_set_bit(b, r) + i * kGroupThreads;
-                run += n;
-            }
+            v = deal_by_ballots(vflags, t, wv);           // more flags than the list holds
         }
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
         unsigned mr = 0u, mp = 0u;
