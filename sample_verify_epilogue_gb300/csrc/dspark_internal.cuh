@@ -30,7 +30,7 @@ constexpr int kTileBf16 = kStageBytes / 2;                     // 24576 elements
 constexpr int kTileF32 = kStageBytes / 4;                      // 12288 elements
 constexpr int kBitmapWordsMax = kTileBf16 / 32;                // 768
 constexpr int kPenCap = 256;                                   // penalised tokens per tile held in smem
-constexpr int kSegTiles = 6;                                   // vocab tiles per segment (target)
+constexpr int kSegTiles = 4;                                   // vocab tiles per segment
 constexpr int kMaxSegTiles = 16;
 constexpr int kCandPenGlobal = 1536;                           // per-segment candidates kept in the workspace
 constexpr int kCandRawGlobal = 1024;
