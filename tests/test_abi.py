@@ -70,3 +70,17 @@ def test_invalid_arguments_rejected_before_any_cuda_call(lib):
     code = lib.dspark_verify_sample(ctypes.c_void_p(256), None, d, None, ctypes.byref(p), ctypes.c_void_p(1024),
                                     ctypes.c_void_p(2048), ctypes.c_void_p(4096), None, None, None)
     assert code == 3                       # no workspace
+
+
+def test_static_scratch_limits(lib):
+    """dspark_verify_sample_static: shapes whose workspace exceeds the fixed 16 MiB scratch are
+    refused with DSPARK_ERR_UNSUPPORTED before any CUDA call; the documented shapes fit."""
+    from sample_verify_epilogue_gb300 import binding as bd
+    cap = bd.DSPARK_STATIC_WORKSPACE_BYTES
+    assert cap == 16 << 20
+    for shape in [(16, 8, 151936), (12, 8, 262144), (4, 4, 32000), (1, 2, 4096)]:
+        assert 0 < bd.dspark_workspace_bytes(*shape, "bf16", 20) <= cap, shape
+    assert bd.dspark_workspace_bytes(64, 8, 262144, "bf16", 20) > cap
+    p = bd.make_params(64, 8, 262144, "bf16", n_top_logprobs=20)
+    d = ctypes.c_void_p(256)
+    assert lib.dspark_verify_sample_static(d, d, d, None, ctypes.byref(p), d, d, d, None, None, None) == 2
