@@ -162,6 +162,15 @@ def dist_env():
     return ws, rank, local
 
 
+def workload_config(ws):
+    """The `config` object of both arms' JSON lines: the bench workload and its settings."""
+    return {"workload": WORKLOAD, "B": 64, "K": 8, "V": 262144,
+            "logits": "bf16", "q": "fp32", "T": 1.0, "top_k": 64, "top_p": 0.95,
+            "penalties": "presence 0.2 / frequency 0.2, 4096-token Zipf histories",
+            "top_logprobs": 20, "l2": "inputs (839 MB) larger than L2, no flush",
+            "parallelism": f"{ws} independent replica(s), no collective"}
+
+
 def time_oracle(batch, requests):
     from oracle import epilogue as O
     t = time.perf_counter()
@@ -191,10 +200,10 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": "one request (9 verify rows) per step", "B": 64, "K": 8,
-                   "V": 262144},
+        "config": workload_config(args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "one request of the workload per step, float64 numpy oracle"},
+                         "sample": "one request (9 verify rows) of the workload per step, float64 numpy oracle, "
+                                   "single thread"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out))
@@ -331,11 +340,7 @@ def run_native(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "B": batch.B, "K": batch.K_max, "V": batch.V,
-                       "logits": "bf16", "q": "fp32", "T": 1.0, "top_k": 64, "top_p": 0.95,
-                       "penalties": "presence 0.2 / frequency 0.2, 4096-token Zipf histories",
-                       "top_logprobs": 20, "l2": "inputs (839 MB) larger than L2, no flush",
-                       "parallelism": f"{ws} independent replica(s), no collective"},
+            "config": workload_config(ws),
             "sampled_tokens_per_s": accepted * args.steps * ws / (elapsed_ms / 1e3),
             "hbm_gbs_per_call": algo_bytes * args.steps * ws / (elapsed_ms / 1e3) / 1e9 / ws,
             "algorithmic_bytes_per_step": algo_bytes,
