@@ -196,10 +196,12 @@ __device__ int nucleus(FinSmem& s, int cnt, float top_p, double* zkept) {
 // ============================================================================ whole-row path
 // Whole-row path: rows whose top-k threshold or nucleus cannot come from candidates
 // (top_k = 0 with top_p < 1, top_k above the candidate limit, tie-heavy rows that overflow
-// the candidate buffers) get an exact whole-row selection here: radix passes over the
-// order-preserving key with count histograms (top-k, top-n) and with fixed-point mass
-// histograms (nucleus), re-reading the row once per pass.  Fixed-point masses make the
-// sums independent of the order of the atomic additions.
+// the candidate buffers) get an exact whole-row selection here, re-reading the row once per
+// pass: radix passes over the order-preserving key with count histograms (top-k, top-n);
+// for the nucleus a fixed-point mass histogram over weight buckets, the boundary bucket and
+// an exact settlement among its elements (full_nucleus), with radix passes over mass
+// histograms as its fallback.  Fixed-point masses make the sums independent of the order of
+// the atomic additions.
 
 constexpr double kFix = 274877906944.0;         // 2^38
 
