@@ -171,6 +171,17 @@ def workload_config(ws):
             "parallelism": f"{ws} independent replica(s), no collective"}
 
 
+def whole_job_rate(dist, local_ms, units_per_rank_step, steps, ws, device=None):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time
+    (max over ranks).  Returns (rate per second, that time in ms)."""
+    if dist is not None:
+        import torch
+        t = torch.tensor([float(local_ms)], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        local_ms = float(t.item())
+    return units_per_rank_step * steps * ws / (local_ms / 1e3), local_ms
+
+
 def time_oracle(batch, requests):
     from oracle import epilogue as O
     t = time.perf_counter()
@@ -269,14 +280,9 @@ def run_native(args):
     elapsed_ms = t_start.elapsed_time(t_end)
     kern_ms = statistics.mean(stage_ev.ms(i) for i in range(args.steps))
     stage_ev.close()
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-
     rows_per_step = batch.verify_rows()
     algo_bytes = batch.algorithmic_bytes()
-    value = rows_per_step * args.steps * ws / (elapsed_ms / 1e3)
+    value, elapsed_ms = whole_job_rate(dist, elapsed_ms, rows_per_step, args.steps, ws, device)
     peak, peak_kind = peaks()
     achieved = algo_bytes / (kern_ms / 1e3) / 1e9
     traffic = measured_traffic()
