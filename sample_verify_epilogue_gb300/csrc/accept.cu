@@ -11,10 +11,11 @@
 // the smallest id whose cumulative mass exceeds u * total.  Whole-vocabulary supports are
 // left to finish_kernel.
 //
-// finish_kernel: one CTA per request.  Whole-row inverse-CDF draws (two passes over the
-// row in fixed-size chunks, fixed summation order so both passes agree bit for bit), then
-// the logprob outputs: raw log-softmax at each emitted token and the top-n list (mlx-dspark
-// Changelog, [0.2.0] Added, logprobs / top_logprobs).
+// finish_kernel: one CTA per request.  Whole-row inverse-CDF draws (every thread sums the
+// weights of a contiguous range of ids, a block scan of those sums finds the range holding
+// the draw, and its thread walks it), then the logprob outputs: raw log-softmax at each
+// emitted token and the top-n list (mlx-dspark Changelog, [0.2.0] Added, logprobs /
+// top_logprobs).
 #include "block_utils.cuh"
 
 namespace dspark {
