@@ -45,7 +45,10 @@
  *     reported per request in row_status (after the stream is synchronised); kernels never
  *     trap.  A request with a non-zero status gets accept_len = -1 and all tokens -1.
  *   - Calls that share a workspace must not overlap on the GPU.
- *   - Thread-safe: no global mutable state.
+ *   - dspark_verify_sample and dspark_verify_sample_host keep no global mutable state and may
+ *     be called from several host threads at once (each with its own workspace).
+ *     dspark_verify_sample_static is the exception: every call on a device shares one
+ *     scratch array (see its comment).
  */
 #ifndef DSPARK_H
 #define DSPARK_H
@@ -162,20 +165,25 @@ dspark_status_t dspark_verify_sample_host(const void* logits, const float* q, co
 #define DSPARK_STATIC_WORKSPACE_BYTES (16u << 20)
 
 /*
- * dspark_verify_sample with no workspace argument and no allocation: the scratch is a
- * file-scope device array of DSPARK_STATIC_WORKSPACE_BYTES (16 MiB) per device, so the call
- * makes no cudaMalloc / cudaFree or other allocating call and can be captured in a CUDA
- * graph.  This entry point has no counterpart in the mlx-dspark pages: it exists for callers
- * that must not allocate (graph capture, allocator-free serving loops).
- *   - Arguments, layouts and results are those of dspark_verify_sample;
- *     params->workspace and params->workspace_bytes are ignored.
+ * dspark_verify_sample with no workspace argument, for callers that cannot call cudaMalloc:
+ * for instance a serving loop that reserved all device memory up front and hands out no
+ * allocator, or a plugin inside a host framework that owns the device memory and does not
+ * expose its allocator.  The scratch is a file-scope device array of
+ * DSPARK_STATIC_WORKSPACE_BYTES (16 MiB), which every device that loads the library holds
+ * until the process exits; the call makes no cudaMalloc / cudaFree or other allocating call.
+ * This entry point has no counterpart in the mlx-dspark pages.
+ *   - Arguments, layouts and results are those of dspark_verify_sample; the caller still
+ *     passes inputs and outputs.  params->workspace and params->workspace_bytes are ignored.
  *   - Shapes whose dspark_workspace_bytes exceeds DSPARK_STATIC_WORKSPACE_BYTES are rejected
  *     with DSPARK_ERR_UNSUPPORTED before any CUDA call.
- *   - The first call on a device looks the array's address up (cudaGetSymbolAddress, with
- *     that device current) and caches it; make that first call before any stream capture.
- *     A failed lookup returns DSPARK_ERR_CUDA.
+ *   - Set-up: the first call on a device looks the array's address up (cudaGetSymbolAddress,
+ *     with that device current) and caches it for that device; make that first call before
+ *     any stream capture.  A failed lookup returns DSPARK_ERR_CUDA.  The cached address
+ *     belongs to the device's primary context: after cudaDeviceReset it is stale, so do not
+ *     call this entry point again in that process.
  *   - Nothing in the scratch has to start at zero: every call clears the one record it reads
- *     before writing (with cudaMemsetAsync on params->stream).
+ *     before writing (with cudaMemsetAsync on params->stream).  The array keeps the last
+ *     call's contents.
  *   - All calls on one device share the array: calls that overlap on the GPU (other streams,
  *     other host threads) race and give undefined results.  Serialise them.
  */

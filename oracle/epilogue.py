@@ -39,9 +39,23 @@ Readings taken where the pages are silent (each listed in the design notes):
   * Q'(d) = 0 with P'(d) > 0 accepts; both zero rejects; an all-zero residual draws
     from P';
   * logprobs are the raw (unpenalised, untempered, untruncated) log-softmax.
-Every discrete decision that floating point takes (nucleus boundary, accept test,
-inverse-CDF boundary, empty residual) records its margin; a request whose smallest
-margin is below ``MARGIN_EPS`` is "fragile" and is exempt from bit-exact comparison.
+
+Near ties.  Every discrete decision that floating point takes records a ``Decision``: its
+distance from the threshold, in the threshold's own unit, and the branch the other side
+of the threshold leads to.
+  * accept test: |u - P'/Q'| in uniform units;
+  * residual / bonus draw: the distance of u from the nearer edge of the drawn token's
+    interval [C(t-1)/C(V-1), C(t)/C(V-1)) of the normalised cumulative weights, in uniform
+    units;
+  * nucleus boundary: top_p minus the mass above the last kept tie group, and the mass
+    above the first dropped group minus top_p, in probability units (the unit top_p is
+    stated in);
+  * empty residual: the residual mass.
+A decision whose distance is below ``MARGIN_EPS`` is a near tie.  ``outcomes`` follows
+both sides of every near-tie accept test and nucleus boundary, and a near-tie draw admits
+every token whose interval reaches within ``MARGIN_EPS`` of u; a result is correct iff it
+is one of these outcomes.  Decisions taken on identical float32 values on both sides
+(penalised argmax, top-k threshold, top-n ids) have no margin.
 """
 from __future__ import annotations
 
@@ -91,46 +105,58 @@ def order_desc(values):
     return np.lexsort((np.arange(v.size), -v))
 
 
-def truncate_full_sort(values, weights, top_k, top_p):
+def _nucleus_groups(g_above, top_p, flip):
+    """Number of tie groups the nucleus keeps, and its two margins.
+
+    g_above: mass strictly above each tie group (non-decreasing).  Kept groups are those
+    with g_above < top_p, a prefix.  Margins: top_p minus the last kept group's mass above
+    (none for the top group, whose mass above is exactly 0 on any machine) and the first
+    dropped group's mass above minus top_p.  flip "drop_last" / "keep_next" takes the other
+    side of one of those two boundaries."""
+    nk = int(np.count_nonzero(g_above < top_p))
+    last = float(g_above[nk - 1])
+    m_last = float(top_p - last) if last > 0.0 else np.inf
+    m_next = float(g_above[nk] - top_p) if nk < g_above.size else np.inf
+    if flip == "drop_last" and nk > 1:
+        nk -= 1
+    elif flip == "keep_next" and nk < g_above.size:
+        nk += 1
+    return nk, (m_last, m_next)
+
+
+def truncate_full_sort(values, weights, top_k, top_p, flip=None):
     """Top-k then top-p truncation by one full sort of the vocabulary.
 
     values: the ordering key (penalised logit or draft probability); weights: the
     unnormalised probabilities, monotone non-decreasing in ``values``.
-    Returns (keep mask, nucleus margin).  mlx-dspark Changelog, [0.1.0] Added
-    (lossless top-p / top-k on draft and target)."""
+    Returns (keep mask, (margin of the last kept group, margin of the first dropped
+    group)).  mlx-dspark Changelog, [0.1.0] Added (lossless top-p / top-k on draft and
+    target)."""
     V = values.size
     order = order_desc(values)
     keep = np.ones(V, bool)
     if 0 < top_k < V:
         tau_k = values[order[top_k - 1]]
         keep = values >= tau_k
-    margin = np.inf
+    margins = (np.inf, np.inf)
     if top_p < 1.0:
         idx = order[keep[order]]                  # kept ids, value desc / id asc
         vs = values[idx]
         w = weights[idx].astype(np.float64)
         pk = w / w.sum()
         excl = np.concatenate(([0.0], np.cumsum(pk)[:-1]))
-        # mass strictly above each token's value = exclusive prefix at its tie group's start
+        # tie groups: the mass strictly above a group is the exclusive prefix at its start
         start = np.ones(vs.size, bool)
         start[1:] = vs[1:] != vs[:-1]
-        first = np.maximum.accumulate(np.where(start, np.arange(vs.size), 0))
-        above = excl[first]
-        kept_sorted = above < top_p
+        starts = np.nonzero(start)[0]
+        nk, margins = _nucleus_groups(excl[starts], top_p, flip)
+        end = starts[nk] if nk < starts.size else vs.size
         keep = np.zeros(V, bool)
-        keep[idx[kept_sorted]] = True
-        # margins: the last kept group's mass-above vs top_p, and the first dropped group's
-        g_above = above[start]
-        g_kept = g_above < top_p
-        last = float(g_above[g_kept].max())
-        # the top group's mass-above is exactly 0 on any machine: that decision has no margin
-        margin = float(top_p - last) if last > 0.0 else np.inf
-        if (~g_kept).any():
-            margin = min(margin, float(g_above[~g_kept].min() - top_p))
-    return keep, margin
+        keep[idx[:end]] = True
+    return keep, margins
 
 
-def truncate_grouped(values, weights, top_k, top_p, group=1024):
+def truncate_grouped(values, weights, top_k, top_p, group=1024, flip=None):
     """The same truncation from small per-group sorts instead of one full sort.
 
     mlx-dspark Changelog, [0.20.2] Changed: the top-k threshold and the nucleus cutoff come
@@ -138,7 +164,7 @@ def truncate_grouped(values, weights, top_k, top_p, group=1024):
     of ``group`` consecutive ids is sorted on its own; the k-th largest value of the whole
     row is the k-th largest of the merged per-group leaders (every member of the global
     top-k is within its group's top-k), and the nucleus walks a lazy merge of the sorted
-    groups' heads."""
+    groups' heads, one tie group (across all groups) at a time."""
     V = values.size
     vals = np.asarray(values)
     groups = [np.arange(s, min(s + group, V)) for s in range(0, V, group)]
@@ -153,69 +179,63 @@ def truncate_grouped(values, weights, top_k, top_p, group=1024):
         lv = np.sort(vals[leaders].astype(np.float64))[::-1]
         tau_k = lv[top_k - 1]
         keep = vals >= tau_k
-    margin = np.inf
+    margins = (np.inf, np.inf)
     if top_p < 1.0:
-        # survivors of each group, still sorted; lazy k-way merge by (value desc, id asc)
         heads = [o[vals[o] >= tau_k] for o in sorted_groups]
         Z = float(sum(weights[h].astype(np.float64).sum() for h in heads))
         pos = [0] * len(heads)
-        keep = np.zeros(V, bool)
+        ties, above = [], []            # tie groups in merge order, mass strictly above each
         mass_above = 0.0
-        last_kept = None
-        dropped_first = None
         while True:
             best = None
-            for gi, h in enumerate(heads):
-                if pos[gi] < h.size:
-                    t = h[pos[gi]]
+            for h, p0 in zip(heads, pos):
+                if p0 < h.size:
+                    t = h[p0]
                     if best is None or (vals[t] > vals[best]) or (vals[t] == vals[best] and t < best):
                         best = t
-                        bg = gi
             if best is None:
                 break
             v = vals[best]
-            # take the whole tie group with value v across all groups
             grp = []
             for gi, h in enumerate(heads):
                 while pos[gi] < h.size and vals[h[pos[gi]]] == v:
                     grp.append(h[pos[gi]])
                     pos[gi] += 1
-            if mass_above < top_p:
-                keep[np.array(grp)] = True
-                last_kept = mass_above
-                mass_above += float(weights[np.array(grp)].astype(np.float64).sum()) / Z
-            else:
-                dropped_first = mass_above
+            ties.append(np.array(grp))
+            above.append(mass_above)
+            if mass_above >= top_p:     # first dropped group found: nothing later can be kept
                 break
-        margin = float(top_p - last_kept) if last_kept > 0.0 else np.inf
-        if dropped_first is not None:
-            margin = min(margin, float(dropped_first - top_p))
-    return keep, margin
+            mass_above += float(weights[np.array(grp)].astype(np.float64).sum()) / Z
+        nk, margins = _nucleus_groups(np.array(above), top_p, flip)
+        keep = np.zeros(V, bool)
+        for grp in ties[:nk]:
+            keep[grp] = True
+    return keep, margins
 
 
 # ----------------------------------------------------------------------------- distributions
-def target_probs(xp32, T, top_k, top_p, truncate=truncate_full_sort):
+def target_probs(xp32, T, top_k, top_p, truncate=truncate_full_sort, flip=None):
     """P' = truncate(softmax(x'/T)) renormalised.  v0.0.2 release notes, Highlights
     (temperature sampling); Changelog [0.1.0] Added (top-p / top-k on the target)."""
     s = np.asarray(xp32, np.float64)
     w = np.exp((s - s.max()) / float(T))
-    keep, margin = truncate(np.asarray(xp32, np.float32), w, top_k, top_p)
+    keep, margins = truncate(np.asarray(xp32, np.float32), w, top_k, top_p, flip=flip)
     P = np.where(keep, w, 0.0)
-    return P / P.sum(), margin
+    return P / P.sum(), margins
 
 
-def draft_probs(q32, T, top_k, top_p, truncate=truncate_full_sort):
+def draft_probs(q32, T, top_k, top_p, truncate=truncate_full_sort, flip=None):
     """Q' = truncate(q^(1/T)) renormalised: the draft input holds T=1 probabilities and the
     request's temperature and truncation apply to it as to the target (Changelog [0.1.0]
     Added: truncation applied to both draft and target)."""
     q = np.asarray(q32, np.float64)
     w = q ** (1.0 / float(T))
-    keep, margin = truncate(np.asarray(q32, np.float32), w, top_k, top_p)
+    keep, margins = truncate(np.asarray(q32, np.float32), w, top_k, top_p, flip=flip)
     Q = np.where(keep, w, 0.0)
     Z = Q.sum()
     if not Z > 0:
-        return None, margin
-    return Q / Z, margin
+        return None, margins
+    return Q / Z, margins
 
 
 # ----------------------------------------------------------------------------- accept / draw
@@ -227,7 +247,7 @@ def accept_probability(p, q):
 
 
 def accept_test(p, q, u):
-    """The accept decision for one draft with uniform u, and its margin."""
+    """The accept decision for one draft with uniform u, and its margin |u - p/q|."""
     if q == 0.0:
         return p > 0.0, np.inf
     ratio = p / q
@@ -242,8 +262,8 @@ def residual(P, Q):
 def inverse_cdf(w, u):
     """Smallest id t with sum_{s<=t} w_s > u * sum(w) (ascending ids); returns (t, margin).
 
-    The margin is the distance, in mass units, from u*sum(w) to the nearer edge of t's
-    cumulative interval."""
+    The margin is the distance of u from the nearer edge of t's interval
+    [C(t-1)/total, C(t)/total), in uniform units."""
     C = np.cumsum(np.asarray(w, np.float64))
     total = C[-1]
     target = float(u) * total
@@ -253,7 +273,18 @@ def inverse_cdf(w, u):
         return t, 0.0
     t = int(hits[0])
     lo = C[t - 1] if t > 0 else 0.0
-    return t, float(min(target - lo, C[t] - target))
+    return t, float(min(target - lo, C[t] - target) / total)
+
+
+def draw_admissible(w, u, eps=MARGIN_EPS):
+    """Every id t with w_t > 0 whose interval [C(t-1)/total, C(t)/total) reaches within eps
+    of u: the tokens an inverse-CDF draw may return when u is moved by at most eps."""
+    w = np.asarray(w, np.float64)
+    C = np.cumsum(w)
+    total = C[-1]
+    lo = np.concatenate(([0.0], C[:-1])) / total
+    hi = C / total
+    return np.nonzero((w > 0) & (lo < float(u) + eps) & (hi > float(u) - eps))[0].astype(np.int64)
 
 
 # ----------------------------------------------------------------------------- logprobs
@@ -272,6 +303,21 @@ def top_n(x32, n):
 
 # ----------------------------------------------------------------------------- one request
 @dataclass
+class Decision:
+    """One floating-point decision of a request: the test, its position, the distance of its
+    operand from the threshold (in the threshold's unit) and the flip that takes the other
+    side ("" for a draw, whose other sides are listed as admissible tokens)."""
+    kind: str            # "nucleus_p", "nucleus_q", "accept", "residual_mass", "draw"
+    pos: int
+    margin: float
+    alt: str = ""
+
+    @property
+    def fragile(self):
+        return self.margin < MARGIN_EPS
+
+
+@dataclass
 class RequestResult:
     accept_len: int
     tokens: np.ndarray            # int32 [K_max+1], -1 past the emitted token
@@ -279,12 +325,22 @@ class RequestResult:
     top_ids: np.ndarray           # int32 [K_max+1, n]
     top_logprobs: np.ndarray      # float64 [K_max+1, n]
     status: int = ROW_OK
-    min_margin: float = np.inf
-    margins: list = field(default_factory=list)
+    decisions: list = field(default_factory=list)
+    admissible: np.ndarray = None        # ids the emitted token may be (the drawn id first)
+    admissible_logprobs: np.ndarray = None
+    flips: dict = field(default_factory=dict)
+
+    @property
+    def min_margin(self):
+        return min((d.margin for d in self.decisions), default=np.inf)
 
     @property
     def fragile(self):
-        return self.min_margin < MARGIN_EPS
+        return any(d.fragile for d in self.decisions)
+
+    def near_ties(self):
+        """Kinds of the near-tie decisions of this outcome."""
+        return [d.kind for d in self.decisions if d.fragile]
 
 
 def _validate(batch, b):
@@ -304,8 +360,12 @@ def _validate(batch, b):
     return st
 
 
-def verify_request(batch, b, truncate=truncate_full_sort) -> RequestResult:
-    """The whole epilogue for request b of a ``workloads`` batch."""
+def verify_request(batch, b, truncate=truncate_full_sort, flips=None) -> RequestResult:
+    """The whole epilogue for request b of a ``workloads`` batch.
+
+    flips: {(kind, position): alternative} takes the other side of those near-tie decisions
+    (used by ``outcomes``); None follows every decision as float64 takes it."""
+    flips = dict(flips or {})
     V, Km = batch.V, batch.K_max
     n = batch.n_top_logprobs
     tokens = np.full(Km + 1, -1, np.int32)
@@ -314,7 +374,7 @@ def verify_request(batch, b, truncate=truncate_full_sort) -> RequestResult:
     tlp = np.full((Km + 1, n), -np.inf)
     st = _validate(batch, b)
     if st != ROW_OK:
-        return RequestResult(-1, tokens, lps, tids, tlp, status=st)
+        return RequestResult(-1, tokens, lps, tids, tlp, status=st, flips=flips)
     r = batch.rows[b]
     T, k, p = float(r["temperature"]), int(r["top_k"]), float(r["top_p"])
     pres, freq, K = r["presence_penalty"], r["frequency_penalty"], int(r["num_drafts"])
@@ -324,17 +384,32 @@ def verify_request(batch, b, truncate=truncate_full_sort) -> RequestResult:
     hid, hc = batch.history(b)
     for j in range(K + 1):
         if not np.all(np.isfinite(x[j])):
-            return RequestResult(-1, tokens, lps, tids, tlp, status=ROW_NONFINITE)
+            return RequestResult(-1, tokens, lps, tids, tlp, status=ROW_NONFINITE, flips=flips)
     if T > 0:
         for i in range(K):
             qi = batch.q[b, i]
             if not (np.all(np.isfinite(qi)) and qi.min() >= 0.0):
-                return RequestResult(-1, tokens, lps, tids, tlp, status=ROW_NONFINITE)
+                return RequestResult(-1, tokens, lps, tids, tlp, status=ROW_NONFINITE, flips=flips)
 
     def xp(j):
         return penalised_logits(x[j], count_vector(V, hid, hc, d[:j]), pres, freq)
 
-    margins = []
+    decisions = []
+    cache = {}
+
+    def dist(kind, j):
+        """P'_j or Q'_j (memoised), recording its nucleus decisions once."""
+        if (kind, j) not in cache:
+            fl = flips.get((kind, j))
+            if kind == "nucleus_p":
+                D, (m_last, m_next) = target_probs(xp(j), T, k, p, truncate, flip=fl)
+            else:
+                D, (m_last, m_next) = draft_probs(batch.q[b, j], T, k, p, truncate, flip=fl)
+            decisions.append(Decision(kind, j, m_last, "drop_last"))
+            decisions.append(Decision(kind, j, m_next, "keep_next"))
+            cache[(kind, j)] = D
+        return cache[(kind, j)]
+
     if T == 0.0:
         # greedy: accept while the draft equals the penalised argmax (lowest id on ties)
         a = K
@@ -343,48 +418,93 @@ def verify_request(batch, b, truncate=truncate_full_sort) -> RequestResult:
                 a = i
                 break
         tok = int(np.argmax(xp(a)))
+        adm = np.array([tok], np.int64)
     else:
         a = K
         for i in range(K):
-            P, mp = target_probs(xp(i), T, k, p, truncate)
-            Q, mq = draft_probs(batch.q[b, i], T, k, p, truncate)
+            P = dist("nucleus_p", i)
+            Q = dist("nucleus_q", i)
             if Q is None:
-                return RequestResult(-1, tokens, lps, tids, tlp, status=ROW_NONFINITE)
-            margins += [("nucleus_p", i, mp), ("nucleus_q", i, mq)]
+                return RequestResult(-1, tokens, lps, tids, tlp, status=ROW_NONFINITE, flips=flips)
             acc, m = accept_test(P[d[i]], Q[d[i]], u[i, 0])
-            margins.append(("accept", i, m))
+            decisions.append(Decision("accept", i, m, "flip"))
+            if flips.get(("accept", i)) == "flip":
+                acc = not acc
             if not acc:
                 a = i
                 break
-        P, mp = target_probs(xp(a), T, k, p, truncate)
-        margins.append(("nucleus_p", a, mp))
+        P = dist("nucleus_p", a)
+        w = P
+        tiny_residual = False
         if a < K:
-            Q, mq = draft_probs(batch.q[b, a], T, k, p, truncate)
-            margins.append(("nucleus_q", a, mq))
+            Q = dist("nucleus_q", a)
             w = residual(P, Q)
             tot = w.sum()
-            margins.append(("residual_mass", a, float(tot)))
+            decisions.append(Decision("residual_mass", a, float(tot)))
+            # a near-empty residual: float32 rounding of P - Q may leave any id of P' standing
+            tiny_residual = tot < MARGIN_EPS
             if not tot > 0.0:
                 w = P
-        else:
-            w = P
         tok, m = inverse_cdf(w, u[a, 1])
-        margins.append(("draw", a, m))
+        decisions.append(Decision("draw", a, m))
+        adm = draw_admissible(w, u[a, 1])
+        if tiny_residual:
+            adm = np.union1d(adm, np.nonzero(P > 0)[0])
+        adm = np.concatenate(([tok], adm[adm != tok])).astype(np.int64)
     tokens[:a] = d[:a]
     tokens[a] = tok
+    adm_lp = None
     if batch.want_logprobs or n > 0:
         for j in range(a + 1):
             ls = raw_log_softmax(x[j])
             lps[j] = ls[tokens[j]]
+            if j == a:
+                adm_lp = ls[adm]
             if n > 0:
                 ids = top_n(x[j], n)
                 tids[j] = ids
                 tlp[j] = ls[ids]
-    mm = min([m for (_, _, m) in margins], default=np.inf)
-    return RequestResult(a, tokens, lps, tids, tlp, status=ROW_OK, min_margin=mm, margins=margins)
+    return RequestResult(a, tokens, lps, tids, tlp, status=ROW_OK, decisions=decisions, admissible=adm,
+                         admissible_logprobs=adm_lp, flips=flips)
+
+
+def outcomes(batch, b, truncate=truncate_full_sort, max_outcomes=16):
+    """Every outcome request b may correctly have: the float64 one first, then, for each
+    near-tie accept test or nucleus boundary, the outcome with that decision taken the other
+    way (recursively, up to ``max_outcomes``).  Near-tie draws need no branch: each
+    outcome lists its admissible emitted tokens."""
+    base = verify_request(batch, b, truncate)
+    found = [base]
+    if base.status != ROW_OK:
+        return found
+    seen = {frozenset()}
+    stack = [base]
+    while stack and len(found) < max_outcomes:
+        res = stack.pop()
+        for dcs in res.decisions:
+            if not dcs.fragile or not dcs.alt or (dcs.kind, dcs.pos) in res.flips:
+                continue
+            nf = dict(res.flips)
+            nf[(dcs.kind, dcs.pos)] = dcs.alt
+            key = frozenset(nf.items())
+            if key in seen:
+                continue
+            seen.add(key)
+            alt = verify_request(batch, b, truncate, flips=nf)
+            found.append(alt)
+            stack.append(alt)
+            if len(found) >= max_outcomes:
+                break
+    return found
 
 
 def verify_batch(batch, requests=None, truncate=truncate_full_sort):
     """Run ``verify_request`` over the given requests (default: all)."""
     reqs = range(batch.B) if requests is None else requests
     return {b: verify_request(batch, b, truncate) for b in reqs}
+
+
+def outcomes_batch(batch, requests=None, truncate=truncate_full_sort):
+    """``outcomes`` over the given requests (default: all)."""
+    reqs = range(batch.B) if requests is None else requests
+    return {b: outcomes(batch, b, truncate) for b in reqs}

@@ -317,6 +317,7 @@ __device__ int whole_row_draw(FinishSmem& s, DrawCtx& c, float u) {
         if (mine > 0.0 && ex + mine > target) atomicMin(&s.found_chunk, tid);
         __syncthreads();
         int owner = s.found_chunk;
+        __syncthreads();                                // every thread has read it before it changes
         if (owner == nt) {                              // rounding: the last range with mass
             if (tid == 0) {
                 int last = -1;
@@ -331,6 +332,7 @@ __device__ int whole_row_draw(FinishSmem& s, DrawCtx& c, float u) {
         // otherwise in rounds), scanned in double in id order
         const double before = s.th_ex[owner];
         const int o0 = min(a.V, owner * span), o1 = min(a.V, o0 + span);
+        __syncthreads();                                // found_chunk and th_ex[owner] read by all
         if (tid == 0) { s.found_chunk = a.V; s.tok = -1; }
         double run = before;
         for (int base = o0; base < o1; base += nt) {

@@ -254,7 +254,10 @@ dspark_status_t dspark_verify_sample_host(const void* logits, const float* q, co
         ok = ok && h2d(h.hcnt, counts->counts, static_cast<size_t>(nnz) * 4);
     }
     ok = ok && h2d(h.u, uniforms, B * W * 2 * 4);
-    if (!ok) return DSPARK_ERR_CUDA;
+    // on any failure after the first copy was enqueued, wait for the stream before returning:
+    // the caller may reuse its host buffers as soon as the call returns
+    auto fail = [&](dspark_status_t e) { cudaStreamSynchronize(s); return e; };
+    if (!ok) return fail(DSPARK_ERR_CUDA);
     dspark_counts_t dc{reinterpret_cast<const int32_t*>(ws + h.hoff), reinterpret_cast<const int32_t*>(ws + h.hids),
                        reinterpret_cast<const int32_t*>(ws + h.hcnt)};
     dspark_params_t dp = *params;
@@ -267,12 +270,12 @@ dspark_status_t dspark_verify_sample_host(const void* logits, const float* q, co
                              reinterpret_cast<int32_t*>(ws + h.tok), out_logprobs ? reinterpret_cast<float*>(ws + h.lp) : nullptr,
                              n ? reinterpret_cast<int32_t*>(ws + h.tid) : nullptr,
                              n ? reinterpret_cast<float*>(ws + h.tlp) : nullptr);
-    if (st != DSPARK_OK) return st;
+    if (st != DSPARK_OK) return fail(st);
     ok = d2h(out_accept_len, h.acc, B * 4) && d2h(out_tokens, h.tok, B * W * 4) && d2h(params->row_status, h.st, B * 4);
     if (out_logprobs) ok = ok && d2h(out_logprobs, h.lp, B * W * 4);
     if (n && out_top_ids) ok = ok && d2h(out_top_ids, h.tid, B * W * n * 4);
     if (n && out_top_logprobs) ok = ok && d2h(out_top_logprobs, h.tlp, B * W * n * 4);
-    if (!ok) return DSPARK_ERR_CUDA;
+    if (!ok) return fail(DSPARK_ERR_CUDA);
     if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }

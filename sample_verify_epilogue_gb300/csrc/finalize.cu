@@ -896,6 +896,7 @@ __device__ void finalize_row(const Args& a, FinSmem& s, int slot) {
 // The rows the warp finalize left (fin_list), each by a whole block.
 __global__ void __launch_bounds__(kFinThreads, 2) row_finalize_kernel(Args a) {
     pdl_enter();
+    if (a.plan->pad[0]) return;                           // streaming statistics incomplete
     extern __shared__ __align__(16) unsigned char fin_raw[];
     FinSmem& s = *reinterpret_cast<FinSmem*>(fin_raw);
     const int n = a.fin_list[0];

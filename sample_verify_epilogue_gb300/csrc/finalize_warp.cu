@@ -443,6 +443,9 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock) row_finalize_warp_kernel(Args a) {
     pdl_enter();
+    // a bounded wait of the streaming pass gave up: its statistics are incomplete and every
+    // request reports DSPARK_ROW_INTERNAL, so nothing here may read them
+    if (a.plan->pad[0]) return;
     extern __shared__ __align__(16) unsigned char wfin_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     WarpSmem& w = reinterpret_cast<WarpSmem*>(wfin_raw)[warp];

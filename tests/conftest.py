@@ -8,3 +8,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Per-batch parity counts (requests compared, near-tie decisions by kind)."""
+    from tests._compare import REPORT
+    if REPORT:
+        terminalreporter.section("parity with the oracle")
+        for ln in REPORT:
+            terminalreporter.write_line(ln)

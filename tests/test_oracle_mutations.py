@@ -19,9 +19,15 @@ MUTATIONS = {
     "cdf_non_strict": ("hits = np.nonzero(C > target)[0]", "hits = np.nonzero(C >= target)[0]"),
     "topk_off_by_one": ("tau_k = values[order[top_k - 1]]", "tau_k = values[order[top_k]]"),
     "draft_temperature_missing": ("w = q ** (1.0 / float(T))", "w = q"),
-    "bonus_wrong_position": ("        P, mp = target_probs(xp(a), T, k, p, truncate)\n",
-                             "        P, mp = target_probs(xp(max(a - 1, 0)), T, k, p, truncate)\n"),
+    "bonus_wrong_position": ("        P = dist(\"nucleus_p\", a)\n",
+                             "        P = dist(\"nucleus_p\", max(a - 1, 0))\n"),
     "logprob_penalised": ("            ls = raw_log_softmax(x[j])", "            ls = raw_log_softmax(xp(j))"),
+    "draw_margin_in_mass_units": ("return t, float(min(target - lo, C[t] - target) / total)",
+                                  "return t, float(min(target - lo, C[t] - target))"),
+    "admissible_without_slack": ("(lo < float(u) + eps) & (hi > float(u) - eps)", "(lo <= float(u)) & (hi > float(u))"),
+    "accept_flip_ignored": ("                acc = not acc\n", "                acc = acc\n"),
+    "nucleus_flip_ignored": ("    if flip == \"drop_last\" and nk > 1:\n        nk -= 1\n",
+                             "    if flip == \"drop_last\" and nk > 1:\n        nk -= 0\n"),
 }
 
 

@@ -119,9 +119,9 @@ def test_nucleus_hand_examples():
         w = np.array([float(v) for v in probs.split()])
         want = sorted(int(v) for v in kept.split())
         for trunc in (O.truncate_full_sort, lambda v, ww, kk, pp: O.truncate_grouped(v, ww, kk, pp, group=2)):
-            keep, margin = trunc(w.astype(np.float32), w, int(k), float(p))
+            keep, margins = trunc(w.astype(np.float32), w, int(k), float(p))
             assert sorted(np.nonzero(keep)[0].tolist()) == want, name
-            assert margin > 1e-6, name
+            assert min(margins) > 1e-6, name
 
 
 def _trunc_cases(rng):
@@ -145,7 +145,8 @@ def test_grouped_select_equals_full_sort(seed):
                     a, ma = O.truncate_full_sort(vals, w, k, p)
                     b, mb = O.truncate_grouped(vals, w, k, p, group=256)
                     assert np.array_equal(a, b), (k, p)
-                    assert abs(ma - mb) < 1e-12 or (np.isinf(ma) and np.isinf(mb))
+                    for x, y in zip(ma, mb):
+                        assert abs(x - y) < 1e-12 or (np.isinf(x) and np.isinf(y))
 
 
 def test_topk_brute_force_small():
@@ -406,3 +407,105 @@ def test_workloads_smoke_oracle_small():
     assert 0 <= r.accept_len <= 2 and r.tokens[r.accept_len] >= 0
     g = O.verify_request(configs.build("b1k2v4096_greedy"), 0)
     assert 0 <= g.accept_len <= 2
+
+
+# ------------------------------------------------------------------ near-tie bookkeeping
+def test_draw_margin_in_uniform_units():
+    """A residual of total mass 0.25 (weights 0.1, 0.15): u * 0.25 lying 5e-7 of mass above
+    the first boundary is 2e-6 away in uniform units, so the draw is not a near tie and only
+    token 1 is admissible; 2e-7 of mass (8e-7 in u) is a near tie admitting tokens 0 and 1."""
+    w = np.array([0.1, 0.15])
+    u = (0.1 + 5e-7) / 0.25
+    t, m = O.inverse_cdf(w, u)
+    assert t == 1 and abs(m - 2e-6) < 1e-12
+    assert O.draw_admissible(w, u).tolist() == [1]
+    u = (0.1 + 2e-7) / 0.25
+    t, m = O.inverse_cdf(w, u)
+    assert t == 1 and abs(m - 8e-7) < 1e-12 and m < O.MARGIN_EPS
+    assert O.draw_admissible(w, u).tolist() == [0, 1]
+    # zero-weight ids are never admissible, even next to u
+    assert O.draw_admissible(np.array([0.1, 0.0, 0.15]), u).tolist() == [0, 2]
+
+
+def _residual_quarter_request(u_draw):
+    """K=1, T=1, no truncation: P = softmax(x1), Q = q; the draft is rejected (u0 > P/Q) and
+    the residual max(0, P - Q) is drawn with u_draw."""
+    x = np.log(np.array([[0.4, 0.35, 0.25], [0.2, 0.3, 0.5]], np.float64)).astype(np.float32)
+    q = np.array([[0.3, 0.25, 0.45]], np.float32)
+    P = scipy.special.softmax(x[0].astype(np.float64))
+    Q = q[0].astype(np.float64) / q[0].astype(np.float64).sum()
+    return one_request(x, q, [2], T=1.0, uniforms=[[0.9, u_draw], [0.0, 0.0]]), P, Q
+
+
+def test_request_draw_margin_uses_uniform_units():
+    """Through verify_request: the residual max(0, P - Q) has total ~0.2; u placed 5e-7 of
+    mass above its first boundary is a draw with margin ~2.5e-6 in u, not a near tie."""
+    _, P, Q = _residual_quarter_request(0.0)
+    r = np.maximum(0.0, P - Q)
+    u = (r[0] + 5e-7) / r.sum()
+    b, _, _ = _residual_quarter_request(u)
+    res = O.verify_request(b, 0)
+    assert res.accept_len == 0 and res.tokens[0] == 1
+    draw = [d for d in res.decisions if d.kind == "draw"][0]
+    assert abs(draw.margin - 5e-7 / r.sum()) < 1e-7          # u is rounded to float32
+    assert not draw.fragile and res.admissible.tolist() == [1]
+
+
+def test_nucleus_margins_and_flips_hand_example():
+    """Weights 0.5, 0.3, 0.2: the mass above the smallest group is 0.8.  top_p = 0.8 + 3e-7
+    keeps it with a last-kept margin of 3e-7 (its flip drops it); top_p = 0.8 - 3e-7 drops it
+    with a first-dropped margin of 3e-7 (its flip keeps it)."""
+    w = np.array([0.5, 0.3, 0.2])
+    v = w.astype(np.float32)
+    for trunc in (O.truncate_full_sort, lambda *a, **k: O.truncate_grouped(*a, group=2, **k)):
+        keep, (m_last, m_next) = trunc(v, w, 0, 0.8 + 3e-7)
+        assert keep.tolist() == [True, True, True]
+        assert abs(m_last - 3e-7) < 1e-12 and np.isinf(m_next)
+        keep, _ = trunc(v, w, 0, 0.8 + 3e-7, flip="drop_last")
+        assert keep.tolist() == [True, True, False]
+        keep, (m_last, m_next) = trunc(v, w, 0, 0.8 - 3e-7)
+        assert keep.tolist() == [True, True, False]
+        assert abs(m_next - 3e-7) < 1e-12 and abs(m_last - (0.3 - 3e-7)) < 1e-12
+        keep, _ = trunc(v, w, 0, 0.8 - 3e-7, flip="keep_next")
+        assert keep.tolist() == [True, True, True]
+
+
+def test_accept_near_tie_has_both_outcomes():
+    """u within 4e-7 below P'(d)/Q'(d): float64 accepts (then the bonus draw from P'_1); the
+    other side rejects and draws from the residual at position 0.  Both outcomes, and only
+    these, are correct, each as the closed-form sequential computation gives it."""
+    x = np.log(np.array([[0.4, 0.35, 0.25], [0.2, 0.3, 0.5]], np.float64)).astype(np.float32)
+    q = np.array([[0.3, 0.25, 0.45]], np.float32)
+    P0 = scipy.special.softmax(x[0].astype(np.float64))
+    P1 = scipy.special.softmax(x[1].astype(np.float64))
+    Q0 = q[0].astype(np.float64) / q[0].astype(np.float64).sum()
+    ratio = P0[2] / Q0[2]
+    u_draw = 0.55
+    b = one_request(x, q, [2], T=1.0, uniforms=[[ratio - 4e-7, u_draw], [0.0, u_draw]])
+    outs = O.outcomes(b, 0)
+    assert len(outs) == 2
+    acc, rej = outs
+    assert acc.accept_len == 1 and acc.tokens[0] == 2
+    assert acc.tokens[1] == int(np.searchsorted(np.cumsum(P1), u_draw, side="right"))
+    assert rej.accept_len == 0
+    r = np.maximum(0.0, P0 - Q0)
+    assert rej.tokens[0] == int(np.searchsorted(np.cumsum(r), u_draw * r.sum(), side="right"))
+    assert [d.kind for d in acc.decisions if d.fragile] == ["accept"]
+    # far from the ratio there is one outcome
+    far = one_request(x, q, [2], T=1.0, uniforms=[[ratio - 1e-3, u_draw], [0.0, u_draw]])
+    assert len(O.outcomes(far, 0)) == 1
+
+
+def test_subset_batches_equal_the_whole_batch():
+    """A request built on its own equals the same request of the whole batch, bit for bit."""
+    full = configs.build("b4k8v151936_mixed")
+    for b in (0, 3):
+        one = configs.build("b4k8v151936_mixed", requests=[b])
+        assert one.B == 1 and one.requests == (b,)
+        assert np.array_equal(one.x[0], full.x[b]) and np.array_equal(one.q[0], full.q[b])
+        assert np.array_equal(one.draft_ids[0], full.draft_ids[b])
+        assert np.array_equal(one.uniforms[0], full.uniforms[b])
+        assert np.array_equal(one.rows[0], full.rows[b])
+        hi, hc = full.history(b)
+        oi, oc = one.history(0)
+        assert np.array_equal(hi, oi) and np.array_equal(hc, oc)

@@ -39,20 +39,32 @@ def _mixed18(B, K):
     return rows
 
 
-def build(name: str, *, B=None):
-    """Build a workload by name. ``B`` overrides the batch size (for bounded samples)."""
+DEFAULT_B = {"b1k2v4096": 1, "b1k2v4096_greedy": 1, "b1k4v151936": 1, "b4k8v151936_mixed": 4,
+             "b64k8v262144": 64, "b256k16v262144_mixed": 256}
+
+
+def build_size(name: str, B=None) -> int:
+    """Number of requests ``build(name, B=B)`` makes."""
+    return B or DEFAULT_B[name]
+
+
+def build(name: str, *, B=None, requests=None):
+    """Build a workload by name.  ``B`` overrides the batch size (for bounded samples);
+    ``requests`` builds only those requests of the batch (each identical to the same request
+    of the whole batch)."""
     i = WORKLOADS.index(name)
     if name in ("b1k2v4096", "b1k2v4096_greedy"):
         T = 0.0 if name.endswith("greedy") else 0.7
         Bn = B or 1
         return make_batch(B=Bn, K_max=2, V=4096, logits_dtype="fp32",
                           rows=[row_params(T, 20, 0.95, 0, 0, 2)] * Bn, seed=1000, philox_seed=0,
-                          x_sigma=2.0, draft_sigma=0.5, want_logprobs=False, name=name)
+                          x_sigma=2.0, draft_sigma=0.5, want_logprobs=False, name=name, requests=requests)
     if name == "b1k4v151936":
         Bn = B or 1
         return make_batch(B=Bn, K_max=4, V=151936, logits_dtype="bf16",
                           rows=[row_params(0.6, 20, 0.95, 0.5, 0.3, 4)] * Bn, seed=1000 + i, philox_seed=i,
-                          x_sigma=3.0, draft_sigma=0.7, boost_frac=0.05, history_len=2048, name=name)
+                          x_sigma=3.0, draft_sigma=0.7, boost_frac=0.05, history_len=2048, name=name,
+                          requests=requests)
     if name == "b4k8v151936_mixed":
         Bn = B or 4
         rng = np.random.default_rng(2000 + i)
@@ -61,16 +73,16 @@ def build(name: str, *, B=None):
         rows = [row_params(*kinds[b % 4], 0.0, 0.0, int(Ks[b])) for b in range(Bn)]
         return make_batch(B=Bn, K_max=8, V=151936, logits_dtype="bf16", rows=rows,
                           seed=1000 + i, philox_seed=i, x_sigma=3.0, draft_sigma=0.7, boost_frac=0.05,
-                          argmax_frac=0.3, name=name)
+                          argmax_frac=0.3, name=name, requests=requests)
     if name == "b64k8v262144":
         Bn = B or 64
         return make_batch(B=Bn, K_max=8, V=262144, logits_dtype="bf16",
                           rows=[row_params(1.0, 64, 0.95, 0.2, 0.2, 8)] * Bn, seed=1000 + i, philox_seed=i,
                           x_sigma=3.0, draft_sigma=1.0, history_len=4096, want_logprobs=True,
-                          n_top_logprobs=20, name=name)
+                          n_top_logprobs=20, name=name, requests=requests)
     if name == "b256k16v262144_mixed":
         Bn = B or 256
         return make_batch(B=Bn, K_max=16, V=262144, logits_dtype="bf16", rows=_mixed18(Bn, 16),
                           seed=1000 + i, philox_seed=i, x_sigma=3.0, draft_sigma=1.0, history_len=4096,
-                          want_logprobs=True, n_top_logprobs=5, name=name)
+                          want_logprobs=True, n_top_logprobs=5, name=name, requests=requests)
     raise KeyError(name)

@@ -64,6 +64,7 @@ class Batch:
     want_logprobs: bool = False
     n_top_logprobs: int = 0
     name: str = ""
+    requests: tuple = ()              # index of each request in the full workload batch
     meta: dict = field(default_factory=dict)
 
     def x_f32(self, b=None) -> np.ndarray:
@@ -88,6 +89,25 @@ class Batch:
 
     def verify_rows(self) -> int:
         return int(np.sum(self.rows["num_drafts"].astype(np.int64) + 1))
+
+    def subset(self, reqs) -> "Batch":
+        """A batch of the given requests of this one (copies of their arrays)."""
+        reqs = [int(b) for b in reqs]
+        ids, cnt, offs = [], [], [0]
+        for b in reqs:
+            i, c = self.history(b)
+            ids.append(i)
+            cnt.append(c)
+            offs.append(offs[-1] + len(i))
+        orig = self.requests if self.requests else tuple(range(self.B))
+        return Batch(B=len(reqs), K_max=self.K_max, V=self.V, logits_dtype=self.logits_dtype,
+                     x=self.x[reqs].copy(), q=self.q[reqs].copy(), draft_ids=self.draft_ids[reqs].copy(),
+                     hist_offsets=np.array(offs, np.int32),
+                     hist_ids=np.concatenate(ids).astype(np.int32) if ids else np.zeros(0, np.int32),
+                     hist_counts=np.concatenate(cnt).astype(np.int32) if cnt else np.zeros(0, np.int32),
+                     rows=self.rows[reqs].copy(), uniforms=self.uniforms[reqs].copy(),
+                     want_logprobs=self.want_logprobs, n_top_logprobs=self.n_top_logprobs, name=self.name,
+                     requests=tuple(orig[b] for b in reqs), meta=dict(self.meta))
 
 
 def zipf_history(rng, V, H, s, perm):
@@ -115,7 +135,7 @@ def _softmax_f32(z64: np.ndarray) -> np.ndarray:
 def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
                x_sigma=3.0, draft_sigma=1.0, boost_frac=0.0, boost=8.0,
                history_len=0, zipf_s=1.1, draft_mode="q", argmax_frac=0.0,
-               x_quant=None, want_logprobs=False, n_top_logprobs=0, name="") -> Batch:
+               x_quant=None, want_logprobs=False, n_top_logprobs=0, name="", requests=None) -> Batch:
     """Build one seeded batch.
 
     rows: sequence of row_params tuples (length B).
@@ -126,28 +146,37 @@ def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
     argmax_frac: after drawing, that fraction of draft tokens (seeded) is replaced by the
                  raw target argmax at its position.
     x_quant: if set, target logits are rounded to multiples of this step (tie-heavy rows).
+    requests: build only these requests of the B-request batch; request i of the result is
+              request requests[i] of the full batch, bit for bit (each request draws from
+              its own seeded stream, so any subset can be built on its own).
     """
-    rng = np.random.default_rng(seed)
-    rows_arr = np.array(list(rows), dtype=ROW_DTYPE)
-    assert rows_arr.shape == (B,)
+    # shared draws (boosted rows, the history permutation) come from stream 0, request b's
+    # draws from stream 1 + b
+    g = np.random.default_rng(np.random.SeedSequence(seed, spawn_key=(0,)))
+    rows_all = np.array(list(rows), dtype=ROW_DTYPE)
+    assert rows_all.shape == (B,)
+    reqs = list(range(B)) if requests is None else [int(b) for b in requests]
     n_rows = B * (K_max + 1)
     boosted = np.zeros(n_rows, bool)
     if boost_frac > 0:
         nb = int(np.ceil(boost_frac * n_rows))
-        boosted[rng.choice(n_rows, size=nb, replace=False)] = True
+        boosted[g.choice(n_rows, size=nb, replace=False)] = True
     boosted = boosted.reshape(B, K_max + 1)
+    perm = g.permutation(V)
 
-    x_store = np.empty((B, K_max + 1, V), np.uint16 if logits_dtype == "bf16" else np.float32)
-    q = np.empty((B, K_max, V), np.float32)
-    d = np.zeros((B, K_max), np.int32)
-    perm = rng.permutation(V)
+    Bn = len(reqs)
+    rows_arr = rows_all[reqs]
+    x_store = np.empty((Bn, K_max + 1, V), np.uint16 if logits_dtype == "bf16" else np.float32)
+    q = np.empty((Bn, K_max, V), np.float32)
+    d = np.zeros((Bn, K_max), np.int32)
     offs = [0]
     h_ids, h_cnt = [], []
-    for b in range(B):
+    for b, b_full in enumerate(reqs):
+        rng = np.random.default_rng(np.random.SeedSequence(seed, spawn_key=(1 + b_full,)))
         xf = rng.standard_normal((K_max + 1, V), dtype=np.float32) * np.float32(x_sigma)
         if x_quant is not None:
             xf = (np.round(xf / np.float32(x_quant)) * np.float32(x_quant)).astype(np.float32)
-        for j in np.nonzero(boosted[b])[0]:
+        for j in np.nonzero(boosted[b_full])[0]:
             t = int(np.argmax(xf[j]))
             xf[j, t] += np.float32(boost)
         if logits_dtype == "bf16":
@@ -182,12 +211,12 @@ def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
         h_cnt.append(cnt)
         offs.append(offs[-1] + len(ids))
     batch = Batch(
-        B=B, K_max=K_max, V=V, logits_dtype=logits_dtype, x=x_store, q=q, draft_ids=d,
+        B=Bn, K_max=K_max, V=V, logits_dtype=logits_dtype, x=x_store, q=q, draft_ids=d,
         hist_offsets=np.array(offs, np.int32),
         hist_ids=np.concatenate(h_ids).astype(np.int32) if h_ids else np.zeros(0, np.int32),
         hist_counts=np.concatenate(h_cnt).astype(np.int32) if h_cnt else np.zeros(0, np.int32),
-        rows=rows_arr, uniforms=epilogue_uniforms(philox_seed, B, K_max),
-        want_logprobs=want_logprobs, n_top_logprobs=n_top_logprobs, name=name,
+        rows=rows_arr, uniforms=epilogue_uniforms(philox_seed, B, K_max)[reqs],
+        want_logprobs=want_logprobs, n_top_logprobs=n_top_logprobs, name=name, requests=tuple(reqs),
         meta=dict(seed=seed, philox_seed=philox_seed, x_sigma=x_sigma, draft_sigma=draft_sigma,
                   boost_frac=boost_frac, history_len=history_len, draft_mode=draft_mode,
                   argmax_frac=argmax_frac),
