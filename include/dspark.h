@@ -195,7 +195,8 @@ dspark_status_t dspark_verify_sample_static(const void* logits, const float* q, 
 /* Human-readable name of a status code. */
 const char* dspark_status_string(dspark_status_t status);
 
-/* Number of kernel launches one dspark_verify_sample call makes. */
+/* Number of kernel launches one dspark_verify_sample call makes when it asks for logprobs
+ * (want_logprobs or n_top_logprobs > 0); one fewer otherwise. */
 int32_t dspark_launches_per_call(void);
 
 #ifdef __cplusplus

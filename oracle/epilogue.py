@@ -38,7 +38,9 @@ Readings taken where the pages are silent (each listed in the design notes):
     smallest t with cumulative mass > u * total;
   * Q'(d) = 0 with P'(d) > 0 accepts; both zero rejects; an all-zero residual draws
     from P';
-  * logprobs are the raw (unpenalised, untempered, untruncated) log-softmax.
+  * logprobs are the raw (unpenalised, untempered, untruncated) log-softmax;
+  * a target logit of -inf is a token of zero probability (a masked token); NaN or +inf, or a
+    row with no finite logit, has no distribution and makes the request non-finite.
 
 Near ties.  Every discrete decision that floating point takes records a ``Decision``: its
 distance from the threshold, in the threshold's own unit, and the branch the other side
@@ -343,6 +345,13 @@ class RequestResult:
         return [d.kind for d in self.decisions if d.fragile]
 
 
+def bad_logit_row(x32):
+    """NaN or +inf anywhere, or no finite logit at all: the row defines no distribution.
+    A logit of -inf is allowed: that token has probability zero."""
+    x = np.asarray(x32, np.float32)
+    return bool(np.isnan(x).any() or (x == np.inf).any() or not np.isfinite(x).any())
+
+
 def _validate(batch, b):
     r = batch.rows[b]
     T, k, p, K = float(r["temperature"]), int(r["top_k"]), float(r["top_p"]), int(r["num_drafts"])
@@ -383,7 +392,7 @@ def verify_request(batch, b, truncate=truncate_full_sort, flips=None) -> Request
     u = batch.uniforms[b].astype(np.float64)
     hid, hc = batch.history(b)
     for j in range(K + 1):
-        if not np.all(np.isfinite(x[j])):
+        if bad_logit_row(x[j]):
             return RequestResult(-1, tokens, lps, tids, tlp, status=ROW_NONFINITE, flips=flips)
     if T > 0:
         for i in range(K):

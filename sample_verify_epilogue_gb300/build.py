@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libdspark.so")
-SOURCES = ("prep.cu", "stream_stats.cu", "finalize.cu", "finalize_warp.cu", "accept.cu", "api.cu")
+SOURCES = ("prep.cu", "stream_stats.cu", "finalize.cu", "finalize_warp.cu", "accept.cu", "logprobs.cu", "api.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 

@@ -11,11 +11,12 @@
 // the smallest id whose cumulative mass exceeds u * total.  Whole-vocabulary supports are
 // left to finish_kernel.
 //
+// The request's emitted positions j <= a are listed for the logprob pass (logprob_kernel).
+//
 // finish_kernel: one CTA per request.  Whole-row inverse-CDF draws (every thread sums the
 // weights of a contiguous range of ids, a block scan of those sums finds the range holding
-// the draw, and its thread walks it), then the logprob outputs: raw log-softmax at each
-// emitted token and the top-n list (mlx-dspark Changelog, [0.2.0] Added, logprobs /
-// top_logprobs).
+// the draw, and its thread walks it), then the logprob outputs past the emitted token (-inf,
+// top ids -1); the emitted positions' values come from logprob_kernel.
 #include "block_utils.cuh"
 
 namespace dspark {
@@ -172,6 +173,10 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
     if (tid == 0) {
         a.out_accept[b] = acc_len;
         a.req[b] = ReqOut{acc_len, draw, 0, 0};
+        if (a.want_lp || a.n_top > 0) {                     // rows of the logprob pass
+            const int base = atomicAdd(&a.lp_list[0], acc_len + 1);
+            for (int j = 0; j <= acc_len; ++j) a.lp_list[1 + base + j] = static_cast<int>(xs0) + j;
+        }
     }
 }
 
@@ -392,29 +397,12 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(Args a) {
         if (tid == 0) a.out_tokens[xs0 + acc_len] = tok;
         __syncthreads();
     }
-    // ---- logprob outputs
-    if (a.out_lp || (a.n_top > 0 && (a.out_top_ids || a.out_top_lp))) {
-        for (int j = tid; j < W; j += blockDim.x) {
-            float lp = -INFINITY;
-            if (j <= acc_len) {
-                const int t = a.out_tokens[xs0 + j];
-                const XRowOut xo = a.xout[xs0 + j];
-                if (t >= 0) lp = load_x(a.x, a.sx, (xs0 + j) * a.V + t) - xo.lse;
-            }
-            if (a.out_lp) a.out_lp[xs0 + j] = lp;
-        }
-        for (int e = tid; e < W * a.n_top; e += blockDim.x) {
-            const int j = e / a.n_top, q = e % a.n_top;
-            int id = -1;
-            float v = -INFINITY;
-            if (j <= acc_len) {
-                const TopEntry te = a.topn[(xs0 + j) * DSPARK_MAX_TOP_LOGPROBS + q];
-                id = te.id;
-                v = te.v - a.xout[xs0 + j].lse;
-            }
-            if (a.out_top_ids) a.out_top_ids[xs0 * a.n_top + e] = id;
-            if (a.out_top_lp) a.out_top_lp[xs0 * a.n_top + e] = v;
-        }
+    // ---- logprob outputs past the emitted token (the emitted positions: logprob_kernel)
+    if (a.out_lp)
+        for (int j = acc_len + 1 + tid; j < W; j += blockDim.x) a.out_lp[xs0 + j] = -INFINITY;
+    for (int e = (acc_len + 1) * a.n_top + tid; e < W * a.n_top; e += blockDim.x) {
+        if (a.out_top_ids) a.out_top_ids[xs0 * a.n_top + e] = -1;
+        if (a.out_top_lp) a.out_top_lp[xs0 * a.n_top + e] = -INFINITY;
     }
 }
 

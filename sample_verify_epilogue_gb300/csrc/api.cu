@@ -17,10 +17,12 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 constexpr int kMaxGrid = 1024;           // streaming CTAs on any device (an SM count bound)
 
 struct Layout {
-    int tile_x, tiles_x, tile_q, tiles_q, bm_words, xslots, qslots, nseg_x, nseg_q;
+    int tile_x, tiles_x, tile_q, tiles_q, bm_words, xslots, qslots, nseg_x, nseg_q, lp_chunks;
     long long seg_max;
-    size_t off_plan, off_req_n, off_fin_list, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_raw, off_cand_q;
-    size_t off_pen_hdr, off_pen_bm, off_pen_ent, off_draft_base, off_xout, off_kept, off_topn, off_qout, off_req;
+    size_t off_plan, off_req_n, off_fin_list, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_q;
+    size_t off_pen_hdr, off_pen_bm, off_pen_ent, off_draft_base, off_xout, off_kept, off_qout, off_req;
+    size_t off_lp_part;
+    size_t zero_bytes;   // the call record cleared by every call: plan, logprob row counters, list count
     size_t total;
 };
 
@@ -47,13 +49,16 @@ Layout make_layout(const dspark_params_t* p) {
     L.qslots = static_cast<int>(B * Km);
     L.nseg_x = (L.tiles_x + kSegTiles - 1) / kSegTiles;
     L.nseg_q = (L.tiles_q + kSegTiles - 1) / kSegTiles;
+    L.lp_chunks = static_cast<int>((V + kLpChunkBytes / sx - 1) / (kLpChunkBytes / sx));
     const size_t xt = static_cast<size_t>(L.xslots) * L.nseg_x;
     const size_t qt = static_cast<size_t>(L.qslots) * L.nseg_q;
     const size_t pt = static_cast<size_t>(B) * L.tiles_x;
     L.seg_max = static_cast<long long>(xt + qt);
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
-    L.off_plan = take(sizeof(Plan));
+    // call record: Plan, then lp_done [xslots], then lp_list [1 + xslots] (its count cleared too)
+    L.zero_bytes = sizeof(Plan) + static_cast<size_t>(L.xslots + 1) * sizeof(int);
+    L.off_plan = take(L.zero_bytes + static_cast<size_t>(L.xslots) * sizeof(int));
     L.off_req_n = take(static_cast<size_t>(2 * B) * sizeof(int));
     L.off_fin_list = take(static_cast<size_t>(1 + L.xslots + L.qslots) * sizeof(int));
     // segment streams: grid x groups x ceil(S / (groups*grid)) entries <= S + groups*grid
@@ -61,7 +66,6 @@ Layout make_layout(const dspark_params_t* p) {
     L.off_ts_x = take(xt * sizeof(TileStats));
     L.off_ts_q = take(qt * sizeof(TileStats));
     L.off_cand_x = take(xt * kCandPenGlobal * sizeof(Cand));
-    L.off_cand_raw = take(p->n_top_logprobs > 0 ? xt * kCandRawGlobal * sizeof(Cand) : 0);
     L.off_cand_q = take(qt * kCandPenGlobal * sizeof(Cand));
     L.off_pen_hdr = take(pt * sizeof(PenHdr));
     L.off_pen_bm = take(pt * L.bm_words * sizeof(unsigned));
@@ -69,9 +73,9 @@ Layout make_layout(const dspark_params_t* p) {
     L.off_draft_base = take(static_cast<size_t>(B * Km) * sizeof(int) + 4);
     L.off_xout = take(static_cast<size_t>(L.xslots) * sizeof(XRowOut));
     L.off_kept = take(static_cast<size_t>(L.xslots) * kKeptCap * sizeof(KeptEntry));
-    L.off_topn = take(static_cast<size_t>(L.xslots) * DSPARK_MAX_TOP_LOGPROBS * sizeof(TopEntry));
     L.off_qout = take(static_cast<size_t>(L.qslots) * sizeof(QRowOut) + 16);
     L.off_req = take(static_cast<size_t>(B) * sizeof(ReqOut));
+    L.off_lp_part = take(static_cast<size_t>(L.xslots) * L.lp_chunks * sizeof(LpPartial));
     L.total = o;
     return L;
 }
@@ -102,7 +106,7 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     Args a{};
     a.B = p->B; a.Km = p->K_max; a.V = p->V; a.sx = sx; a.xdtype = p->logits_dtype;
     a.tile_x = L.tile_x; a.tiles_x = L.tiles_x; a.tile_q = L.tile_q; a.tiles_q = L.tiles_q; a.bm_words = L.bm_words;
-    a.nseg_x = L.nseg_x; a.nseg_q = L.nseg_q;
+    a.nseg_x = L.nseg_x; a.nseg_q = L.nseg_q; a.lp_chunks = L.lp_chunks;
     a.n_top = p->n_top_logprobs; a.want_lp = p->want_logprobs ? 1 : 0;
     a.xslots = L.xslots; a.qslots = L.qslots;
     a.x = logits; a.q = q; a.d = draft_ids; a.rows = p->rows;
@@ -119,7 +123,6 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     a.ts_x = at<TileStats>(ws, L.off_ts_x);
     a.ts_q = at<TileStats>(ws, L.off_ts_q);
     a.cand_x = at<Cand>(ws, L.off_cand_x);
-    a.cand_raw = at<Cand>(ws, L.off_cand_raw);
     a.cand_q = at<Cand>(ws, L.off_cand_q);
     a.pen_hdr = at<PenHdr>(ws, L.off_pen_hdr);
     a.pen_bm = at<unsigned>(ws, L.off_pen_bm);
@@ -127,9 +130,11 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     a.draft_base = at<int>(ws, L.off_draft_base);
     a.xout = at<XRowOut>(ws, L.off_xout);
     a.kept = at<KeptEntry>(ws, L.off_kept);
-    a.topn = at<TopEntry>(ws, L.off_topn);
     a.qout = at<QRowOut>(ws, L.off_qout);
     a.req = at<ReqOut>(ws, L.off_req);
+    a.lp_done = reinterpret_cast<int*>(a.plan + 1);
+    a.lp_list = a.lp_done + L.xslots;
+    a.lp_part = at<LpPartial>(ws, L.off_lp_part);
 
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
@@ -139,7 +144,7 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     a.max_seg = static_cast<int>((L.seg_max + 2LL * sms - 1) / (2LL * sms));
 
     if (cudaMemsetAsync(p->row_status, 0, sizeof(int32_t) * p->B, s) != cudaSuccess) return DSPARK_ERR_CUDA;
-    if (cudaMemsetAsync(a.plan, 0, sizeof(Plan), s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (cudaMemsetAsync(a.plan, 0, L.zero_bytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_prep(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     cudaEvent_t ev0 = static_cast<cudaEvent_t>(p->stage_events[0]);
     cudaEvent_t ev1 = static_cast<cudaEvent_t>(p->stage_events[1]);
@@ -152,6 +157,7 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     if (launch_row_finalize(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_accept(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_finish(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if ((a.want_lp || a.n_top > 0) && launch_logprobs(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }
 
@@ -316,6 +322,6 @@ const char* dspark_status_string(dspark_status_t status) {
     return "unknown status";
 }
 
-int32_t dspark_launches_per_call(void) { return 6; }
+int32_t dspark_launches_per_call(void) { return 7; }
 
 }  // extern "C"

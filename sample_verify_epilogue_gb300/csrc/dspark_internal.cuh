@@ -6,7 +6,8 @@
 //   row_finalize_kernel  per verify row: merge segments, top-k threshold, nucleus, normaliser
 //                        (rows needing a whole-vocabulary threshold get it in the same block)
 //   accept_kernel        per request: accept scan, residual / bonus draw over candidates
-//   finish_kernel        per request: whole-vocabulary draws (rare) and logprob outputs
+//   finish_kernel        per request: whole-vocabulary draws (rare), padding of the outputs
+//   logprob_kernel       the emitted positions' raw log-softmax and top_logprobs
 #pragma once
 
 #include <utility>
@@ -33,11 +34,11 @@ constexpr int kPenCap = 256;                                   // penalised toke
 constexpr int kSegTiles = 4;                                   // vocab tiles per segment
 constexpr int kMaxSegTiles = 16;
 constexpr int kCandPenGlobal = 1536;                           // per-segment candidates kept in the workspace
-constexpr int kCandRawGlobal = 1024;
 constexpr int kMaxCandTopK = 256;                              // top_k above this uses the whole-row path
 constexpr int kKeptCap = 1024;                                 // truncated support held as a list
 constexpr int kFinalizeThreads = 512;
 constexpr int kMergeCap = 8192;                                // merged candidates per row (smem)
+constexpr int kLpChunkBytes = 32 * 1024;                       // bytes of logits per chunk of the logprob pass
 constexpr int kMaxB = DSPARK_MAX_B;
 
 // ---------------------------------------------------------------- records in the workspace
@@ -45,7 +46,7 @@ enum UnitKind : int { kUnitX = 0, kUnitQ = 1 };
 
 struct Plan {
     int n_units;         // unused
-    int pad[3];          // pad[0]: error flag set by the streaming pass
+    int pad[3];          // pad[0]: error flag set by the streaming pass; pad[1]: logprob work counter
 };
 
 // One segment (consecutive vocab tiles [t0, t1) of one row) with its request's parameters.
@@ -65,16 +66,15 @@ struct UnitDesc {
 
 struct TileStats {       // per (row, segment)
     float m_raw;         // x: raw max           | q: max
-    float s_raw;         // x: sum exp(x-m_raw)  | q: sum q
+    float s_raw;         // x: 0                 | q: sum q
     float m_pen;         // x: penalised max
     int   arg_pen;       // x: lowest id attaining m_pen
     float s_temp;        // x: sum exp((x'-m_pen)/T) | q: sum (q/max)^(1/T)
     int   n_pen;         // candidates written (penalised x / q)
-    int   n_raw;         // raw-logit candidates written
+    int   pad;
     int   flags;         // kTileOverflow, kTileBad
 };
 constexpr int kTileOverflowPen = 1;
-constexpr int kTileOverflowRaw = 2;
 constexpr int kTileBad = 4;
 
 struct Cand { float v; int id; };
@@ -100,9 +100,9 @@ struct XRowOut {
     int    mode;
     int    argmax;       // penalised argmax (lowest id on ties)
     float  m_pen;        // penalised max
-    float  lse;          // raw log-sum-exp
     float  tau;          // support threshold on x'
     float  c_l2e;        // log2(e)/T
+    float  pad0;
     int    n_kept;
     int    top_k;        // top_k still to apply (whole-row path), 0 = none
     double Z;            // sum of support weights exp2((x'-m_pen)*c_l2e)
@@ -125,6 +125,15 @@ struct QRowOut {
 struct KeptEntry { int id; float w; };
 struct TopEntry { int id; float v; };
 
+// One chunk of a row in the logprob pass: its maximum, sum of exp relative to it, top-n list.
+struct LpPartial {
+    float m;
+    float s;
+    int n;
+    int pad;
+    TopEntry top[DSPARK_MAX_TOP_LOGPROBS];
+};
+
 struct ReqOut {
     int a;               // accepted drafts
     int draw;            // 0 none pending, 1 residual over the whole row, 2 target row over the whole row
@@ -138,6 +147,7 @@ struct Args {
     int B, Km, V, sx, xdtype;
     int tile_x, tiles_x, tile_q, tiles_q, bm_words;
     int nseg_x, nseg_q;    // segments per target / draft row
+    int lp_chunks;         // chunks per row in the logprob pass
     int grid_ss;           // CTAs of the streaming pass
     int max_seg;           // segments per (CTA, group) stream, upper bound
     int n_top, want_lp;
@@ -164,7 +174,6 @@ struct Args {
     TileStats* ts_x;       // [xslots * nseg_x]
     TileStats* ts_q;       // [qslots * nseg_q]
     Cand* cand_x;          // [xslots * nseg_x * kCandPenGlobal]
-    Cand* cand_raw;        // [xslots * nseg_x * kCandRawGlobal]
     Cand* cand_q;          // [qslots * nseg_q * kCandPenGlobal]
     PenHdr* pen_hdr;       // [B * tiles_x]
     unsigned* pen_bm;      // [B * tiles_x * bm_words]
@@ -174,9 +183,11 @@ struct Args {
     int* fin_list;         // [1 + xslots + qslots]: count, then the rows left to the block finalize
     XRowOut* xout;         // [xslots]
     KeptEntry* kept;       // [xslots * kKeptCap]
-    TopEntry* topn;        // [xslots * DSPARK_MAX_TOP_LOGPROBS]
     QRowOut* qout;         // [qslots]
     ReqOut* req;           // [B]
+    int* lp_list;          // [1 + xslots]: count, then the rows (b*W + j) the logprob pass reads
+    int* lp_done;          // [xslots]: chunks of each row done (zeroed by every call)
+    LpPartial* lp_part;    // [xslots * lp_chunks]
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -420,5 +431,6 @@ cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid, bool pd
 cudaError_t launch_row_finalize(const Args& a, cudaStream_t s);
 cudaError_t launch_accept(const Args& a, cudaStream_t s);
 cudaError_t launch_finish(const Args& a, cudaStream_t s);
+cudaError_t launch_logprobs(const Args& a, cudaStream_t s);
 
 }  // namespace dspark

@@ -1,7 +1,7 @@
 // row_finalize_kernel: one CTA per verify row left by the warp finalize (target position (b, j)
 // or draft position (b, i)).  Merges the per-segment statistics of the streaming pass and settles the row's
 // truncated distribution:
-//   - target rows: raw log-sum-exp (logprobs), penalised max and argmax (greedy), the top-k
+//   - target rows: penalised max and argmax (greedy), the top-k
 //     threshold tau_k = k-th largest penalised logit among the merged segment candidates (exact:
 //     every member of the row's top-k is a candidate of its own segment), the survivors
 //     {x' >= tau_k} sorted by (value desc, id asc), their weights exp((x'-max)/T), and the
@@ -51,11 +51,11 @@ struct CandSet {
 
 // Offsets of the row's candidate lists (from the segment statistics) and, when they fit, the
 // keys staged in shared memory.  Returns the set, total = -1 when any list overflowed.
-__device__ CandSet stage_candidates(FinSmem& s, const TileStats* ts, const Cand* base, int cap, int nseg, bool raw) {
+__device__ CandSet stage_candidates(FinSmem& s, const TileStats* ts, const Cand* base, int cap, int nseg) {
     const int tid = threadIdx.x;
     CandSet cs{base, cap, nseg, 0};
     if (nseg > kMaxSegs) { cs.total = -1; return cs; }
-    for (int t = tid; t < nseg; t += blockDim.x) s.off[t + 1] = raw ? ts[t].n_raw : ts[t].n_pen;
+    for (int t = tid; t < nseg; t += blockDim.x) s.off[t + 1] = ts[t].n_pen;
     __syncthreads();
     if (tid == 0) {
         s.off[0] = 0;
@@ -213,9 +213,7 @@ struct FullSmem {
     int bcast[32];
     unsigned long long ubcast[4];
     int tl_n, tl_over;
-    int top_ids[64];
-    float top_v[64];
-    int n_gt, n_eq;
+    int n_gt;
     double dwarp_plim;
     uint4 tb[2][kStageBytes / 32];     // double-buffered half vocab tile (cp.async)
 };
@@ -581,70 +579,12 @@ __device__ uint32_t full_nucleus(FullSmem& s, const RowSource& src, uint32_t flo
     return tau;
 }
 
-// Raw top-n with ties broken by lower id, over the whole row.
-__device__ void full_topn(FullSmem& s, const RowSource& src, int nt, TopEntry* dst) {
-    const int tid = threadIdx.x;
-    const uint32_t kth = full_kth(s, src, nt, true);
-    if (tid == 0) { s.n_gt = 0; s.n_eq = 0; }
-    __syncthreads();
-    // elements strictly above the n-th value (fewer than nt of them)
-    for_each_elem(s, src, [&](int e, float, float raw) {
-        if (fkey(raw) > kth) {
-            const int p = atomicAdd(&s.n_gt, 1);
-            if (p < 64) { s.top_ids[p] = e; s.top_v[p] = raw; }
-        }
-    });
-    // the lowest ids equal to the n-th value fill the rest, found in id order by an ordered
-    // block compaction over consecutive chunks of the row
-    const int have = min(s.n_gt, 64);
-    const int need = nt - have;
-    const int lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-    int got = 0;
-    for (int base = 0; base < src.a->V && got < need; base += blockDim.x) {
-        const int e = base + tid;
-        float raw = 0.f;
-        bool flag = false;
-        if (e < src.a->V) {
-            raw = src.is_x ? load_x(src.a->x, src.a->sx, src.base + e) : src.a->q[src.base + e];
-            flag = fkey(raw) == kth;
-        }
-        const unsigned bal = __ballot_sync(0xffffffffu, flag);
-        if (lane == 0) s.bcast[warp] = __popc(bal);
-        __syncthreads();
-        int woff = 0, tot = 0;
-        for (int w = 0; w < nw; ++w) { if (w < warp) woff += s.bcast[w]; tot += s.bcast[w]; }
-        const int pos = got + woff + __popc(bal & ((1u << lane) - 1u));
-        if (flag && pos < need) { s.top_ids[have + pos] = e; s.top_v[have + pos] = raw; }
-        got += tot;
-        __syncthreads();
-    }
-    got = min(got, need);
-    if (tid == 0) {
-        // order: value desc, id asc (at most 20 entries: insertion sort)
-        const int tot = have + got;
-        for (int i = 1; i < tot; ++i) {
-            const int id = s.top_ids[i];
-            const float v = s.top_v[i];
-            int q = i - 1;
-            while (q >= 0 && (s.top_v[q] < v || (s.top_v[q] == v && s.top_ids[q] > id))) {
-                s.top_ids[q + 1] = s.top_ids[q]; s.top_v[q + 1] = s.top_v[q]; --q;
-            }
-            s.top_ids[q + 1] = id; s.top_v[q + 1] = v;
-        }
-        for (int i = 0; i < nt && i < tot; ++i) dst[i] = TopEntry{s.top_ids[i], s.top_v[i]};
-    }
-    __syncthreads();
-}
-
 // Whole-row selection for a target row whose support could not come from candidates;
-// updates o (threshold, normaliser, mode) and, when its candidate list overflowed, the
-// raw top-n list.
+// updates o (threshold, normaliser, mode).
 __device__ void whole_row_x(const Args& a, FullSmem& s, int slot, int b, int j, XRowOut& o) {
     const dspark_row_params_t r = a.rows[b];
     RowSource src{&a, true, static_cast<long long>(slot) * a.V, b, j, r.frequency_penalty, r.presence_penalty,
                   has_penalty(r)};
-    const bool need_top = a.n_top > 0 && (o.flags & kTileOverflowRaw);
-    if (need_top) full_topn(s, src, min(a.n_top, a.V), a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS);
     if (o.mode == kModeNeedFull) {
         uint32_t floor_key = fkey(o.tau);
         if (o.top_k > 0) floor_key = full_kth(s, src, o.top_k, false);
@@ -717,21 +657,18 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
         return;
     }
     int arg = 0x7FFFFFFF;
-    double sraw = 0.0, stemp = 0.0;
+    double stemp = 0.0;
     const bool greedy = !(r.temperature > 0.f);
     const float c_l2e = greedy ? 0.f : kL2E / r.temperature;
     for (int t = tid; t < nseg; t += blockDim.x) {
         const TileStats x = ts[t];
         if (x.m_pen == mp) arg = min(arg, x.arg_pen);
-        sraw += static_cast<double>(x.s_raw) * static_cast<double>(exp2f((x.m_raw - mr) * kL2E));
         if (!greedy) stemp += static_cast<double>(x.s_temp) * static_cast<double>(exp2f((x.m_pen - mp) * c_l2e));
     }
     arg = block_min_i(arg, s.iwarp);
-    sraw = block_sum_d(sraw, s.dwarp);
     stemp = block_sum_d(stemp, s.dwarp);
     o.argmax = arg;
     o.m_pen = mp;
-    o.lse = mr + logf(static_cast<float>(sraw));
     o.c_l2e = c_l2e;
     o.top_p = r.top_p;
     o.tau = -INFINITY;
@@ -745,7 +682,7 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
         CandSet cs{nullptr, 0, 0, -1};
         if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
             cs = stage_candidates(s, ts, a.cand_x + static_cast<long long>(slot) * nseg * kCandPenGlobal,
-                                  kCandPenGlobal, nseg, false);
+                                  kCandPenGlobal, nseg);
         if (cs.total >= k) {
             const uint32_t kth = kth_largest(s, cs, k);
             const int cnt = sorted_survivors(s, cs, kth);
@@ -774,28 +711,8 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
         o.Z = stemp;
         o.mode = (r.top_p < 1.f) ? kModeNeedFull : kModeFull;
     }
-    // raw top-n for top_logprobs
-    if (a.n_top > 0) {
-        bool done = false;
-        if (!(fl & kTileOverflowRaw)) {
-            const CandSet cs = stage_candidates(s, ts, a.cand_raw + static_cast<long long>(slot) * nseg * kCandRawGlobal,
-                                                kCandRawGlobal, nseg, true);
-            const int nt = min(a.n_top, a.V);
-            if (cs.total >= nt) {
-                const uint32_t kth = kth_largest(s, cs, nt);
-                const int cnt = sorted_survivors(s, cs, kth);
-                if (cnt >= nt) {
-                    TopEntry* dst = a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS;
-                    for (int i = tid; i < nt; i += blockDim.x) dst[i] = TopEntry{ckey_id(s.sk[i]), ckey_v(s.sk[i])};
-                    done = true;
-                }
-            }
-        }
-        if (!done) o.flags |= kTileOverflowRaw;               // the whole-row path fills the list
-    }
     __syncthreads();
-    if (o.mode == kModeNeedFull || (a.n_top > 0 && (o.flags & kTileOverflowRaw)))
-        whole_row_x(a, *reinterpret_cast<FullSmem*>(&s), slot, b, j, o);
+    if (o.mode == kModeNeedFull) whole_row_x(a, *reinterpret_cast<FullSmem*>(&s), slot, b, j, o);
     if (tid == 0) a.xout[slot] = o;
 }
 
@@ -839,7 +756,7 @@ __device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
         CandSet cs{nullptr, 0, 0, -1};
         if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
             cs = stage_candidates(s, ts, a.cand_q + static_cast<long long>(qslot) * nseg * kCandPenGlobal,
-                                  kCandPenGlobal, nseg, false);
+                                  kCandPenGlobal, nseg);
         if (cs.total >= k) {
             const uint32_t kth = kth_largest(s, cs, k);
             const int cnt = sorted_survivors(s, cs, kth);

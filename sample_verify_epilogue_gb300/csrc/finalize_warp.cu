@@ -1,7 +1,7 @@
 // row_finalize_warp_kernel: one WARP per verify row, for the rows whose truncated support
 // settles from the streaming pass's candidates alone (the common case).  It computes the same
 // records as the block-per-row finalize (segment merge, top-k threshold, sorted survivors,
-// weights, nucleus, raw top-n; mlx-dspark Changelog, [0.1.0] Added, top-p / top-k sampling;
+// weights, nucleus; mlx-dspark Changelog, [0.1.0] Added, top-p / top-k sampling;
 // [0.20.2] Changed, selection instead of a full vocabulary sort) with warp shuffles and
 // per-warp shared memory instead of block barriers: the candidates' order-preserving keys
 // are staged (long lists after a first read that bounds the k-th largest key from below, so
@@ -129,13 +129,13 @@ __device__ int warp_stage_t(WarpSmem& w, const WCands& cs, int npairs, int c) {
     return m > kWKeyCap ? -1 : m;
 }
 
-__device__ int warp_stage(WarpSmem& w, const TileStats* ts, const WCands& cs, bool raw, int k) {
+__device__ int warp_stage(WarpSmem& w, const TileStats* ts, const WCands& cs, int k) {
     const int lane = threadIdx.x & 31;
     if (cs.nseg > kWSegCap) return -1;
     int total = 0, npairs = 0;
     for (int t0 = 0; t0 < cs.nseg; t0 += 32) {
         const int t = t0 + lane;
-        const int n = t < cs.nseg ? (raw ? ts[t].n_raw : ts[t].n_pen) : 0;
+        const int n = t < cs.nseg ? ts[t].n_pen : 0;
         const int np = (n + 1) >> 1;
         int incl = np;
 #pragma unroll
@@ -272,23 +272,6 @@ __device__ int warp_nucleus(const WarpSmem& w, int cnt, float top_p, WFn wfn, do
     return kept;
 }
 
-// Raw top-n list of a target row from its raw candidates; false when it needs the block path.
-__device__ bool warp_topn(WarpSmem& w, const Args& a, const TileStats* ts, int slot) {
-    const int lane = threadIdx.x & 31;
-    const int nseg = a.nseg_x;
-    const WCands cs{a.cand_raw + static_cast<long long>(slot) * nseg * kCandRawGlobal, kCandRawGlobal, nseg};
-    const int n = warp_stage(w, ts, cs, true, min(a.n_top, a.V));
-    const int nt = min(a.n_top, a.V);
-    if (n < nt) return false;                  // also n = -1
-    const uint32_t kth = warp_kth(w, n, nt);
-    const int cnt = warp_survivors(w, n, kth);
-    if (cnt < nt) return false;
-    TopEntry* dst = a.topn + static_cast<long long>(slot) * DSPARK_MAX_TOP_LOGPROBS;
-    for (int i = lane; i < nt; i += 32) dst[i] = TopEntry{ckey_id(w.sk[i]), ckey_v(w.sk[i])};
-    __syncwarp();
-    return true;
-}
-
 // Target row (b, j).  Returns false when the row needs the block path (nothing final written).
 __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
     const int lane = threadIdx.x & 31;
@@ -324,23 +307,19 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
     // rows that need a whole-row pass go to the block path straight away
     if (!greedy && !list && r.top_p < 1.f) return false;
     if (list && (k > kMaxCandTopK || (fl & kTileOverflowPen))) return false;
-    if (a.n_top > 0 && (fl & kTileOverflowRaw)) return false;
     int arg = 0x7FFFFFFF;
-    double sraw = 0.0, stemp = 0.0;
+    double stemp = 0.0;
     for (int t = lane; t < nseg; t += 32) {
         const TileStats x = ts[t];
         if (x.m_pen == mp) arg = min(arg, x.arg_pen);
-        sraw += static_cast<double>(x.s_raw) * static_cast<double>(exp2f((x.m_raw - mr) * kL2E));
         if (!greedy) stemp += static_cast<double>(x.s_temp) * static_cast<double>(exp2f((x.m_pen - mp) * c_l2e));
     }
     for (int off = 16; off; off >>= 1) {
         arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, off));
-        sraw += __shfl_xor_sync(0xffffffffu, sraw, off);
         stemp += __shfl_xor_sync(0xffffffffu, stemp, off);
     }
     o.argmax = arg;
     o.m_pen = mp;
-    o.lse = mr + logf(static_cast<float>(sraw));
     o.c_l2e = c_l2e;
     o.top_p = r.top_p;
     o.tau = -INFINITY;
@@ -351,7 +330,7 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
         o.mode = kModeGreedy;
     } else if (list) {
         const WCands cs{a.cand_x + static_cast<long long>(slot) * nseg * kCandPenGlobal, kCandPenGlobal, nseg};
-        const int n = warp_stage(w, ts, cs, false, k);
+        const int n = warp_stage(w, ts, cs, k);
         if (n < k) return false;               // too many candidates to stage, or fewer than k
         const uint32_t kth = warp_kth(w, n, k);
         const int cnt = warp_survivors(w, n, kth);
@@ -368,7 +347,6 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
         o.Z = stemp;
         o.mode = kModeFull;                    // top_p >= 1 here
     }
-    if (a.n_top > 0 && !warp_topn(w, a, ts, slot)) return false;
     if (lane == 0) a.xout[slot] = o;
     return true;
 }
@@ -418,7 +396,7 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
     o.flags = fl;
     if (list) {
         const WCands cs{a.cand_q + static_cast<long long>(qslot) * nseg * kCandPenGlobal, kCandPenGlobal, nseg};
-        const int n = warp_stage(w, ts, cs, false, k);
+        const int n = warp_stage(w, ts, cs, k);
         if (n < k) return false;
         const uint32_t kth = warp_kth(w, n, k);
         const int cnt = warp_survivors(w, n, kth);

@@ -8,14 +8,14 @@
 // tile's penalty bitmap and penalised-token list, serving both groups' segment streams.
 //
 // A group processes a segment in one sweep:
-//   first tile: pass 1 gives per-thread maxima of the raw and the penalised logits
+//   first tile: pass 1 gives per-thread maxima of the penalised logits
 //     (x' = x - ((f*c) + p), mlx-dspark Changelog [0.2.0] Added, penalties); every warp sorts
 //     its lanes' maxima and takes the c-th largest (c = ceil(k/8)); theta = the least of the
 //     8 warps' values, so at least 8*c >= k distinct logits of the first tile are >= theta,
 //     hence every member of the segment's top-k is >= theta.  Pass 2 then accumulates and
 //     filters as below;
-//   later tiles: one pass each: running maxima with rescaled sums of exp (raw: the
-//     log-softmax of logprobs; penalised and tempered: the normaliser when there is no
+//   later tiles: one pass each: the raw maximum (a non-finite logit shows there), the
+//     penalised maximum with a rescaled sum of exp (the normaliser when there is no
 //     top-k), the lowest index attaining the penalised max (greedy), and the candidates
 //     >= theta (the top-k threshold of the row comes from these, mlx-dspark Changelog
 //     [0.20.2] Changed: small selections instead of a full vocabulary sort);
@@ -23,6 +23,8 @@
 //     straight to the segment's lists in global memory as they were found, positions taken
 //     from counters in shared memory).
 // Draft tiles get the same treatment with q as the key (top-k of q^(1/T) is top-k of q).
+// The raw log-softmax and the raw top-n of logprobs are not taken here: they are needed at
+// the emitted positions only, which logprob_kernel reads after the draws.
 #include "dspark_internal.cuh"
 
 namespace dspark {
@@ -71,7 +73,7 @@ struct GroupSmem {
     float4 red1[kGroupWarps];    // first-tile maxima and thresholds
     float4 red[kGroupWarps];     // end-of-segment partials
     float4 red2[kGroupWarps];
-    int n_pen, n_raw;            // entries appended to the segment's global candidate lists
+    int n_pen;                   // entries appended to the segment's global candidate list
     int error;
     unsigned short flist[kGroupWarps][64];   // per warp: the tile's flagged vectors, (slot << 5) | lane
 };
@@ -248,43 +250,6 @@ __device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsign
     }
 }
 
-// Append the raw candidates (`mr`, to list r) and the penalised candidates (`mp`, to list p)
-// of one 16-byte vector with a single prefix (both counts packed in one word) across lanes.
-template <int SX>
-__device__ __forceinline__ void warp_append2(Cand* bufr, int* cntr, int capr, Cand* bufp, int* cntp, int capp,
-                                             unsigned mr, unsigned mp, const uint4& w, int e) {
-    const unsigned any = __ballot_sync(0xffffffffu, (mr | mp) != 0u);
-    if (!any) return;
-    const int lane = threadIdx.x & 31;
-    const int n = __popc(mr) | (__popc(mp) << 16);
-    int incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    int base_r = 0, base_p = 0;
-    if (lane == 31) {
-        if (incl & 0xFFFF) base_r = atomicAdd(cntr, incl & 0xFFFF);
-        if (incl >> 16) base_p = atomicAdd(cntp, incl >> 16);
-    }
-    const int ex = incl - n;
-    base_r = __shfl_sync(0xffffffffu, base_r, 31) + (ex & 0xFFFF);
-    base_p = __shfl_sync(0xffffffffu, base_p, 31) + (ex >> 16);
-    while (mr) {
-        const int q = __ffs(mr) - 1;
-        mr &= mr - 1u;
-        if (base_r < capr) bufr[base_r] = Cand{elem<SX>(w, q), e + q};
-        ++base_r;
-    }
-    while (mp) {
-        const int q = __ffs(mp) - 1;
-        mp &= mp - 1u;
-        if (base_p < capp) bufp[base_p] = Cand{elem<SX>(w, q), e + q};
-        ++base_p;
-    }
-}
-
 // Append every element flagged in this thread's (f0, f1) bit set (bit EPV*i+q: element q of
 // the thread's i-th vector of the tile in shared memory), warp-cooperatively: one prefix and
 // one shared atomic per warp and tile.  All lanes of the warp call it.
@@ -355,17 +320,16 @@ __device__ __noinline__ int deal_by_ballots(unsigned vflags, int t, int wv) {
 }
 
 // Candidate extraction from the vectors the threads flagged during a scan (bit i of
-// `vflags`: the thread's i-th vector of the tile has an element at or above the lower
+// `vflags`: the thread's i-th vector of the tile has an element at or above the
 // threshold).  The warp's flagged vectors are dealt out to its lanes 32 at a time, so a lane
 // with many flags does not hold up the others: a prefix over the lanes' flag counts places
-// them in a per-warp list (more than 64 fall back to slot-wise ballots).  For each vector:
-// RAW appends the elements >= th_r to the raw list `lr`; the elements >= th_p without a
-// penalty bit are appended to the penalised list `lp` (CAND; both with one prefix) and
-// folded into the running penalised maximum and the lowest index attaining it (TRACK).
+// them in a per-warp list (more than 64 fall back to slot-wise ballots).  For each vector,
+// the elements >= th_p without a penalty bit are appended to the candidate list `lp` (CAND)
+// and folded into the running penalised maximum and the lowest index attaining it (TRACK).
 // Every lane of the warp calls it.
-template <int SX, bool PEN, bool RAW, bool CAND, bool TRACK>
-__device__ __forceinline__ void flush_vectors(GroupSmem& gs, Cand* lr, Cand* lp, unsigned vflags, const unsigned char* data,
-                                              const unsigned* bm, int vec_e0, int bit0, int gt, float th_r,
+template <int SX, bool PEN, bool CAND, bool TRACK>
+__device__ __forceinline__ void flush_vectors(GroupSmem& gs, Cand* lp, unsigned vflags, const unsigned char* data,
+                                              const unsigned* bm, int vec_e0, int bit0, int gt,
                                               float th_p, float& m_p, int& arg) {
     constexpr int EPV = 16 / SX;
     const int lane = threadIdx.x & 31;
@@ -397,18 +361,15 @@ __device__ __forceinline__ void flush_vectors(GroupSmem& gs, Cand* lr, Cand* lp,
             v = deal_by_ballots(vflags, t, wv);           // more flags than the list holds
         }
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        unsigned mr = 0u, mp = 0u;
+        unsigned mp = 0u;
         int e = 0;
         if (v >= 0) {
             w = *reinterpret_cast<const uint4*>(data + v * 16);
             e = vec_e0 + v * EPV;
             const unsigned bits = PEN ? bitmap_bits(bm, bit0 + v * EPV, EPV) : 0u;
-            if (RAW) mr = ge_mask<SX>(w, th_r);
             mp = ge_mask<SX>(w, th_p) & ~bits;
         }
-        if (RAW && CAND) warp_append2<SX>(lr, &gs.n_raw, kCandRawGlobal, lp, &gs.n_pen, kCandPenGlobal, mr, mp, w, e);
-        else if (RAW) warp_append<SX>(lr, &gs.n_raw, kCandRawGlobal, mr, w, e, 0);
-        else if (CAND) warp_append<SX>(lp, &gs.n_pen, kCandPenGlobal, mp, w, e, 0);
+        if (CAND) warp_append<SX>(lp, &gs.n_pen, kCandPenGlobal, mp, w, e, 0);
         if (TRACK) {
             while (mp) {
                 const int q = __ffs(mp) - 1;
@@ -424,10 +385,10 @@ __device__ __forceinline__ void flush_vectors(GroupSmem& gs, Cand* lr, Cand* lp,
 
 // ------------------------------------------------------------------ target-logit segments
 struct XState {
-    float m_r, s_r;      // raw running max, sum of 2^((x - m_r)*L2E)
+    float m_r;           // raw running max (NaN-propagating: shows a non-finite logit)
     float m_p, s_t;      // penalised running max, sum of 2^((x' - m_p)*c_l2e)
     int arg;             // lowest index attaining m_p seen by this thread
-    float th_p, th_r;    // candidate thresholds (segment-wide)
+    float th_p;          // candidate threshold (segment-wide)
 };
 
 template <int SX>
@@ -437,10 +398,9 @@ struct XCtx {
     GroupSmem& gs;
     int g, stage;
     const StageMeta& m;
-    bool greedy, need_lp, need_raw, need_cand, need_temp;
+    bool greedy, need_cand, need_temp;
     float f, p, c_l2e;
     Cand* lp;            // the segment's penalised-candidate list (global)
-    Cand* lr;            // the segment's raw-candidate list (global)
 };
 
 // Raw value of element e of the current tile: shared memory for the aligned interior,
@@ -476,25 +436,14 @@ __device__ __forceinline__ void pen_fold(const XCtx<SX>& c, XState& st, float xp
     if (xp >= st.th_p) push(c.lp, &c.gs.n_pen, kCandPenGlobal, xp, e);
 }
 
-// One 16-byte vector: raw statistics over all its elements, penalised statistics over the
+// One 16-byte vector: the raw maximum over all its elements, penalised statistics over the
 // elements without a penalty bit (the penalised ones are folded in by x_entries).
 template <int SX>
 __device__ __forceinline__ void x_vec(const XCtx<SX>& c, XState& st, const uint4& w, int e, unsigned bits,
-                                      unsigned& mask_r, unsigned& mask_p) {
+                                      unsigned& mask_p) {
     constexpr int EPV = 16 / SX;
     const float vm = vec_max<SX>(w);
-    // raw log-sum-exp with a running max (rescale only when the max grows)
-    if (c.need_lp) {
-        if (!(vm <= st.m_r)) {
-            const float nm = max_nan(st.m_r, vm);
-            st.s_r = (st.m_r > -INFINITY && nm == nm) ? st.s_r * ex2_approx((st.m_r - nm) * kL2E) : 0.f;
-            st.m_r = nm;
-        }
-        const float2 t = vec_exp_sum<SX>(w, make_float2(0.f, 0.f), kL2E, st.m_r * kL2E);
-        st.s_r += t.x + t.y;
-    } else {
-        st.m_r = max_nan(st.m_r, vm);
-    }
+    st.m_r = max_nan(st.m_r, vm);
     // penalised max over unpenalised elements
     float vp = vm;
     if (bits != 0u) {
@@ -521,9 +470,8 @@ __device__ __forceinline__ void x_vec(const XCtx<SX>& c, XState& st, const uint4
         const float2 t = vec_exp_sum<SX>(w, make_float2(0.f, 0.f), c.c_l2e, st.m_p * c.c_l2e);
         st.s_t += t.x + t.y;
     }
-    // candidates: raw values for top-n, unpenalised values for top-k (penalised: x_entries);
-    // the caller appends them warp-cooperatively
-    mask_r = (c.need_raw && vm >= st.th_r) ? ge_mask<SX>(w, st.th_r) : 0u;
+    // candidates: unpenalised values for top-k (penalised: x_entries); the caller appends
+    // them warp-cooperatively
     mask_p = (c.need_cand && vp >= st.th_p) ? (ge_mask<SX>(w, st.th_p) & ~bits) : 0u;
 }
 
@@ -605,15 +553,13 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
     return make_uint4(ni, ni, ni, ni);
 }
 
-// The scan of one tile for every row that needs neither the tempered sum nor the overflow
-// path: raw maximum (and with LP the raw sum of 2^((x - m_r)*log2e), in two f32x2
-// accumulators), and one flag bit per vector whose maximum is >= th.  All per-element work
-// on candidates is left to flush_vectors.
-template <int SX, bool LP>
+// The scan of one tile for every row that does not need the tempered sum: raw maximum, and
+// one flag bit per vector whose maximum is >= th.  All per-element work on candidates is
+// left to flush_vectors.
+template <int SX>
 __device__ __forceinline__ unsigned x_scan_flags(XState& st, const unsigned char* data, int gt, int nvec, float th) {
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-    float mrl = st.m_r * kL2E;
     unsigned fl = 0u;
+    float m0 = st.m_r, m1 = -INFINITY;
 #pragma unroll
     for (int i = 0; i < kVecPerThread; i += 2) {
         const int v0 = gt + i * kGroupThreads, v1 = v0 + kGroupThreads;
@@ -622,35 +568,21 @@ __device__ __forceinline__ unsigned x_scan_flags(XState& st, const unsigned char
         const uint4 w0 = *reinterpret_cast<const uint4*>(data + v0 * 16);
         const uint4 w1 = ok1 ? *reinterpret_cast<const uint4*>(data + v1 * 16) : neg_inf_vec<SX>();
         const float vm0 = vec_max<SX>(w0), vm1 = vec_max<SX>(w1);
-        if (LP) {
-            const float vmb = max_nan(vm0, vm1);
-            if (!(vmb <= st.m_r)) {
-                const float nm = max_nan(st.m_r, vmb);
-                const float f = (st.m_r > -INFINITY && nm == nm) ? ex2_approx((st.m_r - nm) * kL2E) : 0.f;
-                st.s_r *= f;
-                acc0 = make_float2(acc0.x * f, acc0.y * f);
-                acc1 = make_float2(acc1.x * f, acc1.y * f);
-                st.m_r = nm;
-                mrl = nm * kL2E;
-            }
-            acc0 = vec_exp_sum<SX>(w0, acc0, kL2E, mrl);
-            acc1 = vec_exp_sum<SX>(w1, acc1, kL2E, mrl);
-        } else {
-            st.m_r = max_nan(st.m_r, max_nan(vm0, vm1));
-        }
+        m0 = max_nan(m0, vm0);
+        m1 = max_nan(m1, vm1);
         // the filler past the end of the tile is never flagged
         fl |= (vm0 >= th ? 1u : 0u) << i;
         fl |= ((ok1 && vm1 >= th) ? 1u : 0u) << (i + 1);
     }
-    if (LP) st.s_r += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    st.m_r = max_nan(m0, m1);
     return fl;
 }
 
-template <int SX, bool PEN, bool RAW>
-__device__ __forceinline__ void x_flush_cand(bool cand, GroupSmem& gs, Cand* lr, Cand* lp, unsigned fl, const unsigned char* data,
+template <int SX, bool PEN>
+__device__ __forceinline__ void x_flush_cand(bool cand, GroupSmem& gs, Cand* lp, unsigned fl, const unsigned char* data,
                                              const unsigned* bm, int vec_e0, int bit0, int gt, XState& st) {
-    if (cand) flush_vectors<SX, PEN, RAW, true, true>(gs, lr, lp, fl, data, bm, vec_e0, bit0, gt, st.th_r, st.th_p, st.m_p, st.arg);
-    else flush_vectors<SX, PEN, RAW, false, true>(gs, lr, lp, fl, data, bm, vec_e0, bit0, gt, st.th_r, st.th_p, st.m_p, st.arg);
+    if (cand) flush_vectors<SX, PEN, true, true>(gs, lp, fl, data, bm, vec_e0, bit0, gt, st.th_p, st.m_p, st.arg);
+    else flush_vectors<SX, PEN, false, true>(gs, lp, fl, data, bm, vec_e0, bit0, gt, st.th_p, st.m_p, st.arg);
 }
 
 // Scan and candidate flush of one tile on the fast path.
@@ -658,17 +590,10 @@ template <int SX>
 __device__ __forceinline__ void x_fast_pass(const XCtx<SX>& c, XState& st, const unsigned char* data,
                                             const unsigned* bm, int gt) {
     const StageMeta& m = c.m;
-    const float th = fminf(st.th_p, st.th_r);
-    const unsigned fl = c.need_lp ? x_scan_flags<SX, true>(st, data, gt, m.nvec, th)
-                                  : x_scan_flags<SX, false>(st, data, gt, m.nvec, th);
+    const unsigned fl = x_scan_flags<SX>(st, data, gt, m.nvec, st.th_p);
     const int bit0 = m.vec_e0 - m.e0;
-    if (m.pen) {
-        if (c.need_raw) x_flush_cand<SX, true, true>(c.need_cand, c.gs, c.lr, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
-        else x_flush_cand<SX, true, false>(c.need_cand, c.gs, c.lr, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
-    } else {
-        if (c.need_raw) x_flush_cand<SX, false, true>(c.need_cand, c.gs, c.lr, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
-        else x_flush_cand<SX, false, false>(c.need_cand, c.gs, c.lr, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
-    }
+    if (m.pen) x_flush_cand<SX, true>(c.need_cand, c.gs, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
+    else x_flush_cand<SX, false>(c.need_cand, c.gs, c.lp, fl, data, bm, m.vec_e0, bit0, gt, st);
 }
 
 template <int SX>
@@ -736,16 +661,13 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
             wr = max_nan(wr, __shfl_xor_sync(0xffffffffu, wr, o));
             wp = max_nan(wp, __shfl_xor_sync(0xffffffffu, wp, o));
         }
-        float thp = 0.f, thr = 0.f;
-        if (c.need_cand || c.need_raw) {
-            float sp = lane_pen, sr = lane_raw;
-            warp_sort2_desc(sp, sr);
-            const int cp = c.need_cand ? (m.top_k + kGroupWarps - 1) / kGroupWarps : 1;
-            const int cr = c.need_raw ? (c.a.n_top + kGroupWarps - 1) / kGroupWarps : 1;
-            thp = __shfl_sync(0xffffffffu, sp, cp - 1);
-            thr = __shfl_sync(0xffffffffu, sr, cr - 1);
+        float thp = 0.f;
+        if (c.need_cand) {
+            float sp = lane_pen, unused = 0.f;
+            warp_sort2_desc(sp, unused);
+            thp = __shfl_sync(0xffffffffu, sp, (m.top_k + kGroupWarps - 1) / kGroupWarps - 1);
         }
-        if (lane == 0) c.gs.red1[warp] = make_float4(wr, wp, thp, thr);
+        if (lane == 0) c.gs.red1[warp] = make_float4(wr, wp, thp, INFINITY);
         group_sync(c.g);
         const float4 r = group_reduce_mmnn(c.gs.red1);
         // The segment starts from the first tile's maxima.  Each lane value above is the
@@ -756,18 +678,16 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
         // segment's penalised maximum and argmax are found among the values >= th_p.
         st.m_r = r.x;
         st.m_p = fast ? -INFINITY : r.y;
-        st.s_r = 0.f;
         st.s_t = 0.f;
         st.arg = 0x7FFFFFFF;
         st.th_p = c.need_cand ? r.z : (fast ? r.y : INFINITY);
-        st.th_r = c.need_raw ? r.w : INFINITY;
     }
 
     // ---- the accumulation / filter pass over this tile.  General path: candidate flags
     // are kept per thread (bit EPV*i+q: element q of the thread's i-th vector) and appended
     // once at the end.
     float unused = 0.f;
-    unsigned long long fr0 = 0ull, fr1 = 0ull, fp0 = 0ull, fp1 = 0ull;
+    unsigned long long fp0 = 0ull, fp1 = 0ull;
     if (fast) {
         x_fast_pass<SX>(c, st, data, bm, gt);
         if (overflow) x_overflow_fast<SX>(c, st, data, bm, gt);
@@ -779,31 +699,19 @@ __device__ void x_tile(const XCtx<SX>& c, XState& st) {
         const uint4 w = *reinterpret_cast<const uint4*>(data + v * 16);
         const int e = m.vec_e0 + v * EPV;
         const unsigned bits = m.pen ? bitmap_bits(bm, e - m.e0, EPV) : 0u;
-        unsigned mr = 0u, mp = 0u;
-        x_vec<SX>(c, st, w, e, bits, mr, mp);
+        unsigned mp = 0u;
+        x_vec<SX>(c, st, w, e, bits, mp);
         if (overflow && bits) x_vec_overflow<SX>(c, st, w, e, bits, false, unused);
         const int sh = i * EPV;
-        if (sh < 64) { fr0 |= static_cast<unsigned long long>(mr) << sh; fp0 |= static_cast<unsigned long long>(mp) << sh; }
-        else { fr1 |= static_cast<unsigned long long>(mr) << (sh - 64); fp1 |= static_cast<unsigned long long>(mp) << (sh - 64); }
+        if (sh < 64) fp0 |= static_cast<unsigned long long>(mp) << sh;
+        else fp1 |= static_cast<unsigned long long>(mp) << (sh - 64);
     }
-    if (!fast && c.need_raw) flush_flags<SX>(c.lr, &c.gs.n_raw, kCandRawGlobal, fr0, fr1, data, m.vec_e0, gt, 0);
     if (!fast && c.need_cand) flush_flags<SX>(c.lp, &c.gs.n_pen, kCandPenGlobal, fp0, fp1, data, m.vec_e0, gt, 0);
     if (gt < 2) {
         const int lo = gt == 0 ? m.e0 : e_tail, hi = gt == 0 ? m.vec_e0 : m.e1;
         for (int e = lo; e < hi; ++e) {
             const float xv = load_x(c.a.x, SX, xrow + e);
-            // raw statistics and raw candidates
-            if (c.need_lp) {
-                if (!(xv <= st.m_r)) {
-                    const float nm = max_nan(st.m_r, xv);
-                    st.s_r = (st.m_r > -INFINITY && nm == nm) ? st.s_r * ex2_approx((st.m_r - nm) * kL2E) : 0.f;
-                    st.m_r = nm;
-                }
-                st.s_r += ex2_approx((xv - st.m_r) * kL2E);
-            } else {
-                st.m_r = max_nan(st.m_r, xv);
-            }
-            if (xv >= st.th_r) push(c.lr, &c.gs.n_raw, kCandRawGlobal, xv, e);
+            st.m_r = max_nan(st.m_r, xv);
             const bool bit = m.pen && bitmap_bit(bm, e - m.e0);
             if (fast) {
                 if (!bit) fold_fast(c, st, xv, e);
@@ -824,16 +732,16 @@ __device__ void x_finish(const XCtx<SX>& c, XState& st) {
     const StageMeta& m = c.m;
     const int gt = threadIdx.x - c.g * kGroupThreads;
     const int lane = threadIdx.x & 31, warp = gt >> 5;
-    float mr = st.m_r, sr = st.s_r, mp = st.m_p, stt = st.s_t;
+    float mr = st.m_r, mp = st.m_p, stt = st.s_t;
     // argmax: lowest index among lanes whose running max equals the warp max
     float wp = mp;
     for (int o = 16; o; o >>= 1) wp = max_nan(wp, __shfl_xor_sync(0xffffffffu, wp, o));
     int arg = (mp == wp) ? st.arg : 0x7FFFFFFF;
     arg = warp_min_i(arg);
-    warp_merge_ms(mr, sr, kL2E);
+    for (int o = 16; o; o >>= 1) mr = max_nan(mr, __shfl_xor_sync(0xffffffffu, mr, o));
     warp_merge_ms(mp, stt, c.c_l2e);
     if (lane == 0) {
-        c.gs.red[warp] = make_float4(mr, sr, mp, stt);
+        c.gs.red[warp] = make_float4(mr, 0.f, mp, stt);
         c.gs.red2[warp] = make_float4(__int_as_float(arg), 0.f, 0.f, 0.f);
     }
     group_sync(c.g);                                      // partials written, every append done
@@ -841,27 +749,26 @@ __device__ void x_finish(const XCtx<SX>& c, XState& st) {
     if (warp == 0) {
         float4 r = lane < kGroupWarps ? c.gs.red[lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
         int ag = lane < kGroupWarps ? __float_as_int(c.gs.red2[lane].x) : 0x7FFFFFFF;
-        float Mr = r.x, Sr = r.y, Mp = r.z, St = r.w;
+        float Mr = r.x, Mp = r.z, St = r.w;
         float Mp_all = Mp;
         for (int o = 16; o; o >>= 1) Mp_all = max_nan(Mp_all, __shfl_xor_sync(0xffffffffu, Mp_all, o));
         ag = (Mp == Mp_all) ? ag : 0x7FFFFFFF;
         ag = warp_min_i(ag);
-        warp_merge_ms(Mr, Sr, kL2E);
+        for (int o = 16; o; o >>= 1) Mr = max_nan(Mr, __shfl_xor_sync(0xffffffffu, Mr, o));
         warp_merge_ms(Mp, St, c.c_l2e);
         if (lane == 0) {
-            const int n_pen = c.gs.n_pen, n_raw = c.gs.n_raw;
+            const int n_pen = c.gs.n_pen;
             TileStats ts;
-            ts.m_raw = Mr; ts.s_raw = Sr; ts.m_pen = Mp; ts.arg_pen = ag; ts.s_temp = St;
+            ts.m_raw = Mr; ts.s_raw = 0.f; ts.m_pen = Mp; ts.arg_pen = ag; ts.s_temp = St;
             ts.flags = 0;
             ts.n_pen = c.need_cand ? n_pen : 0;
-            ts.n_raw = c.need_raw ? n_raw : 0;
             if (c.need_cand && n_pen > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
-            if (c.need_raw && n_raw > kCandRawGlobal) { ts.flags |= kTileOverflowRaw; ts.n_raw = 0; }
-            if (!isfinite(Mr) || !isfinite(Mp)) ts.flags |= kTileBad;
+            // NaN or +inf anywhere shows in the maxima; -inf logits are allowed (zero probability)
+            if (Mr != Mr || Mr == INFINITY || Mp != Mp || Mp == INFINITY) ts.flags |= kTileBad;
             c.a.ts_x[ti] = ts;
             // counters for the next segment: its first append follows its first-tile barrier,
             // which this warp reaches only after this write
-            c.gs.n_pen = 0; c.gs.n_raw = 0;
+            c.gs.n_pen = 0;
         }
     }
 }
@@ -957,8 +864,7 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
         st.mn = fminf(mn0, mn1);
         float m_unused = 0.f;
         int a_unused = 0;
-        flush_vectors<4, false, false, true, false>(gs, nullptr, lp, vfl, data, nullptr, m.vec_e0, 0, gt, INFINITY, th, m_unused,
-                                                    a_unused);
+        flush_vectors<4, false, true, false>(gs, lp, vfl, data, nullptr, m.vec_e0, 0, gt, th, m_unused, a_unused);
     }
 #pragma unroll 2
     for (int i = 0; i < (need_cand ? 0 : kVecPerThread); ++i) {
@@ -1026,13 +932,13 @@ __device__ void q_finish(const Args& a, GroupSmem& gs, int g, const StageMeta& m
             const int n = gs.n_pen;                       // draft segments append no raw entries
             TileStats ts;
             ts.m_raw = Mg; ts.s_raw = t_one ? s : 0.f; ts.m_pen = mnn; ts.arg_pen = 0; ts.s_temp = t_one ? 0.f : s;
-            ts.n_pen = need_cand ? n : 0; ts.n_raw = 0; ts.flags = 0;
+            ts.n_pen = need_cand ? n : 0; ts.pad = 0; ts.flags = 0;
             if (need_cand && n > kCandPenGlobal) { ts.flags |= kTileOverflowPen; ts.n_pen = 0; }
             if (!(mnn >= 0.f) || !(Mg <= 3.0e38f)) ts.flags |= kTileBad;
             a.ts_q[ti] = ts;
             // counters for the next segment: its first append follows its first-tile barrier,
             // which this warp reaches only after this write
-            gs.n_pen = 0; gs.n_raw = 0;
+            gs.n_pen = 0;
         }
     }
 }
@@ -1135,7 +1041,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) { mbar_init(&sm.full[s], 1); mbar_init(&sm.empty[s], kGroupWarps); }
         for (int g = 0; g < kGroups; ++g) {
-            sm.grp[g].n_pen = 0; sm.grp[g].n_raw = 0; sm.grp[g].error = 0;
+            sm.grp[g].n_pen = 0; sm.grp[g].error = 0;
         }
         fence_mbar_init();
     }
@@ -1305,10 +1211,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
                 const bool greedy = !(m.temperature > 0.f);
                 const int k = m.top_k;
                 const long long ti = static_cast<long long>(m.slot) * a.nseg_x + m.seg;
-                XCtx<SX> ctx{a, sm, gs, g, stage, m, greedy, a.want_lp || a.n_top > 0, a.n_top > 0,
+                XCtx<SX> ctx{a, sm, gs, g, stage, m, greedy,
                              !greedy && k > 0 && k < a.V && k <= kMaxCandTopK, !greedy && (k == 0 || k >= a.V),
                              m.frequency, m.presence, (!greedy && (k == 0 || k >= a.V)) ? kL2E / m.temperature : 0.f,
-                             a.cand_x + ti * kCandPenGlobal, a.cand_raw + ti * kCandRawGlobal};
+                             a.cand_x + ti * kCandPenGlobal};
                 x_tile<SX>(ctx, xs);
                 if (last) x_finish<SX>(ctx, xs);
             } else {

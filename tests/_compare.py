@@ -37,6 +37,13 @@ class Tally:
                 f"{self.near_tie_requests} requests; {self.off_float64} GPU results on the other side of a near tie")
 
 
+def _close(got, want, tol):
+    """Element-wise: equal (both -inf included) or within tol."""
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    return (got == want) | (np.abs(got - np.where(np.isfinite(want), want, 0.0)) <= tol) & np.isfinite(want)
+
+
 def _matching(outs, a_g, toks):
     for o in outs:
         if o.accept_len != a_g or not np.array_equal(toks[:a_g], o.tokens[:a_g]):
@@ -85,14 +92,14 @@ def compare(batch, got, want, lp_tol=LOGPROB_TOL, tally=None):
             lp = got["logprobs"][b]
             want_lp = np.array(o.logprobs[: a_g + 1])
             want_lp[a_g] = o.admissible_logprobs[ia]
-            err = np.abs(lp[: a_g + 1] - want_lp)
-            assert np.all(err <= lp_tol), f"request {b}: logprobs {lp[: a_g + 1]} != oracle {want_lp}"
+            assert np.all(_close(lp[: a_g + 1], want_lp, lp_tol)), \
+                f"request {b}: logprobs {lp[: a_g + 1]} != oracle {want_lp}"
             assert np.all(np.isneginf(lp[a_g + 1: W]))
         if "top_ids" in got:
             ti, tl = got["top_ids"][b], got["top_logprobs"][b]
             assert np.array_equal(ti[: a_g + 1], o.top_ids[: a_g + 1]), \
                 f"request {b}: top ids {ti[: a_g + 1]} != oracle {o.top_ids[: a_g + 1]}"
-            assert np.all(np.abs(tl[: a_g + 1] - o.top_logprobs[: a_g + 1]) <= lp_tol), \
+            assert np.all(_close(tl[: a_g + 1], o.top_logprobs[: a_g + 1], lp_tol)), \
                 f"request {b}: top logprobs {tl[: a_g + 1]} != oracle {o.top_logprobs[: a_g + 1]}"
             assert np.all(ti[a_g + 1:] == -1) and np.all(np.isneginf(tl[a_g + 1:]))
     return tally

@@ -509,3 +509,28 @@ def test_subset_batches_equal_the_whole_batch():
         hi, hc = full.history(b)
         oi, oc = one.history(0)
         assert np.array_equal(hi, oi) and np.array_equal(hc, oc)
+
+
+def test_masked_logits_have_zero_probability():
+    """A -inf logit is a token of probability zero: never drawn, never accepted, logprob -inf;
+    NaN, +inf or an all -inf row make the request non-finite."""
+    x = np.array([[0.0, -np.inf, 1.0, 0.5], [2.0, 0.0, -np.inf, -np.inf]], np.float32)
+    q = np.array([[0.1, 0.6, 0.2, 0.1]], np.float32)
+    for u0 in (0.0, 0.3, 0.9):
+        for u1 in (0.0, 0.4, 0.99):
+            r = O.verify_request(one_request(x, q, [1], T=1.0, uniforms=[[u0, u1], [0.0, u1]], n_top=4,
+                                             want_logprobs=True), 0)
+            assert r.status == O.ROW_OK and r.accept_len == 0       # P'(1) = 0: draft 1 is rejected
+            assert r.tokens[0] != 1
+            assert r.top_ids[0].tolist() == [2, 3, 0, 1] and np.isneginf(r.top_logprobs[0][3])
+    g = O.verify_request(one_request(x, q, [2], T=0.0), 0)
+    assert g.accept_len == 1 and g.tokens.tolist() == [2, 0]
+    g = O.verify_request(one_request(x, q, [1], T=0.0), 0)
+    assert g.accept_len == 0 and g.tokens[0] == 2
+    for bad in (np.nan, np.inf):
+        xb = x.copy()
+        xb[1, 1] = bad
+        assert O.verify_request(one_request(xb, q, [2], T=1.0), 0).status == O.ROW_NONFINITE
+    xb = x.copy()
+    xb[0, :] = -np.inf
+    assert O.verify_request(one_request(xb, q, [2], T=1.0), 0).status == O.ROW_NONFINITE

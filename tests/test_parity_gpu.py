@@ -206,3 +206,24 @@ def test_b64k8_full_size(runner):
 def test_b256k16_full_size(runner):
     got = _full_size(runner, "b256k16v262144_mixed")
     assert np.all(got["row_status"] == 0)
+
+
+def test_masked_logits(runner):
+    """Logits of -inf are tokens of probability zero (masked vocabulary): 30% of the tokens
+    masked in half the requests, and a request whose rows keep only three finite logits (its
+    top_logprobs lists run into the masked tokens)."""
+    rows = [row_params(1.0, 0, 1.0, 0.2, 0.1, 3), row_params(0.7, 20, 0.9, 0.0, 0.0, 3),
+            row_params(0.0, 0, 1.0, 0.3, 0.3, 3), row_params(1.0, 5, 1.0, 0.0, 0.0, 3),
+            row_params(0.9, 0, 0.8, 0.0, 0.0, 3), row_params(0.0, 0, 1.0, 0.0, 0.0, 3)]
+    batch = make_batch(B=6, K_max=3, V=5000, logits_dtype="bf16", rows=rows, seed=31, philox_seed=31,
+                       history_len=40, want_logprobs=True, n_top_logprobs=5)
+    rng = np.random.default_rng(31)
+    ninf = np.uint16(0xFF80)                                # bf16 -inf
+    for b in (0, 1, 2):
+        mask = rng.random(batch.V) < 0.3
+        batch.x[b][:, mask] = ninf
+    keep = np.array([7, 1234, 4999])
+    row = np.full(batch.V, ninf, np.uint16)
+    batch.x[5][:, :] = row
+    batch.x[5][:, keep] = batch.x[4][:, keep]
+    _run(runner, batch, "masked logits V=5000")
