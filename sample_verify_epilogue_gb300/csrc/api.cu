@@ -49,7 +49,7 @@ Layout make_layout(const dspark_params_t* p) {
     L.qslots = static_cast<int>(B * Km);
     L.nseg_x = (L.tiles_x + kSegTiles - 1) / kSegTiles;
     L.nseg_q = (L.tiles_q + kSegTiles - 1) / kSegTiles;
-    L.lp_chunks = static_cast<int>((V + kLpChunkBytes / sx - 1) / (kLpChunkBytes / sx));
+    L.lp_chunks = 1;                                   // the logprob pass: one partial per row
     const size_t xt = static_cast<size_t>(L.xslots) * L.nseg_x;
     const size_t qt = static_cast<size_t>(L.qslots) * L.nseg_q;
     const size_t pt = static_cast<size_t>(B) * L.tiles_x;

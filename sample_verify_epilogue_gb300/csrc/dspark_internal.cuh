@@ -38,7 +38,6 @@ constexpr int kMaxCandTopK = 256;                              // top_k above th
 constexpr int kKeptCap = 1024;                                 // truncated support held as a list
 constexpr int kFinalizeThreads = 512;
 constexpr int kMergeCap = 8192;                                // merged candidates per row (smem)
-constexpr int kLpChunkBytes = 32 * 1024;                       // bytes of logits per chunk of the logprob pass
 constexpr int kMaxB = DSPARK_MAX_B;
 
 // ---------------------------------------------------------------- records in the workspace
@@ -46,7 +45,7 @@ enum UnitKind : int { kUnitX = 0, kUnitQ = 1 };
 
 struct Plan {
     int n_units;         // unused
-    int pad[3];          // pad[0]: error flag set by the streaming pass; pad[1]: logprob work counter
+    int pad[3];          // pad[0]: error flag set by the streaming pass
 };
 
 // One segment (consecutive vocab tiles [t0, t1) of one row) with its request's parameters.
@@ -147,7 +146,7 @@ struct Args {
     int B, Km, V, sx, xdtype;
     int tile_x, tiles_x, tile_q, tiles_q, bm_words;
     int nseg_x, nseg_q;    // segments per target / draft row
-    int lp_chunks;         // chunks per row in the logprob pass
+    int lp_chunks;         // partials per row in the logprob pass (one)
     int grid_ss;           // CTAs of the streaming pass
     int max_seg;           // segments per (CTA, group) stream, upper bound
     int n_top, want_lp;
@@ -186,7 +185,7 @@ struct Args {
     QRowOut* qout;         // [qslots]
     ReqOut* req;           // [B]
     int* lp_list;          // [1 + xslots]: count, then the rows (b*W + j) the logprob pass reads
-    int* lp_done;          // [xslots]: chunks of each row done (zeroed by every call)
+    int* lp_done;          // [xslots]: unused by the one-CTA-per-row logprob pass (zeroed by every call)
     LpPartial* lp_part;    // [xslots * lp_chunks]
 };
 

@@ -2,35 +2,32 @@
 // position (mlx-dspark Changelog, [0.2.0] Added, "logprobs / top_logprobs": the raw target
 // log-softmax of each committed token plus the top candidates, gathered on the GPU only when
 // requested).  Only the positions a request emits from (j <= accept length) need them, so
-// they are taken after the draws, from those rows alone: accept_kernel lists the R rows.
+// they are taken after the draws, from those rows alone: accept_kernel lists the rows.
 //
-// Every row is cut into S = max(1, grid / R) chunks, so that the R * S chunks run in one wave
-// of the persistent grid; each CTA takes chunks from a counter.  A chunk CTA streams its logits
-// from HBM in batches of kLpVec 16-byte vectors per thread, the next batch's loads in flight
-// while the current one is reduced, and leaves in the workspace
-//   - the chunk's maximum m and its sum of exp(x - m) (running maximum, the sum rescaled at most
-//     once per batch);
-//   - the chunk's n largest logits by (value descending, id ascending).  After the first batch,
-//     theta = the least over warps of each warp's ceil(n/8)-th largest thread maximum: at least
-//     n distinct logits of that batch reach it, so every one of the chunk's top n does, and the
-//     logits >= theta of every batch are gathered as they stream by; each warp sorts its share
-//     and one warp merges the eight sorted lists.  When ties put more logits >= theta than fit,
-//     the chunk is settled exactly from L2: the n-th largest value v by a bitwise search over
-//     counts, the logits above v, then the lowest ids equal to v.
-// The CTA that completes a row (a counter per row) merges its chunks in a fixed order:
-// LSE = M + log(sum_s S_s exp(m_s - M)) with M the largest m_s, the row's top-n among the
-// chunks' sorted lists, and writes logprob = x[token] - LSE and the top list.  Results do not
-// depend on scheduling.
+// One CTA of 1024 threads per listed row (the launch has one CTA per possible row; the rest
+// return at once).  It streams the row from HBM in batches of kLpVec 16-byte vectors per
+// thread, the next batch's loads in flight while the current one is reduced, for
+//   - the row's maximum m and its sum of exp(x - m) (per thread a running maximum, the sum
+//     rescaled at most once per batch; then a fixed reduction order);
+//   - the row's n largest logits by (value descending, id ascending).  After the first batch,
+//     theta = the least over the 32 warps of each warp's ceil(n/32)-th largest thread maximum:
+//     at least n distinct logits of that batch reach it, so every one of the row's top n does,
+//     and the logits >= theta of every batch are gathered as they stream by; each warp sorts
+//     its share and one warp merges the 32 sorted lists.  When ties put more logits >= theta
+//     than fit, the row is settled exactly from L2: the n-th largest value v by a bitwise
+//     search over counts, the logits above v, then the lowest ids equal to v.
+// It then writes logprob = x[token] - (m + log s) and the top list.  Results do not depend on
+// scheduling.
 #include "block_utils.cuh"
 
 namespace dspark {
 
 namespace {
 
-constexpr int kLpThreads = 256;
+constexpr int kLpThreads = 1024;
 constexpr int kLpWarps = kLpThreads / 32;
 constexpr int kLpCandCap = 4096;
-constexpr int kLpVec = 8;                    // 16-byte vectors per thread and batch
+constexpr int kLpVec = 4;                    // 16-byte vectors per thread and batch
 constexpr int kLpWarpCap = kLpCandCap / kLpWarps;
 constexpr int kLpMergeLists = 256;           // chunk partials the merge copies to shared memory
 constexpr float kL2E = 1.4426950408889634f;
@@ -602,52 +599,25 @@ __device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j,
 }
 
 template <int SX>
-__global__ void __launch_bounds__(kLpThreads, 2) logprob_kernel(Args a) {
+__global__ void __launch_bounds__(kLpThreads, 1) logprob_kernel(Args a) {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char lp_raw[];
     LpSmem& s = *reinterpret_cast<LpSmem*>(lp_raw);
+    if (static_cast<int>(blockIdx.x) >= a.lp_list[0]) return;
     const int W = a.Km + 1;
-    const int R = a.lp_list[0];
-    if (R == 0) return;
-    // chunks per row: all R * S chunks in one wave of this grid, S <= the workspace's capacity
-    const int S = max(1, min(a.lp_chunks, static_cast<int>(gridDim.x) / R));
-    const int chunk = ((a.V + S - 1) / S + 7) / 8 * 8;
-    const int items = R * S;
-    for (;;) {
-        // the next (row, chunk) item, taken from a counter: no CTA idles while items remain
-        if (threadIdx.x == 0) s.item = atomicAdd(&a.plan->pad[1], 1);
-        __syncthreads();
-        const int it = s.item;
-        __syncthreads();
-        if (it >= items) break;
-        const int row = a.lp_list[1 + it / S];            // b * W + j
-        const int c = it % S;
-        const int b = row / W, j = row % W;
-        const long long slot = row;
-        LpPartial* part = a.lp_part + static_cast<long long>(row) * a.lp_chunks;
-        const int c0 = min(a.V, c * chunk), c1 = min(a.V, c0 + chunk);
-        lp_chunk<SX>(a, s, slot, c0, c1, part + c);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            // the block's partial (ordered before this thread by the barrier) is released to the
-            // GPU before the row counter moves
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
-            s.last = atomicAdd(&a.lp_done[row], 1) == S - 1;
-        }
-        __syncthreads();
-        if (s.last) {
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");      // acquire the other chunks' partials
-            lp_merge(a, s, slot, b, j, part, S);
-        }
-        __syncthreads();                                   // shared memory reused by the next item
-    }
+    const int row = a.lp_list[1 + blockIdx.x];            // b * W + j
+    const int b = row / W, j = row % W;
+    LpPartial* part = a.lp_part + row;
+    lp_chunk<SX>(a, s, row, 0, a.V, part);
+    __syncthreads();                                      // the partial (global) is visible to the CTA
+    lp_merge(a, s, row, b, j, part, 1);
 }
 
 }  // namespace
 
 cudaError_t launch_logprobs(const Args& a, cudaStream_t s) {
     const size_t smem = sizeof(LpSmem);
-    const int grid = 2 * a.grid_ss;                        // resident: two CTAs per SM
+    const int grid = a.xslots;                             // one CTA per row that may be listed
     if (a.sx == 2) {
         cudaError_t e = cudaFuncSetAttribute(logprob_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
