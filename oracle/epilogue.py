@@ -40,7 +40,22 @@ Readings taken where the pages are silent (each listed in the design notes):
     from P';
   * logprobs are the raw (unpenalised, untempered, untruncated) log-softmax;
   * a target logit of -inf is a token of zero probability (a masked token); NaN or +inf, or a
-    row with no finite logit, has no distribution and makes the request non-finite.
+    row with no finite logit, has no distribution and makes the request non-finite;
+  * a draft given sparsely (lookup mode's one-hot proposal, or any m (id, probability)
+    pairs) is the dense draft row with zeros elsewhere (Changelog [0.2.0] Added, "--mode
+    lookup": one-hot-proposal speculative sampling); a draft over a reduced vocabulary is
+    widened onto the target vocabulary, target id = draft id + d2t[draft id], before the
+    accept test (Changelog [0.8.0] Added, reduced draft vocabularies);  the widened row then
+    goes through the same temperature and truncation;
+  * a request with an end-of-sequence token stops after the first accepted draft equal to
+    it: the accepted length counts that draft and nothing is drawn after it (Changelog
+    [0.2.0] Fixed, stop when an accepted draft contains eos mid-block);
+  * per-position acceptance counts (Changelog [0.9.0] Added, per-position acceptance with
+    honest denominators): position i is attempted when the request verified its draft i
+    (every earlier draft accepted, no stop before it), accepted when that draft was accepted;
+  * with logprob_mode "penalised", logprobs and top_logprobs are the log-softmax of the
+    penalised logits x' instead of the raw ones (the alternative reading of "raw target
+    log-softmax").
 
 Near ties.  Every discrete decision that floating point takes records a ``Decision``: its
 distance from the threshold, in the threshold's own unit, and the branch the other side
@@ -331,6 +346,9 @@ class RequestResult:
     admissible: np.ndarray = None        # ids the emitted token may be (the drawn id first)
     admissible_logprobs: np.ndarray = None
     flips: dict = field(default_factory=dict)
+    stopped: bool = False                # an accepted draft was the end-of-sequence token
+    attempted: np.ndarray = None         # int [K_max]: drafts verified, by position
+    accepted: np.ndarray = None          # int [K_max]: drafts accepted, by position
 
     @property
     def min_margin(self):
@@ -352,6 +370,36 @@ def bad_logit_row(x32):
     return bool(np.isnan(x).any() or (x == np.inf).any() or not np.isfinite(x).any())
 
 
+def widened_draft(batch, b, i):
+    """Draft probabilities of request b at position i over the target vocabulary (float32):
+    the dense row, or the sparse pairs / reduced-vocabulary row scattered onto V with zeros
+    elsewhere."""
+    if batch.q_layout == "dense":
+        return np.asarray(batch.q[b, i], np.float32)
+    out = np.zeros(batch.V, np.float32)
+    if batch.q_layout == "sparse":
+        out[np.asarray(batch.q_ids[b, i], np.int64)] = batch.q[b, i]
+    else:
+        dv = np.arange(batch.q.shape[-1], dtype=np.int64)
+        out[dv + np.asarray(batch.d2t, np.int64)] = batch.q[b, i]
+    return out
+
+
+def draft_layout_ok(batch, b, K):
+    """Sparse ids of request b in [0, V) and distinct per row; a d2t table mapping every draft
+    id into [0, V) without collisions."""
+    if batch.q_layout == "sparse":
+        for i in range(K):
+            ids = np.asarray(batch.q_ids[b, i], np.int64)
+            if ids.min() < 0 or ids.max() >= batch.V or np.unique(ids).size != ids.size:
+                return False
+    elif batch.q_layout == "reduced":
+        t = np.arange(batch.d2t.size, dtype=np.int64) + np.asarray(batch.d2t, np.int64)
+        if t.min() < 0 or t.max() >= batch.V or np.unique(t).size != t.size:
+            return False
+    return True
+
+
 def _validate(batch, b):
     r = batch.rows[b]
     T, k, p, K = float(r["temperature"]), int(r["top_k"]), float(r["top_p"]), int(r["num_drafts"])
@@ -365,6 +413,8 @@ def _validate(batch, b):
         st |= ROW_BAD_HISTORY
     d = batch.draft_ids[b, :K]
     if d.size and (d.min() < 0 or d.max() >= batch.V):
+        st |= ROW_BAD_DRAFT
+    if T > 0 and K > 0 and not draft_layout_ok(batch, b, K):
         st |= ROW_BAD_DRAFT
     return st
 
@@ -399,6 +449,12 @@ def verify_request(batch, b, truncate=truncate_full_sort, flips=None) -> Request
             qi = batch.q[b, i]
             if not (np.all(np.isfinite(qi)) and qi.min() >= 0.0):
                 return RequestResult(-1, tokens, lps, tids, tlp, status=ROW_NONFINITE, flips=flips)
+    qrows = {}
+
+    def qrow(i):
+        if i not in qrows:
+            qrows[i] = widened_draft(batch, b, i)
+        return qrows[i]
 
     def xp(j):
         return penalised_logits(x[j], count_vector(V, hid, hc, d[:j]), pres, freq)
@@ -413,7 +469,7 @@ def verify_request(batch, b, truncate=truncate_full_sort, flips=None) -> Request
             if kind == "nucleus_p":
                 D, (m_last, m_next) = target_probs(xp(j), T, k, p, truncate, flip=fl)
             else:
-                D, (m_last, m_next) = draft_probs(batch.q[b, j], T, k, p, truncate, flip=fl)
+                D, (m_last, m_next) = draft_probs(qrow(j), T, k, p, truncate, flip=fl)
             decisions.append(Decision(kind, j, m_last, "drop_last"))
             decisions.append(Decision(kind, j, m_next, "keep_next"))
             cache[(kind, j)] = D
@@ -460,21 +516,43 @@ def verify_request(batch, b, truncate=truncate_full_sort, flips=None) -> Request
         if tiny_residual:
             adm = np.union1d(adm, np.nonzero(P > 0)[0])
         adm = np.concatenate(([tok], adm[adm != tok])).astype(np.int64)
+    # per-position acceptance before any stop: drafts 0..a-1 accepted, draft a rejected (a < K)
+    attempted = np.zeros(Km, np.int64)
+    accepted = np.zeros(Km, np.int64)
+    attempted[:min(a + 1, K)] = 1
+    accepted[:a] = 1
+    # an accepted draft equal to the end-of-sequence token ends the request's output there
+    stopped = False
+    eos = -1 if batch.eos_ids is None else int(batch.eos_ids[b])
+    if eos >= 0:
+        hit = np.nonzero(d[:a] == eos)[0]
+        if hit.size:
+            a = int(hit[0]) + 1
+            stopped = True
+            attempted[a:] = 0
+            accepted[a:] = 0
+            adm = np.array([-1], np.int64)
+            # decisions past the stop shape nothing that is emitted
+            decisions = [dc for dc in decisions if dc.pos < a and dc.kind not in ("draw", "residual_mass")]
     tokens[:a] = d[:a]
-    tokens[a] = tok
+    if not stopped:
+        tokens[a] = tok
+    last = a if not stopped else a - 1                       # last emitted position
     adm_lp = None
     if batch.want_logprobs or n > 0:
-        for j in range(a + 1):
-            ls = raw_log_softmax(x[j])
+        for j in range(last + 1):
+            row = xp(j) if batch.logprob_mode == "penalised" else x[j]
+            ls = raw_log_softmax(row)
             lps[j] = ls[tokens[j]]
             if j == a:
                 adm_lp = ls[adm]
             if n > 0:
-                ids = top_n(x[j], n)
+                ids = top_n(row, n)
                 tids[j] = ids
                 tlp[j] = ls[ids]
     return RequestResult(a, tokens, lps, tids, tlp, status=ROW_OK, decisions=decisions, admissible=adm,
-                         admissible_logprobs=adm_lp, flips=flips)
+                         admissible_logprobs=adm_lp, flips=flips, stopped=stopped, attempted=attempted,
+                         accepted=accepted)
 
 
 def outcomes(batch, b, truncate=truncate_full_sort, max_outcomes=16):

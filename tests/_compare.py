@@ -6,7 +6,10 @@ with the emitted tokens its draw admits (a near-tie draw admits the tokens whose
 reach within 1e-6 of u).  A request of the CUDA path is correct iff its accept length and
 tokens are exactly one of those outcomes; its logprobs and top-logprob lists are then
 checked at every emitted position: ids bit for bit, values within LOGPROB_TOL.
-Nothing is exempt: every request of every batch is compared.
+Nothing is exempt: every request of every batch is compared.  A request that stopped on its
+end-of-sequence token emits positions 0..accept_len-1 only (its token at accept_len is -1);
+the per-position acceptance counts of the matched outcomes are summed into the tally, for
+comparison with the device's counters.
 """
 from __future__ import annotations
 
@@ -29,12 +32,17 @@ class Tally:
     decisions: int = 0         # floating-point decisions the oracle took
     near_ties: Counter = field(default_factory=Counter)   # near-tie decisions by kind
     off_float64: int = 0       # requests whose GPU result is not the float64 outcome itself
+    attempted: np.ndarray = None   # per draft position: requests that verified it (matched outcomes)
+    accepted: np.ndarray = None    # per draft position: requests that accepted it
+    stopped: int = 0               # requests stopped by their end-of-sequence token
 
     def line(self, name):
         kinds = ", ".join(f"{k} {v}" for k, v in sorted(self.near_ties.items())) or "none"
+        stop = f"; {self.stopped} stopped at eos" if self.stopped else ""
         return (f"{name}: {self.requests} requests compared, {self.single} with a single correct result; "
                 f"near-tie decisions {sum(self.near_ties.values())} of {self.decisions} ({kinds}) in "
-                f"{self.near_tie_requests} requests; {self.off_float64} GPU results on the other side of a near tie")
+                f"{self.near_tie_requests} requests; {self.off_float64} GPU results on the other side of a near tie"
+                f"{stop}")
 
 
 def _close(got, want, tol):
@@ -60,6 +68,9 @@ def compare(batch, got, want, lp_tol=LOGPROB_TOL, tally=None):
     returns the tally."""
     tally = tally if tally is not None else Tally()
     W = batch.K_max + 1
+    if tally.attempted is None:
+        tally.attempted = np.zeros(batch.K_max, np.int64)
+        tally.accepted = np.zeros(batch.K_max, np.int64)
     for b, outs in want.items():
         base = outs[0]
         st = int(got["row_status"][b])
@@ -88,20 +99,27 @@ def compare(batch, got, want, lp_tol=LOGPROB_TOL, tally=None):
         tally.near_tie_requests += bool(ties)
         tally.single += len(outs) == 1 and base.admissible.size == 1
         tally.off_float64 += not (o is base and ia == 0)
+        tally.attempted += o.attempted
+        tally.accepted += o.accepted
+        tally.stopped += bool(o.stopped)
+        if "stopped" in got:
+            assert bool(got["stopped"][b]) == o.stopped, f"request {b}: stopped {got['stopped'][b]} != {o.stopped}"
+        n_em = a_g if o.stopped else a_g + 1              # emitted positions
         if "logprobs" in got:
             lp = got["logprobs"][b]
-            want_lp = np.array(o.logprobs[: a_g + 1])
-            want_lp[a_g] = o.admissible_logprobs[ia]
-            assert np.all(_close(lp[: a_g + 1], want_lp, lp_tol)), \
-                f"request {b}: logprobs {lp[: a_g + 1]} != oracle {want_lp}"
-            assert np.all(np.isneginf(lp[a_g + 1: W]))
+            want_lp = np.array(o.logprobs[:n_em])
+            if not o.stopped:
+                want_lp[a_g] = o.admissible_logprobs[ia]
+            assert np.all(_close(lp[:n_em], want_lp, lp_tol)), \
+                f"request {b}: logprobs {lp[:n_em]} != oracle {want_lp}"
+            assert np.all(np.isneginf(lp[n_em:W]))
         if "top_ids" in got:
             ti, tl = got["top_ids"][b], got["top_logprobs"][b]
-            assert np.array_equal(ti[: a_g + 1], o.top_ids[: a_g + 1]), \
-                f"request {b}: top ids {ti[: a_g + 1]} != oracle {o.top_ids[: a_g + 1]}"
-            assert np.all(_close(tl[: a_g + 1], o.top_logprobs[: a_g + 1], lp_tol)), \
-                f"request {b}: top logprobs {tl[: a_g + 1]} != oracle {o.top_logprobs[: a_g + 1]}"
-            assert np.all(ti[a_g + 1:] == -1) and np.all(np.isneginf(tl[a_g + 1:]))
+            assert np.array_equal(ti[:n_em], o.top_ids[:n_em]), \
+                f"request {b}: top ids {ti[:n_em]} != oracle {o.top_ids[:n_em]}"
+            assert np.all(_close(tl[:n_em], o.top_logprobs[:n_em], lp_tol)), \
+                f"request {b}: top logprobs {tl[:n_em]} != oracle {o.top_logprobs[:n_em]}"
+            assert np.all(ti[n_em:] == -1) and np.all(np.isneginf(tl[n_em:]))
     return tally
 
 

@@ -114,3 +114,31 @@ def test_near_tie_accept_admits_both_sides():
     got["tokens"][0] = [2, -1]                # rejected, but the residual draw never emits 2 here
     with pytest.raises(AssertionError):
         compare(b, got, want)
+
+
+def test_eos_stop_outcome_and_counts():
+    """A request stopped by its end-of-sequence draft: the stopped result passes, one that
+    ignores the stop (emits the draw) fails, and the tally sums the per-position counts."""
+    import dataclasses
+    x = np.zeros((4, 8), np.float32)
+    for j, t in enumerate([5, 7, 2, 6]):
+        x[j, t] = 3.0
+    b = one_request(x, np.full((3, 8), 1 / 8), [5, 7, 2], T=0.0, want_logprobs=True, n_top=2)
+    b = dataclasses.replace(b, eos_ids=np.array([7], np.int32))
+    want = O.outcomes_batch(b)
+    got = _as_got(b, want)
+    got["stopped"] = np.array([1], np.int32)
+    t = compare(b, got, want)
+    assert t.stopped == 1 and t.attempted.tolist() == [1, 1, 0] and t.accepted.tolist() == [1, 1, 0]
+    bad = {k: v.copy() for k, v in got.items()}
+    bad["tokens"][0, 2] = 2
+    with pytest.raises(AssertionError):
+        compare(b, bad, want)
+    bad = {k: v.copy() for k, v in got.items()}
+    bad["stopped"][0] = 0
+    with pytest.raises(AssertionError):
+        compare(b, bad, want)
+    bad = {k: v.copy() for k, v in got.items()}
+    bad["logprobs"][0, 2] = -1.0
+    with pytest.raises(AssertionError):
+        compare(b, bad, want)

@@ -21,7 +21,15 @@ MUTATIONS = {
     "draft_temperature_missing": ("w = q ** (1.0 / float(T))", "w = q"),
     "bonus_wrong_position": ("        P = dist(\"nucleus_p\", a)\n",
                              "        P = dist(\"nucleus_p\", max(a - 1, 0))\n"),
-    "logprob_penalised": ("            ls = raw_log_softmax(x[j])", "            ls = raw_log_softmax(xp(j))"),
+    "logprob_penalised": ("row = xp(j) if batch.logprob_mode == \"penalised\" else x[j]", "row = xp(j)"),
+    "penalised_mode_ignored": ("row = xp(j) if batch.logprob_mode == \"penalised\" else x[j]", "row = x[j]"),
+    "sparse_ids_ignored": ("out[np.asarray(batch.q_ids[b, i], np.int64)] = batch.q[b, i]",
+                           "out[np.arange(batch.q.shape[-1])] = batch.q[b, i]"),
+    "d2t_sign": ("out[dv + np.asarray(batch.d2t, np.int64)] = batch.q[b, i]",
+                 "out[dv - np.asarray(batch.d2t, np.int64)] = batch.q[b, i]"),
+    "layout_check_skipped": ("if T > 0 and K > 0 and not draft_layout_ok(batch, b, K):", "if False:"),
+    "eos_draft_excluded": ("            a = int(hit[0]) + 1\n", "            a = int(hit[0])\n"),
+    "rejected_position_not_attempted": ("attempted[:min(a + 1, K)] = 1", "attempted[:a] = 1"),
     "draw_margin_in_mass_units": ("return t, float(min(target - lo, C[t] - target) / total)",
                                   "return t, float(min(target - lo, C[t] - target))"),
     "admissible_without_slack": ("(lo < float(u) + eps) & (hi > float(u) - eps)", "(lo <= float(u)) & (hi > float(u))"),
@@ -49,7 +57,8 @@ def test_planted_mistake_is_caught(name, tmp_path):
         oracle.epilogue = m
         import pytest
         sys.exit(pytest.main(['-x', '-q', '-p', 'no:cacheprovider',
-                              {os.path.join(ROOT, 'tests', 'test_oracle_pins.py')!r}]))
+                              {os.path.join(ROOT, 'tests', 'test_oracle_pins.py')!r},
+                              {os.path.join(ROOT, 'tests', 'test_oracle_extensions.py')!r}]))
     """)
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=600)
     assert r.returncode != 0, f"mutation {name} survived:\n{r.stdout[-2000:]}"
