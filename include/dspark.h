@@ -34,7 +34,15 @@
  *     u * total.  An all-zero residual draws from P'_a;
  *   - logprobs: raw (unpenalised, untempered, untruncated) target log-softmax at each
  *     emitted token, and the n largest raw logits (value descending, id ascending) with
- *     their log-softmax (Changelog, [0.2.0] Added, "logprobs / top_logprobs").
+ *     their log-softmax (Changelog, [0.2.0] Added, "logprobs / top_logprobs"); on request
+ *     the same over the penalised logits x' instead (dspark_extras_t.logprob_mode);
+ *   - optional (dspark_extras_t): draft rows given as m (id, probability) pairs, such as the
+ *     one-hot proposal of prompt-lookup drafts (Changelog, [0.2.0] Added, "--mode lookup"),
+ *     or over a reduced draft vocabulary widened through a d2t offset table, target id =
+ *     draft id + d2t[draft id] (Changelog, [0.8.0] Added, reduced draft vocabularies); a
+ *     per-request end-of-sequence token that ends the output at the first accepted draft
+ *     equal to it (Changelog, [0.2.0] Fixed); per-position acceptance counters (Changelog,
+ *     [0.9.0] Added, per-position acceptance with honest denominators).
  *
  * Conventions for every entry point:
  *   - All tensor pointers of dspark_verify_sample are DEVICE pointers owned by the caller.
@@ -73,7 +81,10 @@ typedef enum { DSPARK_BF16 = 0, DSPARK_FP32 = 1 } dspark_dtype_t;
 /* Per-request status bits written to row_status[b] (0 = fine). */
 #define DSPARK_ROW_BAD_PARAMS  1   /* T < 0 or not finite, top_p <= 0 or NaN, top_k < 0,
                                       num_drafts outside [0, K_max], non-finite penalty */
-#define DSPARK_ROW_BAD_DRAFT   2   /* a draft id d[b][i], i < num_drafts, outside [0, V) */
+#define DSPARK_ROW_BAD_DRAFT   2   /* a draft id d[b][i], i < num_drafts, outside [0, V); with
+                                      T > 0, a sparse draft row (i < num_drafts) with an id
+                                      outside [0, V) or a repeated id, or a d2t table that maps
+                                      a draft id outside [0, V) or two draft ids to one target */
 #define DSPARK_ROW_NONFINITE   4   /* a non-finite target logit, a negative / non-finite
                                       draft probability, or a draft row with no mass */
 #define DSPARK_ROW_BAD_HISTORY 8   /* history ids outside [0, V) / not strictly ascending,
@@ -85,6 +96,7 @@ typedef enum { DSPARK_BF16 = 0, DSPARK_FP32 = 1 } dspark_dtype_t;
 #define DSPARK_MAX_V          (1 << 24)
 #define DSPARK_MAX_K          64
 #define DSPARK_MAX_TOP_LOGPROBS 20
+#define DSPARK_MAX_SPARSE_M   256  /* (id, probability) pairs per sparse draft row */
 
 /* Sampling parameters of one request (24 bytes, device array of B). */
 typedef struct {
@@ -105,6 +117,40 @@ typedef struct {
     const int32_t* counts;        /* [nnz] */
 } dspark_counts_t;
 
+/* Layout of the draft input q. */
+typedef enum {
+    DSPARK_Q_DENSE = 0,           /* q [B, K_max, V]: probabilities over the target vocabulary  */
+    DSPARK_Q_SPARSE = 1,          /* q [B, K_max, m] probabilities of the ids q_ids [B, K_max, m];
+                                     every other token has probability 0 (m = 1, q = 1: the
+                                     one-hot proposal of a lookup draft)                         */
+    DSPARK_Q_REDUCED = 2          /* q [B, K_max, Vd] over a draft vocabulary of Vd ids; draft id
+                                     e stands for target id e + d2t[e], every other target id
+                                     has probability 0                                           */
+} dspark_q_layout_t;
+
+typedef enum {
+    DSPARK_LOGPROBS_RAW = 0,      /* log-softmax of the raw target logits x                     */
+    DSPARK_LOGPROBS_PENALISED = 1 /* log-softmax of the penalised logits x' (no temperature)    */
+} dspark_logprob_mode_t;
+
+/* Options beyond the dense call (host struct; its arrays are device pointers, or host pointers
+ * for dspark_verify_sample_host).  A NULL dspark_params_t.extras means: dense q, no
+ * end-of-sequence tokens, no counters, raw logprobs. */
+typedef struct {
+    dspark_q_layout_t q_layout;
+    int32_t q_row_len;            /* sparse: m in 1..DSPARK_MAX_SPARSE_M; reduced: Vd in 1..V;
+                                     dense: ignored                                              */
+    const int32_t* q_ids;         /* sparse: [B, K_max, m] target ids (distinct within a row)    */
+    const int32_t* d2t;           /* reduced: [Vd] offsets                                       */
+    const int32_t* eos_ids;       /* [B] end-of-sequence token per request (< 0: none) or NULL    */
+    int32_t* out_stopped;         /* [B] or NULL: 1 when the request stopped on its eos token    */
+    unsigned long long* pos_counts; /* [2, K_max] or NULL.  ADDED to, never cleared: row 0, i: the
+                                     requests that verified draft i (every earlier draft accepted,
+                                     no stop before it, i < num_drafts); row 1, i: those that
+                                     accepted it.  Zero it once, then it accumulates over calls.  */
+    dspark_logprob_mode_t logprob_mode;
+} dspark_extras_t;
+
 typedef struct {
     int32_t B;                    /* requests, 1..DSPARK_MAX_B                        */
     int32_t K_max;                /* drafted tokens at most, 0..DSPARK_MAX_K          */
@@ -120,23 +166,28 @@ typedef struct {
     void*   stage_events[2];      /* optional cudaEvent_t pair recorded on the stream
                                      right before and right after the streaming-stats
                                      kernel (for its roofline timing); NULL = none     */
+    const dspark_extras_t* extras;  /* host pointer or NULL (see dspark_extras_t)      */
 } dspark_params_t;
 
 /* Scratch bytes dspark_verify_sample needs for these shapes (B, K_max, V, logits_dtype,
- * n_top_logprobs).  Returns 0 if the shapes are unsupported. */
+ * n_top_logprobs, and the draft layout of params->extras).  Returns 0 if the shapes are
+ * unsupported. */
 size_t dspark_workspace_bytes(const dspark_params_t* params);
 
 /*
  * The verify-and-sample epilogue on device buffers.
  *   logits            x [B, K_max+1, V] of params->logits_dtype, 4-byte aligned
- *   q                 [B, K_max, V] fp32; may be NULL when every request is greedy
+ *   q                 [B, K_max, V] fp32 (other layouts: dspark_extras_t), 4-byte aligned;
+ *                     may be NULL when every request is greedy
  *   draft_ids         [B, K_max] int32 (entries past num_drafts are ignored)
  *   counts            history (may be NULL)
  *   uniforms          [B, K_max+1, 2] fp32 in [0, 1): [.., j, 0] accept draw at j,
  *                     [.., j, 1] resample / bonus draw at j
  *   out_accept_len    [B] int32: accepted drafts a (-1 for a request with an error)
  *   out_tokens        [B, K_max+1] int32: d_0..d_{a-1}, then the drawn token, then -1
- *   out_logprobs      [B, K_max+1] fp32 or NULL; -inf past the emitted token
+ *                     (a request stopped on its eos token: d_0..d_{a-1} with d_{a-1} = eos,
+ *                     then -1; nothing is drawn)
+ *   out_logprobs      [B, K_max+1] fp32 or NULL; -inf past the last emitted token
  *   out_top_ids       [B, K_max+1, n_top_logprobs] int32 or NULL; -1 past the emitted token
  *   out_top_logprobs  [B, K_max+1, n_top_logprobs] fp32 or NULL; -inf past the emitted token
  */
@@ -151,8 +202,9 @@ size_t dspark_host_workspace_bytes(const dspark_params_t* params, int64_t counts
 
 /*
  * The same epilogue from HOST buffers (same layouts as above; pinned host memory gives
- * full copy bandwidth).  params->rows, params->row_status and the dspark_counts_t arrays
- * are HOST pointers here; params->workspace is a device buffer of at least
+ * full copy bandwidth).  params->rows, params->row_status, the dspark_counts_t arrays and the
+ * arrays of params->extras are HOST pointers here (pos_counts is read, added to and written
+ * back); params->workspace is a device buffer of at least
  * dspark_host_workspace_bytes.  The call copies the inputs to the device, runs the
  * epilogue, copies the outputs back and synchronises params->stream before returning.
  */

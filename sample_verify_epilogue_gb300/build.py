@@ -67,5 +67,35 @@ def build(verbose: bool = False, force: bool = False) -> str:
     return LIB
 
 
+def build_variant(name: str, defines, sources) -> str:
+    """A test build: ``sources`` recompiled with ``defines`` (the other objects shared with
+    libdspark.so) and linked into lib/libdspark_<name>.so; returns its path."""
+    build()
+    vdir = os.path.join(BUILD, name)
+    os.makedirs(vdir, exist_ok=True)
+    headers = [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith(".cuh")]
+    headers.append(os.path.join(os.path.dirname(PKG), "include", "dspark.h"))
+    cc = nvcc()
+    objs = []
+    for src in SOURCES:
+        if src in sources:
+            s = os.path.join(CSRC, src)
+            o = os.path.join(vdir, src.replace(".cu", ".o"))
+            if _stale(o, [s] + headers):
+                r = subprocess.run([cc, *ARCH, *FLAGS, *defines, "-c", s, "-o", o], capture_output=True, text=True)
+                if r.returncode != 0:
+                    raise RuntimeError(f"nvcc failed on {src} ({name}):\n{r.stdout}\n{r.stderr}")
+            objs.append(o)
+        else:
+            objs.append(os.path.join(BUILD, src.replace(".cu", ".o")))
+    lib = os.path.join(LIBDIR, f"libdspark_{name}.so")
+    if _stale(lib, objs):
+        r = subprocess.run([cc, *ARCH, "-shared", "-o", lib + ".tmp", *objs], capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed ({name}):\n{r.stdout}\n{r.stderr}")
+        os.replace(lib + ".tmp", lib)
+    return lib
+
+
 if __name__ == "__main__":
     print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))

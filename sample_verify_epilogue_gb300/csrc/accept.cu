@@ -11,7 +11,13 @@
 // the smallest id whose cumulative mass exceeds u * total.  Whole-vocabulary supports are
 // left to finish_kernel.
 //
-// The request's emitted positions j <= a are listed for the logprob pass (logprob_kernel).
+// A request with an end-of-sequence token stops at the first accepted draft equal to it: its
+// accepted length counts that draft, and nothing is drawn (mlx-dspark Changelog, [0.2.0]
+// Fixed: stop when an accepted draft is eos mid-block).  Per-position counters record, for
+// each draft position, the requests that verified it and those that accepted it (Changelog,
+// [0.9.0] Added: per-position acceptance with honest denominators).
+//
+// The request's emitted positions are listed for the logprob pass (logprob_kernel).
 //
 // finish_kernel: one CTA per request.  Whole-row inverse-CDF draws (every thread sums the
 // weights of a contiguous range of ids, a block scan of those sums finds the range holding
@@ -58,7 +64,7 @@ __device__ __forceinline__ double target_prob_of_draft(const Args& a, const XRow
 
 __device__ __forceinline__ double draft_prob(const Args& a, const QRowOut& qo, int b, int i, int t, bool t_one) {
     const long long qs = static_cast<long long>(b) * a.Km + i;
-    const float qv = __ldg(a.q + qs * a.V + t);
+    const float qv = draft_value(a, qs, t);
     if (!(qv >= qo.tau)) return 0.0;
     return static_cast<double>(draft_weight(qv, qo.qmax, qo.inv_t, t_one)) / qo.Z;
 }
@@ -76,6 +82,8 @@ __device__ void write_error(const Args& a, int b, int st) {
     }
     if (tid == 0) {
         a.out_accept[b] = -1;
+        a.row_status[b] = st;
+        if (a.out_stopped) a.out_stopped[b] = 0;
         a.req[b] = ReqOut{-1, 0, st, 0};
     }
 }
@@ -86,9 +94,15 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
     AccSmem& s = *reinterpret_cast<AccSmem*>(acc_raw);
     const int b = blockIdx.x, tid = threadIdx.x;
     int st = a.row_status[b];
+    const dspark_row_params_t r = a.rows[b];
+    // a d2t table that does not invert makes every sampled request with drafts invalid
+    if (a.q_layout == kQReduced && a.plan->pad[1] && !(st & DSPARK_ROW_BAD_PARAMS) && r.temperature > 0.f &&
+        r.num_drafts > 0)
+        st |= DSPARK_ROW_BAD_DRAFT;
+    // an invalid request reports what is wrong with its inputs, not what its rows then gave
+    if (st & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_HISTORY | DSPARK_ROW_BAD_DRAFT)) st &= ~DSPARK_ROW_NONFINITE;
     if (a.plan->pad[0]) st |= DSPARK_ROW_INTERNAL;
     if (st) { write_error(a, b, st); return; }
-    const dspark_row_params_t r = a.rows[b];
     const int K = r.num_drafts;
     const bool greedy = !(r.temperature > 0.f);
     const bool t_one = r.temperature == 1.f;
@@ -114,12 +128,27 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
     __syncthreads();
     int first = K;
     if (tid < K && !s.acc[tid]) first = tid;
-    const int acc_len = block_min_i(first, s.iwarp);
-    // ---- the emitted token at position acc_len
+    const int verified = block_min_i(first, s.iwarp);     // accepted drafts before any stop
+    // ---- end-of-sequence stop: the first accepted draft equal to the request's eos token
+    const int eos = a.eos ? a.eos[b] : -1;
+    int stop_at = W;
+    if (eos >= 0 && tid < verified && a.d[qs0 + tid] == eos) stop_at = tid;
+    stop_at = block_min_i(stop_at, s.iwarp);
+    const bool stopped = stop_at < verified;
+    const int acc_len = stopped ? stop_at + 1 : verified;
+    // ---- per-position counters: verified positions (the first rejected one included), accepted ones
+    if (a.pos_counts && tid < K) {
+        const bool attempted = stopped ? tid < acc_len : tid <= verified;
+        if (attempted) atomicAdd(a.pos_counts + tid, 1ull);
+        if (tid < acc_len) atomicAdd(a.pos_counts + a.Km + tid, 1ull);
+    }
+    // ---- the emitted token at position acc_len (none after a stop)
     int draw = 0;
     int tok = -1;
     const XRowOut xa = a.xout[xs0 + acc_len];
-    if (greedy) {
+    if (stopped) {
+        // nothing to draw
+    } else if (greedy) {
         tok = xa.argmax;
     } else if (xa.mode == kModeList) {
         const int n = xa.n_kept;
@@ -172,10 +201,12 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
     }
     if (tid == 0) {
         a.out_accept[b] = acc_len;
-        a.req[b] = ReqOut{acc_len, draw, 0, 0};
+        if (a.out_stopped) a.out_stopped[b] = stopped ? 1 : 0;
+        a.req[b] = ReqOut{acc_len, draw, 0, stopped ? 1 : 0};
         if (a.want_lp || a.n_top > 0) {                     // rows of the logprob pass
-            const int base = atomicAdd(&a.lp_list[0], acc_len + 1);
-            for (int j = 0; j <= acc_len; ++j) a.lp_list[1 + base + j] = static_cast<int>(xs0) + j;
+            const int n_em = stopped ? acc_len : acc_len + 1;
+            const int base = atomicAdd(&a.lp_list[0], n_em);
+            for (int j = 0; j < n_em; ++j) a.lp_list[1 + base + j] = static_cast<int>(xs0) + j;
         }
     }
 }
@@ -187,6 +218,8 @@ struct FinishSmem {
     double dwarp[33];
     double th_ex[kFinishThreads + 1];
     double th_sum[kFinishThreads];
+    int sp_ids[DSPARK_MAX_SPARSE_M];      // a sparse draft row, ids ascending
+    float sp_val[DSPARK_MAX_SPARSE_M];
     int found_chunk;
     int tok;
 };
@@ -200,67 +233,24 @@ struct DrawCtx {
     bool residual, t_one, pen, use_p_only;
     float f, p;
     float inv_zp, inv_zq;      // 1/Z of the target and draft supports (Z lies in [1, V])
+    const int* sp_ids;         // sparse draft row (shared memory), ids ascending
+    const float* sp_val;
+    int sp_m;
 };
 
-// Count of token `tok` at the draw position (history + own draft prefix), from the request's
-// penalty index in global memory: the tile's sorted history entries by binary search, then
-// its draft-only entries; an overflowed tile looks the history up directly.
-__device__ int draw_count(const DrawCtx& c, int tok) {
-    const Args& a = *c.a;
-    const long long pt = static_cast<long long>(c.b) * a.tiles_x + tok / a.tile_x;
-    const PenHdr h = a.pen_hdr[pt];
-    if (!h.overflow) {
-        const PenEntry* ent = a.pen_ent + pt * kPenCap;
-        const int nh = h.pad[0];
-        int l = 0, hi = nh;
-        while (l < hi) { const int m = (l + hi) >> 1; if (ent[m].token < tok) l = m + 1; else hi = m; }
-        int e = -1;
-        if (l < nh && ent[l].token == tok) e = l;
-        else for (int k = nh; k < h.n; ++k) if (ent[k].token == tok) { e = k; break; }
-        if (e < 0) return 0;
-        const PenEntry pe = ent[e];
-        const unsigned long long mask = (static_cast<unsigned long long>(pe.mask_hi) << 32) | pe.mask_lo;
-        const unsigned long long low = (c.row_j >= 64) ? ~0ull : ((1ull << c.row_j) - 1ull);
-        return pe.base + __popcll(mask & low);
-    }
-    int base = 0;
-    const int hlo = a.h_off ? a.h_off[c.b] : 0, hhi = a.h_off ? a.h_off[c.b + 1] : 0;
-    int l = hlo, hi = hhi;
-    while (l < hi) { const int m = (l + hi) >> 1; if (a.h_ids[m] < tok) l = m + 1; else hi = m; }
-    if (l < hhi && a.h_ids[l] == tok) base = a.h_cnt[l];
-    return base + prefix_count(a, c.b, c.row_j, tok);
-}
-
-// Penalty bit of token t of the draw row.
-__device__ __forceinline__ bool pen_bit(const DrawCtx& c, int t) {
-    const Args& a = *c.a;
-    const int tile = t / a.tile_x, tl = t - tile * a.tile_x;
-    const long long pt = static_cast<long long>(c.b) * a.tiles_x + tile;
-    return (a.pen_bm[pt * a.bm_words + (tl >> 5)] >> (tl & 31)) & 1u;
-}
-
-// Penalty bits of tokens [e0, e0 + n), n <= 16 (bit q: token e0 + q), one or two bitmap words
-// per tile the range touches.
-__device__ __forceinline__ unsigned pen_bits16(const DrawCtx& c, int e0, int n) {
-    const Args& a = *c.a;
-    unsigned bits = 0u;
-    for (int e = e0; e < e0 + n;) {
-        const int tile = e / a.tile_x, tl = e - tile * a.tile_x;
-        const int cnt = min(e0 + n - e, a.tile_x - tl);
-        const unsigned* bm = a.pen_bm + (static_cast<long long>(c.b) * a.tiles_x + tile) * a.bm_words;
-        const int w0 = tl >> 5, sh = tl & 31;
-        unsigned long long win = bm[w0];
-        if (sh + cnt > 32) win |= static_cast<unsigned long long>(bm[w0 + 1]) << 32;
-        bits |= (static_cast<unsigned>(win >> sh) & ((1u << cnt) - 1u)) << (e - e0);
-        e += cnt;
-    }
-    return bits;
+// Draft input of token t at the draw row: a binary search of the staged sparse row, else the
+// dense or reduced row.
+__device__ __forceinline__ float draw_q(const DrawCtx& c, int t) {
+    if (c.a->q_layout != kQSparse) return draft_value(*c.a, c.qslot, t);
+    int l = 0, h = c.sp_m;
+    while (l < h) { const int m = (l + h) >> 1; if (c.sp_ids[m] < t) l = m + 1; else h = m; }
+    return (l < c.sp_m && c.sp_ids[l] == t) ? c.sp_val[l] : 0.f;
 }
 
 // Residual (or target) weight of token t of the draw row.  Per element in float (FP64 is
 // slow on this part); sums over elements are compensated or taken in double.
 __device__ __forceinline__ float draw_weight_of(const DrawCtx& c, int t, float xv, float qv, bool penalised) {
-    if (penalised) xv = penalise(xv, draw_count(c, t), c.f, c.p);
+    if (penalised) xv = penalise(xv, token_count(*c.a, c.b, c.row_j, t), c.f, c.p);
     float P = 0.f;
     if (xv >= c.xo.tau) P = target_weight(xv, c.xo.m_pen, c.xo.c_l2e) * c.inv_zp;
     if (!c.residual || c.use_p_only) return P;
@@ -280,9 +270,9 @@ __device__ double range_sum(const DrawCtx& c, int r0, int r1) {
         for (int q = 0; q < 16; ++q) {
             const int e = e0 + q;
             xv[q] = e < r1 ? load_x(a.x, a.sx, c.xslot * a.V + e) : -INFINITY;
-            qv[q] = (need_q && e < r1) ? __ldg(a.q + c.qslot * a.V + e) : 0.f;
+            qv[q] = (need_q && e < r1) ? draw_q(c, e) : 0.f;
         }
-        const unsigned pb = c.pen ? pen_bits16(c, e0, min(16, r1 - e0)) : 0u;
+        const unsigned pb = c.pen ? pen_bits_range(a, c.b, e0, min(16, r1 - e0)) : 0u;
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
             const float w = e0 + q < r1 ? draw_weight_of(c, e0 + q, xv[q], qv[q], (pb >> q) & 1u) : 0.f;
@@ -344,8 +334,9 @@ __device__ int whole_row_draw(FinishSmem& s, DrawCtx& c, float u) {
             const int e = base + tid;
             float w = 0.f;
             if (e < o1) {
-                const float qv = (c.residual && !c.use_p_only) ? __ldg(a.q + c.qslot * a.V + e) : 0.f;
-                w = draw_weight_of(c, e, load_x(a.x, a.sx, c.xslot * a.V + e), qv, c.pen && pen_bit(c, e));
+                const float qv = (c.residual && !c.use_p_only) ? draw_q(c, e) : 0.f;
+                w = draw_weight_of(c, e, load_x(a.x, a.sx, c.xslot * a.V + e), qv,
+                                   c.pen && (pen_bits_range(a, c.b, e, 1) & 1u));
             }
             __syncthreads();
             s.th_sum[tid] = static_cast<double>(w);
@@ -393,14 +384,32 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(Args a) {
         c.p = r.presence_penalty;
         c.inv_zp = c.xo.Z > 0.0 ? static_cast<float>(1.0 / c.xo.Z) : 0.f;
         c.inv_zq = (c.residual && c.qo.Z > 0.0) ? static_cast<float>(1.0 / c.qo.Z) : 0.f;
+        c.sp_ids = s.sp_ids;
+        c.sp_val = s.sp_val;
+        c.sp_m = 0;
+        if (c.residual && a.q_layout == kQSparse) {
+            // stage the sparse row sorted by id (ids of a valid row are distinct): rank = ids below
+            const int m = a.Lq;
+            const int* ids = a.q_ids + c.qslot * m;
+            for (int e = tid; e < m; e += blockDim.x) {
+                const int id = ids[e];
+                int rank = 0;
+                for (int k = 0; k < m; ++k) rank += ids[k] < id;
+                s.sp_ids[rank] = id;
+                s.sp_val[rank] = a.q[c.qslot * m + e];
+            }
+            c.sp_m = m;
+            __syncthreads();
+        }
         const int tok = whole_row_draw(s, c, a.u[(xs0 + acc_len) * 2 + 1]);
         if (tid == 0) a.out_tokens[xs0 + acc_len] = tok;
         __syncthreads();
     }
-    // ---- logprob outputs past the emitted token (the emitted positions: logprob_kernel)
+    // ---- logprob outputs past the last emitted token (the emitted positions: logprob_kernel)
+    const int n_em = ro.stopped ? acc_len : acc_len + 1;
     if (a.out_lp)
-        for (int j = acc_len + 1 + tid; j < W; j += blockDim.x) a.out_lp[xs0 + j] = -INFINITY;
-    for (int e = (acc_len + 1) * a.n_top + tid; e < W * a.n_top; e += blockDim.x) {
+        for (int j = n_em + tid; j < W; j += blockDim.x) a.out_lp[xs0 + j] = -INFINITY;
+    for (int e = n_em * a.n_top + tid; e < W * a.n_top; e += blockDim.x) {
         if (a.out_top_ids) a.out_top_ids[xs0 * a.n_top + e] = -1;
         if (a.out_top_lp) a.out_top_lp[xs0 * a.n_top + e] = -INFINITY;
     }

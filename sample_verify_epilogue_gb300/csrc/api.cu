@@ -16,12 +16,24 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 constexpr int kMaxGrid = 1024;           // streaming CTAs on any device (an SM count bound)
 
+// The draft layout of a call (dense unless params->extras says otherwise).
+struct QOpts {
+    int layout;          // QLayout
+    int Lq;              // entries of one draft row
+};
+
+QOpts q_opts(const dspark_params_t* p) {
+    const dspark_extras_t* x = p->extras;
+    if (!x || x->q_layout == DSPARK_Q_DENSE) return QOpts{kQDense, p->V};
+    return QOpts{x->q_layout == DSPARK_Q_SPARSE ? kQSparse : kQReduced, x->q_row_len};
+}
+
 struct Layout {
-    int tile_x, tiles_x, tile_q, tiles_q, bm_words, xslots, qslots, nseg_x, nseg_q, lp_chunks;
+    int tile_x, tiles_x, tile_q, tiles_q, bm_words, xslots, qslots, nseg_x, nseg_q, lp_chunks, Lq;
     long long seg_max;
     size_t off_plan, off_req_n, off_fin_list, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_q;
     size_t off_pen_hdr, off_pen_bm, off_pen_ent, off_draft_base, off_xout, off_kept, off_qout, off_req;
-    size_t off_lp_part;
+    size_t off_lp_part, off_t2d;
     size_t zero_bytes;   // the call record cleared by every call: plan, logprob row counters, list count
     size_t total;
 };
@@ -33,6 +45,16 @@ bool shapes_ok(const dspark_params_t* p) {
     if (p->V < 1 || p->V > DSPARK_MAX_V) return false;
     if (p->logits_dtype != DSPARK_BF16 && p->logits_dtype != DSPARK_FP32) return false;
     if (p->n_top_logprobs < 0 || p->n_top_logprobs > DSPARK_MAX_TOP_LOGPROBS) return false;
+    if (const dspark_extras_t* x = p->extras) {
+        if (x->logprob_mode != DSPARK_LOGPROBS_RAW && x->logprob_mode != DSPARK_LOGPROBS_PENALISED) return false;
+        if (x->q_layout == DSPARK_Q_SPARSE) {
+            if (x->q_row_len < 1 || x->q_row_len > DSPARK_MAX_SPARSE_M) return false;
+        } else if (x->q_layout == DSPARK_Q_REDUCED) {
+            if (x->q_row_len < 1 || x->q_row_len > p->V) return false;
+        } else if (x->q_layout != DSPARK_Q_DENSE) {
+            return false;
+        }
+    }
     return true;
 }
 
@@ -43,7 +65,9 @@ Layout make_layout(const dspark_params_t* p) {
     L.tile_x = sx == 2 ? kTileBf16 : kTileF32;
     L.tile_q = kTileF32;
     L.tiles_x = static_cast<int>((V + L.tile_x - 1) / L.tile_x);
-    L.tiles_q = static_cast<int>((V + L.tile_q - 1) / L.tile_q);
+    const QOpts qo = q_opts(p);
+    L.Lq = qo.Lq;
+    L.tiles_q = static_cast<int>((static_cast<long long>(L.Lq) + L.tile_q - 1) / L.tile_q);
     L.bm_words = ((L.tile_x + 31) / 32 + 3) / 4 * 4;
     L.xslots = static_cast<int>(B * (Km + 1));
     L.qslots = static_cast<int>(B * Km);
@@ -76,6 +100,7 @@ Layout make_layout(const dspark_params_t* p) {
     L.off_qout = take(static_cast<size_t>(L.qslots) * sizeof(QRowOut) + 16);
     L.off_req = take(static_cast<size_t>(B) * sizeof(ReqOut));
     L.off_lp_part = take(static_cast<size_t>(L.xslots) * L.lp_chunks * sizeof(LpPartial));
+    L.off_t2d = take(qo.layout == kQReduced ? static_cast<size_t>(V) * sizeof(int) : 0);
     L.total = o;
     return L;
 }
@@ -97,6 +122,11 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
         return DSPARK_ERR_INVALID_ARG;
     const bool has_hist = counts && counts->row_offsets;
     if (has_hist && (!counts->token_ids || !counts->counts)) return DSPARK_ERR_INVALID_ARG;
+    const dspark_extras_t* ex = p->extras;
+    const QOpts qo = q_opts(p);
+    if (qo.layout == kQSparse && q && (!ex->q_ids || reinterpret_cast<uintptr_t>(ex->q_ids) % 4))
+        return DSPARK_ERR_INVALID_ARG;
+    if (qo.layout == kQReduced && q && !ex->d2t) return DSPARK_ERR_INVALID_ARG;
     const Layout L = make_layout(p);
     if (!p->workspace || p->workspace_bytes < L.total) return DSPARK_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(p->workspace) % kAlign) return DSPARK_ERR_WORKSPACE;
@@ -107,6 +137,13 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     a.B = p->B; a.Km = p->K_max; a.V = p->V; a.sx = sx; a.xdtype = p->logits_dtype;
     a.tile_x = L.tile_x; a.tiles_x = L.tiles_x; a.tile_q = L.tile_q; a.tiles_q = L.tiles_q; a.bm_words = L.bm_words;
     a.nseg_x = L.nseg_x; a.nseg_q = L.nseg_q; a.lp_chunks = L.lp_chunks;
+    a.Lq = L.Lq; a.q_layout = qo.layout;
+    a.lp_pen = (ex && ex->logprob_mode == DSPARK_LOGPROBS_PENALISED) ? 1 : 0;
+    a.q_ids = ex ? ex->q_ids : nullptr;
+    a.d2t = ex ? ex->d2t : nullptr;
+    a.eos = ex ? ex->eos_ids : nullptr;
+    a.out_stopped = ex ? ex->out_stopped : nullptr;
+    a.pos_counts = (ex && p->K_max > 0) ? ex->pos_counts : nullptr;
     a.n_top = p->n_top_logprobs; a.want_lp = p->want_logprobs ? 1 : 0;
     a.xslots = L.xslots; a.qslots = L.qslots;
     a.x = logits; a.q = q; a.d = draft_ids; a.rows = p->rows;
@@ -135,6 +172,7 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     a.lp_done = reinterpret_cast<int*>(a.plan + 1);
     a.lp_list = a.lp_done + L.xslots;
     a.lp_part = at<LpPartial>(ws, L.off_lp_part);
+    a.t2d = qo.layout == kQReduced ? at<int>(ws, L.off_t2d) : nullptr;
 
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;
@@ -145,6 +183,8 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
 
     if (cudaMemsetAsync(p->row_status, 0, sizeof(int32_t) * p->B, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (cudaMemsetAsync(a.plan, 0, L.zero_bytes, s) != cudaSuccess) return DSPARK_ERR_CUDA;
+    if (a.t2d && cudaMemsetAsync(a.t2d, 0xFF, sizeof(int) * static_cast<size_t>(p->V), s) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
     if (launch_prep(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     cudaEvent_t ev0 = static_cast<cudaEvent_t>(p->stage_events[0]);
     cudaEvent_t ev1 = static_cast<cudaEvent_t>(p->stage_events[1]);
@@ -192,7 +232,8 @@ dspark_status_t dspark_verify_sample(const void* logits, const float* q, const i
 
 namespace {
 struct HostStage {
-    size_t x, q, d, rows, hoff, hids, hcnt, u, acc, tok, lp, tid, tlp, st, total;
+    size_t x, q, d, rows, hoff, hids, hcnt, u, acc, tok, lp, tid, tlp, st;
+    size_t qids, d2t, eos, stopped, counts, total;
 };
 HostStage host_stage(const dspark_params_t* p, int64_t nnz, size_t base) {
     HostStage h{};
@@ -200,8 +241,10 @@ HostStage host_stage(const dspark_params_t* p, int64_t nnz, size_t base) {
     const size_t sx = p->logits_dtype == DSPARK_BF16 ? 2 : 4;
     size_t o = base;
     auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
+    const QOpts qo = q_opts(p);
+    const size_t Lq = static_cast<size_t>(qo.Lq);
     h.x = take(B * W * V * sx);
-    h.q = take(B * Km * V * 4);
+    h.q = take(B * Km * Lq * 4);
     h.d = take(B * Km * 4 + 4);
     h.rows = take(B * sizeof(dspark_row_params_t));
     h.hoff = take((B + 1) * 4);
@@ -214,6 +257,11 @@ HostStage host_stage(const dspark_params_t* p, int64_t nnz, size_t base) {
     h.tid = take(B * W * n * 4 + 4);
     h.tlp = take(B * W * n * 4 + 4);
     h.st = take(B * 4);
+    h.qids = take(qo.layout == kQSparse ? B * Km * Lq * 4 : 0);
+    h.d2t = take(qo.layout == kQReduced ? Lq * 4 : 0);
+    h.eos = take(B * 4);
+    h.stopped = take(B * 4);
+    h.counts = take(2 * Km * 8 + 8);
     h.total = o;
     return h;
 }
@@ -250,8 +298,17 @@ dspark_status_t dspark_verify_sample_host(const void* logits, const float* q, co
     auto d2h = [&](void* dst, size_t off, size_t bytes) {
         return bytes == 0 || cudaMemcpyAsync(dst, ws + off, bytes, cudaMemcpyDeviceToHost, s) == cudaSuccess;
     };
+    const dspark_extras_t* ex = params->extras;
+    const QOpts qo = q_opts(params);
+    const size_t Lq = static_cast<size_t>(qo.Lq);
+    if (qo.layout == kQSparse && q && !ex->q_ids) return DSPARK_ERR_INVALID_ARG;
+    if (qo.layout == kQReduced && q && !ex->d2t) return DSPARK_ERR_INVALID_ARG;
     bool ok = h2d(h.x, logits, B * W * V * sx);
-    if (q) ok = ok && h2d(h.q, q, B * Km * V * 4);
+    if (q) ok = ok && h2d(h.q, q, B * Km * Lq * 4);
+    if (q && qo.layout == kQSparse) ok = ok && h2d(h.qids, ex->q_ids, B * Km * Lq * 4);
+    if (q && qo.layout == kQReduced) ok = ok && h2d(h.d2t, ex->d2t, Lq * 4);
+    if (ex && ex->eos_ids) ok = ok && h2d(h.eos, ex->eos_ids, B * 4);
+    if (ex && ex->pos_counts && Km) ok = ok && h2d(h.counts, ex->pos_counts, 2 * Km * 8);
     if (Km) ok = ok && h2d(h.d, draft_ids, B * Km * 4);
     ok = ok && h2d(h.rows, params->rows, B * sizeof(dspark_row_params_t));
     if (has_hist) {
@@ -270,6 +327,16 @@ dspark_status_t dspark_verify_sample_host(const void* logits, const float* q, co
     dp.rows = reinterpret_cast<const dspark_row_params_t*>(ws + h.rows);
     dp.row_status = reinterpret_cast<int32_t*>(ws + h.st);
     dp.workspace_bytes = dev;
+    dspark_extras_t dx{};
+    if (ex) {
+        dx = *ex;
+        dx.q_ids = qo.layout == kQSparse ? reinterpret_cast<const int32_t*>(ws + h.qids) : nullptr;
+        dx.d2t = qo.layout == kQReduced ? reinterpret_cast<const int32_t*>(ws + h.d2t) : nullptr;
+        dx.eos_ids = ex->eos_ids ? reinterpret_cast<const int32_t*>(ws + h.eos) : nullptr;
+        dx.out_stopped = ex->out_stopped ? reinterpret_cast<int32_t*>(ws + h.stopped) : nullptr;
+        dx.pos_counts = ex->pos_counts ? reinterpret_cast<unsigned long long*>(ws + h.counts) : nullptr;
+        dp.extras = &dx;
+    }
     dspark_status_t st = run(ws + h.x, q ? reinterpret_cast<const float*>(ws + h.q) : nullptr,
                              Km ? reinterpret_cast<const int32_t*>(ws + h.d) : nullptr, has_hist ? &dc : nullptr, &dp,
                              reinterpret_cast<const float*>(ws + h.u), reinterpret_cast<int32_t*>(ws + h.acc),
@@ -281,6 +348,8 @@ dspark_status_t dspark_verify_sample_host(const void* logits, const float* q, co
     if (out_logprobs) ok = ok && d2h(out_logprobs, h.lp, B * W * 4);
     if (n && out_top_ids) ok = ok && d2h(out_top_ids, h.tid, B * W * n * 4);
     if (n && out_top_logprobs) ok = ok && d2h(out_top_logprobs, h.tlp, B * W * n * 4);
+    if (ex && ex->out_stopped) ok = ok && d2h(ex->out_stopped, h.stopped, B * 4);
+    if (ex && ex->pos_counts && Km) ok = ok && d2h(ex->pos_counts, h.counts, 2 * Km * 8);
     if (!ok) return fail(DSPARK_ERR_CUDA);
     if (cudaStreamSynchronize(s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;

@@ -45,8 +45,10 @@ enum UnitKind : int { kUnitX = 0, kUnitQ = 1 };
 
 struct Plan {
     int n_units;         // unused
-    int pad[3];          // pad[0]: error flag set by the streaming pass
+    int pad[3];          // pad[0]: error flag set by the streaming pass; pad[1]: bad d2t table
 };
+
+enum QLayout : int { kQDense = 0, kQSparse = 1, kQReduced = 2 };
 
 // One segment (consecutive vocab tiles [t0, t1) of one row) with its request's parameters.
 struct UnitDesc {
@@ -134,10 +136,10 @@ struct LpPartial {
 };
 
 struct ReqOut {
-    int a;               // accepted drafts
+    int a;               // accepted drafts (up to and including the eos draft when stopped)
     int draw;            // 0 none pending, 1 residual over the whole row, 2 target row over the whole row
     int status;
-    int pad;
+    int stopped;         // 1: an accepted draft was the eos token; nothing is drawn
 };
 
 // Device-side view of the workspace and the call's arguments.
@@ -147,6 +149,9 @@ struct Args {
     int tile_x, tiles_x, tile_q, tiles_q, bm_words;
     int nseg_x, nseg_q;    // segments per target / draft row
     int lp_chunks;         // partials per row in the logprob pass (one)
+    int Lq;                // entries of one draft row: V (dense), m (sparse), Vd (reduced)
+    int q_layout;          // QLayout
+    int lp_pen;            // logprobs over the penalised logits
     int grid_ss;           // CTAs of the streaming pass
     int max_seg;           // segments per (CTA, group) stream, upper bound
     int n_top, want_lp;
@@ -160,6 +165,9 @@ struct Args {
     const int* h_ids;
     const int* h_cnt;
     const float* u;
+    const int* q_ids;      // sparse: [B * Km * Lq] target ids of the draft entries
+    const int* d2t;        // reduced: [Lq] offsets, target id = draft id + d2t[draft id]
+    const int* eos;        // [B] end-of-sequence token (< 0: none) or null
     // outputs (device)
     int* out_accept;
     int* out_tokens;
@@ -167,6 +175,8 @@ struct Args {
     int* out_top_ids;
     float* out_top_lp;
     int* row_status;
+    int* out_stopped;      // [B] or null
+    unsigned long long* pos_counts;   // [2 * Km] or null: attempts, then accepts, added to
     // workspace
     Plan* plan;
     UnitDesc* units;       // [grid_ss * kGroups * max_seg] segment streams
@@ -187,6 +197,7 @@ struct Args {
     int* lp_list;          // [1 + xslots]: count, then the rows (b*W + j) the logprob pass reads
     int* lp_done;          // [xslots]: unused by the one-CTA-per-row logprob pass (zeroed by every call)
     LpPartial* lp_part;    // [xslots * lp_chunks]
+    int* t2d;              // reduced: [V] draft id of each target id, -1 for none (built by prep)
 };
 
 // ---------------------------------------------------------------- small helpers
@@ -385,25 +396,69 @@ __device__ __forceinline__ int params_status(const Args& a, const dspark_row_par
     return 0;
 }
 
-// Status bits that follow from the parameters and the draft ids alone.
-__device__ __forceinline__ int request_status(const Args& a, int b) {
-    const dspark_row_params_t r = a.rows[b];
-    int st = 0;
-    const bool t_ok = isfinite(r.temperature) && r.temperature >= 0.f;
-    const bool p_ok = r.top_p > 0.f && isfinite(r.top_p);
-    if (!t_ok || !p_ok || r.top_k < 0 || r.num_drafts < 0 || r.num_drafts > a.Km ||
-        !isfinite(r.presence_penalty) || !isfinite(r.frequency_penalty))
-        return DSPARK_ROW_BAD_PARAMS;
-    if (r.temperature > 0.f && r.num_drafts > 0 && a.q == nullptr) return DSPARK_ROW_BAD_PARAMS;
-    for (int i = 0; i < r.num_drafts; ++i) {
-        const int t = a.d[static_cast<long long>(b) * a.Km + i];
-        if (t < 0 || t >= a.V) st |= DSPARK_ROW_BAD_DRAFT;
-    }
-    return st;
-}
-
 __device__ __forceinline__ bool has_penalty(const dspark_row_params_t& r) {
     return r.presence_penalty != 0.f || r.frequency_penalty != 0.f;
+}
+
+// Count of token `tok` at verify position j of request b (history + own draft prefix), from the
+// request's penalty index: the tile's sorted history entries by binary search, then its
+// draft-only entries; a tile whose list overflowed looks the history up directly.
+__device__ __forceinline__ int token_count(const Args& a, int b, int j, int tok) {
+    const long long pt = static_cast<long long>(b) * a.tiles_x + tok / a.tile_x;
+    const PenHdr h = a.pen_hdr[pt];
+    if (!h.overflow) {
+        const PenEntry* ent = a.pen_ent + pt * kPenCap;
+        const int nh = h.pad[0];
+        int l = 0, hi = nh;
+        while (l < hi) { const int m = (l + hi) >> 1; if (ent[m].token < tok) l = m + 1; else hi = m; }
+        int e = -1;
+        if (l < nh && ent[l].token == tok) e = l;
+        else for (int k = nh; k < h.n; ++k) if (ent[k].token == tok) { e = k; break; }
+        if (e < 0) return 0;
+        const PenEntry pe = ent[e];
+        const unsigned long long mask = (static_cast<unsigned long long>(pe.mask_hi) << 32) | pe.mask_lo;
+        const unsigned long long low = (j >= 64) ? ~0ull : ((1ull << j) - 1ull);
+        return pe.base + __popcll(mask & low);
+    }
+    int base = 0;
+    const int hlo = a.h_off ? a.h_off[b] : 0, hhi = a.h_off ? a.h_off[b + 1] : 0;
+    int l = hlo, hi = hhi;
+    while (l < hi) { const int m = (l + hi) >> 1; if (a.h_ids[m] < tok) l = m + 1; else hi = m; }
+    if (l < hhi && a.h_ids[l] == tok) base = a.h_cnt[l];
+    for (int q = 0; q < j; ++q) base += (a.d[static_cast<long long>(b) * a.Km + q] == tok);
+    return base;
+}
+
+// Penalty-index bits of tokens [e0, e0 + n) of request b, n <= 16 (bit q: token e0 + q): one or
+// two bitmap words for each vocab tile the range touches.
+__device__ __forceinline__ unsigned pen_bits_range(const Args& a, int b, int e0, int n) {
+    unsigned bits = 0u;
+    for (int e = e0; e < e0 + n;) {
+        const int tile = e / a.tile_x, tl = e - tile * a.tile_x;
+        const int cnt = min(e0 + n - e, a.tile_x - tl);
+        const unsigned* bm = a.pen_bm + (static_cast<long long>(b) * a.tiles_x + tile) * a.bm_words;
+        const int w0 = tl >> 5, sh = tl & 31;
+        unsigned long long win = bm[w0];
+        if (sh + cnt > 32) win |= static_cast<unsigned long long>(bm[w0 + 1]) << 32;
+        bits |= (static_cast<unsigned>(win >> sh) & ((1u << cnt) - 1u)) << (e - e0);
+        e += cnt;
+    }
+    return bits;
+}
+
+// Draft probability input (before temperature and truncation) of target token t in draft row
+// qs = b*Km + i, whatever the layout: the dense entry, the reduced row's entry of the draft id
+// standing for t, or the sparse entry with id t (0 where the row has none).
+__device__ __forceinline__ float draft_value(const Args& a, long long qs, int t) {
+    if (a.q_layout == kQDense) return __ldg(a.q + qs * a.V + t);
+    if (a.q_layout == kQReduced) {
+        const int e = __ldg(a.t2d + t);
+        return e >= 0 ? __ldg(a.q + qs * a.Lq + e) : 0.f;
+    }
+    const int* ids = a.q_ids + qs * a.Lq;
+    for (int e = 0; e < a.Lq; ++e)
+        if (__ldg(ids + e) == t) return __ldg(a.q + qs * a.Lq + e);
+    return 0.f;
 }
 
 // ---------------------------------------------------------------- launchers (one per .cu)

@@ -280,10 +280,11 @@ __device__ void for_each_elem_t(FullSmem& s, const RowSource& src, Fn fn) {
                                          : reinterpret_cast<const unsigned char*>(a.q + src.base);
     const int head = static_cast<int>(((16u - static_cast<unsigned>(reinterpret_cast<uintptr_t>(rowp) & 15u)) & 15u) / SX);
     const int tile_n = (src.is_x ? a.tile_x : kStageBytes / 4) / 2;   // chunk: half a tile
-    const int ntiles = (a.V + tile_n - 1) / tile_n;
+    const int row_n = src.is_x ? a.V : a.Lq;              // a draft row holds Lq entries
+    const int ntiles = (row_n + tile_n - 1) / tile_n;
     // aligned interior [va, vb) of tile t: element e starts a vector iff (e - head) % EPV == 0
     auto interior = [&](int t, int& va, int& vb) {
-        const int e0 = t * tile_n, e1 = min(a.V, e0 + tile_n);
+        const int e0 = t * tile_n, e1 = min(row_n, e0 + tile_n);
         const int lo = max(e0, head);
         va = min(e1, head + ((lo - head + EPV - 1) / EPV) * EPV);
         vb = (e1 >= va + EPV) ? head + ((e1 - head) / EPV) * EPV : va;
@@ -301,7 +302,7 @@ __device__ void for_each_elem_t(FullSmem& s, const RowSource& src, Fn fn) {
     __syncthreads();                                      // the buffers are free
     issue(0);
     for (int t = 0; t < ntiles; ++t) {
-        const int e0 = t * tile_n, e1 = min(a.V, e0 + tile_n);
+        const int e0 = t * tile_n, e1 = min(row_n, e0 + tile_n);
         __syncthreads();                                  // tile t-1 visited: its buffer is free
         issue(t + 1);
         int nh = 0, n = 0, over = 0;
@@ -606,7 +607,7 @@ __device__ void whole_row_x(const Args& a, FullSmem& s, int slot, int b, int j, 
 }
 
 __device__ void whole_row_q(const Args& a, FullSmem& s, int qs, int b, int i, QRowOut& o) {
-    RowSource src{&a, false, static_cast<long long>(qs) * a.V, b, i, 0.f, 0.f, false};
+    RowSource src{&a, false, static_cast<long long>(qs) * a.Lq, b, i, 0.f, 0.f, false};
     uint32_t floor_key = fkey(o.tau);
     if (o.top_k > 0) floor_key = full_kth(s, src, o.top_k, false);
     const float qmax = o.qmax, inv_t = o.inv_t;
@@ -752,7 +753,7 @@ __device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
     o.top_p = r.top_p;
     o.flags = fl;
     const int k = r.top_k;
-    if (k > 0 && k < a.V) {
+    if (k > 0 && k < a.Lq) {
         CandSet cs{nullptr, 0, 0, -1};
         if (k <= kMaxCandTopK && !(fl & kTileOverflowPen))
             cs = stage_candidates(s, ts, a.cand_q + static_cast<long long>(qslot) * nseg * kCandPenGlobal,
@@ -792,7 +793,7 @@ __device__ void finalize_q(const Args& a, FinSmem& s, int qslot, int b, int i) {
 __device__ void finalize_row(const Args& a, FinSmem& s, int slot) {
     if (slot < a.xslots) {
         const int b = slot / (a.Km + 1), j = slot % (a.Km + 1);
-        if ((request_status(a, b) & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || j > a.rows[b].num_drafts) {
+        if ((a.row_status[b] & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || j > a.rows[b].num_drafts) {
             if (threadIdx.x == 0) { XRowOut o{}; o.mode = kModeInactive; a.xout[slot] = o; }
             return;
         }
@@ -801,7 +802,7 @@ __device__ void finalize_row(const Args& a, FinSmem& s, int slot) {
         const int qs = slot - a.xslots;
         const int b = qs / a.Km, i = qs % a.Km;
         const dspark_row_params_t r = a.rows[b];
-        if ((request_status(a, b) & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || i >= r.num_drafts ||
+        if ((a.row_status[b] & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || i >= r.num_drafts ||
             !(r.temperature > 0.f)) {
             if (threadIdx.x == 0) { QRowOut o{}; o.mode = kModeInactive; a.qout[qs] = o; }
             return;

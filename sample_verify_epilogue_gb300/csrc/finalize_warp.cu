@@ -385,7 +385,7 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
         return true;
     }
     const int k = r.top_k;
-    const bool list = k > 0 && k < a.V;
+    const bool list = k > 0 && k < a.Lq;
     if (!list && r.top_p < 1.f) return false;
     if (list && (k > kMaxCandTopK || (fl & kTileOverflowPen))) return false;
     o.qmax = qmax;

@@ -18,6 +18,12 @@
 //     search over counts, the logits above v, then the lowest ids equal to v.
 // It then writes logprob = x[token] - (m + log s) and the top list.  Results do not depend on
 // scheduling.
+//
+// Penalised mode (the other reading of "raw target log-softmax"): the same over the penalised
+// logits x' of the position.  Tokens the penalty index flags for the request (history and
+// drafts) have their logit replaced by x' as each batch arrives: the vector's lane is set to
+// -inf for the packed reduction and x' is folded into the thread's maximum and sum, and
+// gathered, on its own.  Every other logit is its own x'.
 #include "block_utils.cuh"
 
 namespace dspark {
@@ -163,21 +169,46 @@ __device__ __forceinline__ void lp_push(LpSmem& s, float v, int id) {
 // Exact top-n of a chunk whose logits >= theta did not fit the key buffer (ties): the n-th
 // largest value v (with multiplicity) by a bitwise search over counts, the logits above v (fewer
 // than n), then the lowest ids equal to v in id order.  Reads the chunk from L2 again.
-template <int SX>
-__device__ int lp_exact_top(const Args& a, LpSmem& s, long long slot, int c0, int c1, int va, int vb, int n_top) {
+// The logit of position j of request b at token e as the pass sees it: x, or x' in penalised mode.
+struct LpRow {
+    int b, j;
+    float f, p;
+};
+template <bool PEN>
+__device__ __forceinline__ float lp_value(const Args& a, const LpRow& r, int e, float x) {
+    if (!PEN || !(pen_bits_range(a, r.b, e, 1) & 1u)) return x;
+    return penalise(x, token_count(a, r.b, r.j, e), r.f, r.p);
+}
+
+template <int SX, bool PEN>
+__device__ int lp_exact_top(const Args& a, LpSmem& s, long long slot, int c0, int c1, int va, int vb, int n_top,
+                            const LpRow& pr) {
     constexpr int EPV = 16 / SX;
     const int tid = threadIdx.x;
-    const unsigned char* rowp = static_cast<const unsigned char*>(a.x) + slot * a.V * SX;
-    const uint4* g = reinterpret_cast<const uint4*>(rowp + static_cast<long long>(va) * SX);
+    auto val = [&](int e) { return lp_value<PEN>(a, pr, e, load_x(a.x, SX, slot * a.V + e)); };
+    auto vload = [&](int v, float (&xs)[EPV]) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(a.x) +
+                                                             (slot * a.V + va) * SX) + v);
+#pragma unroll
+        for (int q = 0; q < EPV; ++q) xs[q] = lp_elem<SX>(w, q);
+        if (PEN) {
+            const unsigned bits = pen_bits_range(a, pr.b, va + v * EPV, EPV);
+            if (bits)
+#pragma unroll
+                for (int q = 0; q < EPV; ++q)
+                    if ((bits >> q) & 1u) xs[q] = penalise(xs[q], token_count(a, pr.b, pr.j, va + v * EPV + q), pr.f, pr.p);
+        }
+    };
     const int nv = (vb - va) / EPV;
     auto count_ge = [&](uint32_t key) {
         int c = 0;
-        for (int e = c0 + tid; e < va; e += kLpThreads) c += fkey(load_x(a.x, SX, slot * a.V + e)) >= key;
-        for (int e = vb + tid; e < c1; e += kLpThreads) c += fkey(load_x(a.x, SX, slot * a.V + e)) >= key;
+        for (int e = c0 + tid; e < va; e += kLpThreads) c += fkey(val(e)) >= key;
+        for (int e = vb + tid; e < c1; e += kLpThreads) c += fkey(val(e)) >= key;
         for (int v = tid; v < nv; v += kLpThreads) {
-            const uint4 w = __ldg(g + v);
+            float xs[EPV];
+            vload(v, xs);
 #pragma unroll
-            for (int q = 0; q < EPV; ++q) c += fkey(lp_elem<SX>(w, q)) >= key;
+            for (int q = 0; q < EPV; ++q) c += fkey(xs[q]) >= key;
         }
         int tot = 0;
         block_excl_count(s, c, &tot);
@@ -190,18 +221,19 @@ __device__ int lp_exact_top(const Args& a, LpSmem& s, long long slot, int c0, in
     if (tid == 0) s.n = 0;
     __syncthreads();
     for (int e = c0 + tid; e < va; e += kLpThreads) {
-        const float x = load_x(a.x, SX, slot * a.V + e);
+        const float x = val(e);
         if (fkey(x) > kth) { const int p = atomicAdd(&s.n, 1); s.keys[p] = ckey(x, e); }
     }
     for (int e = vb + tid; e < c1; e += kLpThreads) {
-        const float x = load_x(a.x, SX, slot * a.V + e);
+        const float x = val(e);
         if (fkey(x) > kth) { const int p = atomicAdd(&s.n, 1); s.keys[p] = ckey(x, e); }
     }
     for (int v = tid; v < nv; v += kLpThreads) {
-        const uint4 w = __ldg(g + v);
+        float xs[EPV];
+        vload(v, xs);
 #pragma unroll
         for (int q = 0; q < EPV; ++q) {
-            const float x = lp_elem<SX>(w, q);
+            const float x = xs[q];
             if (fkey(x) > kth) { const int p = atomicAdd(&s.n, 1); s.keys[p] = ckey(x, va + v * EPV + q); }
         }
     }
@@ -218,19 +250,17 @@ __device__ int lp_exact_top(const Args& a, LpSmem& s, long long slot, int c0, in
         int ne = 0;
         if (r < rounds_h) {
             const int e = c0 + r * kLpThreads + tid;
-            if (e < va) { xs[0] = load_x(a.x, SX, slot * a.V + e); ne = 1; base_id = e; }
+            if (e < va) { xs[0] = val(e); ne = 1; base_id = e; }
         } else if (r < rounds_h + rounds_v) {
             const int v = (r - rounds_h) * kLpThreads + tid;
             if (v < nv) {
-                const uint4 w = __ldg(g + v);
-#pragma unroll
-                for (int q = 0; q < EPV; ++q) xs[q] = lp_elem<SX>(w, q);
+                vload(v, xs);
                 ne = EPV;
                 base_id = va + v * EPV;
             }
         } else {
             const int e = vb + (r - rounds_h - rounds_v) * kLpThreads + tid;
-            if (e < c1) { xs[0] = load_x(a.x, SX, slot * a.V + e); ne = 1; base_id = e; }
+            if (e < c1) { xs[0] = val(e); ne = 1; base_id = e; }
         }
 #pragma unroll
         for (int q = 0; q < EPV; ++q) mine += (q < ne && fkey(xs[q]) == kth) ? 1 : 0;
@@ -300,8 +330,8 @@ __device__ void lp_sort_warp_lists(LpSmem& s) {
 
 // One chunk [c0, c1) of target row `slot`: its maximum, its sum of exp relative to it and its
 // top-n list, written to *out.
-template <int SX>
-__device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c1, LpPartial* out) {
+template <int SX, bool PEN>
+__device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c1, LpPartial* out, const LpRow& pr) {
     constexpr int EPV = 16 / SX;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned char* rowp = static_cast<const unsigned char*>(a.x) + slot * a.V * SX;
@@ -319,7 +349,8 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
     const int eh1 = tid == 0 ? va : (tid == 1 ? c1 : 0);
     float edge[EPV];
 #pragma unroll
-    for (int q = 0; q < EPV; ++q) edge[q] = eh0 + q < eh1 ? load_x(a.x, SX, slot * a.V + eh0 + q) : -INFINITY;
+    for (int q = 0; q < EPV; ++q)
+        edge[q] = eh0 + q < eh1 ? lp_value<PEN>(a, pr, eh0 + q, load_x(a.x, SX, slot * a.V + eh0 + q)) : -INFINITY;
     float tm = -INFINITY, ts = 0.f;
 #pragma unroll
     for (int q = 0; q < EPV; ++q) tm = fmaxf(tm, edge[q]);
@@ -380,11 +411,75 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
             ts += (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
     };
+    // penalised mode: the flagged tokens of a batch leave the packed words (-inf) and enter the
+    // thread's maximum and sum as x', gathered at once when theta is known (later, for batch 0)
+    auto fold = [&](float xp) {
+        if (xp > tm) {
+            ts = (tm > -INFINITY) ? ts * ex2_approx((tm - xp) * kL2E) : 0.f;
+            tm = xp;
+        }
+        if (tm > -INFINITY) ts += ex2_approx((xp - tm) * kL2E);
+    };
+    auto pen_fix = [&](uint4 (&w)[kLpVec], int v0, bool gather_now) {
+        unsigned long long* k = s.keys + warp * kLpWarpCap;
+#pragma unroll
+        for (int i = 0; i < kLpVec; ++i) {
+            const int v = v0 + tid + i * kLpThreads;
+            if (v >= nv) continue;
+            const int e0 = va + v * EPV;
+            const unsigned bits = pen_bits_range(a, pr.b, e0, EPV);
+            if (!bits) continue;
+#pragma unroll
+            for (int q = 0; q < EPV; ++q) {
+                if (!((bits >> q) & 1u)) continue;
+                const float xp = penalise(lp_elem<SX>(w[i], q), token_count(a, pr.b, pr.j, e0 + q), pr.f, pr.p);
+                fold(xp);
+                if (gather_now && xp >= theta && n_top > 0) {
+                    const int pos = atomicAdd(&s.wn[warp], 1);
+                    if (pos < kLpWarpCap) k[pos] = ckey(xp, e0 + q);
+                }
+            }
+            // the flagged lanes leave the packed words: -inf in their halves (bf16) or words (fp32)
+            uint32_t* wd[4] = {&w[i].x, &w[i].y, &w[i].z, &w[i].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                if (SX == 2) {
+                    const unsigned two = (bits >> (2 * h)) & 3u;
+                    const uint32_t keep = ((two & 1u) ? 0u : 0x0000FFFFu) | ((two & 2u) ? 0u : 0xFFFF0000u);
+                    const uint32_t set = ((two & 1u) ? 0x0000FF80u : 0u) | ((two & 2u) ? 0xFF800000u : 0u);
+                    *wd[h] = (*wd[h] & keep) | set;
+                } else if ((bits >> h) & 1u) {
+                    *wd[h] = 0xFF800000u;
+                }
+            }
+        }
+    };
+    // batch 0's flagged tokens once theta is known (their logits re-read; the words were masked)
+    auto pen_gather0 = [&]() {
+        unsigned long long* k = s.keys + warp * kLpWarpCap;
+        for (int i = 0; i < kLpVec; ++i) {
+            const int v = tid + i * kLpThreads;
+            if (v >= nv) continue;
+            const int e0 = va + v * EPV;
+            unsigned bits = pen_bits_range(a, pr.b, e0, EPV);
+            while (bits) {
+                const int q = __ffs(bits) - 1;
+                bits &= bits - 1;
+                const float xp = penalise(load_x(a.x, SX, slot * a.V + e0 + q), token_count(a, pr.b, pr.j, e0 + q),
+                                          pr.f, pr.p);
+                if (xp >= theta) {
+                    const int pos = atomicAdd(&s.wn[warp], 1);
+                    if (pos < kLpWarpCap) k[pos] = ckey(xp, e0 + q);
+                }
+            }
+        }
+    };
     constexpr int kStep = kLpVec * kLpThreads;
     load(wa, 0);
     for (int v0 = 0; v0 < max(nv, 1); v0 += 2 * kStep) {
         // batch v0 in wa (loaded), batch v0 + kStep into wb while wa is reduced
         if (v0 + kStep < nv) load(wb, v0 + kStep);
+        if (PEN) pen_fix(wa, v0, v0 > 0);
         reduce(wa);
         if (v0 == 0 && n_top > 0) {
             // theta from the first batch and the edges
@@ -401,10 +496,12 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
                     const int pos = atomicAdd(&s.wn[warp], 1);
                     if (pos < kLpWarpCap) k[pos] = ckey(edge[q], eh0 + q);
                 }
+            if (PEN) pen_gather0();
         }
         if (n_top > 0) gather(wa, v0);
         if (v0 + kStep >= nv) break;
         if (v0 + 2 * kStep < nv) load(wa, v0 + 2 * kStep);
+        if (PEN) pen_fix(wb, v0 + kStep, true);
         reduce(wb);
         if (n_top > 0) gather(wb, v0 + kStep);
     }
@@ -451,7 +548,7 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
             __syncthreads();
             cnt = s.n;
         } else {
-            cnt = min(lp_exact_top<SX>(a, s, slot, c0, c1, va, vb, n_top), n_top);
+            cnt = min(lp_exact_top<SX, PEN>(a, s, slot, c0, c1, va, vb, n_top, pr), n_top);
             for (int i = tid; i < cnt; i += blockDim.x) out->top[i] = TopEntry{ckey_id(s.keys[i]), ckey_v(s.keys[i])};
         }
     }
@@ -470,7 +567,8 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
 
 // Rows of more than kLpMergeLists chunks (vocabularies above 4M): the row's top-n by sorting
 // the chunk lists in batches that fit the key buffer, keeping the best n after each batch.
-__device__ void lp_merge_large(const Args& a, LpSmem& s, long long slot, int b, int j, const LpPartial* part, int S) {
+__device__ void lp_merge_large(const Args& a, LpSmem& s, long long slot, int b, int j, const LpPartial* part, int S,
+                               const LpRow& pr, bool pen) {
     const int tid = threadIdx.x;
     const int W = a.Km + 1;
     const int n_top = a.n_top;
@@ -487,7 +585,8 @@ __device__ void lp_merge_large(const Args& a, LpSmem& s, long long slot, int b, 
     const float lse = mm + logf(sum);
     if (tid == 0 && a.out_lp) {
         const int t = a.out_tokens[static_cast<long long>(b) * W + j];
-        a.out_lp[static_cast<long long>(b) * W + j] = t >= 0 ? load_x(a.x, a.sx, slot * a.V + t) - lse : -INFINITY;
+        const float xt = t >= 0 ? load_x(a.x, a.sx, slot * a.V + t) : 0.f;
+        a.out_lp[static_cast<long long>(b) * W + j] = t >= 0 ? (pen ? lp_value<true>(a, pr, t, xt) : xt) - lse : -INFINITY;
     }
     int have = 0;
     for (int c0 = 0; c0 < S;) {
@@ -520,14 +619,15 @@ __device__ void lp_merge_large(const Args& a, LpSmem& s, long long slot, int b, 
 // l, l + 32, ... in order, then a fixed shuffle tree), and the row's top-n by an n-round merge
 // of the chunks' sorted lists (every round the lanes offer the largest head among their lists
 // and the winner's list advances).
-__device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j, const LpPartial* part, int S) {
+__device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j, const LpPartial* part, int S,
+                         const LpRow& pr, bool pen) {
     const int tid = threadIdx.x, lane = tid & 31;
     const int W = a.Km + 1;
     const int n_top = a.n_top;
     // the partials were written by other CTAs of this launch: read them from L2 (__ldcg)
     const bool staged = S <= kLpMergeLists && S * n_top <= kLpCandCap;
     if (S > kLpMergeLists && n_top > 0) {
-        lp_merge_large(a, s, slot, b, j, part, S);
+        lp_merge_large(a, s, slot, b, j, part, S, pr, pen);
         return;
     }
     for (int c = tid; c < S && c < kLpMergeLists; c += blockDim.x) {   // (more are read from L2)
@@ -556,7 +656,8 @@ __device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j,
     const float lse = mm + logf(sum);
     if (lane == 0 && a.out_lp) {
         const int t = a.out_tokens[static_cast<long long>(b) * W + j];
-        a.out_lp[static_cast<long long>(b) * W + j] = t >= 0 ? load_x(a.x, a.sx, slot * a.V + t) - lse : -INFINITY;
+        const float xt = t >= 0 ? load_x(a.x, a.sx, slot * a.V + t) : 0.f;
+        a.out_lp[static_cast<long long>(b) * W + j] = t >= 0 ? (pen ? lp_value<true>(a, pr, t, xt) : xt) - lse : -INFINITY;
     }
     if (n_top <= 0) return;
     // cursor of every chunk list: a chunk list c is read at position cur[c / 32] of lane c % 32's
@@ -598,7 +699,9 @@ __device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j,
     }
 }
 
-template <int SX>
+// PEN_MODE: the call asked for penalised logprobs (rows of requests without a penalty still
+// take the raw path: their x' is x and they have no penalty index).
+template <int SX, bool PEN_MODE>
 __global__ void __launch_bounds__(kLpThreads, 1) logprob_kernel(Args a) {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char lp_raw[];
@@ -608,24 +711,30 @@ __global__ void __launch_bounds__(kLpThreads, 1) logprob_kernel(Args a) {
     const int row = a.lp_list[1 + blockIdx.x];            // b * W + j
     const int b = row / W, j = row % W;
     LpPartial* part = a.lp_part + row;
-    lp_chunk<SX>(a, s, row, 0, a.V, part);
+    const dspark_row_params_t r = a.rows[b];
+    const LpRow pr{b, j, r.frequency_penalty, r.presence_penalty};
+    const bool pen = PEN_MODE && has_penalty(r);
+    if (PEN_MODE && pen) lp_chunk<SX, PEN_MODE>(a, s, row, 0, a.V, part, pr);
+    else lp_chunk<SX, false>(a, s, row, 0, a.V, part, pr);
     __syncthreads();                                      // the partial (global) is visible to the CTA
-    lp_merge(a, s, row, b, j, part, 1);
+    lp_merge(a, s, row, b, j, part, 1, pr, pen);
 }
 
 }  // namespace
 
-cudaError_t launch_logprobs(const Args& a, cudaStream_t s) {
+template <int SX, bool PEN>
+cudaError_t launch_lp(const Args& a, cudaStream_t s) {
     const size_t smem = sizeof(LpSmem);
     const int grid = a.xslots;                             // one CTA per row that may be listed
-    if (a.sx == 2) {
-        cudaError_t e = cudaFuncSetAttribute(logprob_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        return launch_k(logprob_kernel<2>, dim3(grid), dim3(kLpThreads), smem, s, true, a);
-    }
-    cudaError_t e = cudaFuncSetAttribute(logprob_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = cudaFuncSetAttribute(logprob_kernel<SX, PEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_k(logprob_kernel<4>, dim3(grid), dim3(kLpThreads), smem, s, true, a);
+    return launch_k(logprob_kernel<SX, PEN>, dim3(grid), dim3(kLpThreads), smem, s, true, a);
+}
+
+cudaError_t launch_logprobs(const Args& a, cudaStream_t s) {
+    if (a.sx == 2) return a.lp_pen ? launch_lp<2, true>(a, s) : launch_lp<2, false>(a, s);
+    return a.lp_pen ? launch_lp<4, true>(a, s) : launch_lp<4, false>(a, s);
 }
 
 }  // namespace dspark

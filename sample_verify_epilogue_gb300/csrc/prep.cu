@@ -12,6 +12,12 @@
 // c = base + popcount(mask & ((1 << j) - 1)), i.e. the history plus its own draft prefix
 // (mlx-dspark Changelog, [0.2.0] Added, "presence_penalty / frequency_penalty").  A bitmap
 // over the tile marks those tokens so the streaming pass tests eight logits per byte.
+//
+// Draft layouts other than dense: block t = 0 of a sampled request checks its sparse draft rows
+// (ids in [0, V), no id twice in a row).  For a reduced draft vocabulary, blocks past the
+// B * tiles_x request blocks invert the d2t table into t2d (target id -> draft id, -1 for none),
+// flagging a target id outside [0, V) or reached twice (mlx-dspark Changelog, [0.8.0] Added:
+// a draft id d stands for target id d + d2t[d]; a mismatched table is refused, never decoded).
 #include "dspark_internal.cuh"
 
 namespace dspark {
@@ -68,6 +74,18 @@ __device__ void penalty_index_block(const Args& a, int b, int t) {
     const int pst = params_status(a, r);
     if (pst == 0)
         for (int i = tid; i < K; i += kPrepThreads) if (s_d[i] < 0 || s_d[i] >= a.V) s_bad = 1;
+    if (t == 0 && pst == 0 && a.q_layout == kQSparse && r.temperature > 0.f && a.q != nullptr) {
+        const int m = a.Lq;
+        int bad = 0;
+        for (int e = tid; e < K * m; e += kPrepThreads) {
+            const int i = e / m, k = e - i * m;
+            const int* ids = a.q_ids + (static_cast<long long>(b) * a.Km + i) * m;
+            const int id = __ldg(ids + k);
+            if (id < 0 || id >= a.V) bad = 1;
+            for (int k2 = 0; k2 < k; ++k2) bad |= (__ldg(ids + k2) == id);
+        }
+        if (__syncthreads_or(bad) && tid == 0) s_bad = 1;
+    }
     __syncthreads();
     if (t == 0 && tid == 0) {
         const int st = pst ? pst : (s_bad ? DSPARK_ROW_BAD_DRAFT : 0);
@@ -154,15 +172,34 @@ __device__ void penalty_index_block(const Args& a, int b, int t) {
     }
 }
 
+// Blocks past the request blocks: the inverse of the d2t table, four draft ids per thread.
+__device__ void d2t_block(const Args& a, int blk) {
+    int bad = 0;
+    for (int k = 0; k < 4; ++k) {
+        const long long e = (static_cast<long long>(blk) * 4 + k) * kPrepThreads + threadIdx.x;
+        if (e >= a.Lq) break;
+        const long long t = e + static_cast<long long>(__ldg(a.d2t + e));
+        if (t < 0 || t >= a.V) { bad = 1; continue; }
+        if (atomicCAS(a.t2d + t, -1, static_cast<int>(e)) != -1) bad = 1;
+    }
+    if (bad) atomicOr(&a.plan->pad[1], 1);
+}
+
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(Args a) {
     pdl_trigger();
+    const int nreq = a.B * a.tiles_x;
+    if (static_cast<int>(blockIdx.x) >= nreq) {
+        d2t_block(a, blockIdx.x - nreq);
+        return;
+    }
     penalty_index_block(a, blockIdx.x / a.tiles_x, blockIdx.x % a.tiles_x);
 }
 
 }  // namespace
 
 cudaError_t launch_prep(const Args& a, cudaStream_t s) {
-    const int grid = a.B * a.tiles_x;
+    const int nd2t = (a.q_layout == kQReduced && a.q) ? (a.Lq + 4 * kPrepThreads - 1) / (4 * kPrepThreads) : 0;
+    const int grid = a.B * a.tiles_x + nd2t;
     return launch_k(prep_kernel, dim3(grid), dim3(kPrepThreads), 0, s, false, a);
 }
 

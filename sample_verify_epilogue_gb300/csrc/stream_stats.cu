@@ -22,7 +22,10 @@
 //   end of segment: one reduction and one write of the statistics (the candidates went
 //     straight to the segment's lists in global memory as they were found, positions taken
 //     from counters in shared memory).
-// Draft tiles get the same treatment with q as the key (top-k of q^(1/T) is top-k of q).
+// Draft tiles get the same treatment with q as the key (top-k of q^(1/T) is top-k of q).  A
+// draft row given sparsely or over a reduced vocabulary is streamed as it is stored (its m or
+// Vd entries): the truncated draft distribution depends on the multiset of values alone, and
+// the tokens the row leaves out have probability 0.
 // The raw log-softmax and the raw top-n of logprobs are not taken here: they are needed at
 // the emitted positions only, which logprob_kernel reads after the draws.
 #include "dspark_internal.cuh"
@@ -32,6 +35,16 @@ namespace dspark {
 namespace {
 
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s: no healthy wait comes close
+#ifdef DSPARK_TEST_EXPIRED_WAITS
+// Test build only: every consumer wait for a tile counts as expired at once, and the producer
+// gives up after 100 us without progress, so each call ends with DSPARK_ROW_INTERNAL on every
+// valid request.  The producer's final wait for its own copies in flight keeps the 2 s bound.
+constexpr bool kExpireAtOnce = true;
+constexpr unsigned long long kIdleNs = 100000ull;
+#else
+constexpr bool kExpireAtOnce = false;
+constexpr unsigned long long kIdleNs = kWaitNs;
+#endif
 
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
@@ -50,6 +63,7 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, unsigned parity) {
 
 // The same, giving up at once when *err is set (another thread of the group already gave up).
 __device__ __forceinline__ bool wait_phase_or_err(uint64_t* bar, unsigned parity, const volatile int* err) {
+    if (kExpireAtOnce) return false;
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (!mbar_try_wait(bar, parity))
@@ -795,11 +809,11 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
     const int lane = threadIdx.x & 31, warp = gt >> 5;
     const unsigned char* data = sm.data[stage];
     const int k = m.top_k;
-    const bool need_cand = k > 0 && k < a.V && k <= kMaxCandTopK;
-    const bool need_sum = !need_cand && (k == 0 || k >= a.V);
+    const bool need_cand = k > 0 && k < a.Lq && k <= kMaxCandTopK;
+    const bool need_sum = !need_cand && (k == 0 || k >= a.Lq);
     const bool t_one = m.temperature == 1.f;
     const float inv_t = 1.f / m.temperature;
-    const long long qrow = static_cast<long long>(m.slot) * a.V;
+    const long long qrow = static_cast<long long>(m.slot) * a.Lq;
     const int e_tail = m.vec_e0 + m.nvec * 4;
     Cand* const lp = a.cand_q + (static_cast<long long>(m.slot) * a.nseg_q + m.seg) * kCandPenGlobal;
     if (m.first) {
@@ -903,8 +917,8 @@ __device__ void q_finish(const Args& a, GroupSmem& gs, int g, const StageMeta& m
     const int gt = threadIdx.x - g * kGroupThreads;
     const int lane = threadIdx.x & 31, warp = gt >> 5;
     const int k = m.top_k;
-    const bool need_cand = k > 0 && k < a.V && k <= kMaxCandTopK;
-    const bool need_sum = !need_cand && (k == 0 || k >= a.V);
+    const bool need_cand = k > 0 && k < a.Lq && k <= kMaxCandTopK;
+    const bool need_sum = !need_cand && (k == 0 || k >= a.Lq);
     const bool t_one = m.temperature == 1.f;
     const float inv_t = 1.f / m.temperature;
     float mx = st.mx, mn = st.mn, sum = st.sum;
@@ -1111,10 +1125,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
                     const bool isx = kind == kUnitX;
                     const int es = isx ? SX : 4;
                     const int tile_n = isx ? a.tile_x : a.tile_q;
-                    const int e0 = tile * tile_n, e1 = min(a.V, e0 + tile_n);
+                    const int row_n = isx ? a.V : a.Lq;
+                    const int e0 = tile * tile_n, e1 = min(row_n, e0 + tile_n);
                     const unsigned char* row = isx
                         ? static_cast<const unsigned char*>(a.x) + static_cast<long long>(slot) * a.V * es
-                        : reinterpret_cast<const unsigned char*>(a.q) + static_cast<long long>(slot) * a.V * 4;
+                        : reinterpret_cast<const unsigned char*>(a.q) + static_cast<long long>(slot) * a.Lq * 4;
                     const uintptr_t A0 = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(e0) * es;
                     const uintptr_t A1 = reinterpret_cast<uintptr_t>(row) + static_cast<uintptr_t>(e1) * es;
                     uintptr_t c0 = (A0 + 15) & ~static_cast<uintptr_t>(15);
@@ -1162,7 +1177,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
             }
             if (!progressed) {
                 if (idle == 0) idle = globaltimer();
-                else if (globaltimer() - idle > kWaitNs) failed = true;
+                else if (globaltimer() - idle > kIdleNs) failed = true;
                 __nanosleep(128);
             } else {
                 idle = 0;
@@ -1184,8 +1199,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
     const int nseg = stream_len(S, G, c, g);
     // The tile counts come from this group's segment descriptors, so every warp of the group
     // walks the same tiles and meets the same group barriers (one in the first tile's pass,
-    // two in a segment's finish) whatever happens to the data; warps are not synchronised
-    // tile by tile.  A tile whose wait gave up is skipped with only its barriers.
+    // one in a segment's finish) whatever happens to the data; warps are not synchronised
+    // tile by tile.  A tile whose wait gave up is skipped with only its barriers, so a warp
+    // that gave up and one whose tile arrived still pass the same barriers.
     const UnitDesc* my = a.units + (static_cast<long long>(c) * kGroups + g) * a.max_seg;
     int nt_next = nseg > 0 ? my[0].t1 - my[0].t0 : 0;
     int cnt = 0;                                           // tiles consumed by this group
@@ -1200,7 +1216,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
             if (!wait_phase_or_err(&sm.full[stage], parity, &gs.error)) {
                 gs.error = 1;
                 if (ti == 0) group_sync(g);
-                if (ti == ntile - 1) { group_sync(g); group_sync(g); }
+                if (ti == ntile - 1) group_sync(g);
                 continue;
             }
             StageMeta m = sm.meta[stage];

@@ -227,3 +227,25 @@ def test_masked_logits(runner):
     batch.x[5][:, :] = row
     batch.x[5][:, keep] = batch.x[4][:, keep]
     _run(runner, batch, "masked logits V=5000")
+
+
+def test_expired_waits_report_internal(runner):
+    """A test build whose streaming-pass waits all count as expired: every valid request reports
+    DSPARK_ROW_INTERNAL (an invalid one keeps its own bits too), with no output but the error
+    padding, and the GPU context stays usable (the normal build then matches the oracle)."""
+    from sample_verify_epilogue_gb300 import binding, build
+    lib = binding.open_library(build.build_variant("expired_waits", ["-DDSPARK_TEST_EXPIRED_WAITS"],
+                                                   ["stream_stats.cu"]))
+    batch = configs.build("b256k16v262144_mixed", B=18)
+    batch.rows["temperature"][4] = -1.0                    # an invalid request
+    call = runner(batch)
+    call.run(lib=lib)
+    got = call.results()
+    st = got["row_status"]
+    assert np.all(st & 16), st
+    assert st[4] & 1
+    assert np.all(got["accept_len"] == -1) and np.all(got["tokens"] == -1)
+    assert np.all(np.isneginf(got["logprobs"])) and np.all(got["top_ids"] == -1)
+    call.run()
+    want = O.outcomes_batch(batch)
+    report("after expired waits (b256k16v262144_mixed B=18)", compare(batch, call.results(), want))

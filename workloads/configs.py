@@ -13,7 +13,7 @@ import numpy as np
 from .generate import make_batch, row_params
 
 WORKLOADS = ("b1k2v4096", "b1k2v4096_greedy", "b1k4v151936", "b4k8v151936_mixed",
-             "b64k8v262144", "b256k16v262144_mixed")
+             "b64k8v262144", "b256k16v262144_mixed", "b64k8v262144_onehot", "b64k8v262144_d2t32000")
 
 DESCRIPTIONS = {
     "b1k2v4096": "B=1 K=2 V=4096 fp32 logits N(0,2^2), draft = target + N(0,0.5^2), T=0.7 top_k=20 top_p=0.95",
@@ -26,6 +26,11 @@ DESCRIPTIONS = {
                     "presence/frequency 0.2/0.2 over 4096-token Zipf(1.1) histories, top_logprobs=20",
     "b256k16v262144_mixed": "B=256 K=16 V=262144 bf16 as b64k8v262144; (T, top_k, top_p) = combination b mod 18 of "
                             "{0,0.6,1}x{0,20,64}x{0.9,1}; penalties 0.2/0.2 on requests b<128; top_logprobs=5",
+    "b64k8v262144_onehot": "as b64k8v262144 with prompt-lookup drafts: a one-hot proposal (sparse q, m=1) per "
+                           "position; 30% of verify rows' argmax +8, 70% of drafts are the target argmax",
+    "b64k8v262144_d2t32000": "as b64k8v262144 with a reduced draft vocabulary of 32000 ids (a seeded ascending "
+                             "subset, d2t offsets) from which the drafts are drawn; target logits of those "
+                             "ids +2 (the frequent tokens)",
 }
 
 
@@ -40,7 +45,8 @@ def _mixed18(B, K):
 
 
 DEFAULT_B = {"b1k2v4096": 1, "b1k2v4096_greedy": 1, "b1k4v151936": 1, "b4k8v151936_mixed": 4,
-             "b64k8v262144": 64, "b256k16v262144_mixed": 256}
+             "b64k8v262144": 64, "b256k16v262144_mixed": 256, "b64k8v262144_onehot": 64,
+             "b64k8v262144_d2t32000": 64}
 
 
 def build_size(name: str, B=None) -> int:
@@ -85,4 +91,18 @@ def build(name: str, *, B=None, requests=None):
         return make_batch(B=Bn, K_max=16, V=262144, logits_dtype="bf16", rows=_mixed18(Bn, 16),
                           seed=1000 + i, philox_seed=i, x_sigma=3.0, draft_sigma=1.0, history_len=4096,
                           want_logprobs=True, n_top_logprobs=5, name=name, requests=requests)
+    if name == "b64k8v262144_onehot":
+        Bn = B or 64
+        return make_batch(B=Bn, K_max=8, V=262144, logits_dtype="bf16",
+                          rows=[row_params(1.0, 64, 0.95, 0.2, 0.2, 8)] * Bn, seed=1000 + i, philox_seed=i,
+                          x_sigma=3.0, draft_sigma=1.0, boost_frac=0.3, argmax_frac=0.7, history_len=4096,
+                          want_logprobs=True, n_top_logprobs=20, name=name, requests=requests,
+                          q_layout="sparse", q_m=1)
+    if name == "b64k8v262144_d2t32000":
+        Bn = B or 64
+        return make_batch(B=Bn, K_max=8, V=262144, logits_dtype="bf16",
+                          rows=[row_params(1.0, 64, 0.95, 0.2, 0.2, 8)] * Bn, seed=1000 + i, philox_seed=i,
+                          x_sigma=3.0, draft_sigma=1.0, history_len=4096, want_logprobs=True,
+                          n_top_logprobs=20, name=name, requests=requests, q_layout="reduced",
+                          draft_vocab=32000, subset_boost=2.0)
     raise KeyError(name)

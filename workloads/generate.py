@@ -154,7 +154,8 @@ def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
                x_sigma=3.0, draft_sigma=1.0, boost_frac=0.0, boost=8.0,
                history_len=0, zipf_s=1.1, draft_mode="q", argmax_frac=0.0,
                x_quant=None, want_logprobs=False, n_top_logprobs=0, name="", requests=None,
-               q_layout="dense", q_m=1, draft_vocab=None, eos_pos=None, logprob_mode="raw") -> Batch:
+               q_layout="dense", q_m=1, draft_vocab=None, eos_pos=None, logprob_mode="raw",
+               subset_boost=0.0) -> Batch:
     """Build one seeded batch.
 
     rows: sequence of row_params tuples (length B).
@@ -172,7 +173,9 @@ def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
               the m-1 other largest entries of the dense row, in a seeded order (q_m = 1 is
               a one-hot proposal, q = 1 at the drafted id); "reduced" -- the draft vocabulary
               is a seeded ascending subset S of draft_vocab target ids, d2t[i] = S[i] - i, q
-              is the softmax of the draft logits over S and drafts are drawn from it.
+              is the softmax of the draft logits over S and drafts are drawn from it;
+              subset_boost is added to the target logits of S (the frequent tokens a
+              reduced draft vocabulary keeps) before rounding.
     eos_pos: if set, request b's end-of-sequence token is its draft at position
              min(eos_pos, K_b - 1) (none when K_b = 0).
     """
@@ -205,6 +208,8 @@ def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
         xf = rng.standard_normal((K_max + 1, V), dtype=np.float32) * np.float32(x_sigma)
         if x_quant is not None:
             xf = (np.round(xf / np.float32(x_quant)) * np.float32(x_quant)).astype(np.float32)
+        if sub is not None and subset_boost:
+            xf[:, sub] += np.float32(subset_boost)
         for j in np.nonzero(boosted[b_full])[0]:
             t = int(np.argmax(xf[j]))
             xf[j, t] += np.float32(boost)
@@ -267,6 +272,7 @@ def make_batch(*, B, K_max, V, logits_dtype="bf16", rows, seed=0, philox_seed=0,
         eos_ids=eos_ids, logprob_mode=logprob_mode,
         meta=dict(seed=seed, philox_seed=philox_seed, x_sigma=x_sigma, draft_sigma=draft_sigma,
                   boost_frac=boost_frac, history_len=history_len, draft_mode=draft_mode,
-                  argmax_frac=argmax_frac, q_layout=q_layout, q_m=q_m, draft_vocab=draft_vocab, eos_pos=eos_pos),
+                  argmax_frac=argmax_frac, q_layout=q_layout, q_m=q_m, draft_vocab=draft_vocab, eos_pos=eos_pos,
+                  subset_boost=subset_boost),
     )
     return batch
