@@ -10,7 +10,9 @@ Prints one JSON line: verify rows/s (whole job) of the call as shipped, the stre
 kernel's roofline (timed in a second loop with events around it), clocks seen during the
 timed region, an end-to-end figure through the host-buffer entry point, the float64 oracle
 timed on all host cores over the whole batch (and on one thread over a sample), and the
-parity of the timed call's results with the oracle's, near ties counted.
+parity of the timed call's results with the oracle's, near ties counted.  On one GPU it also
+times, with their parity, the same call on the workload's draft-layout variants (one-hot
+lookup drafts; a reduced draft vocabulary) and with every option of dspark_extras_t on.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 """
@@ -234,6 +236,70 @@ class OraclePool:
         self.ex.shutdown()
 
 
+VARIANTS = (
+    ("b64k8v262144_onehot", None),
+    ("b64k8v262144_d2t32000", None),
+    ("b64k8v262144", "options"),
+)
+
+
+def measure_variant(name, option, steps, device, pool):
+    """ms per call, verify rows/s, algorithmic GB/s of the call and of the streaming kernel
+    (events around it, as in the headline), and parity with the oracle on every request, for
+    one variant of the workload."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    from sample_verify_epilogue_gb300.runner import EpilogueCall
+    from tests._compare import compare
+    from workloads import configs
+
+    batch = configs.build(name)
+    label = name
+    if option == "options":
+        # eos = each request's draft 3, per-position counters, penalised logprobs
+        batch = dataclasses.replace(batch, eos_ids=batch.draft_ids[:, 3].copy(), logprob_mode="penalised")
+        label = name + " +eos +counters +penalised logprobs"
+    call = EpilogueCall(batch, device=device, counters=True)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(5):
+        call.run()
+    torch.cuda.synchronize(device)
+    call.pos_counts.zero_()
+    call.run()
+    res = call.results()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        call.run()
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = t0.elapsed_time(t1) / steps
+    kn = max(1, min(steps, 100))
+    ev = DriverEvents(kn)
+    for i in range(kn):
+        call.run(stage_events=ev.pairs[i])
+    torch.cuda.synchronize(device)
+    kern_ms = statistics.mean(ev.ms(i) for i in range(kn))
+    ev.close()
+    outs, _ = pool.outcomes(batch, range(batch.B))
+    tally = compare(batch, res, outs)
+    counters_ok = bool(np.array_equal(res["pos_counts"][0], tally.attempted) and
+                       np.array_equal(res["pos_counts"][1], tally.accepted))
+    algo = batch.algorithmic_bytes()
+    del call
+    torch.cuda.empty_cache()
+    return {"workload": label, "q_layout": batch.q_layout, "draft_row_len": batch.draft_row_len(),
+            "ms_per_step": ms, "value": batch.verify_rows() / (ms / 1e3), "unit": UNIT,
+            "algorithmic_bytes_per_step": algo, "call_gbs": algo / (ms / 1e3) / 1e9,
+            "kernel_ms": kern_ms, "kernel_gbs": algo / (kern_ms / 1e3) / 1e9,
+            "parity": {"requests": tally.requests, "matched": tally.requests, "single_result": tally.single,
+                       "near_tie_decisions": dict(tally.near_ties), "stopped": tally.stopped,
+                       "counters_match": counters_ok}}
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if ws > 1:
@@ -389,12 +455,19 @@ def run_native(args):
         assert np.array_equal(hout["accept_len"].numpy(), res["accept_len"])
 
     cpu = parity = None
+    variants = None
     if rank == 0 and ws == 1:
         # the oracle on every request of this very batch, all host cores (spawn-started pool):
         # the all-cores baseline, and the parity of the timed call's results with the oracle
         from tests._compare import compare
         pool = OraclePool()
         outs, wall = pool.outcomes(batch, range(batch.B))
+        peak_v, _ = peaks()
+        variants = []
+        for name, option in VARIANTS:
+            v = measure_variant(name, option, max(1, min(args.steps, 500)), device, pool)
+            v["kernel_frac"] = v["kernel_gbs"] / peak_v
+            variants.append(v)
         pool.close()
         tally = compare(batch, res, outs)
         parity = {"requests": tally.requests, "matched": tally.requests, "single_result": tally.single,
@@ -434,6 +507,7 @@ def run_native(args):
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "variants": variants,
         }
         print(json.dumps(out))
     if dist is not None:

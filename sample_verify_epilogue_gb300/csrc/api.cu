@@ -73,7 +73,8 @@ Layout make_layout(const dspark_params_t* p) {
     L.qslots = static_cast<int>(B * Km);
     L.nseg_x = (L.tiles_x + kSegTiles - 1) / kSegTiles;
     L.nseg_q = (L.tiles_q + kSegTiles - 1) / kSegTiles;
-    L.lp_chunks = 1;                                   // the logprob pass: one partial per row
+    // the logprob pass: R listed rows of S chunks, R * S <= its grid when S > 1, else R <= xslots
+    L.lp_chunks = L.xslots > kLpMaxGrid ? L.xslots : kLpMaxGrid;
     const size_t xt = static_cast<size_t>(L.xslots) * L.nseg_x;
     const size_t qt = static_cast<size_t>(L.qslots) * L.nseg_q;
     const size_t pt = static_cast<size_t>(B) * L.tiles_x;
@@ -99,7 +100,7 @@ Layout make_layout(const dspark_params_t* p) {
     L.off_kept = take(static_cast<size_t>(L.xslots) * kKeptCap * sizeof(KeptEntry));
     L.off_qout = take(static_cast<size_t>(L.qslots) * sizeof(QRowOut) + 16);
     L.off_req = take(static_cast<size_t>(B) * sizeof(ReqOut));
-    L.off_lp_part = take(static_cast<size_t>(L.xslots) * L.lp_chunks * sizeof(LpPartial));
+    L.off_lp_part = take(static_cast<size_t>(L.lp_chunks) * sizeof(LpPartial));
     L.off_t2d = take(qo.layout == kQReduced ? static_cast<size_t>(V) * sizeof(int) : 0);
     L.total = o;
     return L;

@@ -39,13 +39,16 @@ constexpr int kKeptCap = 1024;                                 // truncated supp
 constexpr int kFinalizeThreads = 512;
 constexpr int kMergeCap = 8192;                                // merged candidates per row (smem)
 constexpr int kMaxB = DSPARK_MAX_B;
+constexpr int kLpMaxChunks = 16;                               // chunks per row in the logprob pass
+constexpr int kLpMaxGrid = 4 * 1024;                           // CTAs of the logprob pass at most
 
 // ---------------------------------------------------------------- records in the workspace
 enum UnitKind : int { kUnitX = 0, kUnitQ = 1 };
 
 struct Plan {
     int n_units;         // unused
-    int pad[3];          // pad[0]: error flag set by the streaming pass; pad[1]: bad d2t table
+    int pad[3];          // pad[0]: error flag set by the streaming pass; pad[1]: bad d2t table;
+                         // pad[2]: the logprob pass's item counter
 };
 
 enum QLayout : int { kQDense = 0, kQSparse = 1, kQReduced = 2 };
@@ -148,7 +151,7 @@ struct Args {
     int B, Km, V, sx, xdtype;
     int tile_x, tiles_x, tile_q, tiles_q, bm_words;
     int nseg_x, nseg_q;    // segments per target / draft row
-    int lp_chunks;         // partials per row in the logprob pass (one)
+    int lp_chunks;         // logprob partials the workspace holds (one per logprob CTA)
     int Lq;                // entries of one draft row: V (dense), m (sparse), Vd (reduced)
     int q_layout;          // QLayout
     int lp_pen;            // logprobs over the penalised logits
@@ -195,8 +198,8 @@ struct Args {
     QRowOut* qout;         // [qslots]
     ReqOut* req;           // [B]
     int* lp_list;          // [1 + xslots]: count, then the rows (b*W + j) the logprob pass reads
-    int* lp_done;          // [xslots]: unused by the one-CTA-per-row logprob pass (zeroed by every call)
-    LpPartial* lp_part;    // [xslots * lp_chunks]
+    int* lp_done;          // [xslots]: chunks done of each listed row (zeroed by every call)
+    LpPartial* lp_part;    // [lp_chunks]: the listed rows' chunk partials, row p's S at [p*S, p*S+S)
     int* t2d;              // reduced: [V] draft id of each target id, -1 for none (built by prep)
 };
 

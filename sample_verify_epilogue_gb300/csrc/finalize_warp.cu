@@ -129,13 +129,15 @@ __device__ int warp_stage_t(WarpSmem& w, const WCands& cs, int npairs, int c) {
     return m > kWKeyCap ? -1 : m;
 }
 
-__device__ int warp_stage(WarpSmem& w, const TileStats* ts, const WCands& cs, int k) {
+// lane_n: this lane's segment's candidate count when the caller holds it (rows of at most 32
+// segments), else -1.
+__device__ int warp_stage(WarpSmem& w, const TileStats* ts, const WCands& cs, int k, int lane_n) {
     const int lane = threadIdx.x & 31;
     if (cs.nseg > kWSegCap) return -1;
     int total = 0, npairs = 0;
     for (int t0 = 0; t0 < cs.nseg; t0 += 32) {
         const int t = t0 + lane;
-        const int n = t < cs.nseg ? ts[t].n_pen : 0;
+        const int n = t < cs.nseg ? (lane_n >= 0 ? lane_n : ts[t].n_pen) : 0;
         const int np = (n + 1) >> 1;
         int incl = np;
 #pragma unroll
@@ -179,7 +181,38 @@ __device__ uint32_t kth_key_bits(const uint32_t* keys, int n, int k) {
     return prefix;
 }
 
-__device__ __forceinline__ uint32_t warp_kth(WarpSmem& w, int n, int k) { return kth_key_bits(w.keys, n, k); }
+// The same with each lane's keys held in registers (n <= 32 * E).
+template <int E>
+__device__ uint32_t kth_key_regs(const uint32_t* keys, int n, int k) {
+    const int lane = threadIdx.x & 31;
+    uint32_t kr[E];
+    uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+#pragma unroll
+    for (int h = 0; h < E; ++h) {
+        const int i = lane + 32 * h;
+        kr[h] = i < n ? keys[i] : 0u;
+        if (i < n) { mx = max(mx, kr[h]); mn = min(mn, kr[h]); }
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    if (mx == mn) return mx;
+    const int hb = 31 - __clz(mx ^ mn);
+    uint32_t prefix = hb == 31 ? 0u : (mx & ~((2u << hb) - 1u));
+    for (int b = hb; b >= 0; --b) {
+        const uint32_t cand = prefix | (1u << b);
+        unsigned c = 0u;
+#pragma unroll
+        for (int h = 0; h < E; ++h) c += kr[h] >= cand ? 1u : 0u;     // padding keys (0) never count
+        if (static_cast<int>(__reduce_add_sync(0xffffffffu, c)) >= k) prefix = cand;
+    }
+    return prefix;
+}
+
+__device__ __forceinline__ uint32_t warp_kth(WarpSmem& w, int n, int k) {
+    if (n <= 128) return kth_key_regs<4>(w.keys, n, k);
+    if (n <= 512) return kth_key_regs<16>(w.keys, n, k);
+    return kth_key_bits(w.keys, n, k);
+}
 
 // Staged candidates with key >= kth, sorted by (value desc, id asc) into w.sk[0..count);
 // returns the count, or -1 when there are more than kWSurvCap.
@@ -199,22 +232,27 @@ __device__ int warp_survivors(WarpSmem& w, int n, uint32_t kth) {
         cnt += __popc(b);
     }
     if (cnt > kWSurvCap) return -1;
-    const int P = next_pow2(max(cnt, 2));
-    for (int i = cnt + lane; i < P; i += 32) w.sk[i] = 0ull;
     __syncwarp();
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = lane; i < P / 2; i += 32) {
-                const int lo = 2 * i - (i & (stride - 1));
-                const int hi = lo + stride;
-                const bool desc = (lo & size) == 0;
-                const unsigned long long x = w.sk[lo], y = w.sk[hi];
-                if ((x < y) == desc) { w.sk[lo] = y; w.sk[hi] = x; }
-            }
-            __syncwarp();
-        }
+    // sort by rank (keys are distinct): key i goes to the number of keys above it, through the
+    // staged-key area, which is free now
+    unsigned long long* tmp = reinterpret_cast<unsigned long long*>(w.keys);
+    static_assert(sizeof(w.keys) >= kWSurvCap * sizeof(unsigned long long), "rank sort buffer");
+    for (int i = lane; i < cnt; i += 32) {
+        const unsigned long long x = w.sk[i];
+        int r = 0;
+        for (int j = 0; j < cnt; ++j) r += w.sk[j] > x;
+        tmp[r] = x;
     }
+    __syncwarp();
+    for (int i = lane; i < cnt; i += 32) w.sk[i] = tmp[i];
+    __syncwarp();
     return cnt;
+}
+
+// Survivors of the staged keys for a top-k (1 <= k <= n): the k-th largest key, then the keys
+// reaching it, sorted.
+__device__ int warp_topk_survivors(WarpSmem& w, int n, int k) {
+    return warp_survivors(w, n, warp_kth(w, n, k));
 }
 
 // Nucleus over the sorted survivors w.sk[0..cnt) with weights wfn(value) (fixed order: lane
@@ -278,10 +316,14 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
     const dspark_row_params_t r = a.rows[b];
     const int nseg = a.nseg_x;
     const TileStats* ts = a.ts_x + static_cast<long long>(slot) * nseg;
+    // each lane's segment statistics, read once when the row has at most 32 segments
+    const bool cached = nseg <= 32;
+    TileStats mine{};
+    if (cached && lane < nseg) mine = ts[lane];
     float mr = -INFINITY, mp = -INFINITY;
     int fl = 0;
     for (int t = lane; t < nseg; t += 32) {
-        const TileStats x = ts[t];
+        const TileStats x = cached ? mine : ts[t];
         mr = nan_max(mr, x.m_raw);
         mp = nan_max(mp, x.m_pen);
         fl |= x.flags;
@@ -310,7 +352,7 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
     int arg = 0x7FFFFFFF;
     double stemp = 0.0;
     for (int t = lane; t < nseg; t += 32) {
-        const TileStats x = ts[t];
+        const TileStats x = cached ? mine : ts[t];
         if (x.m_pen == mp) arg = min(arg, x.arg_pen);
         if (!greedy) stemp += static_cast<double>(x.s_temp) * static_cast<double>(exp2f((x.m_pen - mp) * c_l2e));
     }
@@ -330,10 +372,9 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
         o.mode = kModeGreedy;
     } else if (list) {
         const WCands cs{a.cand_x + static_cast<long long>(slot) * nseg * kCandPenGlobal, kCandPenGlobal, nseg};
-        const int n = warp_stage(w, ts, cs, k);
+        const int n = warp_stage(w, ts, cs, k, cached ? mine.n_pen : -1);
         if (n < k) return false;               // too many candidates to stage, or fewer than k
-        const uint32_t kth = warp_kth(w, n, k);
-        const int cnt = warp_survivors(w, n, kth);
+        const int cnt = warp_topk_survivors(w, n, k);
         if (cnt <= 0) return false;
         double zk;
         const int kept = warp_nucleus(w, cnt, r.top_p, [&](float v) { return target_weight(v, mp, c_l2e); }, &zk,
@@ -357,10 +398,13 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
     const dspark_row_params_t r = a.rows[b];
     const int nseg = a.nseg_q;
     const TileStats* ts = a.ts_q + static_cast<long long>(qslot) * nseg;
+    const bool cached = nseg <= 32;
+    TileStats mine{};
+    if (cached && lane < nseg) mine = ts[lane];
     float qmax = -INFINITY;
     int fl = 0;
     for (int t = lane; t < nseg; t += 32) {
-        const TileStats x = ts[t];
+        const TileStats x = cached ? mine : ts[t];
         qmax = nan_max(qmax, x.m_raw);
         fl |= x.flags;
     }
@@ -372,7 +416,7 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
     const float inv_t = 1.f / r.temperature;
     double z = 0.0;
     for (int t = lane; t < nseg; t += 32) {
-        const TileStats x = ts[t];
+        const TileStats x = cached ? mine : ts[t];
         if (t_one) z += static_cast<double>(x.s_raw);
         else if (x.m_raw > 0.f)
             z += static_cast<double>(x.s_temp) * static_cast<double>(exp2f(inv_t * log2f(x.m_raw / qmax)));
@@ -382,6 +426,31 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
     o.mode = kModeInactive;
     if ((fl & kTileBad) || !(qmax > 0.f) || !isfinite(qmax)) {
         if (lane == 0) { atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE); a.qout[qslot] = o; }
+        return true;
+    }
+    if (a.Lq <= kWSurvCap) {
+        // a short draft row (sparse pairs, a small draft vocabulary): settled from its values
+        const long long base = static_cast<long long>(qslot) * a.Lq;
+        for (int e = lane; e < a.Lq; e += 32) {
+            w.keys[e] = fkey(__ldg(a.q + base + e));
+            w.ids[e] = e;
+        }
+        __syncwarp();
+        const int kk = r.top_k;
+        const int cnt = warp_topk_survivors(w, a.Lq, (kk > 0 && kk < a.Lq) ? kk : a.Lq);
+        double zk;
+        const int kept = warp_nucleus(w, cnt, r.top_p,
+                                      [&](float v) { return draft_weight(v, qmax, inv_t, t_one); }, &zk, nullptr);
+        o.qmax = qmax;
+        o.inv_t = inv_t;
+        o.top_k = 0;
+        o.top_p = r.top_p;
+        o.flags = fl;
+        o.mode = kModeList;
+        o.Z = zk;
+        o.tau = ckey_v(w.sk[kept - 1]);
+        __syncwarp();
+        if (lane == 0) a.qout[qslot] = o;
         return true;
     }
     const int k = r.top_k;
@@ -396,10 +465,9 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
     o.flags = fl;
     if (list) {
         const WCands cs{a.cand_q + static_cast<long long>(qslot) * nseg * kCandPenGlobal, kCandPenGlobal, nseg};
-        const int n = warp_stage(w, ts, cs, k);
+        const int n = warp_stage(w, ts, cs, k, cached ? mine.n_pen : -1);
         if (n < k) return false;
-        const uint32_t kth = warp_kth(w, n, k);
-        const int cnt = warp_survivors(w, n, kth);
+        const int cnt = warp_topk_survivors(w, n, k);
         if (cnt <= 0) return false;
         double zk;
         const int kept = warp_nucleus(w, cnt, r.top_p,

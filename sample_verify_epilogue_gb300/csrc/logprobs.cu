@@ -4,41 +4,51 @@
 // requested).  Only the positions a request emits from (j <= accept length) need them, so
 // they are taken after the draws, from those rows alone: accept_kernel lists the rows.
 //
-// One CTA of 1024 threads per listed row (the launch has one CTA per possible row; the rest
-// return at once).  It streams the row from HBM in batches of kLpVec 16-byte vectors per
-// thread, the next batch's loads in flight while the current one is reduced, for
-//   - the row's maximum m and its sum of exp(x - m) (per thread a running maximum, the sum
+// The R listed rows are cut into S chunks each, S = min(16, grid / R, V / 8192) at least 1, so
+// that the R * S chunks fill the persistent grid (four 256-thread CTAs per SM) in one wave and
+// the emitted rows of a call are read by every SM, not by one SM per row; each CTA takes chunks
+// from a counter.  A chunk streams from HBM in batches of kLpVec 16-byte vectors per thread,
+// the next batch's loads in flight while the current one is reduced, for
+//   - the chunk's maximum m and its sum of exp(x - m) (per thread a running maximum, the sum
 //     rescaled at most once per batch; then a fixed reduction order);
-//   - the row's n largest logits by (value descending, id ascending).  After the first batch,
-//     theta = the least over the 32 warps of each warp's ceil(n/32)-th largest thread maximum:
-//     at least n distinct logits of that batch reach it, so every one of the row's top n does,
-//     and the logits >= theta of every batch are gathered as they stream by; each warp sorts
-//     its share and one warp merges the 32 sorted lists.  When ties put more logits >= theta
-//     than fit, the row is settled exactly from L2: the n-th largest value v by a bitwise
+//   - the chunk's n largest logits by (value descending, id ascending).  After the first batch,
+//     theta = the least over the 8 warps of each warp's ceil(n/8)-th largest thread maximum:
+//     at least n distinct logits of that batch reach it, so every one of the chunk's top n does,
+//     and the logits >= theta of every batch are gathered as they stream by; the chunk's top n
+//     are then the gathered logits of rank < n (each counts the gathered logits above it).  When ties put more logits >= theta
+//     than fit, the chunk is settled exactly from L2: the n-th largest value v by a bitwise
 //     search over counts, the logits above v, then the lowest ids equal to v.
-// It then writes logprob = x[token] - (m + log s) and the top list.  Results do not depend on
+// The CTA that completes a row's last chunk (a counter per row) merges the S partials in a
+// fixed order: LSE = M + log(sum_c s_c exp(m_c - M)) and the row's top n among the chunks'
+// sorted lists.
+// It then writes logprob = x[token] - LSE and the top list.  Results do not depend on
 // scheduling.
 //
 // Penalised mode (the other reading of "raw target log-softmax"): the same over the penalised
 // logits x' of the position.  Tokens the penalty index flags for the request (history and
-// drafts) have their logit replaced by x' as each batch arrives: the vector's lane is set to
-// -inf for the packed reduction and x' is folded into the thread's maximum and sum, and
-// gathered, on its own.  Every other logit is its own x'.
+// drafts) are set to -inf in the streamed vectors; after the stream, each thread takes the
+// flagged tokens of its share of the chunk's bitmap words one by one, as x' = x less the
+// penalty of its count at that position, into its maximum and sum and, at or above theta,
+// its warp's candidates.  Every other logit is its own x'.
 #include "block_utils.cuh"
 
 namespace dspark {
 
 namespace {
 
-constexpr int kLpThreads = 1024;
+constexpr int kLpThreads = 256;
+constexpr int kLpBlocksPerSm = 4;
 constexpr int kLpWarps = kLpThreads / 32;
-constexpr int kLpCandCap = 4096;
+constexpr int kLpCandCap = 2048;
 constexpr int kLpVec = 4;                    // 16-byte vectors per thread and batch
 constexpr int kLpWarpCap = kLpCandCap / kLpWarps;
-constexpr int kLpMergeLists = 256;           // chunk partials the merge copies to shared memory
+constexpr int kLpMergeLists = kLpMaxChunks;  // chunk partials the merge copies to shared memory
+constexpr int kLpMinChunk = 8192;            // logits per chunk at least
 constexpr float kL2E = 1.4426950408889634f;
 
 struct LpSmem {
+    uint4 stage[2][kLpVec * kLpThreads];   // two batches of the chunk, filled by bulk copies
+    unsigned long long full[2];            // their mbarriers
     unsigned long long keys[kLpCandCap];   // (fkey(value) << 32) | (0xFFFFFFFF - id); warp w: [w*kLpWarpCap, ...)
     float tmax[kLpThreads];
     float wth[kLpWarps];
@@ -52,7 +62,6 @@ struct LpSmem {
     int item;
     float theta;
     unsigned long long top[2 * DSPARK_MAX_TOP_LOGPROBS];
-    int mcur[kLpMergeLists];               // the merge's list cursors
     float mm[kLpMergeLists];               // the merge's copies of the chunk partials
     float ms[kLpMergeLists];
     int mn[kLpMergeLists];
@@ -122,6 +131,22 @@ __device__ int block_excl_count(LpSmem& s, int c, int* total) {
     return off + incl - c;
 }
 
+__device__ __forceinline__ unsigned long long lp_gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for a batch's copy with a 2 s bound; false when the bound expires.
+__device__ __forceinline__ bool lp_wait(unsigned long long* bar, unsigned parity) {
+    uint64_t* b = reinterpret_cast<uint64_t*>(bar);
+    if (mbar_try_wait(b, parity)) return true;
+    const unsigned long long t0 = lp_gtimer();
+    while (!mbar_try_wait(b, parity))
+        if (lp_gtimer() - t0 > 2000000000ull) return false;
+    return true;
+}
+
 template <int SX>
 __device__ __forceinline__ float lp_elem(const uint4& w, int q) {
     if (SX == 2) {
@@ -160,11 +185,6 @@ __device__ __forceinline__ float vmax_float(uint32_t m) {
     return __uint_as_float(m);
 }
 
-// Append element (v, id) to the gathered keys when there is room.
-__device__ __forceinline__ void lp_push(LpSmem& s, float v, int id) {
-    const int p = atomicAdd(&s.n, 1);
-    if (p < kLpCandCap) s.keys[p] = ckey(v, id);
-}
 
 // Exact top-n of a chunk whose logits >= theta did not fit the key buffer (ties): the n-th
 // largest value v (with multiplicity) by a bitwise search over counts, the logits above v (fewer
@@ -280,58 +300,33 @@ __device__ int lp_exact_top(const Args& a, LpSmem& s, long long slot, int c0, in
     return cnt;
 }
 
-// Each warp sorts its gathered keys (descending) in place; warp w's keys sit at
-// s.keys[w * kLpWarpCap, + s.wn[w]).  Lists longer than 64 are sorted by the warp with a
-// bitonic network over shared memory.
-__device__ void lp_sort_warp_lists(LpSmem& s) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    unsigned long long* k = s.keys + warp * kLpWarpCap;
-    const int cnt = min(s.wn[warp], kLpWarpCap);
-    if (cnt <= 64) {
-        unsigned long long r[2];
-        r[0] = lane < cnt ? k[lane] : 0ull;
-        r[1] = lane + 32 < cnt ? k[lane + 32] : 0ull;
-        for (int size = 2; size <= 64; size <<= 1)
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                if (stride == 32) {
-                    const unsigned long long hi = r[0] > r[1] ? r[0] : r[1];
-                    const unsigned long long lo = r[0] > r[1] ? r[1] : r[0];
-                    r[0] = hi;
-                    r[1] = lo;
-                } else {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int pos = lane + 32 * h;
-                        const unsigned long long o = __shfl_xor_sync(0xffffffffu, r[h], stride);
-                        const bool keep_max = ((pos & stride) == 0) == ((pos & size) == 0);
-                        r[h] = keep_max ? (r[h] > o ? r[h] : o) : (r[h] < o ? r[h] : o);
-                    }
-                }
-            }
-        if (lane < cnt) k[lane] = r[0];
-        if (lane + 32 < cnt) k[lane + 32] = r[1];
-        __syncwarp();
-        return;
-    }
-    const int P = next_pow2(cnt);
-    for (int i = cnt + lane; i < P; i += 32) k[i] = 0ull;
-    __syncwarp();
-    for (int size = 2; size <= P; size <<= 1)
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = lane; i < P / 2; i += 32) {
-                const int lo = 2 * i - (i & (stride - 1)), hi = lo + stride;
-                const bool desc = (lo & size) == 0;
-                const unsigned long long x = k[lo], y = k[hi];
-                if ((x < y) == desc) { k[lo] = y; k[hi] = x; }
-            }
-            __syncwarp();
+// The n largest of the keys held in `lists` shared-memory lists (list l: n_l keys at
+// keys + l * stride), by rank: every key counts the keys above it (keys are distinct), and a
+// key of rank r < n lands in top[r].  All threads take part; returns min(n, total).
+__device__ int rank_select(const unsigned long long* keys, const int* nl, int lists, int stride, int n,
+                           unsigned long long* top) {
+    int total = 0;
+    for (int l = 0; l < lists; ++l) total += nl[l];
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        int l = 0, r = i;
+        while (r >= nl[l]) { r -= nl[l]; ++l; }
+        const unsigned long long key = keys[l * stride + r];
+        int rank = 0;
+        for (int m = 0; m < lists && rank < n; ++m) {
+            const unsigned long long* km = keys + m * stride;
+            for (int q = 0; q < nl[m]; ++q) rank += km[q] > key;
         }
+        if (rank < n) top[rank] = key;
+    }
+    __syncthreads();
+    return min(n, total);
 }
 
 // One chunk [c0, c1) of target row `slot`: its maximum, its sum of exp relative to it and its
 // top-n list, written to *out.
 template <int SX, bool PEN>
-__device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c1, LpPartial* out, const LpRow& pr) {
+__device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c1, LpPartial* out, const LpRow& pr,
+                         int& nbat) {
     constexpr int EPV = 16 / SX;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned char* rowp = static_cast<const unsigned char*>(a.x) + slot * a.V * SX;
@@ -350,7 +345,8 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
     float edge[EPV];
 #pragma unroll
     for (int q = 0; q < EPV; ++q)
-        edge[q] = eh0 + q < eh1 ? lp_value<PEN>(a, pr, eh0 + q, load_x(a.x, SX, slot * a.V + eh0 + q)) : -INFINITY;
+        edge[q] = (eh0 + q < eh1 && !(PEN && (pen_bits_range(a, pr.b, eh0 + q, 1) & 1u)))
+                      ? load_x(a.x, SX, slot * a.V + eh0 + q) : -INFINITY;
     float tm = -INFINITY, ts = 0.f;
 #pragma unroll
     for (int q = 0; q < EPV; ++q) tm = fmaxf(tm, edge[q]);
@@ -360,12 +356,29 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
     if (lane == 0) s.wn[warp] = 0;                        // keys this warp gathered
     __syncwarp();
     float theta = INFINITY;
-    uint4 wa[kLpVec], wb[kLpVec];
-    auto load = [&](uint4 (&w)[kLpVec], int v0) {
+    // the interior streams through two shared-memory stages, one batch (kLpVec vectors per
+    // thread) each, copied by the bulk-copy engine: CTA batch counter nbat picks the stage
+    // (nbat & 1) and the phase ((nbat >> 1) & 1) of its barrier
+    constexpr int kStep = kLpVec * kLpThreads;
+    const int nb = (nv + kStep - 1) / kStep;
+    auto issue = [&](int q) {                             // thread 0: batch q of this chunk
+        const int st = (nbat + q) & 1;
+        const unsigned bytes = 16u * static_cast<unsigned>(min(kStep, nv - q * kStep));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(reinterpret_cast<uint64_t*>(&s.full[st]), bytes);
+        bulk_g2s(s.stage[st], g + static_cast<long long>(q) * kStep, bytes, reinterpret_cast<uint64_t*>(&s.full[st]));
+    };
+    bool dead = false;                                    // a wait of this thread gave up
+    auto load = [&](uint4 (&w)[kLpVec], int q) {
+        const int st = (nbat + q) & 1;
+        if (!dead && !lp_wait(&s.full[st], ((nbat + q) >> 1) & 1)) {
+            dead = true;
+            atomicOr(&a.row_status[pr.b], DSPARK_ROW_INTERNAL);
+        }
 #pragma unroll
         for (int i = 0; i < kLpVec; ++i) {
-            const int v = v0 + tid + i * kLpThreads;
-            w[i] = v < nv ? __ldg(g + v) : make_uint4(ninf, ninf, ninf, ninf);
+            const int v = q * kStep + tid + i * kLpThreads;
+            w[i] = v < nv ? s.stage[st][tid + i * kLpThreads] : make_uint4(ninf, ninf, ninf, ninf);
         }
     };
     // the logits >= theta of a batch, appended to the warp's list by the lanes holding them
@@ -411,35 +424,14 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
             ts += (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
     };
-    // penalised mode: the flagged tokens of a batch leave the packed words (-inf) and enter the
-    // thread's maximum and sum as x', gathered at once when theta is known (later, for batch 0)
-    auto fold = [&](float xp) {
-        if (xp > tm) {
-            ts = (tm > -INFINITY) ? ts * ex2_approx((tm - xp) * kL2E) : 0.f;
-            tm = xp;
-        }
-        if (tm > -INFINITY) ts += ex2_approx((xp - tm) * kL2E);
-    };
-    auto pen_fix = [&](uint4 (&w)[kLpVec], int v0, bool gather_now) {
-        unsigned long long* k = s.keys + warp * kLpWarpCap;
+    // penalised mode: the tokens the penalty index flags leave the streamed words (-inf); after
+    // the stream they are taken one by one as x' (pen_tail)
+    auto pen_mask = [&](uint4 (&w)[kLpVec], int v0) {
 #pragma unroll
         for (int i = 0; i < kLpVec; ++i) {
             const int v = v0 + tid + i * kLpThreads;
             if (v >= nv) continue;
-            const int e0 = va + v * EPV;
-            const unsigned bits = pen_bits_range(a, pr.b, e0, EPV);
-            if (!bits) continue;
-#pragma unroll
-            for (int q = 0; q < EPV; ++q) {
-                if (!((bits >> q) & 1u)) continue;
-                const float xp = penalise(lp_elem<SX>(w[i], q), token_count(a, pr.b, pr.j, e0 + q), pr.f, pr.p);
-                fold(xp);
-                if (gather_now && xp >= theta && n_top > 0) {
-                    const int pos = atomicAdd(&s.wn[warp], 1);
-                    if (pos < kLpWarpCap) k[pos] = ckey(xp, e0 + q);
-                }
-            }
-            // the flagged lanes leave the packed words: -inf in their halves (bf16) or words (fp32)
+            const unsigned bits = pen_bits_range(a, pr.b, va + v * EPV, EPV);
             uint32_t* wd[4] = {&w[i].x, &w[i].y, &w[i].z, &w[i].w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
@@ -454,57 +446,71 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
             }
         }
     };
-    // batch 0's flagged tokens once theta is known (their logits re-read; the words were masked)
-    auto pen_gather0 = [&]() {
+    // the flagged tokens of [c0, c1), 32 per bitmap word: x' into the thread's maximum and sum,
+    // and gathered when >= theta
+    auto pen_tail = [&]() {
         unsigned long long* k = s.keys + warp * kLpWarpCap;
-        for (int i = 0; i < kLpVec; ++i) {
-            const int v = tid + i * kLpThreads;
-            if (v >= nv) continue;
-            const int e0 = va + v * EPV;
-            unsigned bits = pen_bits_range(a, pr.b, e0, EPV);
+        const int w0 = c0 >> 5, w1 = (c1 + 31) >> 5;
+        for (int w = w0 + tid; w < w1; w += kLpThreads) {
+            const int t0 = w << 5;
+            const int tile = t0 / a.tile_x;
+            unsigned bits = a.pen_bm[(static_cast<long long>(pr.b) * a.tiles_x + tile) * a.bm_words +
+                                     ((t0 - tile * a.tile_x) >> 5)];
+            if (t0 < c0) bits &= ~0u << (c0 - t0);
+            if (t0 + 32 > c1) bits &= (c1 - t0 >= 32) ? ~0u : ((1u << (c1 - t0)) - 1u);
             while (bits) {
-                const int q = __ffs(bits) - 1;
+                const int t = t0 + __ffs(bits) - 1;
                 bits &= bits - 1;
-                const float xp = penalise(load_x(a.x, SX, slot * a.V + e0 + q), token_count(a, pr.b, pr.j, e0 + q),
-                                          pr.f, pr.p);
-                if (xp >= theta) {
+                const float xp = penalise(load_x(a.x, SX, slot * a.V + t), token_count(a, pr.b, pr.j, t), pr.f, pr.p);
+                if (xp > tm) {
+                    ts = (tm > -INFINITY) ? ts * ex2_approx((tm - xp) * kL2E) : 0.f;
+                    tm = xp;
+                }
+                if (tm > -INFINITY) ts += ex2_approx((xp - tm) * kL2E);
+                if (n_top > 0 && xp >= theta) {
                     const int pos = atomicAdd(&s.wn[warp], 1);
-                    if (pos < kLpWarpCap) k[pos] = ckey(xp, e0 + q);
+                    if (pos < kLpWarpCap) k[pos] = ckey(xp, t);
                 }
             }
         }
     };
-    constexpr int kStep = kLpVec * kLpThreads;
-    load(wa, 0);
-    for (int v0 = 0; v0 < max(nv, 1); v0 += 2 * kStep) {
-        // batch v0 in wa (loaded), batch v0 + kStep into wb while wa is reduced
-        if (v0 + kStep < nv) load(wb, v0 + kStep);
-        if (PEN) pen_fix(wa, v0, v0 > 0);
-        reduce(wa);
-        if (v0 == 0 && n_top > 0) {
+    if (tid == 0) {
+        if (nb > 0) issue(0);
+        if (nb > 1) issue(1);
+    }
+    for (int q = 0; q < max(nb, 1); ++q) {
+        const int v0 = q * kStep;
+        uint4 w[kLpVec];
+        if (q < nb) {
+            load(w, q);
+        } else {
+#pragma unroll
+            for (int i = 0; i < kLpVec; ++i) w[i] = make_uint4(ninf, ninf, ninf, ninf);
+        }
+        __syncthreads();                                  // the stage is read: refill it
+        if (tid == 0 && q + 2 < nb) issue(q + 2);
+        if (PEN) pen_mask(w, v0);
+        reduce(w);
+        if (q == 0 && n_top > 0) {
             // theta from the first batch and the edges
             const float wk = warp_kth_largest(tm, (n_top + kLpWarps - 1) / kLpWarps);
             if (lane == 0) s.wth[warp] = wk;
             __syncthreads();
             theta = s.wth[0];
-            for (int q = 1; q < kLpWarps; ++q) theta = fminf(theta, s.wth[q]);
+            for (int k2 = 1; k2 < kLpWarps; ++k2) theta = fminf(theta, s.wth[k2]);
             // the edges' logits >= theta
             unsigned long long* k = s.keys + warp * kLpWarpCap;
 #pragma unroll
-            for (int q = 0; q < EPV; ++q)
-                if (eh0 + q < eh1 && edge[q] >= theta) {
+            for (int e = 0; e < EPV; ++e)
+                if (eh0 + e < eh1 && edge[e] >= theta) {
                     const int pos = atomicAdd(&s.wn[warp], 1);
-                    if (pos < kLpWarpCap) k[pos] = ckey(edge[q], eh0 + q);
+                    if (pos < kLpWarpCap) k[pos] = ckey(edge[e], eh0 + e);
                 }
-            if (PEN) pen_gather0();
         }
-        if (n_top > 0) gather(wa, v0);
-        if (v0 + kStep >= nv) break;
-        if (v0 + 2 * kStep < nv) load(wa, v0 + 2 * kStep);
-        if (PEN) pen_fix(wb, v0 + kStep, true);
-        reduce(wb);
-        if (n_top > 0) gather(wb, v0 + kStep);
+        if (n_top > 0) gather(w, v0);
     }
+    nbat += nb;
+    if (PEN) pen_tail();
     // block (max, sum): warp trees, then the warps in order
     {
         float m = tm, sm = ts;
@@ -523,30 +529,9 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
         bool fits = true;
         for (int q = 0; q < kLpWarps; ++q) fits = fits && s.wn[q] <= kLpWarpCap;
         if (fits) {
-            lp_sort_warp_lists(s);
-            __syncthreads();
-            // warp 0 merges the eight sorted lists: n rounds, lane q < 8 offers list q's head
-            if (tid < 32) {
-                int cur = 0;
-                const int mine_n = lane < kLpWarps ? s.wn[lane] : 0;
-                for (int r = 0; r < n_top; ++r) {
-                    const unsigned long long h = cur < mine_n ? s.keys[lane * kLpWarpCap + cur] : 0ull;
-                    unsigned long long best = h;
-                    for (int off = 16; off; off >>= 1) {
-                        const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, off);
-                        best = y > best ? y : best;
-                    }
-                    if (best == 0ull) break;
-                    if (h == best) ++cur;                  // keys are unique: one lane holds it
-                    if (lane == 0) s.top[r] = best;
-                    cnt = r + 1;
-                }
-                cnt = __shfl_sync(0xffffffffu, cnt, 0);
-                for (int i = lane; i < cnt; i += 32) out->top[i] = TopEntry{ckey_id(s.top[i]), ckey_v(s.top[i])};
-                if (lane == 0) s.n = cnt;
-            }
-            __syncthreads();
-            cnt = s.n;
+            // the chunk's n largest among the warps' gathered keys, by rank
+            cnt = rank_select(s.keys, s.wn, kLpWarps, kLpWarpCap, n_top, s.top);
+            for (int i = tid; i < cnt; i += blockDim.x) out->top[i] = TopEntry{ckey_id(s.top[i]), ckey_v(s.top[i])};
         } else {
             cnt = min(lp_exact_top<SX, PEN>(a, s, slot, c0, c1, va, vb, n_top, pr), n_top);
             for (int i = tid; i < cnt; i += blockDim.x) out->top[i] = TopEntry{ckey_id(s.keys[i]), ckey_v(s.keys[i])};
@@ -565,159 +550,111 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
     }
 }
 
-// Rows of more than kLpMergeLists chunks (vocabularies above 4M): the row's top-n by sorting
-// the chunk lists in batches that fit the key buffer, keeping the best n after each batch.
-__device__ void lp_merge_large(const Args& a, LpSmem& s, long long slot, int b, int j, const LpPartial* part, int S,
-                               const LpRow& pr, bool pen) {
-    const int tid = threadIdx.x;
-    const int W = a.Km + 1;
-    const int n_top = a.n_top;
-    float mm = -INFINITY;
-    for (int c = tid; c < S; c += blockDim.x) mm = fmaxf(mm, __ldcg(&part[c].m));
-    mm = block_max_nan(mm, s.tmax);
-    float sum = 0.f;
-    if (mm > -INFINITY)
-        for (int c = tid; c < S; c += blockDim.x) {
-            const float mc = __ldcg(&part[c].m);
-            if (mc > -INFINITY) sum += __ldcg(&part[c].s) * ex2_approx((mc - mm) * kL2E);
-        }
-    sum = static_cast<float>(block_sum_d(static_cast<double>(sum), s.dwarp));
-    const float lse = mm + logf(sum);
-    if (tid == 0 && a.out_lp) {
-        const int t = a.out_tokens[static_cast<long long>(b) * W + j];
-        const float xt = t >= 0 ? load_x(a.x, a.sx, slot * a.V + t) : 0.f;
-        a.out_lp[static_cast<long long>(b) * W + j] = t >= 0 ? (pen ? lp_value<true>(a, pr, t, xt) : xt) - lse : -INFINITY;
-    }
-    int have = 0;
-    for (int c0 = 0; c0 < S;) {
-        int c1 = c0, room = kLpCandCap - have;
-        while (c1 < S && __ldcg(&part[c1].n) <= room) { room -= __ldcg(&part[c1].n); ++c1; }
-        int base = have;
-        for (int c = c0; c < c1; ++c) {
-            const int nc = __ldcg(&part[c].n);
-            for (int i = tid; i < nc; i += blockDim.x)
-                s.keys[base + i] = ckey(__ldcg(&part[c].top[i].v), __ldcg(&part[c].top[i].id));
-            base += nc;
-        }
-        __syncthreads();
-        sort_keys_desc(s, base);
-        have = min(base, n_top);
-        c0 = c1;
-    }
-    const long long o = (static_cast<long long>(b) * W + j) * n_top;
-    for (int q = tid; q < n_top; q += blockDim.x) {
-        const bool ok = q < have;
-        if (a.out_top_ids) a.out_top_ids[o + q] = ok ? ckey_id(s.keys[q]) : -1;
-        if (a.out_top_lp) a.out_top_lp[o + q] = ok ? ckey_v(s.keys[q]) - lse : -INFINITY;
-    }
-}
-
 // The CTA that completed row `slot` (request b, position j): merge the S chunk partials and
 // write logprob and top_logprobs.  The whole CTA first copies the partials into shared memory
-// in one parallel read (the merge would otherwise wait on L2 once per step), then one warp:
-// LSE = M + log(sum_s S_s exp(m_s - M)) with the chunks in a fixed order (lane l takes chunks
-// l, l + 32, ... in order, then a fixed shuffle tree), and the row's top-n by an n-round merge
-// of the chunks' sorted lists (every round the lanes offer the largest head among their lists
-// and the winner's list advances).
+// in one parallel read; then one warp forms LSE = M + log(sum_c s_c exp(m_c - M)) with the
+// chunks in a fixed order (lane l takes chunks l, l + 32, ... in order, then a fixed shuffle
+// tree), and all threads select the row's top n among the chunks' lists by rank.
 __device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j, const LpPartial* part, int S,
                          const LpRow& pr, bool pen) {
     const int tid = threadIdx.x, lane = tid & 31;
     const int W = a.Km + 1;
     const int n_top = a.n_top;
-    // the partials were written by other CTAs of this launch: read them from L2 (__ldcg)
-    const bool staged = S <= kLpMergeLists && S * n_top <= kLpCandCap;
-    if (S > kLpMergeLists && n_top > 0) {
-        lp_merge_large(a, s, slot, b, j, part, S, pr, pen);
-        return;
-    }
-    for (int c = tid; c < S && c < kLpMergeLists; c += blockDim.x) {   // (more are read from L2)
+    // the partials were written by other CTAs of this launch: read them from L2 (__ldcg);
+    // S <= kLpMergeLists and S * n_top <= kLpCandCap always
+    for (int c = tid; c < S; c += blockDim.x) {
         s.mm[c] = __ldcg(&part[c].m);
         s.ms[c] = __ldcg(&part[c].s);
         s.mn[c] = __ldcg(&part[c].n);
     }
-    if (staged)
-        for (int e = tid; e < S * n_top; e += blockDim.x) {
-            const int c = e / n_top, k = e - c * n_top;
-            s.keys[e] = ckey(__ldcg(&part[c].top[k].v), __ldcg(&part[c].top[k].id));
-        }
+    for (int e = tid; e < S * n_top; e += blockDim.x) {
+        const int c = e / n_top, k = e - c * n_top;
+        s.keys[e] = ckey(__ldcg(&part[c].top[k].v), __ldcg(&part[c].top[k].id));
+    }
     __syncthreads();
-    if (tid >= 32) return;
-    auto pm = [&](int c) { return c < kLpMergeLists ? s.mm[c] : __ldcg(&part[c].m); };
-    auto ps = [&](int c) { return c < kLpMergeLists ? s.ms[c] : __ldcg(&part[c].s); };
-    auto pn = [&](int c) { return c < kLpMergeLists ? s.mn[c] : __ldcg(&part[c].n); };
-    float mm = -INFINITY;
-    for (int c = lane; c < S; c += 32) mm = fmaxf(mm, pm(c));
-    mm = warp_max(mm);
-    float sum = 0.f;
-    if (mm > -INFINITY)
-        for (int c = lane; c < S; c += 32)
-            if (pm(c) > -INFINITY) sum += ps(c) * ex2_approx((pm(c) - mm) * kL2E);
-    sum = warp_sum(sum);
-    const float lse = mm + logf(sum);
-    if (lane == 0 && a.out_lp) {
-        const int t = a.out_tokens[static_cast<long long>(b) * W + j];
-        const float xt = t >= 0 ? load_x(a.x, a.sx, slot * a.V + t) : 0.f;
-        a.out_lp[static_cast<long long>(b) * W + j] = t >= 0 ? (pen ? lp_value<true>(a, pr, t, xt) : xt) - lse : -INFINITY;
+    if (tid < 32) {
+        float mm = -INFINITY;
+        for (int c = lane; c < S; c += 32) mm = fmaxf(mm, s.mm[c]);
+        mm = warp_max(mm);
+        float sum = 0.f;
+        if (mm > -INFINITY)
+            for (int c = lane; c < S; c += 32)
+                if (s.mm[c] > -INFINITY) sum += s.ms[c] * ex2_approx((s.mm[c] - mm) * kL2E);
+        sum = warp_sum(sum);
+        const float lse = mm + logf(sum);
+        if (lane == 0) {
+            s.theta = lse;
+            if (a.out_lp) {
+                const int t = a.out_tokens[static_cast<long long>(b) * W + j];
+                const float xt = t >= 0 ? load_x(a.x, a.sx, slot * a.V + t) : 0.f;
+                a.out_lp[static_cast<long long>(b) * W + j] =
+                    t >= 0 ? (pen ? lp_value<true>(a, pr, t, xt) : xt) - lse : -INFINITY;
+            }
+        }
     }
     if (n_top <= 0) return;
-    // cursor of every chunk list: a chunk list c is read at position cur[c / 32] of lane c % 32's
-    // slot c / 32 (kept in shared memory for up to kLpMergeLists lists, else in registers' reach)
-    int* cur = s.mcur;
-    for (int c = lane; c < S && c < kLpMergeLists; c += 32) cur[c] = 0;
-    __syncwarp();
+    // the row's n largest among the chunks' lists, by rank (the lse is in s.theta after the barrier)
+    const int cnt = rank_select(s.keys, s.mn, S, n_top, n_top, s.top);
+    const float lse = s.theta;
     const long long o = (static_cast<long long>(b) * W + j) * n_top;
-    for (int q = 0; q < n_top; ++q) {
-        unsigned long long best = 0ull;
-        int bc = -1;
-        for (int c = lane; c < S && c < kLpMergeLists; c += 32) {
-            const int k = cur[c];
-            if (k < pn(c)) {
-                const unsigned long long key = staged ? s.keys[c * n_top + k]
-                                                      : ckey(__ldcg(&part[c].top[k].v), __ldcg(&part[c].top[k].id));
-                if (bc < 0 || key > best) { best = key; bc = c; }
-            }
-        }
-        unsigned long long wbest = best;
-        for (int off = 16; off; off >>= 1) {
-            const unsigned long long y = __shfl_xor_sync(0xffffffffu, wbest, off);
-            wbest = y > wbest ? y : wbest;
-        }
-        const unsigned who = __ballot_sync(0xffffffffu, bc >= 0 && best == wbest);
-        if (who == 0u) {                                   // fewer logits than n_top in the row
-            if (lane == 0) {
-                if (a.out_top_ids) a.out_top_ids[o + q] = -1;
-                if (a.out_top_lp) a.out_top_lp[o + q] = -INFINITY;
-            }
-            continue;
-        }
-        if (lane == __ffs(who) - 1) cur[bc] += 1;
-        if (lane == 0) {
-            if (a.out_top_ids) a.out_top_ids[o + q] = ckey_id(wbest);
-            if (a.out_top_lp) a.out_top_lp[o + q] = ckey_v(wbest) - lse;
-        }
-        __syncwarp();
+    for (int q = tid; q < n_top; q += blockDim.x) {
+        const bool ok = q < cnt;
+        if (a.out_top_ids) a.out_top_ids[o + q] = ok ? ckey_id(s.top[q]) : -1;
+        if (a.out_top_lp) a.out_top_lp[o + q] = ok ? ckey_v(s.top[q]) - lse : -INFINITY;
     }
 }
 
 // PEN_MODE: the call asked for penalised logprobs (rows of requests without a penalty still
 // take the raw path: their x' is x and they have no penalty index).
 template <int SX, bool PEN_MODE>
-__global__ void __launch_bounds__(kLpThreads, 1) logprob_kernel(Args a) {
+__global__ void __launch_bounds__(kLpThreads, kLpBlocksPerSm) logprob_kernel(Args a) {
     pdl_enter();
     extern __shared__ __align__(16) unsigned char lp_raw[];
     LpSmem& s = *reinterpret_cast<LpSmem*>(lp_raw);
-    if (static_cast<int>(blockIdx.x) >= a.lp_list[0]) return;
+    const int R = a.lp_list[0];
+    if (R == 0) return;
+    if (threadIdx.x == 0) {
+        mbar_init(reinterpret_cast<uint64_t*>(&s.full[0]), 1);
+        mbar_init(reinterpret_cast<uint64_t*>(&s.full[1]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    int nbat = 0;                                         // batches this CTA has streamed
     const int W = a.Km + 1;
-    const int row = a.lp_list[1 + blockIdx.x];            // b * W + j
-    const int b = row / W, j = row % W;
-    LpPartial* part = a.lp_part + row;
-    const dspark_row_params_t r = a.rows[b];
-    const LpRow pr{b, j, r.frequency_penalty, r.presence_penalty};
-    const bool pen = PEN_MODE && has_penalty(r);
-    if (PEN_MODE && pen) lp_chunk<SX, PEN_MODE>(a, s, row, 0, a.V, part, pr);
-    else lp_chunk<SX, false>(a, s, row, 0, a.V, part, pr);
-    __syncthreads();                                      // the partial (global) is visible to the CTA
-    lp_merge(a, s, row, b, j, part, 1, pr, pen);
+    // chunks per row: all R * S chunks in one wave of this grid
+    const int S = max(1, min(min(kLpMaxChunks, static_cast<int>(gridDim.x) / R), a.V / kLpMinChunk));
+    const int chunk = ((a.V + S - 1) / S + 7) / 8 * 8;
+    const int items = R * S;
+    for (;;) {
+        // the next (row, chunk) item, from a counter: no CTA idles while items remain
+        if (threadIdx.x == 0) s.item = atomicAdd(&a.plan->pad[2], 1);
+        __syncthreads();
+        const int it = s.item;
+        __syncthreads();
+        if (it >= items) break;
+        const int p = it / S, c = it - p * S;                 // listed row p, its chunk c
+        const int row = a.lp_list[1 + p];                    // b * W + j
+        const int b = row / W, j = row % W;
+        const int c0 = c * chunk, c1 = min(a.V, c0 + chunk);
+        LpPartial* part = a.lp_part + static_cast<long long>(p) * S;   // the row's S partials
+        const dspark_row_params_t r = a.rows[b];
+        const LpRow pr{b, j, r.frequency_penalty, r.presence_penalty};
+        const bool pen = PEN_MODE && has_penalty(r);
+        if (PEN_MODE && pen) lp_chunk<SX, PEN_MODE>(a, s, row, c0, c1, part + c, pr, nbat);
+        else lp_chunk<SX, false>(a, s, row, c0, c1, part + c, pr, nbat);
+        // the CTA finishing the row's last chunk merges them: partial written, then counted
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            s.last = atomicAdd(&a.lp_done[p], 1) == S - 1;
+        }
+        __syncthreads();
+        if (s.last) {
+            __threadfence();
+            lp_merge(a, s, row, b, j, part, S, pr, pen);
+        }
+        __syncthreads();                                     // shared memory reused by the next item
+    }
 }
 
 }  // namespace
@@ -725,7 +662,7 @@ __global__ void __launch_bounds__(kLpThreads, 1) logprob_kernel(Args a) {
 template <int SX, bool PEN>
 cudaError_t launch_lp(const Args& a, cudaStream_t s) {
     const size_t smem = sizeof(LpSmem);
-    const int grid = a.xslots;                             // one CTA per row that may be listed
+    const int grid = kLpBlocksPerSm * a.grid_ss;           // persistent: four CTAs per SM
     cudaError_t e = cudaFuncSetAttribute(logprob_kernel<SX, PEN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;

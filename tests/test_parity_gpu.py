@@ -233,9 +233,9 @@ def test_expired_waits_report_internal(runner):
     """A test build whose streaming-pass waits all count as expired: every valid request reports
     DSPARK_ROW_INTERNAL (an invalid one keeps its own bits too), with no output but the error
     padding, and the GPU context stays usable (the normal build then matches the oracle)."""
-    from sample_verify_epilogue_gb300 import binding, build
-    lib = binding.open_library(build.build_variant("expired_waits", ["-DDSPARK_TEST_EXPIRED_WAITS"],
-                                                   ["stream_stats.cu"]))
+    from sample_verify_epilogue_gb300 import binding
+    from sample_verify_epilogue_gb300.build import build_variant
+    lib = binding.open_library(build_variant("expired_waits", ["-DDSPARK_TEST_EXPIRED_WAITS"], ["stream_stats.cu"]))
     batch = configs.build("b256k16v262144_mixed", B=18)
     batch.rows["temperature"][4] = -1.0                    # an invalid request
     call = runner(batch)
