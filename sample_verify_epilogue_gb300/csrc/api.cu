@@ -33,7 +33,7 @@ struct Layout {
     long long seg_max;
     size_t off_plan, off_req_n, off_fin_list, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_q;
     size_t off_pen_hdr, off_pen_bm, off_pen_ent, off_draft_base, off_xout, off_kept, off_qout, off_req;
-    size_t off_lp_part, off_t2d;
+    size_t off_lp_part, off_t2d, off_lp_cand;
     size_t zero_bytes;   // the call record cleared by every call: plan, logprob row counters, list count
     size_t total;
 };
@@ -102,6 +102,7 @@ Layout make_layout(const dspark_params_t* p) {
     L.off_req = take(static_cast<size_t>(B) * sizeof(ReqOut));
     L.off_lp_part = take(static_cast<size_t>(L.lp_chunks) * sizeof(LpPartial));
     L.off_t2d = take(qo.layout == kQReduced ? static_cast<size_t>(V) * sizeof(int) : 0);
+    L.off_lp_cand = take(static_cast<size_t>(kLpMaxGrid) * kLpCandPerChunk * sizeof(unsigned long long));
     L.total = o;
     return L;
 }
@@ -174,6 +175,7 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     a.lp_list = a.lp_done + L.xslots;
     a.lp_part = at<LpPartial>(ws, L.off_lp_part);
     a.t2d = qo.layout == kQReduced ? at<int>(ws, L.off_t2d) : nullptr;
+    a.lp_cand = at<unsigned long long>(ws, L.off_lp_cand);
 
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DSPARK_ERR_CUDA;

@@ -41,6 +41,7 @@ constexpr int kMergeCap = 8192;                                // merged candida
 constexpr int kMaxB = DSPARK_MAX_B;
 constexpr int kLpMaxChunks = 16;                               // chunks per row in the logprob pass
 constexpr int kLpMaxGrid = 4 * 1024;                           // CTAs of the logprob pass at most
+constexpr int kLpCandPerChunk = 128;                           // unselected keys a chunk may hand on
 
 // ---------------------------------------------------------------- records in the workspace
 enum UnitKind : int { kUnitX = 0, kUnitQ = 1 };
@@ -133,8 +134,8 @@ struct TopEntry { int id; float v; };
 struct LpPartial {
     float m;
     float s;
-    int n;
-    int pad;
+    int n;               // keys of this chunk: in top[], or (listed) in the candidate buffer
+    int listed;          // 1: the chunk's gathered keys were written unselected to lp_cand
     TopEntry top[DSPARK_MAX_TOP_LOGPROBS];
 };
 
@@ -201,6 +202,7 @@ struct Args {
     int* lp_done;          // [xslots]: chunks done of each listed row (zeroed by every call)
     LpPartial* lp_part;    // [lp_chunks]: the listed rows' chunk partials, row p's S at [p*S, p*S+S)
     int* t2d;              // reduced: [V] draft id of each target id, -1 for none (built by prep)
+    unsigned long long* lp_cand;   // [kLpMaxGrid * kLpCandPerChunk]: chunk keys left to the row merge
 };
 
 // ---------------------------------------------------------------- small helpers

@@ -12,10 +12,11 @@
 //   - the chunk's maximum m and its sum of exp(x - m) (per thread a running maximum, the sum
 //     rescaled at most once per batch; then a fixed reduction order);
 //   - the chunk's n largest logits by (value descending, id ascending).  After the first batch,
-//     theta = the least over the 8 warps of each warp's ceil(n/8)-th largest thread maximum:
+//     theta = the n-th largest of the 256 threads' maxima (a bitwise search over block counts):
 //     at least n distinct logits of that batch reach it, so every one of the chunk's top n does,
 //     and the logits >= theta of every batch are gathered as they stream by; the chunk's top n
-//     are then the gathered logits of rank < n (each counts the gathered logits above it).  When ties put more logits >= theta
+//     are then found among the gathered logits: the n-th largest value by a bitwise search,
+//     and the logits at or above it ranked.  When ties put more logits >= theta
 //     than fit, the chunk is settled exactly from L2: the n-th largest value v by a bitwise
 //     search over counts, the logits above v, then the lowest ids equal to v.
 // The CTA that completes a row's last chunk (a counter per row) merges the S partials in a
@@ -44,6 +45,7 @@ constexpr int kLpVec = 4;                    // 16-byte vectors per thread and b
 constexpr int kLpWarpCap = kLpCandCap / kLpWarps;
 constexpr int kLpMergeLists = kLpMaxChunks;  // chunk partials the merge copies to shared memory
 constexpr int kLpMinChunk = 8192;            // logits per chunk at least
+constexpr int kLpSelCap = 256;               // keys at the n-th largest value and above, ranked directly
 constexpr float kL2E = 1.4426950408889634f;
 
 struct LpSmem {
@@ -51,10 +53,11 @@ struct LpSmem {
     unsigned long long full[2];            // their mbarriers
     unsigned long long keys[kLpCandCap];   // (fkey(value) << 32) | (0xFFFFFFFF - id); warp w: [w*kLpWarpCap, ...)
     float tmax[kLpThreads];
-    float wth[kLpWarps];
     float wm[kLpWarps];
     float wsum[kLpWarps];
     int wcnt[kLpWarps + 1];
+    int scnt[2][kLpWarps];                 // top_select's per-warp counts (two alternating sets)
+    unsigned long long sel[kLpSelCap];     // top_select's keys reaching the threshold
     int wn[kLpWarps];                      // keys each warp gathered
     double dwarp[33];
     int n;
@@ -322,11 +325,74 @@ __device__ int rank_select(const unsigned long long* keys, const int* nl, int li
     return min(n, total);
 }
 
+// The n largest of the keys held in the lists (as rank_select), for many keys: the n-th largest
+// value v (32-bit value key, with multiplicity) by a bitwise search over counts, then only the
+// keys of value >= v (n and their ties) ranked.  Falls back to rank_select over everything when
+// ties put more than kLpSelCap keys at v or above.
+__device__ int top_select(LpSmem& s, const unsigned long long* keys, const int* nl, int lists, int stride, int n,
+                          unsigned long long* top) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int total = 0;
+    for (int l = 0; l < lists; ++l) total += nl[l];
+    if (total <= 2 * n || total > kLpThreads * 8) return rank_select(keys, nl, lists, stride, n, top);
+    uint32_t mine[8];                                     // this thread's keys' value parts (0: none)
+    unsigned long long full[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int i = tid + r * kLpThreads;
+        full[r] = 0ull;
+        if (i < total) {
+            int l = 0, q = i;
+            while (q >= nl[l]) { q -= nl[l]; ++l; }
+            full[r] = keys[l * stride + q];
+        }
+        mine[r] = static_cast<uint32_t>(full[r] >> 32);
+    }
+    // block count of value keys >= cand: warp sums, alternating shared sets (one barrier a step)
+    auto count_ge = [&](uint32_t cand, int set) {
+        int c = 0;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) c += (full[r] != 0ull && mine[r] >= cand) ? 1 : 0;
+        c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c)));
+        if (lane == 0) s.scnt[set][warp] = c;
+        __syncthreads();
+        int t = 0;
+        for (int w = 0; w < kLpWarps; ++w) t += s.scnt[set][w];
+        return t;
+    };
+    uint32_t v = 0u;
+    int set = 0;
+    for (int bit = 31; bit >= 0; --bit, set ^= 1)
+        if (count_ge(v | (1u << bit), set) >= n) v |= 1u << bit;
+    // the keys of value >= v, compacted, then ranked
+    if (tid == 0) s.n = 0;
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        if (full[r] != 0ull && mine[r] >= v) {
+            const int p = atomicAdd(&s.n, 1);
+            if (p < kLpSelCap) s.sel[p] = full[r];
+        }
+    __syncthreads();
+    const int m = s.n;
+    if (m > kLpSelCap) return rank_select(keys, nl, lists, stride, n, top);
+    for (int i = tid; i < m; i += blockDim.x) {
+        const unsigned long long key = s.sel[i];
+        int rank = 0;
+        for (int q = 0; q < m; ++q) rank += s.sel[q] > key;
+        if (rank < n) top[rank] = key;
+    }
+    __syncthreads();
+    return min(n, total);
+}
+
 // One chunk [c0, c1) of target row `slot`: its maximum, its sum of exp relative to it and its
 // top-n list, written to *out.
+// cand: when non-null, a chunk whose gathered keys all fit (at most kLpCandPerChunk) writes them
+// there unselected and leaves the selection to the row merge.
 template <int SX, bool PEN>
 __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c1, LpPartial* out, const LpRow& pr,
-                         int& nbat) {
+                         int& nbat, unsigned long long* cand) {
     constexpr int EPV = 16 / SX;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned char* rowp = static_cast<const unsigned char*>(a.x) + slot * a.V * SX;
@@ -492,12 +558,13 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
         if (PEN) pen_mask(w, v0);
         reduce(w);
         if (q == 0 && n_top > 0) {
-            // theta from the first batch and the edges
-            const float wk = warp_kth_largest(tm, (n_top + kLpWarps - 1) / kLpWarps);
-            if (lane == 0) s.wth[warp] = wk;
-            __syncthreads();
-            theta = s.wth[0];
-            for (int k2 = 1; k2 < kLpWarps; ++k2) theta = fminf(theta, s.wth[k2]);
+            // theta from the first batch and the edges: the n-th largest of the threads' maxima
+            // (a bitwise search over block counts), so at least n logits of the chunk reach it
+            const uint32_t mykey = fkey(tm);
+            uint32_t th = 0u;
+            for (int bit = 31; bit >= 0; --bit)
+                if (__syncthreads_count(mykey >= (th | (1u << bit))) >= n_top) th |= 1u << bit;
+            theta = key_to_f(th);
             // the edges' logits >= theta
             unsigned long long* k = s.keys + warp * kLpWarpCap;
 #pragma unroll
@@ -525,12 +592,23 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
     }
     __syncthreads();
     int cnt = 0;
+    int listed = 0;
     if (n_top > 0) {
         bool fits = true;
-        for (int q = 0; q < kLpWarps; ++q) fits = fits && s.wn[q] <= kLpWarpCap;
-        if (fits) {
+        int total = 0, before = 0;
+        for (int q = 0; q < kLpWarps; ++q) {
+            fits = fits && s.wn[q] <= kLpWarpCap;
+            total += s.wn[q];
+            if (q < warp) before += s.wn[q];
+        }
+        if (fits && cand && total <= kLpCandPerChunk) {
+            // hand the gathered keys on unselected: each warp writes its list at its offset
+            for (int i = lane; i < s.wn[warp]; i += 32) cand[before + i] = s.keys[warp * kLpWarpCap + i];
+            cnt = total;
+            listed = 1;
+        } else if (fits) {
             // the chunk's n largest among the warps' gathered keys, by rank
-            cnt = rank_select(s.keys, s.wn, kLpWarps, kLpWarpCap, n_top, s.top);
+            cnt = top_select(s, s.keys, s.wn, kLpWarps, kLpWarpCap, n_top, s.top);
             for (int i = tid; i < cnt; i += blockDim.x) out->top[i] = TopEntry{ckey_id(s.top[i]), ckey_v(s.top[i])};
         } else {
             cnt = min(lp_exact_top<SX, PEN>(a, s, slot, c0, c1, va, vb, n_top, pr), n_top);
@@ -547,6 +625,7 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
         out->m = m;
         out->s = sm;
         out->n = cnt;
+        out->listed = listed;
     }
 }
 
@@ -555,22 +634,34 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
 // in one parallel read; then one warp forms LSE = M + log(sum_c s_c exp(m_c - M)) with the
 // chunks in a fixed order (lane l takes chunks l, l + 32, ... in order, then a fixed shuffle
 // tree), and all threads select the row's top n among the chunks' lists by rank.
-__device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j, const LpPartial* part, int S,
-                         const LpRow& pr, bool pen) {
+__device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j, const LpPartial* part,
+                         const unsigned long long* cands, int S, const LpRow& pr, bool pen) {
     const int tid = threadIdx.x, lane = tid & 31;
     const int W = a.Km + 1;
     const int n_top = a.n_top;
-    // the partials were written by other CTAs of this launch: read them from L2 (__ldcg);
-    // S <= kLpMergeLists and S * n_top <= kLpCandCap always
+    // the partials were written by other CTAs of this launch: read them from L2 (__ldcg).  Each
+    // chunk's keys (its top list, or its unselected candidates) are staged one after another;
+    // S <= kLpMergeLists chunks of at most kLpCandPerChunk keys fit the key buffer
+    static_assert(kLpMergeLists * kLpCandPerChunk <= kLpCandCap, "merge staging");
     for (int c = tid; c < S; c += blockDim.x) {
         s.mm[c] = __ldcg(&part[c].m);
         s.ms[c] = __ldcg(&part[c].s);
         s.mn[c] = __ldcg(&part[c].n);
     }
-    for (int e = tid; e < S * n_top; e += blockDim.x) {
-        const int c = e / n_top, k = e - c * n_top;
-        s.keys[e] = ckey(__ldcg(&part[c].top[k].v), __ldcg(&part[c].top[k].id));
+    __syncthreads();
+    int off = 0;
+    for (int c = 0; c < S; ++c) {
+        const int nc = s.mn[c];
+        if (__ldcg(&part[c].listed)) {
+            const unsigned long long* src = cands + static_cast<long long>(c) * kLpCandPerChunk;
+            for (int i = tid; i < nc; i += blockDim.x) s.keys[off + i] = __ldcg(src + i);
+        } else {
+            for (int i = tid; i < nc; i += blockDim.x)
+                s.keys[off + i] = ckey(__ldcg(&part[c].top[i].v), __ldcg(&part[c].top[i].id));
+        }
+        off += nc;
     }
+    if (tid == 0) s.wcnt[0] = off;
     __syncthreads();
     if (tid < 32) {
         float mm = -INFINITY;
@@ -594,7 +685,7 @@ __device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j,
     }
     if (n_top <= 0) return;
     // the row's n largest among the chunks' lists, by rank (the lse is in s.theta after the barrier)
-    const int cnt = rank_select(s.keys, s.mn, S, n_top, n_top, s.top);
+    const int cnt = top_select(s, s.keys, s.wcnt, 1, 0, n_top, s.top);
     const float lse = s.theta;
     const long long o = (static_cast<long long>(b) * W + j) * n_top;
     for (int q = tid; q < n_top; q += blockDim.x) {
@@ -640,8 +731,10 @@ __global__ void __launch_bounds__(kLpThreads, kLpBlocksPerSm) logprob_kernel(Arg
         const dspark_row_params_t r = a.rows[b];
         const LpRow pr{b, j, r.frequency_penalty, r.presence_penalty};
         const bool pen = PEN_MODE && has_penalty(r);
-        if (PEN_MODE && pen) lp_chunk<SX, PEN_MODE>(a, s, row, c0, c1, part + c, pr, nbat);
-        else lp_chunk<SX, false>(a, s, row, c0, c1, part + c, pr, nbat);
+        unsigned long long* cands = a.lp_cand + static_cast<long long>(p) * S * kLpCandPerChunk;
+        unsigned long long* cand = S > 1 ? cands + static_cast<long long>(c) * kLpCandPerChunk : nullptr;
+        if (PEN_MODE && pen) lp_chunk<SX, PEN_MODE>(a, s, row, c0, c1, part + c, pr, nbat, cand);
+        else lp_chunk<SX, false>(a, s, row, c0, c1, part + c, pr, nbat, cand);
         // the CTA finishing the row's last chunk merges them: partial written, then counted
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -651,7 +744,7 @@ __global__ void __launch_bounds__(kLpThreads, kLpBlocksPerSm) logprob_kernel(Arg
         __syncthreads();
         if (s.last) {
             __threadfence();
-            lp_merge(a, s, row, b, j, part, S, pr, pen);
+            lp_merge(a, s, row, b, j, part, cands, S, pr, pen);
         }
         __syncthreads();                                     // shared memory reused by the next item
     }
