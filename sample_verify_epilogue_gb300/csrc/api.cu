@@ -1,4 +1,5 @@
 // Host side of the C ABI: argument checks, workspace layout, the launch sequence.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -34,6 +35,7 @@ struct Layout {
     size_t off_plan, off_req_n, off_fin_list, off_units, off_ts_x, off_ts_q, off_cand_x, off_cand_q;
     size_t off_pen_hdr, off_pen_bm, off_pen_ent, off_draft_base, off_xout, off_kept, off_qout, off_req;
     size_t off_lp_part, off_t2d, off_lp_cand;
+    bool lp_cand_alias;
     size_t zero_bytes;   // the call record cleared by every call: plan, logprob row counters, list count
     size_t total;
 };
@@ -102,7 +104,14 @@ Layout make_layout(const dspark_params_t* p) {
     L.off_req = take(static_cast<size_t>(B) * sizeof(ReqOut));
     L.off_lp_part = take(static_cast<size_t>(L.lp_chunks) * sizeof(LpPartial));
     L.off_t2d = take(qo.layout == kQReduced ? static_cast<size_t>(V) * sizeof(int) : 0);
-    L.off_lp_cand = take(static_cast<size_t>(kLpMaxGrid) * kLpCandPerChunk * sizeof(unsigned long long));
+    // the logprob pass's chunk candidates (R * S <= its grid and <= xslots * kLpMaxChunks chunks)
+    // live in the streaming pass's target candidate lists, dead by then, when those are large
+    // enough, else in a region of their own
+    const size_t lp_cand_bytes = static_cast<size_t>(std::min<long long>(kLpMaxGrid, static_cast<long long>(L.xslots) *
+                                                                                      kLpMaxChunks)) *
+                                 kLpCandPerChunk * sizeof(unsigned long long);
+    L.lp_cand_alias = xt * kCandPenGlobal * sizeof(Cand) >= lp_cand_bytes;
+    L.off_lp_cand = L.lp_cand_alias ? L.off_cand_x : take(lp_cand_bytes);
     L.total = o;
     return L;
 }

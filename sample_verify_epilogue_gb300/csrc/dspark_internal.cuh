@@ -202,7 +202,8 @@ struct Args {
     int* lp_done;          // [xslots]: chunks done of each listed row (zeroed by every call)
     LpPartial* lp_part;    // [lp_chunks]: the listed rows' chunk partials, row p's S at [p*S, p*S+S)
     int* t2d;              // reduced: [V] draft id of each target id, -1 for none (built by prep)
-    unsigned long long* lp_cand;   // [kLpMaxGrid * kLpCandPerChunk]: chunk keys left to the row merge
+    unsigned long long* lp_cand;   // chunk keys left to the row merge, kLpCandPerChunk per chunk (may
+                                   // share the target candidate lists' space, unused by then)
 };
 
 // ---------------------------------------------------------------- small helpers
