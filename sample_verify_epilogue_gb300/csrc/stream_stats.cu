@@ -237,25 +237,14 @@ __device__ __forceinline__ void warp_merge_ms(float& m, float& s, float scale) {
 
 // ------------------------------------------------------------------ warp-cooperative appends
 // Append the elements of one 16-byte vector flagged in `mask` (bit q = element q) to one of
-// the segment's candidate lists in global memory: one ballot, one prefix across lanes and one
-// shared atomic (the list's counter) per warp.
-// Every lane of the warp calls it (lanes without candidates pass mask = 0).
+// the segment's candidate lists in global memory: each lane with candidates takes its
+// positions with one shared atomic on the list's counter (a lane-wide prefix and a single
+// atomic per warp was a longer dependency chain in this per-tile step).
 template <int SX>
 __device__ __forceinline__ void warp_append(Cand* buf, int* cnt, int cap, unsigned mask, const uint4& w, int e,
                                             int tag) {
-    const unsigned any = __ballot_sync(0xffffffffu, mask != 0u);
-    if (!any) return;
-    const int lane = threadIdx.x & 31;
-    const int n = __popc(mask);
-    int incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    int base = 0;
-    if (lane == 31) base = atomicAdd(cnt, incl);
-    base = __shfl_sync(0xffffffffu, base, 31) + incl - n;
+    if (!mask) return;
+    int base = atomicAdd(cnt, __popc(mask));
     while (mask) {
         const int q = __ffs(mask) - 1;
         mask &= mask - 1u;
