@@ -107,7 +107,7 @@ struct XRowOut {
     float  m_pen;        // penalised max
     float  tau;          // support threshold on x'
     float  c_l2e;        // log2(e)/T
-    float  pad0;
+    float  kth;          // list rows: the k-th largest x' (top-k threshold); -inf when not known
     int    n_kept;
     int    top_k;        // top_k still to apply (whole-row path), 0 = none
     double Z;            // sum of support weights exp2((x'-m_pen)*c_l2e)

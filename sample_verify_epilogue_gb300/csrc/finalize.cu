@@ -638,6 +638,7 @@ __device__ void finalize_x(const Args& a, FinSmem& s, int slot, int b, int j) {
     const int nseg = a.nseg_x;
     const TileStats* ts = a.ts_x + static_cast<long long>(slot) * nseg;
     XRowOut o{};
+    o.kth = -INFINITY;                                    // not kept by the block path
     o.mode = kModeInactive;
     float mr = -INFINITY, mp = -INFINITY;
     int fl = 0;
@@ -794,7 +795,7 @@ __device__ void finalize_row(const Args& a, FinSmem& s, int slot) {
     if (slot < a.xslots) {
         const int b = slot / (a.Km + 1), j = slot % (a.Km + 1);
         if ((a.row_status[b] & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || j > a.rows[b].num_drafts) {
-            if (threadIdx.x == 0) { XRowOut o{}; o.mode = kModeInactive; a.xout[slot] = o; }
+            if (threadIdx.x == 0) { XRowOut o{}; o.mode = kModeInactive; o.kth = -INFINITY; a.xout[slot] = o; }
             return;
         }
         finalize_x(a, s, slot, b, j);

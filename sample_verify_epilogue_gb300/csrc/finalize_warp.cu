@@ -251,8 +251,10 @@ __device__ int warp_survivors(WarpSmem& w, int n, uint32_t kth) {
 
 // Survivors of the staged keys for a top-k (1 <= k <= n): the k-th largest key, then the keys
 // reaching it, sorted.
-__device__ int warp_topk_survivors(WarpSmem& w, int n, int k) {
-    return warp_survivors(w, n, warp_kth(w, n, k));
+__device__ int warp_topk_survivors(WarpSmem& w, int n, int k, uint32_t* kth_out = nullptr) {
+    const uint32_t kth = warp_kth(w, n, k);
+    if (kth_out) *kth_out = kth;
+    return warp_survivors(w, n, kth);
 }
 
 // Nucleus over the sorted survivors w.sk[0..cnt) with weights wfn(value) (fixed order: lane
@@ -335,6 +337,7 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
     }
     XRowOut o{};
     o.mode = kModeInactive;
+    o.kth = -INFINITY;
     if ((fl & kTileBad) || !isfinite(mr) || !isfinite(mp)) {
         if (lane == 0) {
             atomicOr(&a.row_status[b], DSPARK_ROW_NONFINITE);
@@ -374,8 +377,10 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
         const WCands cs{a.cand_x + static_cast<long long>(slot) * nseg * kCandPenGlobal, kCandPenGlobal, nseg};
         const int n = warp_stage(w, ts, cs, k, cached ? mine.n_pen : -1);
         if (n < k) return false;               // too many candidates to stage, or fewer than k
-        const int cnt = warp_topk_survivors(w, n, k);
+        uint32_t kth = 0u;
+        const int cnt = warp_topk_survivors(w, n, k, &kth);
         if (cnt <= 0) return false;
+        o.kth = key_to_f(kth);
         double zk;
         const int kept = warp_nucleus(w, cnt, r.top_p, [&](float v) { return target_weight(v, mp, c_l2e); }, &zk,
                                       a.kept + static_cast<long long>(slot) * kKeptCap);
@@ -501,7 +506,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) row_finalize_warp_kernel(A
     if (row < a.xslots) {
         const int b = row / (a.Km + 1), j = row % (a.Km + 1);
         if ((a.row_status[b] & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_DRAFT)) || j > a.rows[b].num_drafts) {
-            if (lane == 0) { XRowOut o{}; o.mode = kModeInactive; a.xout[row] = o; }
+            if (lane == 0) { XRowOut o{}; o.mode = kModeInactive; o.kth = -INFINITY; a.xout[row] = o; }
         } else {
             done = warp_finalize_x(w, a, row, b);
         }

@@ -11,7 +11,10 @@
 // the next batch's loads in flight while the current one is reduced, for
 //   - the chunk's maximum m and its sum of exp(x - m) (per thread a running maximum, the sum
 //     rescaled at most once per batch; then a fixed reduction order);
-//   - the chunk's n largest logits by (value descending, id ascending).  After the first batch,
+//   - the chunk's n largest logits by (value descending, id ascending).  For a row settled by
+//     a top-k list (k >= n) theta is the row's k-th largest penalised logit: at least k logits
+//     of the row reach it (their raw values are no smaller when the penalties are not
+//     negative), so every one of the row's top n does.  Otherwise, after the first batch,
 //     theta = the n-th largest of the 256 threads' maxima (a bitwise search over block counts):
 //     at least n distinct logits of that batch reach it, so every one of the chunk's top n does,
 //     and the logits >= theta of every batch are gathered as they stream by; the chunk's top n
@@ -391,8 +394,10 @@ __device__ int top_select(LpSmem& s, const unsigned long long* keys, const int* 
 // cand: when non-null, a chunk whose gathered keys all fit (at most kLpCandPerChunk) writes them
 // there unselected and leaves the selection to the row merge.
 template <int SX, bool PEN>
+// theta_known: a lower bound of the row's n-th largest logit known before the pass (the row's
+// top-k threshold, below), else -inf with known == false.
 __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c1, LpPartial* out, const LpRow& pr,
-                         int& nbat, unsigned long long* cand) {
+                         int& nbat, unsigned long long* cand, bool known, float theta_known) {
     constexpr int EPV = 16 / SX;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const unsigned char* rowp = static_cast<const unsigned char*>(a.x) + slot * a.V * SX;
@@ -558,13 +563,17 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
         if (PEN) pen_mask(w, v0);
         reduce(w);
         if (q == 0 && n_top > 0) {
-            // theta from the first batch and the edges: the n-th largest of the threads' maxima
-            // (a bitwise search over block counts), so at least n logits of the chunk reach it
-            const uint32_t mykey = fkey(tm);
-            uint32_t th = 0u;
-            for (int bit = 31; bit >= 0; --bit)
-                if (__syncthreads_count(mykey >= (th | (1u << bit))) >= n_top) th |= 1u << bit;
-            theta = key_to_f(th);
+            if (known) {
+                theta = theta_known;
+            } else {
+                // theta from the first batch and the edges: the n-th largest of the threads'
+                // maxima (a bitwise search over block counts), so at least n logits reach it
+                const uint32_t mykey = fkey(tm);
+                uint32_t th = 0u;
+                for (int bit = 31; bit >= 0; --bit)
+                    if (__syncthreads_count(mykey >= (th | (1u << bit))) >= n_top) th |= 1u << bit;
+                theta = key_to_f(th);
+            }
             // the edges' logits >= theta
             unsigned long long* k = s.keys + warp * kLpWarpCap;
 #pragma unroll
@@ -731,10 +740,16 @@ __global__ void __launch_bounds__(kLpThreads, kLpBlocksPerSm) logprob_kernel(Arg
         const dspark_row_params_t r = a.rows[b];
         const LpRow pr{b, j, r.frequency_penalty, r.presence_penalty};
         const bool pen = PEN_MODE && has_penalty(r);
+        // a target row settled by a top-k list with k >= n: its k-th largest x' bounds the n-th
+        // largest logit from below (x' itself in penalised mode; the raw x >= x' when the
+        // penalties are not negative), so the pass gathers from there without a search
+        const XRowOut xo = a.xout[row];
+        const bool known = a.n_top > 0 && xo.mode == kModeList && r.top_k >= a.n_top && xo.kth > -INFINITY &&
+                           (pen || (r.presence_penalty >= 0.f && r.frequency_penalty >= 0.f));
         unsigned long long* cands = a.lp_cand + static_cast<long long>(p) * S * kLpCandPerChunk;
         unsigned long long* cand = S > 1 ? cands + static_cast<long long>(c) * kLpCandPerChunk : nullptr;
-        if (PEN_MODE && pen) lp_chunk<SX, PEN_MODE>(a, s, row, c0, c1, part + c, pr, nbat, cand);
-        else lp_chunk<SX, false>(a, s, row, c0, c1, part + c, pr, nbat, cand);
+        if (PEN_MODE && pen) lp_chunk<SX, PEN_MODE>(a, s, row, c0, c1, part + c, pr, nbat, cand, known, xo.kth);
+        else lp_chunk<SX, false>(a, s, row, c0, c1, part + c, pr, nbat, cand, known, xo.kth);
         // the CTA finishing the row's last chunk merges them: partial written, then counted
         __syncthreads();
         if (threadIdx.x == 0) {
