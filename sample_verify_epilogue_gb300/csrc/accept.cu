@@ -9,7 +9,7 @@
 // K drafts were accepted; greedy emits the argmax.  When the target row's support is a short
 // list the draw happens here: weights in double, ids sorted ascending, an exclusive scan, and
 // the smallest id whose cumulative mass exceeds u * total.  Whole-vocabulary supports are
-// left to finish_kernel.
+// drawn afterwards by the same CTA (finish_request).
 //
 // A request with an end-of-sequence token stops at the first accepted draft equal to it: its
 // accepted length counts that draft, and nothing is drawn (mlx-dspark Changelog, [0.2.0]
@@ -19,10 +19,10 @@
 //
 // The request's emitted positions are listed for the logprob pass (logprob_kernel).
 //
-// finish_kernel: one CTA per request.  Whole-row inverse-CDF draws (every thread sums the
-// weights of a contiguous range of ids, a block scan of those sums finds the range holding
-// the draw, and its thread walks it), then the logprob outputs past the emitted token (-inf,
-// top ids -1); the emitted positions' values come from logprob_kernel.
+// finish_request, at the end of the same CTA: whole-row inverse-CDF draws (every thread sums
+// the weights of a contiguous range of ids, a block scan of those sums finds the range holding
+// the draw, and its thread walks it), then the logprob outputs past the last emitted position
+// (-inf, top ids -1); the emitted positions' values come from logprob_kernel.
 #include "block_utils.cuh"
 
 namespace dspark {
@@ -88,131 +88,9 @@ __device__ void write_error(const Args& a, int b, int st) {
     }
 }
 
-__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
-    pdl_enter();
-    extern __shared__ __align__(16) unsigned char acc_raw[];
-    AccSmem& s = *reinterpret_cast<AccSmem*>(acc_raw);
-    const int b = blockIdx.x, tid = threadIdx.x;
-    int st = a.row_status[b];
-    const dspark_row_params_t r = a.rows[b];
-    // a d2t table that does not invert makes every sampled request with drafts invalid
-    if (a.q_layout == kQReduced && a.plan->pad[1] && !(st & DSPARK_ROW_BAD_PARAMS) && r.temperature > 0.f &&
-        r.num_drafts > 0)
-        st |= DSPARK_ROW_BAD_DRAFT;
-    // an invalid request reports what is wrong with its inputs, not what its rows then gave
-    if (st & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_HISTORY | DSPARK_ROW_BAD_DRAFT)) st &= ~DSPARK_ROW_NONFINITE;
-    if (a.plan->pad[0]) st |= DSPARK_ROW_INTERNAL;
-    if (st) { write_error(a, b, st); return; }
-    const int K = r.num_drafts;
-    const bool greedy = !(r.temperature > 0.f);
-    const bool t_one = r.temperature == 1.f;
-    const int W = a.Km + 1;
-    const long long xs0 = static_cast<long long>(b) * W;
-    const long long qs0 = static_cast<long long>(b) * a.Km;
-    // ---- acceptance decisions, one thread per drafted position
-    if (tid < K) {
-        const int t = a.d[qs0 + tid];
-        bool ok;
-        if (greedy) {
-            ok = (t == a.xout[xs0 + tid].argmax);
-        } else {
-            const XRowOut xo = a.xout[xs0 + tid];
-            const QRowOut qo = a.qout[qs0 + tid];
-            const double P = target_prob_of_draft(a, xo, b, tid, t, r);
-            const double Q = draft_prob(a, qo, b, tid, t, t_one);
-            const double u = static_cast<double>(a.u[(xs0 + tid) * 2 + 0]);
-            ok = (Q == 0.0) ? (P > 0.0) : (u < P / Q);
-        }
-        s.acc[tid] = ok ? 1 : 0;
-    }
-    __syncthreads();
-    int first = K;
-    if (tid < K && !s.acc[tid]) first = tid;
-    const int verified = block_min_i(first, s.iwarp);     // accepted drafts before any stop
-    // ---- end-of-sequence stop: the first accepted draft equal to the request's eos token
-    const int eos = a.eos ? a.eos[b] : -1;
-    int stop_at = W;
-    if (eos >= 0 && tid < verified && a.d[qs0 + tid] == eos) stop_at = tid;
-    stop_at = block_min_i(stop_at, s.iwarp);
-    const bool stopped = stop_at < verified;
-    const int acc_len = stopped ? stop_at + 1 : verified;
-    // ---- per-position counters: verified positions (the first rejected one included), accepted ones
-    if (a.pos_counts && tid < K) {
-        const bool attempted = stopped ? tid < acc_len : tid <= verified;
-        if (attempted) atomicAdd(a.pos_counts + tid, 1ull);
-        if (tid < acc_len) atomicAdd(a.pos_counts + a.Km + tid, 1ull);
-    }
-    // ---- the emitted token at position acc_len (none after a stop)
-    int draw = 0;
-    int tok = -1;
-    const XRowOut xa = a.xout[xs0 + acc_len];
-    if (stopped) {
-        // nothing to draw
-    } else if (greedy) {
-        tok = xa.argmax;
-    } else if (xa.mode == kModeList) {
-        const int n = xa.n_kept;
-        const bool residual = acc_len < K;
-        QRowOut qa{};
-        if (residual) qa = a.qout[qs0 + acc_len];
-        const KeptEntry* kl = a.kept + (xs0 + acc_len) * kKeptCap;
-        for (int e = tid; e < n; e += blockDim.x) {
-            const KeptEntry ke = kl[e];
-            const double P = static_cast<double>(ke.w) / xa.Z;
-            double rv = P;
-            if (residual) rv = fmax(0.0, P - draft_prob(a, qa, b, acc_len, ke.id, t_one));
-            s.r[e] = rv;
-            s.sk[e] = (static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<unsigned>(ke.id)) << 32) |
-                      static_cast<unsigned>(e);
-        }
-        const int P2 = next_pow2(max(n, 2));
-        for (int e = n + tid; e < P2; e += blockDim.x) s.sk[e] = 0ull;
-        block_bitonic_desc(s.sk, P2);                   // ascending token id
-        for (int e = tid; e < n; e += blockDim.x) s.rs[e] = s.r[s.sk[e] & 0xFFFFFFFFull];
-        __syncthreads();
-        block_scan_excl_d(s.rs, s.ex, n, s.dwarp);
-        if (!(s.ex[n] > 0.0)) {                          // empty residual: draw from P'
-            for (int e = tid; e < n; e += blockDim.x)
-                s.rs[e] = static_cast<double>(kl[s.sk[e] & 0xFFFFFFFFull].w) / xa.Z;
-            __syncthreads();
-            block_scan_excl_d(s.rs, s.ex, n, s.dwarp);
-        }
-        const double target = static_cast<double>(a.u[(xs0 + acc_len) * 2 + 1]) * s.ex[n];
-        if (tid == 0) s.tok = -1;
-        __syncthreads();
-        for (int e = tid; e < n; e += blockDim.x)
-            if (s.ex[e + 1] > target && s.ex[e] <= target) s.tok = e;
-        __syncthreads();
-        int pos = s.tok;
-        if (pos < 0) {                                    // rounding put u*total at the very top
-            int last = -1;
-            for (int e = tid; e < n; e += blockDim.x) if (s.rs[e] > 0.0) last = max(last, e);
-            pos = -block_min_i(-last, s.iwarp);
-        }
-        tok = pos >= 0 ? static_cast<int>(0xFFFFFFFFu - static_cast<unsigned>(s.sk[pos] >> 32)) : -1;
-    } else {
-        draw = (acc_len < K) ? 1 : 2;                     // whole-row draw in finish_kernel
-    }
-    for (int j = tid; j < W; j += blockDim.x) {
-        int v = -1;
-        if (j < acc_len) v = a.d[qs0 + j];
-        else if (j == acc_len) v = tok;
-        a.out_tokens[xs0 + j] = v;
-    }
-    if (tid == 0) {
-        a.out_accept[b] = acc_len;
-        if (a.out_stopped) a.out_stopped[b] = stopped ? 1 : 0;
-        a.req[b] = ReqOut{acc_len, draw, 0, stopped ? 1 : 0};
-        if (a.want_lp || a.n_top > 0) {                     // rows of the logprob pass
-            const int n_em = stopped ? acc_len : acc_len + 1;
-            const int base = atomicAdd(&a.lp_list[0], n_em);
-            for (int j = 0; j < n_em; ++j) a.lp_list[1 + base + j] = static_cast<int>(xs0) + j;
-        }
-    }
-}
-
 // ============================================================================ finish
 constexpr int kFinishThreads = 512;
+static_assert(kFinishThreads == kAcceptThreads, "the whole-row draw runs in the acceptance CTA");
 
 struct FinishSmem {
     double dwarp[33];
@@ -356,13 +234,10 @@ __device__ int whole_row_draw(FinishSmem& s, DrawCtx& c, float u) {
     return -1;
 }
 
-__global__ void __launch_bounds__(kFinishThreads) finish_kernel(Args a) {
-    pdl_enter();
-    extern __shared__ __align__(16) unsigned char fin_raw[];
-    FinishSmem& s = *reinterpret_cast<FinishSmem*>(fin_raw);
-    const int b = blockIdx.x, tid = threadIdx.x;
-    const ReqOut ro = a.req[b];
-    if (ro.a < 0) return;
+// The request's whole-row draw (when one is pending) and the logprob outputs past its last
+// emitted position; the same CTA, after the acceptance decisions.
+__device__ void finish_request(const Args& a, FinishSmem& s, int b, const ReqOut ro) {
+    const int tid = threadIdx.x;
     const int W = a.Km + 1;
     const long long xs0 = static_cast<long long>(b) * W;
     const int acc_len = ro.a;
@@ -415,20 +290,146 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(Args a) {
     }
 }
 
+// The acceptance kernel's shared memory: the list draw's arrays, then (reused) the whole-row
+// draw's.
+union AcceptSmem {
+    AccSmem acc;
+    FinishSmem fin;
+};
+
+__global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
+    pdl_enter();
+    extern __shared__ __align__(16) unsigned char acc_raw[];
+    AcceptSmem& su = *reinterpret_cast<AcceptSmem*>(acc_raw);
+    AccSmem& s = su.acc;
+    const int b = blockIdx.x, tid = threadIdx.x;
+    int st = a.row_status[b];
+    const dspark_row_params_t r = a.rows[b];
+    // a d2t table that does not invert makes every sampled request with drafts invalid
+    if (a.q_layout == kQReduced && a.plan->pad[1] && !(st & DSPARK_ROW_BAD_PARAMS) && r.temperature > 0.f &&
+        r.num_drafts > 0)
+        st |= DSPARK_ROW_BAD_DRAFT;
+    // an invalid request reports what is wrong with its inputs, not what its rows then gave
+    if (st & (DSPARK_ROW_BAD_PARAMS | DSPARK_ROW_BAD_HISTORY | DSPARK_ROW_BAD_DRAFT)) st &= ~DSPARK_ROW_NONFINITE;
+    if (a.plan->pad[0]) st |= DSPARK_ROW_INTERNAL;
+    if (st) { write_error(a, b, st); return; }
+    const int K = r.num_drafts;
+    const bool greedy = !(r.temperature > 0.f);
+    const bool t_one = r.temperature == 1.f;
+    const int W = a.Km + 1;
+    const long long xs0 = static_cast<long long>(b) * W;
+    const long long qs0 = static_cast<long long>(b) * a.Km;
+    // ---- acceptance decisions, one thread per drafted position
+    if (tid < K) {
+        const int t = a.d[qs0 + tid];
+        bool ok;
+        if (greedy) {
+            ok = (t == a.xout[xs0 + tid].argmax);
+        } else {
+            const XRowOut xo = a.xout[xs0 + tid];
+            const QRowOut qo = a.qout[qs0 + tid];
+            const double P = target_prob_of_draft(a, xo, b, tid, t, r);
+            const double Q = draft_prob(a, qo, b, tid, t, t_one);
+            const double u = static_cast<double>(a.u[(xs0 + tid) * 2 + 0]);
+            ok = (Q == 0.0) ? (P > 0.0) : (u < P / Q);
+        }
+        s.acc[tid] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    int first = K;
+    if (tid < K && !s.acc[tid]) first = tid;
+    const int verified = block_min_i(first, s.iwarp);     // accepted drafts before any stop
+    // ---- end-of-sequence stop: the first accepted draft equal to the request's eos token
+    const int eos = a.eos ? a.eos[b] : -1;
+    int stop_at = W;
+    if (eos >= 0 && tid < verified && a.d[qs0 + tid] == eos) stop_at = tid;
+    stop_at = block_min_i(stop_at, s.iwarp);
+    const bool stopped = stop_at < verified;
+    const int acc_len = stopped ? stop_at + 1 : verified;
+    // ---- per-position counters: verified positions (the first rejected one included), accepted ones
+    if (a.pos_counts && tid < K) {
+        const bool attempted = stopped ? tid < acc_len : tid <= verified;
+        if (attempted) atomicAdd(a.pos_counts + tid, 1ull);
+        if (tid < acc_len) atomicAdd(a.pos_counts + a.Km + tid, 1ull);
+    }
+    // ---- the emitted token at position acc_len (none after a stop)
+    int draw = 0;
+    int tok = -1;
+    const XRowOut xa = a.xout[xs0 + acc_len];
+    if (stopped) {
+        // nothing to draw
+    } else if (greedy) {
+        tok = xa.argmax;
+    } else if (xa.mode == kModeList) {
+        const int n = xa.n_kept;
+        const bool residual = acc_len < K;
+        QRowOut qa{};
+        if (residual) qa = a.qout[qs0 + acc_len];
+        const KeptEntry* kl = a.kept + (xs0 + acc_len) * kKeptCap;
+        for (int e = tid; e < n; e += blockDim.x) {
+            const KeptEntry ke = kl[e];
+            const double P = static_cast<double>(ke.w) / xa.Z;
+            double rv = P;
+            if (residual) rv = fmax(0.0, P - draft_prob(a, qa, b, acc_len, ke.id, t_one));
+            s.r[e] = rv;
+            s.sk[e] = (static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<unsigned>(ke.id)) << 32) |
+                      static_cast<unsigned>(e);
+        }
+        const int P2 = next_pow2(max(n, 2));
+        for (int e = n + tid; e < P2; e += blockDim.x) s.sk[e] = 0ull;
+        block_bitonic_desc(s.sk, P2);                   // ascending token id
+        for (int e = tid; e < n; e += blockDim.x) s.rs[e] = s.r[s.sk[e] & 0xFFFFFFFFull];
+        __syncthreads();
+        block_scan_excl_d(s.rs, s.ex, n, s.dwarp);
+        if (!(s.ex[n] > 0.0)) {                          // empty residual: draw from P'
+            for (int e = tid; e < n; e += blockDim.x)
+                s.rs[e] = static_cast<double>(kl[s.sk[e] & 0xFFFFFFFFull].w) / xa.Z;
+            __syncthreads();
+            block_scan_excl_d(s.rs, s.ex, n, s.dwarp);
+        }
+        const double target = static_cast<double>(a.u[(xs0 + acc_len) * 2 + 1]) * s.ex[n];
+        if (tid == 0) s.tok = -1;
+        __syncthreads();
+        for (int e = tid; e < n; e += blockDim.x)
+            if (s.ex[e + 1] > target && s.ex[e] <= target) s.tok = e;
+        __syncthreads();
+        int pos = s.tok;
+        if (pos < 0) {                                    // rounding put u*total at the very top
+            int last = -1;
+            for (int e = tid; e < n; e += blockDim.x) if (s.rs[e] > 0.0) last = max(last, e);
+            pos = -block_min_i(-last, s.iwarp);
+        }
+        tok = pos >= 0 ? static_cast<int>(0xFFFFFFFFu - static_cast<unsigned>(s.sk[pos] >> 32)) : -1;
+    } else {
+        draw = (acc_len < K) ? 1 : 2;                     // whole-row draw in finish_request
+    }
+    for (int j = tid; j < W; j += blockDim.x) {
+        int v = -1;
+        if (j < acc_len) v = a.d[qs0 + j];
+        else if (j == acc_len) v = tok;
+        a.out_tokens[xs0 + j] = v;
+    }
+    if (tid == 0) {
+        a.out_accept[b] = acc_len;
+        if (a.out_stopped) a.out_stopped[b] = stopped ? 1 : 0;
+        a.req[b] = ReqOut{acc_len, draw, 0, stopped ? 1 : 0};
+        if (a.want_lp || a.n_top > 0) {                     // rows of the logprob pass
+            const int n_em = stopped ? acc_len : acc_len + 1;
+            const int base = atomicAdd(&a.lp_list[0], n_em);
+            for (int j = 0; j < n_em; ++j) a.lp_list[1 + base + j] = static_cast<int>(xs0) + j;
+        }
+    }
+    __syncthreads();                                      // the list draw's shared memory is free
+    finish_request(a, su.fin, b, ReqOut{acc_len, draw, 0, stopped ? 1 : 0});
+}
+
 }  // namespace
 
 cudaError_t launch_accept(const Args& a, cudaStream_t s) {
-    const size_t smem = sizeof(AccSmem);
+    const size_t smem = sizeof(AcceptSmem);
     cudaError_t e = cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     return launch_k(accept_kernel, dim3(a.B), dim3(kAcceptThreads), smem, s, true, a);
-}
-
-cudaError_t launch_finish(const Args& a, cudaStream_t s) {
-    const size_t smem = sizeof(FinishSmem);
-    cudaError_t e = cudaFuncSetAttribute(finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    return launch_k(finish_kernel, dim3(a.B), dim3(kFinishThreads), smem, s, true, a);
 }
 
 }  // namespace dspark

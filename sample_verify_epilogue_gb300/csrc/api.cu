@@ -208,7 +208,6 @@ dspark_status_t run(const void* logits, const float* q, const int32_t* draft_ids
     if (launch_row_finalize_warp(a, s, ev1 == nullptr) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_row_finalize(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if (launch_accept(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
-    if (launch_finish(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     if ((a.want_lp || a.n_top > 0) && launch_logprobs(a, s) != cudaSuccess) return DSPARK_ERR_CUDA;
     return DSPARK_OK;
 }
@@ -403,6 +402,6 @@ const char* dspark_status_string(dspark_status_t status) {
     return "unknown status";
 }
 
-int32_t dspark_launches_per_call(void) { return 7; }
+int32_t dspark_launches_per_call(void) { return 6; }
 
 }  // extern "C"

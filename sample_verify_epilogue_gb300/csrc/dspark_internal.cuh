@@ -5,8 +5,8 @@
 //   stream_stats_kernel  the one HBM pass over x and q: per-tile maxima, sums and candidates
 //   row_finalize_kernel  per verify row: merge segments, top-k threshold, nucleus, normaliser
 //                        (rows needing a whole-vocabulary threshold get it in the same block)
-//   accept_kernel        per request: accept scan, residual / bonus draw over candidates
-//   finish_kernel        per request: whole-vocabulary draws (rare), padding of the outputs
+//   accept_kernel        per request: accept scan, eos stop, counters, residual / bonus draw
+//                        over the kept list or the whole row, padding of the outputs
 //   logprob_kernel       the emitted positions' raw log-softmax and top_logprobs
 #pragma once
 
@@ -490,7 +490,6 @@ cudaError_t launch_row_finalize_warp(const Args& a, cudaStream_t s, bool pdl);
 cudaError_t launch_stream_stats(const Args& a, cudaStream_t s, int grid, bool pdl);
 cudaError_t launch_row_finalize(const Args& a, cudaStream_t s);
 cudaError_t launch_accept(const Args& a, cudaStream_t s);
-cudaError_t launch_finish(const Args& a, cudaStream_t s);
 cudaError_t launch_logprobs(const Args& a, cudaStream_t s);
 
 }  // namespace dspark

@@ -50,7 +50,7 @@ def test_status_strings_and_launches(lib):
     from sample_verify_epilogue_gb300 import binding as bd
     assert bd.dspark_status_string(0) == "ok"
     assert "workspace" in bd.dspark_status_string(3)
-    assert bd.dspark_launches_per_call() == 7
+    assert bd.dspark_launches_per_call() == 6
 
 
 def test_invalid_arguments_rejected_before_any_cuda_call(lib):
