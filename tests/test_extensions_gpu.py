@@ -205,3 +205,24 @@ def test_host_entry_point_with_options(runner):
         assert np.array_equal(out[k], want[k]), k
     assert np.array_equal(stopped, want["stopped"])
     assert np.array_equal(counts.reshape(2, -1).astype(np.int64) - 5, want["pos_counts"])
+
+
+def test_logprob_threshold_paths(runner):
+    """The logprob pass gathers from a top-k row's k-th largest penalised logit only when that
+    bounds the n-th largest logit: k >= n and, in raw mode, no negative penalty.  Rows on
+    either side of each condition, in both modes; sparse rows at the largest m."""
+    rows = [row_params(1.0, 64, 0.95, 0.3, 0.2, 3),      # bound used
+            row_params(1.0, 10, 1.0, 0.3, 0.2, 3),       # k < n: searched
+            row_params(0.8, 64, 1.0, -0.5, -0.3, 3),     # negative penalties: searched in raw mode
+            row_params(0.0, 0, 1.0, 0.4, 0.4, 3),        # greedy: searched
+            row_params(1.2, 0, 0.7, 0.0, 0.0, 3),        # no top-k: searched
+            row_params(0.9, 300, 1.0, 0.0, 0.0, 3)]      # k > 256 (block finalize): searched
+    for mode in ("raw", "penalised"):
+        batch = make_batch(B=6, K_max=3, V=151936, logits_dtype="bf16", rows=rows, seed=101, philox_seed=7,
+                           boost_frac=0.3, argmax_frac=0.5, history_len=2048, want_logprobs=True,
+                           n_top_logprobs=20, logprob_mode=mode)
+        _run(runner, batch, f"logprob threshold paths ({mode})")
+    sp = make_batch(B=6, K_max=3, V=151936, logits_dtype="bf16", rows=rows, seed=102, philox_seed=8,
+                    argmax_frac=0.5, history_len=500, want_logprobs=True, n_top_logprobs=20,
+                    q_layout="sparse", q_m=256)
+    _run(runner, sp, "sparse q m=256")
