@@ -360,6 +360,90 @@ __global__ void __launch_bounds__(kAcceptThreads) accept_kernel(Args a) {
         // nothing to draw
     } else if (greedy) {
         tok = xa.argmax;
+    } else if (xa.mode == kModeList && xa.n_kept <= 64) {
+        // a short kept list: one warp, two entries per lane, sorted by id in registers, scanned
+        // with shuffles (the block-wide sort and scans below cost a barrier per step)
+        if (tid < 32) {
+            const int lane = tid;
+            const int n = xa.n_kept;
+            const bool residual = acc_len < K;
+            QRowOut qa{};
+            if (residual) qa = a.qout[qs0 + acc_len];
+            const KeptEntry* kl = a.kept + (xs0 + acc_len) * kKeptCap;
+            unsigned long long key[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int e = lane + 32 * h;
+                key[h] = 0ull;
+                if (e < n) {
+                    const KeptEntry ke = kl[e];
+                    const double P = static_cast<double>(ke.w) / xa.Z;
+                    double rv = P;
+                    if (residual) rv = fmax(0.0, P - draft_prob(a, qa, b, acc_len, ke.id, t_one));
+                    s.r[e] = rv;
+                    key[h] = (static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<unsigned>(ke.id)) << 32) |
+                             static_cast<unsigned>(e);
+                }
+            }
+            __syncwarp();
+            // bitonic sort of the 64 keys, descending (= ids ascending); key h of lane l sits at l + 32h
+            for (int size = 2; size <= 64; size <<= 1)
+                for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                    if (stride == 32) {
+                        const unsigned long long hi = key[0] > key[1] ? key[0] : key[1];
+                        const unsigned long long lo = key[0] > key[1] ? key[1] : key[0];
+                        key[0] = hi;
+                        key[1] = lo;
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int pos = lane + 32 * h;
+                            const unsigned long long o = __shfl_xor_sync(0xffffffffu, key[h], stride);
+                            const bool keep_max = ((pos & stride) == 0) == ((pos & size) == 0);
+                            key[h] = keep_max ? (key[h] > o ? key[h] : o) : (key[h] < o ? key[h] : o);
+                        }
+                    }
+                }
+            // weights in id order (position p = lane + 32h), inclusive scans of each half
+            auto scan = [&](bool from_p, double (&w)[2], double (&inc)[2]) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int pos = lane + 32 * h;
+                    const int idx = static_cast<int>(key[h] & 0xFFFFFFFFull);
+                    w[h] = pos < n ? (from_p ? static_cast<double>(kl[idx].w) / xa.Z : s.r[idx]) : 0.0;
+                    double v = w[h];
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const double y = __shfl_up_sync(0xffffffffu, v, o);
+                        if (lane >= o) v += y;
+                    }
+                    inc[h] = v;
+                }
+                inc[1] += __shfl_sync(0xffffffffu, inc[0], 31);
+                return __shfl_sync(0xffffffffu, inc[1], 31);
+            };
+            double w[2], inc[2];
+            double total = scan(false, w, inc);
+            if (!(total > 0.0)) total = scan(true, w, inc);      // empty residual: draw from P'
+            const double target = static_cast<double>(a.u[(xs0 + acc_len) * 2 + 1]) * total;
+            // exclusive prefix = the inclusive prefix one position down, so the intervals tile [0, total)
+            double ex0 = __shfl_up_sync(0xffffffffu, inc[0], 1), ex1 = __shfl_up_sync(0xffffffffu, inc[1], 1);
+            const double top0 = __shfl_sync(0xffffffffu, inc[0], 31);
+            if (lane == 0) { ex0 = 0.0; ex1 = top0; }
+            const unsigned h0 = __ballot_sync(0xffffffffu, inc[0] > target && ex0 <= target && lane < n);
+            const unsigned h1 = __ballot_sync(0xffffffffu, inc[1] > target && ex1 <= target && lane + 32 < n);
+            int pos = h0 ? __ffs(h0) - 1 : (h1 ? 32 + __ffs(h1) - 1 : -1);
+            if (pos < 0) {                                    // rounding put u*total at the very top
+                const unsigned m0 = __ballot_sync(0xffffffffu, w[0] > 0.0), m1 = __ballot_sync(0xffffffffu, w[1] > 0.0);
+                pos = m1 ? 32 + 31 - __clz(m1) : (m0 ? 31 - __clz(m0) : -1);
+            }
+            const unsigned long long kp0 = __shfl_sync(0xffffffffu, key[0], pos & 31);
+            const unsigned long long kp1 = __shfl_sync(0xffffffffu, key[1], pos & 31);
+            const unsigned long long kp = pos >= 32 ? kp1 : kp0;
+            if (lane == 0) s.tok = pos >= 0 ? static_cast<int>(0xFFFFFFFFu - static_cast<unsigned>(kp >> 32)) : -1;
+        }
+        __syncthreads();
+        tok = s.tok;
     } else if (xa.mode == kModeList) {
         const int n = xa.n_kept;
         const bool residual = acc_len < K;

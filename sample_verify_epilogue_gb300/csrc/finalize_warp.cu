@@ -357,7 +357,8 @@ __device__ bool warp_finalize_x(WarpSmem& w, const Args& a, int slot, int b) {
     for (int t = lane; t < nseg; t += 32) {
         const TileStats x = cached ? mine : ts[t];
         if (x.m_pen == mp) arg = min(arg, x.arg_pen);
-        if (!greedy) stemp += static_cast<double>(x.s_temp) * static_cast<double>(exp2f((x.m_pen - mp) * c_l2e));
+        // the tempered sum is the normaliser of a row without a top-k list only
+        if (!greedy && !list) stemp += static_cast<double>(x.s_temp) * static_cast<double>(exp2f((x.m_pen - mp) * c_l2e));
     }
     for (int off = 16; off; off >>= 1) {
         arg = min(arg, __shfl_xor_sync(0xffffffffu, arg, off));

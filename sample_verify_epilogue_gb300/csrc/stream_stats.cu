@@ -559,8 +559,43 @@ __device__ __forceinline__ uint4 neg_inf_vec() {
 // The scan of one tile for every row that does not need the tempered sum: raw maximum, and
 // one flag bit per vector whose maximum is >= th.  All per-element work on candidates is
 // left to flush_vectors.
+// bf16 pairs throughout: the vector maximum and the running maximum stay packed, and the
+// threshold is rounded down to bf16 (a vector is flagged at least whenever its float maximum
+// reaches th; the flush compares each element in float).  FULL: the tile fills the stage.
+template <bool FULL>
+__device__ __forceinline__ unsigned x_scan_flags_bf16(XState& st, const unsigned char* data, int gt, int nvec,
+                                                      float th) {
+    unsigned fl = 0u;
+    const __nv_bfloat162 th2 = __bfloat162bfloat162(__float2bfloat16_rd(th));
+    const __nv_bfloat162 ninf = __bfloat162bfloat162(__float2bfloat16(-INFINITY));
+    __nv_bfloat162 r0 = ninf, r1 = ninf;
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; i += 2) {
+        const int v0 = gt + i * kGroupThreads, v1 = v0 + kGroupThreads;
+        if (!FULL && v0 >= nvec) break;
+        const bool ok1 = FULL || v1 < nvec;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(data + v0 * 16);
+        const uint4 w1 = ok1 ? *reinterpret_cast<const uint4*>(data + v1 * 16) : neg_inf_vec<2>();
+        const __nv_bfloat162* p0 = reinterpret_cast<const __nv_bfloat162*>(&w0);
+        const __nv_bfloat162* p1 = reinterpret_cast<const __nv_bfloat162*>(&w1);
+        const __nv_bfloat162 m0 = __hmax2_nan(__hmax2_nan(p0[0], p0[1]), __hmax2_nan(p0[2], p0[3]));
+        const __nv_bfloat162 m1 = __hmax2_nan(__hmax2_nan(p1[0], p1[1]), __hmax2_nan(p1[2], p1[3]));
+        r0 = __hmax2_nan(r0, m0);
+        r1 = __hmax2_nan(r1, m1);
+        fl |= (__hge2_mask(m0, th2) ? 1u : 0u) << i;
+        fl |= ((ok1 && __hge2_mask(m1, th2)) ? 1u : 0u) << (i + 1);
+    }
+    const __nv_bfloat162 r = __hmax2_nan(r0, r1);
+    const uint32_t rw = *reinterpret_cast<const uint32_t*>(&r);
+    st.m_r = max_nan(st.m_r, max_nan(bf16_lo(rw), bf16_hi(rw)));
+    return fl;
+}
+
 template <int SX>
 __device__ __forceinline__ unsigned x_scan_flags(XState& st, const unsigned char* data, int gt, int nvec, float th) {
+    if constexpr (SX == 2)
+        return nvec == kVecPerThread * kGroupThreads ? x_scan_flags_bf16<true>(st, data, gt, nvec, th)
+                                                     : x_scan_flags_bf16<false>(st, data, gt, nvec, th);
     unsigned fl = 0u;
     float m0 = st.m_r, m1 = -INFINITY;
 #pragma unroll
@@ -793,6 +828,49 @@ __device__ __forceinline__ void q_elem(QState& st, float v, bool need_sum, bool 
     if (filt && v >= st.th) push(lp, &gs.n_pen, kCandPenGlobal, v, e);
 }
 
+// The scan of one draft tile of a top-k row.  Raw bit patterns: for values with a clear sign
+// bit the unsigned order is the float order (NaNs above +inf), so one integer max per element
+// gives both the vector flags and the running maximum.  A set sign bit (a negative value, -0.0
+// or a negative NaN) puts its vector above every threshold (ge_mask then decides in float) and
+// sends this thread's part of the tile through the float maximum and minimum.  FULL: the tile
+// fills the stage, so every thread has all its vectors and nothing is bounds-checked.
+template <bool FULL>
+__device__ __forceinline__ unsigned q_scan_flags(QState& st, const unsigned char* data, int gt, int nvec) {
+    unsigned vfl = 0u, u0 = 0u, u1 = 0u;
+    const float th = st.th;
+    const unsigned thb = th > 0.f ? __float_as_uint(th) : 0u;
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; i += 2) {
+        const int v0 = gt + i * kGroupThreads, v1 = v0 + kGroupThreads;
+        if (!FULL && v0 >= nvec) break;
+        const bool ok1 = FULL || v1 < nvec;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(data + v0 * 16);
+        const uint4 w1 = ok1 ? *reinterpret_cast<const uint4*>(data + v1 * 16) : make_uint4(0u, 0u, 0u, 0u);
+        const unsigned vm0 = max(__vimax3_u32(w0.x, w0.y, w0.z), w0.w);
+        const unsigned vm1 = max(__vimax3_u32(w1.x, w1.y, w1.z), w1.w);
+        u0 = max(u0, vm0);
+        u1 = max(u1, vm1);
+        vfl |= (vm0 >= thb ? 1u : 0u) << i;
+        vfl |= ((ok1 && vm1 >= thb) ? 1u : 0u) << (i + 1);
+    }
+    const unsigned ut = max(u0, u1);
+    if (ut < 0x80000000u) {
+        if (FULL || gt < nvec) st.mx = max_nan(st.mx, __uint_as_float(ut));
+    } else {
+        float mx = st.mx, mn = st.mn;
+        for (int i = 0; i < kVecPerThread; ++i) {
+            const int v = gt + i * kGroupThreads;
+            if (v >= nvec) break;
+            const float4 w = *reinterpret_cast<const float4*>(data + v * 16);
+            mx = max_nan(mx, max_nan(max_nan(w.x, w.y), max_nan(w.z, w.w)));
+            mn = fminf(mn, fminf(fminf(w.x, w.y), fminf(w.z, w.w)));
+        }
+        st.mx = mx;
+        st.mn = mn;
+    }
+    return vfl;
+}
+
 __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage, const StageMeta& m, QState& st) {
     const int gt = threadIdx.x - g * kGroupThreads;
     const int lane = threadIdx.x & 31, warp = gt >> 5;
@@ -840,34 +918,13 @@ __device__ void q_tile(const Args& a, Smem& sm, GroupSmem& gs, int g, int stage,
         st.th = need_cand ? r.z : INFINITY;
     }
     if (need_cand) {
-        // common case: maxima / minima, vectors in pairs, one flag per vector whose maximum
-        // reaches the threshold; the flagged vectors' candidates are extracted afterwards
-        unsigned vfl = 0u;
-        float mx0 = st.mx, mx1 = -INFINITY, mn0 = st.mn, mn1 = INFINITY;
-        const float th = st.th;
-#pragma unroll
-        for (int i = 0; i < kVecPerThread; i += 2) {
-            const int v0 = gt + i * kGroupThreads, v1 = v0 + kGroupThreads;
-            if (v0 >= m.nvec) break;
-            const bool ok1 = v1 < m.nvec;
-            const uint4 u0 = *reinterpret_cast<const uint4*>(data + v0 * 16);
-            const uint4 u1 = ok1 ? *reinterpret_cast<const uint4*>(data + v1 * 16) : u0;
-            const float4 w0 = *reinterpret_cast<const float4*>(&u0);
-            const float4 w1 = *reinterpret_cast<const float4*>(&u1);
-            const float vm0 = max_nan(max_nan(w0.x, w0.y), max_nan(w0.z, w0.w));
-            const float vm1 = max_nan(max_nan(w1.x, w1.y), max_nan(w1.z, w1.w));
-            mx0 = max_nan(mx0, vm0);
-            mx1 = max_nan(mx1, vm1);
-            mn0 = fminf(mn0, fminf(fminf(w0.x, w0.y), fminf(w0.z, w0.w)));
-            mn1 = fminf(mn1, fminf(fminf(w1.x, w1.y), fminf(w1.z, w1.w)));
-            vfl |= (vm0 >= th ? 1u : 0u) << i;
-            vfl |= ((ok1 && vm1 >= th) ? 1u : 0u) << (i + 1);
-        }
-        st.mx = max_nan(mx0, mx1);
-        st.mn = fminf(mn0, mn1);
+        // common case: vectors in pairs, one flag per vector whose maximum reaches the
+        // threshold; the flagged vectors' candidates are extracted afterwards
+        const unsigned vfl = m.nvec == kVecPerThread * kGroupThreads ? q_scan_flags<true>(st, data, gt, m.nvec)
+                                                                     : q_scan_flags<false>(st, data, gt, m.nvec);
         float m_unused = 0.f;
         int a_unused = 0;
-        flush_vectors<4, false, true, false>(gs, lp, vfl, data, nullptr, m.vec_e0, 0, gt, th, m_unused, a_unused);
+        flush_vectors<4, false, true, false>(gs, lp, vfl, data, nullptr, m.vec_e0, 0, gt, st.th, m_unused, a_unused);
     }
 #pragma unroll 2
     for (int i = 0; i < (need_cand ? 0 : kVecPerThread); ++i) {

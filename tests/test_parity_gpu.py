@@ -50,6 +50,17 @@ def test_mixed18_all_combinations(runner):
     _run(runner, configs.build("b256k16v262144_mixed", B=18), "b256k16v262144_mixed B=18")
 
 
+def test_list_draw_lengths(runner):
+    """Kept lists of every length class of the draw from a truncated row: one entry, the
+    one-warp path (up to 64 entries, both sides of a half-warp), and the block path above it;
+    flat logits so that drafts are often rejected and the residual is drawn from."""
+    ks = (1, 2, 31, 33, 63, 64, 65, 128, 1000)
+    rows = [row_params(1.0, ks[b % len(ks)], 1.0 if b < len(ks) else 0.9, 0.0, 0.0, 4) for b in range(2 * len(ks))]
+    batch = make_batch(B=len(rows), K_max=4, V=20000, logits_dtype="bf16", rows=rows, seed=65, philox_seed=65,
+                       x_sigma=0.4, argmax_frac=0.5, history_len=0)
+    _run(runner, batch, "kept-list lengths")
+
+
 @pytest.mark.parametrize("dtype,V", [("fp32", 1003), ("bf16", 5001), ("bf16", 24577), ("fp32", 12289), ("bf16", 17)])
 def test_ragged_vocab(runner, dtype, V):
     rows = [row_params(0.9, 10, 0.9, 0.3, 0.2, 3), row_params(0.0, 0, 1.0, 0.3, 0.2, 3),
