@@ -71,6 +71,7 @@ struct LpSmem {
     float mm[kLpMergeLists];               // the merge's copies of the chunk partials
     float ms[kLpMergeLists];
     int mn[kLpMergeLists];
+    int ml[kLpMergeLists];
 };
 
 // Sort s.keys[0..cnt) descending (cnt <= kLpCandCap): one warp with shuffles when cnt <= 64,
@@ -337,7 +338,8 @@ __device__ int top_select(LpSmem& s, const unsigned long long* keys, const int* 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int total = 0;
     for (int l = 0; l < lists; ++l) total += nl[l];
-    if (total <= 2 * n || total > kLpThreads * 8) return rank_select(keys, nl, lists, stride, n, top);
+    // up to one key per thread, ranking every key against all (no barrier per step) is shorter
+    if (total <= kLpThreads || total > kLpThreads * 8) return rank_select(keys, nl, lists, stride, n, top);
     uint32_t mine[8];                                     // this thread's keys' value parts (0: none)
     unsigned long long full[8];
 #pragma unroll
@@ -656,19 +658,32 @@ __device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j,
         s.mm[c] = __ldcg(&part[c].m);
         s.ms[c] = __ldcg(&part[c].s);
         s.mn[c] = __ldcg(&part[c].n);
+        s.ml[c] = __ldcg(&part[c].listed);
     }
     __syncthreads();
+    // A chunk holds at most kLpCandPerChunk unselected keys or n_top listed ones, so a thread
+    // copies at most one key per chunk; four chunks' loads are in flight before their stores.
+    static_assert(kLpCandPerChunk <= kLpThreads && DSPARK_MAX_TOP_LOGPROBS <= kLpThreads, "one key per thread");
+    static_assert(kLpMergeLists % 4 == 0, "chunks in fours");
     int off = 0;
-    for (int c = 0; c < S; ++c) {
-        const int nc = s.mn[c];
-        if (__ldcg(&part[c].listed)) {
-            const unsigned long long* src = cands + static_cast<long long>(c) * kLpCandPerChunk;
-            for (int i = tid; i < nc; i += blockDim.x) s.keys[off + i] = __ldcg(src + i);
-        } else {
-            for (int i = tid; i < nc; i += blockDim.x)
-                s.keys[off + i] = ckey(__ldcg(&part[c].top[i].v), __ldcg(&part[c].top[i].id));
+    for (int c0 = 0; c0 < S; c0 += 4) {
+        unsigned long long kv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u;
+            kv[u] = 0ull;
+            if (c < S && tid < s.mn[c])
+                kv[u] = s.ml[c] ? __ldcg(cands + static_cast<long long>(c) * kLpCandPerChunk + tid)
+                                : ckey(__ldcg(&part[c].top[tid].v), __ldcg(&part[c].top[tid].id));
         }
-        off += nc;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u;
+            if (c < S) {
+                if (tid < s.mn[c]) s.keys[off + tid] = kv[u];
+                off += s.mn[c];
+            }
+        }
     }
     if (tid == 0) s.wcnt[0] = off;
     __syncthreads();
