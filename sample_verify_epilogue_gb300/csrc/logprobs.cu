@@ -67,6 +67,7 @@ struct LpSmem {
     int last;
     int item;
     float theta;
+    float xt;                              // the merge: the emitted token's (penalised) logit
     unsigned long long top[2 * DSPARK_MAX_TOP_LOGPROBS];
     float mm[kLpMergeLists];               // the merge's copies of the chunk partials
     float ms[kLpMergeLists];
@@ -395,21 +396,54 @@ __device__ int top_select(LpSmem& s, const unsigned long long* keys, const int* 
 // top-n list, written to *out.
 // cand: when non-null, a chunk whose gathered keys all fit (at most kLpCandPerChunk) writes them
 // there unselected and leaves the selection to the row merge.
+// The 16-byte-aligned interior [va, vb) of chunk [c0, c1) of target row `slot`: nv vectors
+// from g (element e starts a vector iff (e - head) % EPV == 0).
+template <int SX>
+struct LpGeom {
+    int va, vb, nv;
+    const uint4* g;
+    __device__ LpGeom(const Args& a, long long slot, int c0, int c1) {
+        constexpr int EPV = 16 / SX;
+        const unsigned char* rowp = static_cast<const unsigned char*>(a.x) + slot * a.V * SX;
+        const int head = static_cast<int>(((16u - static_cast<unsigned>(reinterpret_cast<uintptr_t>(rowp) & 15u)) & 15u) / SX);
+        const int lo = max(c0, head);
+        va = min(c1, head + ((lo - head + EPV - 1) / EPV) * EPV);
+        vb = (c1 >= va + EPV) ? head + ((c1 - head) / EPV) * EPV : va;
+        nv = (vb - va) / EPV;
+        g = reinterpret_cast<const uint4*>(rowp + static_cast<long long>(va) * SX);
+    }
+};
+
+constexpr int kLpStep = kLpVec * kLpThreads;             // vectors per batch
+
+// Thread 0: bulk copy of batch q of a chunk into stage (nbat + q) & 1.
+__device__ __forceinline__ void lp_issue(LpSmem& s, const uint4* g, int nv, int nbat, int q) {
+    const int st = (nbat + q) & 1;
+    const unsigned bytes = 16u * static_cast<unsigned>(min(kLpStep, nv - q * kLpStep));
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(reinterpret_cast<uint64_t*>(&s.full[st]), bytes);
+    bulk_g2s(s.stage[st], g + static_cast<long long>(q) * kLpStep, bytes, reinterpret_cast<uint64_t*>(&s.full[st]));
+}
+
+// Thread 0, as soon as the chunk is known: its first two batches (lp_chunk issues the rest).
+template <int SX>
+__device__ __forceinline__ void lp_issue_first(const Args& a, LpSmem& s, long long slot, int c0, int c1, int nbat) {
+    const LpGeom<SX> gm(a, slot, c0, c1);
+    const int nb = (gm.nv + kLpStep - 1) / kLpStep;
+    if (nb > 0) lp_issue(s, gm.g, gm.nv, nbat, 0);
+    if (nb > 1) lp_issue(s, gm.g, gm.nv, nbat, 1);
+}
+
 template <int SX, bool PEN>
 // theta_known: a lower bound of the row's n-th largest logit known before the pass (the row's
-// top-k threshold, below), else -inf with known == false.
+// top-k threshold, below), else -inf with known == false.  Batches 0 and 1 were issued by
+// lp_issue_first.
 __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c1, LpPartial* out, const LpRow& pr,
                          int& nbat, unsigned long long* cand, bool known, float theta_known) {
     constexpr int EPV = 16 / SX;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned char* rowp = static_cast<const unsigned char*>(a.x) + slot * a.V * SX;
-    const int head = static_cast<int>(((16u - static_cast<unsigned>(reinterpret_cast<uintptr_t>(rowp) & 15u)) & 15u) / SX);
-    // aligned interior [va, vb): element e starts a vector iff (e - head) % EPV == 0
-    const int lo = max(c0, head);
-    const int va = min(c1, head + ((lo - head + EPV - 1) / EPV) * EPV);
-    const int vb = (c1 >= va + EPV) ? head + ((c1 - head) / EPV) * EPV : va;
-    const int nv = (vb - va) / EPV;
-    const uint4* g = reinterpret_cast<const uint4*>(rowp + static_cast<long long>(va) * SX);
+    const LpGeom<SX> gm(a, slot, c0, c1);
+    const int va = gm.va, vb = gm.vb, nv = gm.nv;
     const uint32_t ninf = SX == 2 ? 0xFF80FF80u : 0xFF800000u;     // -inf filler past the interior
     const int n_top = min(a.n_top, c1 - c0);
     // edges: thread 0 takes [c0, va), thread 1 takes [vb, c1) (fewer than EPV each)
@@ -432,15 +466,8 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
     // the interior streams through two shared-memory stages, one batch (kLpVec vectors per
     // thread) each, copied by the bulk-copy engine: CTA batch counter nbat picks the stage
     // (nbat & 1) and the phase ((nbat >> 1) & 1) of its barrier
-    constexpr int kStep = kLpVec * kLpThreads;
+    constexpr int kStep = kLpStep;
     const int nb = (nv + kStep - 1) / kStep;
-    auto issue = [&](int q) {                             // thread 0: batch q of this chunk
-        const int st = (nbat + q) & 1;
-        const unsigned bytes = 16u * static_cast<unsigned>(min(kStep, nv - q * kStep));
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(reinterpret_cast<uint64_t*>(&s.full[st]), bytes);
-        bulk_g2s(s.stage[st], g + static_cast<long long>(q) * kStep, bytes, reinterpret_cast<uint64_t*>(&s.full[st]));
-    };
     bool dead = false;                                    // a wait of this thread gave up
     auto load = [&](uint4 (&w)[kLpVec], int q) {
         const int st = (nbat + q) & 1;
@@ -547,10 +574,6 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
             }
         }
     };
-    if (tid == 0) {
-        if (nb > 0) issue(0);
-        if (nb > 1) issue(1);
-    }
     for (int q = 0; q < max(nb, 1); ++q) {
         const int v0 = q * kStep;
         uint4 w[kLpVec];
@@ -561,7 +584,7 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
             for (int i = 0; i < kLpVec; ++i) w[i] = make_uint4(ninf, ninf, ninf, ninf);
         }
         __syncthreads();                                  // the stage is read: refill it
-        if (tid == 0 && q + 2 < nb) issue(q + 2);
+        if (tid == 0 && q + 2 < nb) lp_issue(s, gm.g, nv, nbat, q + 2);
         if (PEN) pen_mask(w, v0);
         reduce(w);
         if (q == 0 && n_top > 0) {
@@ -654,6 +677,12 @@ __device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j,
     // chunk's keys (its top list, or its unselected candidates) are staged one after another;
     // S <= kLpMergeLists chunks of at most kLpCandPerChunk keys fit the key buffer
     static_assert(kLpMergeLists * kLpCandPerChunk <= kLpCandCap, "merge staging");
+    // the emitted token's logit, fetched by the last warp (which stages no keys: every chunk
+    // holds fewer keys than the threads before it) while the others copy the partials
+    constexpr int kTokThread = kLpThreads - 32;
+    static_assert(kLpCandPerChunk <= kTokThread && DSPARK_MAX_TOP_LOGPROBS <= kTokThread, "token thread");
+    int tok = -1;
+    if (tid == kTokThread && a.out_lp) tok = a.out_tokens[static_cast<long long>(b) * W + j];
     for (int c = tid; c < S; c += blockDim.x) {
         s.mm[c] = __ldcg(&part[c].m);
         s.ms[c] = __ldcg(&part[c].s);
@@ -686,6 +715,10 @@ __device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j,
         }
     }
     if (tid == 0) s.wcnt[0] = off;
+    if (tid == kTokThread && a.out_lp) {                  // -inf: no token (its logprob is -inf too)
+        const float xt = tok >= 0 ? load_x(a.x, a.sx, slot * a.V + tok) : -INFINITY;
+        s.xt = tok < 0 ? -INFINITY : (pen ? lp_value<true>(a, pr, tok, xt) : xt);
+    }
     __syncthreads();
     if (tid < 32) {
         float mm = -INFINITY;
@@ -699,12 +732,7 @@ __device__ void lp_merge(const Args& a, LpSmem& s, long long slot, int b, int j,
         const float lse = mm + logf(sum);
         if (lane == 0) {
             s.theta = lse;
-            if (a.out_lp) {
-                const int t = a.out_tokens[static_cast<long long>(b) * W + j];
-                const float xt = t >= 0 ? load_x(a.x, a.sx, slot * a.V + t) : 0.f;
-                a.out_lp[static_cast<long long>(b) * W + j] =
-                    t >= 0 ? (pen ? lp_value<true>(a, pr, t, xt) : xt) - lse : -INFINITY;
-            }
+            if (a.out_lp) a.out_lp[static_cast<long long>(b) * W + j] = s.xt - lse;
         }
     }
     if (n_top <= 0) return;
@@ -740,17 +768,14 @@ __global__ void __launch_bounds__(kLpThreads, kLpBlocksPerSm) logprob_kernel(Arg
     const int S = max(1, min(min(kLpMaxChunks, static_cast<int>(gridDim.x) / R), a.V / kLpMinChunk));
     const int chunk = ((a.V + S - 1) / S + 7) / 8 * 8;
     const int items = R * S;
-    for (;;) {
-        // the next (row, chunk) item, from a counter: no CTA idles while items remain
-        if (threadIdx.x == 0) s.item = atomicAdd(&a.plan->pad[2], 1);
-        __syncthreads();
-        const int it = s.item;
-        __syncthreads();
-        if (it >= items) break;
+    // item blockIdx.x first (S is chosen so that all R * S items fit the grid when R does);
+    // past the grid, the next items come from a counter
+    for (int it = blockIdx.x; it < items;) {
         const int p = it / S, c = it - p * S;                 // listed row p, its chunk c
         const int row = a.lp_list[1 + p];                    // b * W + j
         const int b = row / W, j = row % W;
         const int c0 = c * chunk, c1 = min(a.V, c0 + chunk);
+        if (threadIdx.x == 0) lp_issue_first<SX>(a, s, row, c0, c1, nbat);   // before the row's parameters arrive
         LpPartial* part = a.lp_part + static_cast<long long>(p) * S;   // the row's S partials
         const dspark_row_params_t r = a.rows[b];
         const LpRow pr{b, j, r.frequency_penalty, r.presence_penalty};
@@ -776,7 +801,11 @@ __global__ void __launch_bounds__(kLpThreads, kLpBlocksPerSm) logprob_kernel(Arg
             __threadfence();
             lp_merge(a, s, row, b, j, part, cands, S, pr, pen);
         }
+        if (items <= static_cast<int>(gridDim.x)) break;
         __syncthreads();                                     // shared memory reused by the next item
+        if (threadIdx.x == 0) s.item = static_cast<int>(gridDim.x) + atomicAdd(&a.plan->pad[2], 1);
+        __syncthreads();
+        it = s.item;
     }
 }
 
