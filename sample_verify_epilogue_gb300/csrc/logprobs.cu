@@ -416,13 +416,15 @@ struct LpGeom {
 
 constexpr int kLpStep = kLpVec * kLpThreads;             // vectors per batch
 
-// Thread 0: bulk copy of batch q of a chunk into stage (nbat + q) & 1.
+// Thread 0: bulk copy of batch q of a chunk into stage (nbat + q) & 1.  The logits are read
+// for the last time in the call: evict-first in L2.
 __device__ __forceinline__ void lp_issue(LpSmem& s, const uint4* g, int nv, int nbat, int q) {
     const int st = (nbat + q) & 1;
     const unsigned bytes = 16u * static_cast<unsigned>(min(kLpStep, nv - q * kLpStep));
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive_expect_tx(reinterpret_cast<uint64_t*>(&s.full[st]), bytes);
-    bulk_g2s(s.stage[st], g + static_cast<long long>(q) * kLpStep, bytes, reinterpret_cast<uint64_t*>(&s.full[st]));
+    bulk_g2s_hint(s.stage[st], g + static_cast<long long>(q) * kLpStep, bytes, reinterpret_cast<uint64_t*>(&s.full[st]),
+                  l2_evict_first_policy());
 }
 
 // Thread 0, as soon as the chunk is known: its first two batches (lp_chunk issues the rest).

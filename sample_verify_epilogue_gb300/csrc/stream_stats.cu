@@ -4,8 +4,9 @@
 // Work unit = a segment: a few consecutive vocab tiles of one row.  Persistent CTAs, one per
 // SM; each CTA has two independent consumer groups of 8 warps and a producer warp.  The
 // producer moves tiles into a 4-stage shared-memory ring (two stages per group) with the TMA
-// bulk-copy engine (cp.async.bulk, completion counted on an mbarrier), together with each
-// tile's penalty bitmap and penalised-token list, serving both groups' segment streams.
+// bulk-copy engine (cp.async.bulk, completion counted on an mbarrier; the tiles with an
+// evict-first L2 policy), together with each tile's penalty bitmap and penalised-token list,
+// serving both groups' segment streams.
 //
 // A group processes a segment in one sweep:
 //   first tile: pass 1 gives per-thread maxima of the penalised logits
@@ -1113,6 +1114,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
         // the group's current and next segment; lane 0 issues the copies.
         const int lane = tid & 31;
         const int mg = lane >> 4, ml = lane & 15;
+        // the tiles are read once per call: evict-first in L2, so that the 0.8 GB streamed
+        // through it do not push out the statistics, candidate lists and penalty index that
+        // this and the following kernels write and read
+        const uint64_t stream_policy = l2_evict_first_policy();
         constexpr int kFields = sizeof(UnitDesc) / sizeof(int);
         static_assert(kFields <= 16, "descriptor fields must fit a half warp");
         const int* streams = reinterpret_cast<const int*>(a.units + static_cast<long long>(c) * kGroups * a.max_seg);
@@ -1196,7 +1201,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_stats_kernel(Args a)
                     const unsigned ent_bytes = m.pen && !pover ? static_cast<unsigned>(pn) * 16u : 0u;
                     if (m.pen) tx += bm_bytes + ent_bytes;
                     mbar_arrive_expect_tx(&sm.full[stage], tx);
-                    if (bytes) bulk_g2s(sm.data[stage], reinterpret_cast<const void*>(c0), bytes, &sm.full[stage]);
+                    if (bytes) bulk_g2s_hint(sm.data[stage], reinterpret_cast<const void*>(c0), bytes, &sm.full[stage],
+                                             stream_policy);
                     if (m.pen) {
                         const long long pt = static_cast<long long>(b) * a.tiles_x + tile;
                         bulk_g2s(sm.bm[stage], a.pen_bm + pt * a.bm_words, bm_bytes, &sm.full[stage]);
