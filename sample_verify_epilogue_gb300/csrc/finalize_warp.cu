@@ -257,13 +257,62 @@ __device__ int warp_topk_survivors(WarpSmem& w, int n, int k, uint32_t* kth_out 
     return warp_survivors(w, n, kth);
 }
 
-// Nucleus over the sorted survivors w.sk[0..cnt) with weights wfn(value) (fixed order: lane
-// l sums its consecutive chunk, then the chunk sums are scanned across lanes).  Kept = the
+// Nucleus over the sorted survivors w.sk[0..cnt) with weights wfn(value) (fixed order: up to
+// 64 survivors, two interleaved 32-wide scans; more, lane l sums its consecutive chunk, then
+// the chunk sums are scanned across lanes).  Kept = the
 // tie groups whose exclusive mass is < top_p * Z.  Returns the number kept; *zk = kept mass.
 // With `dst`, the kept entries (id, weight) are written there.
 template <typename WFn>
 __device__ int warp_nucleus(const WarpSmem& w, int cnt, float top_p, WFn wfn, double* zk, KeptEntry* dst) {
     const int lane = threadIdx.x & 31;
+    if (cnt <= 64) {
+        // up to 64 survivors: element i at lane i % 32, half i / 32; the prefix is two 32-wide
+        // shuffle scans side by side (fixed order), not a chain of eight additions per lane
+        double wv[2], inc[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = lane + 32 * h;
+            wv[h] = i < cnt ? static_cast<double>(wfn(ckey_v(w.sk[i]))) : 0.0;
+            inc[h] = wv[h];
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double y0 = __shfl_up_sync(0xffffffffu, inc[0], o);
+            const double y1 = __shfl_up_sync(0xffffffffu, inc[1], o);
+            if (lane >= o) { inc[0] += y0; inc[1] += y1; }
+        }
+        const double tot0 = __shfl_sync(0xffffffffu, inc[0], 31);
+        inc[1] += tot0;
+        const double Z = __shfl_sync(0xffffffffu, inc[1], 31);
+        // exclusive prefix of element i = the inclusive prefix of element i - 1
+        double ex[2];
+        ex[0] = __shfl_up_sync(0xffffffffu, inc[0], 1);
+        ex[1] = __shfl_up_sync(0xffffffffu, inc[1], 1);
+        if (lane == 0) { ex[0] = 0.0; ex[1] = tot0; }
+        int kept = cnt;
+        if (top_p < 1.f) {
+            const double lim = static_cast<double>(top_p) * Z;
+            int first_drop = cnt;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                if (i > 0 && i < cnt && (w.sk[i] >> 32) != (w.sk[i - 1] >> 32) && !(ex[h] < lim))
+                    first_drop = min(first_drop, i);
+            }
+            kept = __reduce_min_sync(0xffffffffu, first_drop);
+        }
+        const double e0 = __shfl_sync(0xffffffffu, ex[0], kept & 31);
+        const double e1 = __shfl_sync(0xffffffffu, ex[1], kept & 31);
+        *zk = kept == cnt ? Z : (kept >= 32 ? e1 : e0);
+        if (dst) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                if (i < kept) dst[i] = KeptEntry{ckey_id(w.sk[i]), static_cast<float>(wv[h])};
+            }
+        }
+        return kept;
+    }
     constexpr int kPer = kWSurvCap / 32;
     const int lo = lane * kPer;
     double wv[kPer];
