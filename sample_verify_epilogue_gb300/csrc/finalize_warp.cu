@@ -542,7 +542,9 @@ __device__ bool warp_finalize_q(WarpSmem& w, const Args& a, int qslot, int b) {
     return true;
 }
 
-__global__ void __launch_bounds__(32 * kRowsPerBlockMax) row_finalize_warp_kernel(Args a) {
+// Blocks of up to 32 * kRowsPerBlockMax threads; the register cap keeps the kernel free of spills
+// (the compiler's default for 256-thread blocks spilled).
+__global__ void __maxnreg__(96) row_finalize_warp_kernel(Args a) {
     pdl_enter();
     // a bounded wait of the streaming pass gave up: its statistics are incomplete and every
     // request reports DSPARK_ROW_INTERNAL, so nothing here may read them
