@@ -50,6 +50,24 @@ def test_mixed18_all_combinations(runner):
     _run(runner, configs.build("b256k16v262144_mixed", B=18), "b256k16v262144_mixed B=18")
 
 
+def test_signed_zero_draft_probabilities(runner):
+    """Draft rows holding -0.0 (a valid zero probability) in top-k and full rows, on both sides
+    of a tile: the streaming pass scans top-k draft rows on raw bit patterns, where -0.0 has
+    the sign bit set, and must fall back to the float maximum for those tiles."""
+    rows = [row_params(1.0, 20, 0.9, 0.0, 0.0, 3), row_params(0.8, 64, 1.0, 0.0, 0.0, 3),
+            row_params(1.0, 0, 1.0, 0.0, 0.0, 3), row_params(0.7, 0, 0.8, 0.0, 0.0, 3)]
+    batch = make_batch(B=4, K_max=3, V=30011, logits_dtype="bf16", rows=rows, seed=303, philox_seed=303,
+                       x_sigma=1.0, argmax_frac=0.5, history_len=0)
+    rng = np.random.default_rng(303)
+    for b in range(4):
+        for i in range(3):
+            z = rng.choice(batch.V, size=500, replace=False)
+            z = z[z != batch.draft_ids[b, i]]
+            batch.q[b, i, z] = -0.0
+    assert np.signbit(batch.q).sum() > 0
+    _run(runner, batch, "signed-zero draft probabilities")
+
+
 def test_list_draw_lengths(runner):
     """Kept lists of every length class of the draw from a truncated row: one entry, the
     one-warp path (up to 64 entries, both sides of a half-warp), and the block path above it;
