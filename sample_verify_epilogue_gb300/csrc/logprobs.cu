@@ -45,6 +45,7 @@ constexpr int kLpBlocksPerSm = 4;
 constexpr int kLpWarps = kLpThreads / 32;
 constexpr int kLpCandCap = 2048;
 constexpr int kLpVec = 4;                    // 16-byte vectors per thread and batch
+constexpr int kLpStages = 2;                 // batches of a chunk in flight
 constexpr int kLpWarpCap = kLpCandCap / kLpWarps;
 constexpr int kLpMergeLists = kLpMaxChunks;  // chunk partials the merge copies to shared memory
 constexpr int kLpMinChunk = 8192;            // logits per chunk at least
@@ -52,8 +53,8 @@ constexpr int kLpSelCap = 256;               // keys at the n-th largest value a
 constexpr float kL2E = 1.4426950408889634f;
 
 struct LpSmem {
-    uint4 stage[2][kLpVec * kLpThreads];   // two batches of the chunk, filled by bulk copies
-    unsigned long long full[2];            // their mbarriers
+    uint4 stage[kLpStages][kLpVec * kLpThreads];   // batches of the chunk, filled by bulk copies
+    unsigned long long full[kLpStages];    // their mbarriers
     unsigned long long keys[kLpCandCap];   // (fkey(value) << 32) | (0xFFFFFFFF - id); warp w: [w*kLpWarpCap, ...)
     float tmax[kLpThreads];
     float wm[kLpWarps];
@@ -416,10 +417,10 @@ struct LpGeom {
 
 constexpr int kLpStep = kLpVec * kLpThreads;             // vectors per batch
 
-// Thread 0: bulk copy of batch q of a chunk into stage (nbat + q) & 1.  The logits are read
+// Thread 0: bulk copy of batch q of a chunk into stage (nbat + q) % kLpStages.  The logits are read
 // for the last time in the call: evict-first in L2.
 __device__ __forceinline__ void lp_issue(LpSmem& s, const uint4* g, int nv, int nbat, int q) {
-    const int st = (nbat + q) & 1;
+    const int st = (nbat + q) % kLpStages;
     const unsigned bytes = 16u * static_cast<unsigned>(min(kLpStep, nv - q * kLpStep));
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive_expect_tx(reinterpret_cast<uint64_t*>(&s.full[st]), bytes);
@@ -427,18 +428,17 @@ __device__ __forceinline__ void lp_issue(LpSmem& s, const uint4* g, int nv, int 
                   l2_evict_first_policy());
 }
 
-// Thread 0, as soon as the chunk is known: its first two batches (lp_chunk issues the rest).
+// Thread 0, as soon as the chunk is known: its first kLpStages batches (lp_chunk issues the rest).
 template <int SX>
 __device__ __forceinline__ void lp_issue_first(const Args& a, LpSmem& s, long long slot, int c0, int c1, int nbat) {
     const LpGeom<SX> gm(a, slot, c0, c1);
     const int nb = (gm.nv + kLpStep - 1) / kLpStep;
-    if (nb > 0) lp_issue(s, gm.g, gm.nv, nbat, 0);
-    if (nb > 1) lp_issue(s, gm.g, gm.nv, nbat, 1);
+    for (int q = 0; q < kLpStages && q < nb; ++q) lp_issue(s, gm.g, gm.nv, nbat, q);
 }
 
 template <int SX, bool PEN>
 // theta_known: a lower bound of the row's n-th largest logit known before the pass (the row's
-// top-k threshold, below), else -inf with known == false.  Batches 0 and 1 were issued by
+// top-k threshold, below), else -inf with known == false.  The first kLpStages batches were issued by
 // lp_issue_first.
 __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c1, LpPartial* out, const LpRow& pr,
                          int& nbat, unsigned long long* cand, bool known, float theta_known) {
@@ -467,13 +467,13 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
     float theta = INFINITY;
     // the interior streams through two shared-memory stages, one batch (kLpVec vectors per
     // thread) each, copied by the bulk-copy engine: CTA batch counter nbat picks the stage
-    // (nbat & 1) and the phase ((nbat >> 1) & 1) of its barrier
+    // (nbat % kLpStages) and the phase ((nbat / kLpStages) & 1) of its barrier
     constexpr int kStep = kLpStep;
     const int nb = (nv + kStep - 1) / kStep;
     bool dead = false;                                    // a wait of this thread gave up
     auto load = [&](uint4 (&w)[kLpVec], int q) {
-        const int st = (nbat + q) & 1;
-        if (!dead && !lp_wait(&s.full[st], ((nbat + q) >> 1) & 1)) {
+        const int st = (nbat + q) % kLpStages;
+        if (!dead && !lp_wait(&s.full[st], ((nbat + q) / kLpStages) & 1)) {
             dead = true;
             atomicOr(&a.row_status[pr.b], DSPARK_ROW_INTERNAL);
         }
@@ -586,7 +586,7 @@ __device__ void lp_chunk(const Args& a, LpSmem& s, long long slot, int c0, int c
             for (int i = 0; i < kLpVec; ++i) w[i] = make_uint4(ninf, ninf, ninf, ninf);
         }
         __syncthreads();                                  // the stage is read: refill it
-        if (tid == 0 && q + 2 < nb) lp_issue(s, gm.g, nv, nbat, q + 2);
+        if (tid == 0 && q + kLpStages < nb) lp_issue(s, gm.g, nv, nbat, q + kLpStages);
         if (PEN) pen_mask(w, v0);
         reduce(w);
         if (q == 0 && n_top > 0) {
@@ -759,8 +759,7 @@ __global__ void __launch_bounds__(kLpThreads, kLpBlocksPerSm) logprob_kernel(Arg
     const int R = a.lp_list[0];
     if (R == 0) return;
     if (threadIdx.x == 0) {
-        mbar_init(reinterpret_cast<uint64_t*>(&s.full[0]), 1);
-        mbar_init(reinterpret_cast<uint64_t*>(&s.full[1]), 1);
+        for (int st = 0; st < kLpStages; ++st) mbar_init(reinterpret_cast<uint64_t*>(&s.full[st]), 1);
         fence_mbar_init();
     }
     __syncthreads();
