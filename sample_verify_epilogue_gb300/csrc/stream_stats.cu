@@ -297,6 +297,20 @@ __device__ __forceinline__ unsigned ge_mask(const uint4& w, float th) {
     return m;
 }
 
+// The same for the flush of a bf16 tile, on bf16 pairs against th2 = th rounded down to bf16:
+// bit q set where element q >= th2 (every element >= th, and those equal to th2 < th besides,
+// which only adds candidates below the threshold).
+__device__ __forceinline__ unsigned ge_mask_bf16(const uint4& w, __nv_bfloat162 th2) {
+    const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&w);
+    unsigned m = 0u;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const unsigned mk = __hge2_mask(p[h], th2);       // 0xFFFF per half that holds
+        m |= ((mk & 1u) | ((mk >> 15) & 2u)) << (2 * h);
+    }
+    return m;
+}
+
 // Position of the r-th (0-based) set bit of b; requires r < popc(b).
 __device__ __forceinline__ int nth_set_bit(unsigned b, int r) {
     int pos = 0;
@@ -328,8 +342,9 @@ __device__ __noinline__ int deal_by_ballots(unsigned vflags, int t, int wv) {
 // threshold).  The warp's flagged vectors are dealt out to its lanes 32 at a time, so a lane
 // with many flags does not hold up the others: a prefix over the lanes' flag counts places
 // them in a per-warp list (more than 64 fall back to slot-wise ballots).  For each vector,
-// the elements >= th_p without a penalty bit are appended to the candidate list `lp` (CAND)
-// and folded into the running penalised maximum and the lowest index attaining it (TRACK).
+// the elements >= th_p (bf16: >= th_p rounded down to bf16) without a penalty bit are
+// appended to the candidate list `lp` (CAND) and folded into the running penalised maximum
+// and the lowest index attaining it (TRACK).
 // Every lane of the warp calls it.
 template <int SX, bool PEN, bool CAND, bool TRACK>
 __device__ __forceinline__ void flush_vectors(GroupSmem& gs, Cand* lp, unsigned vflags, const unsigned char* data,
@@ -338,6 +353,7 @@ __device__ __forceinline__ void flush_vectors(GroupSmem& gs, Cand* lp, unsigned 
     constexpr int EPV = 16 / SX;
     const int lane = threadIdx.x & 31;
     const int wv = gt - lane;                             // vector index of lane 0, slot 0
+    const __nv_bfloat162 th2 = __bfloat162bfloat162(__float2bfloat16_rd(th_p));
     // the warp's flagged vectors in (lane, slot) order: a prefix over the lanes' counts, each
     // lane writing its own into the warp's list
     const int nf = __popc(vflags);
@@ -371,7 +387,8 @@ __device__ __forceinline__ void flush_vectors(GroupSmem& gs, Cand* lp, unsigned 
             w = *reinterpret_cast<const uint4*>(data + v * 16);
             e = vec_e0 + v * EPV;
             const unsigned bits = PEN ? bitmap_bits(bm, bit0 + v * EPV, EPV) : 0u;
-            mp = ge_mask<SX>(w, th_p) & ~bits;
+            if constexpr (SX == 2) mp = ge_mask_bf16(w, th2) & ~bits;
+            else mp = ge_mask<SX>(w, th_p) & ~bits;
         }
         if (CAND) warp_append<SX>(lp, &gs.n_pen, kCandPenGlobal, mp, w, e, 0);
         if (TRACK) {
